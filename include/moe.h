@@ -1,0 +1,200 @@
+/*
+ * moe.h - C ABI of the GB300 (sm_103a) routed Mixture-of-Experts FFN forward.
+ *
+ * The library computes, on one GPU, the routed MoE FFN forward pass
+ *
+ *     topk routes -> count/sort -> gather -> prefix/task map
+ *       -> Gate/Up grouped GEMM -> SwiGLU (+ FP8 re-quantisation)
+ *       -> Down grouped GEMM -> scatter/top-k reduction
+ *
+ * named in "perf: add small-batch route MMA for MoE" (Motivation), with the
+ * index_shuffling and scatter_add_dense_tokens steps of "Port necessary
+ * FBGEMM MoE kernels", and the route-direct small-batch path of the route-MMA
+ * page (Summary: reads the expert from each token/top-k route, bypasses
+ * sorting, gathering, prefix sums and task maps, splits the long Gate/Up K
+ * dimension, fuses split reduction + SwiGLU + Down-input quantisation).
+ *
+ * Definitions used throughout:
+ *   T tokens, E experts, k = top_k, H hidden size, I expert intermediate size,
+ *   R = T*k routes; route r = t*k + j is slot j of token t.
+ *   Routing: ids[t, 0..k-1] = the k experts with the largest router score,
+ *   ordered by score descending, ties to the lower expert id (-0.0 == +0.0);
+ *   w[t, j] = softmax over the k selected scores.
+ *   Gate/Up weights W1 [E, 2I, H]: rows 0..I-1 of W1[e] are the gate
+ *   projection, rows I..2I-1 the up projection.  Down weights W2 [E, H, I].
+ *   y[t] = sum_j w[t, j] * W2[ids[t, j]] (silu(gate) * up), rounded to bf16.
+ *
+ * Conventions for every entry point:
+ *   - All array arguments are DEVICE pointers to row-major, contiguous
+ *     arrays, unless stated otherwise.  Bases of bf16 / e4m3 arrays and of
+ *     the workspace must be 16-byte aligned (a TMA requirement); int32 and
+ *     fp32 arrays 4-byte aligned.
+ *   - The caller owns and allocates every buffer, including outputs and the
+ *     workspace.  The library never allocates, frees or synchronises inside
+ *     moe_route / moe_shuffle / moe_tile_map / moe_forward: work is enqueued
+ *     on `stream` in order, with no device-to-host copy, so these calls can be
+ *     captured in a CUDA graph.  Inputs are never written.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   - Arguments are validated on the host BEFORE anything is enqueued; on a
+ *     validation error nothing is launched and outputs are untouched.
+ *   - A launch failure returns MOE_ERR_CUDA.  Conditions detected on the device
+ *     (a bounded wait that timed out, an index out of range) are recorded in
+ *     a status word at the head of the workspace and reported by
+ *     moe_read_device_status(); the library never traps.
+ *   - Results are deterministic: the same inputs give bitwise identical
+ *     outputs, eager or replayed from a CUDA graph.
+ */
+#ifndef MOE_GB300_MOE_H_
+#define MOE_GB300_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so that the header needs no CUDA headers. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,    /* bad shape, null or misaligned pointer, inconsistent scales */
+  MOE_ERR_UNSUPPORTED = 2,    /* valid, but outside what this build implements (limits below) */
+  MOE_ERR_WORKSPACE = 3,      /* workspace missing or smaller than the *_workspace_size() value */
+  MOE_ERR_CUDA = 4,           /* a CUDA runtime/driver call or a launch failed, or no usable GPU */
+  MOE_ERR_DEVICE_TIMEOUT = 5, /* a kernel's bounded wait expired (reported by moe_read_device_status) */
+  MOE_ERR_DEVICE_BOUNDS = 6   /* a kernel saw an out-of-range index (reported by moe_read_device_status) */
+} moe_status;
+
+typedef enum {
+  MOE_BF16 = 0,           /* bf16 x, W1, W2; bf16 h; fp32 accumulation */
+  MOE_FP8_PER_TENSOR = 1, /* e4m3 W1/W2 with one fp32 scale per expert matrix; x and h quantised to
+                             e4m3 with one dynamic scale each (amax/448 over the whole tensor) */
+  MOE_FP8_BLOCK128 = 2    /* e4m3 W1/W2 with fp32 scales per 128x128 block; x quantised per
+                             (token, 128 columns); h per (route, 128 columns) */
+} moe_quant;
+
+typedef enum {
+  MOE_PATH_AUTO = 0,        /* library chooses (see moe_select_path) */
+  MOE_PATH_GROUPED = 1,     /* count/sort -> tiles -> grouped GEMMs -> combine */
+  MOE_PATH_ROUTE_DIRECT = 2 /* route-order decode path, no sort / gather / tile map */
+} moe_path;
+
+typedef struct {
+  int T, E, k, H, I;
+  moe_quant quant;
+  moe_path path;
+} moe_problem;
+
+/* Limits of this build (MOE_ERR_UNSUPPORTED beyond them):
+ *   1 <= E <= 512;  1 <= k <= min(E, 32);  0 <= T;  T*k < 2^31;
+ *   H % 64 == 0, I % 64 == 0 (bf16);  H % 128 == 0, I % 64 == 0 (FP8 per-tensor);
+ *   H % 128 == 0, I % 128 == 0 (FP8 blockwise);
+ *   MOE_PATH_GROUPED: bf16 only;  MOE_PATH_ROUTE_DIRECT: FP8 only, T*k <= 1024. */
+
+/* ---------------------------------------------------------------- routing
+ * moe_route - top-k routing ("perf: add small-batch route MMA for MoE",
+ * Motivation: topk routes).
+ *   scores [T, E] fp32 (finite; NaN/inf are outside the contract)
+ *   ids    [T, k] int32 out: selected experts in slot order (score desc, id asc)
+ *   w      [T, k] fp32  out: softmax over the k selected scores
+ * ids are exact; w is computed in fp32 (expf, IEEE division).
+ * T == 0 is a no-op.  Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+moe_status moe_route(const float* scores, int T, int E, int k, int32_t* ids, float* w,
+                     moe_stream_t stream);
+
+/* ---------------------------------------------------------------- shuffle
+ * moe_shuffle - index shuffling (index_shuffling of "Port necessary FBGEMM
+ * MoE kernels"; count/sort of the route-MMA page's Motivation).
+ *   ids     [T, k] int32 in: expert of each route, each in [0, E)
+ *   counts  [E]    int32 out: routes per expert
+ *   offsets [E+1]  int32 out: exclusive prefix sum of counts (offsets[E] = R)
+ *   perm    [R]    int32 out: sorted position -> route r; stable (routes of one
+ *                             expert keep increasing r, i.e. token order)
+ *   inv     [R]    int32 out: route -> sorted position (inv[perm[p]] == p)
+ *   ws      device scratch of at least moe_shuffle_workspace_size(T, E, k) bytes
+ * All outputs are unique and therefore bit-exact.  An id outside [0, E) is
+ * recorded as MOE_ERR_DEVICE_BOUNDS in the status word at the head of ws and
+ * that route is left out of the outputs.  Errors: INVALID_ARG, UNSUPPORTED,
+ * WORKSPACE, CUDA. */
+size_t moe_shuffle_workspace_size(int T, int E, int k);
+moe_status moe_shuffle(const int32_t* ids, int T, int E, int k, int32_t* counts, int32_t* offsets,
+                       int32_t* perm, int32_t* inv, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- tile map
+ * moe_tile_map - the grouped GEMMs' task map ("prefix/task map" of the
+ * route-MMA page's Motivation, bounded by the non-empty workload as in its
+ * Code changes), built on the device with no device-to-host copy.
+ *   counts    [E] int32 in (e.g. from moe_shuffle)
+ *   BM        row-tile height (1..1024; moe_forward uses 128)
+ *   tiles     [max_tiles, 4] int32 out: {expert, first sorted row, rows, 0} for
+ *             each tile, experts in id order, ceil(counts[e]/BM) tiles each
+ *   num_tiles [1] int32 out: number of tiles written
+ *   max_tiles capacity of `tiles`; floor(sum(counts)/BM) + E always suffices.
+ * If the tiles do not fit, num_tiles holds the required count, only
+ * max_tiles tiles are written and MOE_ERR_DEVICE_BOUNDS is recorded in the
+ * status word at the head of ws.  ws needs moe_shuffle_workspace_size(0, E, 1)
+ * bytes.  Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
+moe_status moe_tile_map(const int32_t* counts, int E, int BM, int32_t* tiles, int32_t* num_tiles,
+                        int max_tiles, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- forward
+ * moe_select_path - the path moe_forward takes for *p (AUTO resolved):
+ * bf16 -> GROUPED; FP8 -> ROUTE_DIRECT.  Returns p->path when it is not AUTO. */
+moe_path moe_select_path(const moe_problem* p);
+
+/* moe_workspace_size - bytes of device workspace moe_forward needs for *p
+ * (0 if *p is invalid or unsupported). */
+size_t moe_workspace_size(const moe_problem* p);
+
+/* moe_forward - the whole routed MoE FFN forward.
+ *   x        [T, H]  bf16 activations
+ *   scores   [T, E]  fp32 router scores
+ *   w1       [E, 2I, H] bf16 (MOE_BF16) or e4m3 codes (FP8 modes); rows 0..I-1 gate, I..2I-1 up
+ *   w2       [E, H, I]  bf16 or e4m3
+ *   w1_scale NULL (bf16) | fp32 [E] (per-tensor) | fp32 [E, 2I/128, H/128] (blockwise)
+ *   w2_scale NULL (bf16) | fp32 [E] (per-tensor) | fp32 [E, H/128, I/128] (blockwise)
+ *   y        [T, H]  bf16 out, preallocated by the caller (written, never read)
+ *   ws       device workspace of at least moe_workspace_size(p) bytes; its
+ *            contents on entry do not matter and are overwritten
+ * Quantisation (FP8 modes): scale = amax/448 in fp32 (1 when amax == 0),
+ * code = e4m3(v / scale) rounded to nearest even with saturation.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
+moe_status moe_forward(const moe_problem* p, const void* x, const float* scores, const void* w1,
+                       const void* w2, const float* w1_scale, const float* w2_scale, void* y,
+                       void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* moe_forward_views - device pointers to the routing results moe_forward
+ * leaves in the workspace (read-only diagnostics; valid after the call's
+ * work on the stream completed).  Pointers not produced by the path chosen
+ * for *p are set to NULL.  ids/w: [T, k]; counts [E]; offsets [E+1];
+ * perm/inv [R]; tiles [*, 4] and num_tiles [1] as for moe_tile_map (BM 128). */
+typedef struct {
+  const int32_t* ids;
+  const float* w;
+  const int32_t* counts;
+  const int32_t* offsets;
+  const int32_t* perm;
+  const int32_t* inv;
+  const int32_t* tiles;
+  const int32_t* num_tiles;
+} moe_views;
+moe_status moe_forward_views(const moe_problem* p, const void* ws, size_t ws_bytes, moe_views* out);
+
+/* ---------------------------------------------------------------- diagnostics
+ * moe_read_device_status - synchronises `stream`, then returns the status
+ * recorded on the device in the status word at the head of `ws` (MOE_OK,
+ * MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_BOUNDS), or MOE_ERR_CUDA if the
+ * synchronisation failed.  Diagnostic only: it blocks, so it is never part of
+ * the hot path.  Each moe_forward / moe_shuffle / moe_tile_map call resets the
+ * word at its start. */
+moe_status moe_read_device_status(const void* ws, moe_stream_t stream);
+
+/* moe_status_string - static, NUL-terminated description of a status code. */
+const char* moe_status_string(moe_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_MOE_H_ */

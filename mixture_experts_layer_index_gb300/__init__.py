@@ -1,0 +1,181 @@
+"""Python binding of libmoe_gb300.so, the GB300 (sm_103a) routed MoE FFN forward.
+
+Argument marshalling only: every step of the forward runs in the library's
+CUDA kernels.  Functions carry the C ABI's names (include/moe.h) and take
+torch CUDA tensors for device memory (plus the current torch stream by
+default); each raises MoeError when the library returns a non-OK status.
+
+The library must have been built (``build.build()`` or
+``__graft_entry__.build()``); the first call into it raises RuntimeError if it
+is missing - there is no other implementation to fall back on.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmoe_gb300.so")
+
+# moe_status
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_WORKSPACE = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_DEVICE_TIMEOUT = 5
+MOE_ERR_DEVICE_BOUNDS = 6
+# moe_quant
+MOE_BF16 = 0
+MOE_FP8_PER_TENSOR = 1
+MOE_FP8_BLOCK128 = 2
+# moe_path
+MOE_PATH_AUTO = 0
+MOE_PATH_GROUPED = 1
+MOE_PATH_ROUTE_DIRECT = 2
+
+QUANT_BY_NAME = {"bf16": MOE_BF16, "fp8_tensor": MOE_FP8_PER_TENSOR, "fp8_block": MOE_FP8_BLOCK128}
+GEMM_BM = 128  # row-tile height of the grouped GEMMs (tile map of moe_forward)
+
+
+class moe_problem(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("E", ctypes.c_int), ("k", ctypes.c_int), ("H", ctypes.c_int),
+                ("I", ctypes.c_int), ("quant", ctypes.c_int), ("path", ctypes.c_int)]
+
+
+class moe_views(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("ids", "w", "counts", "offsets", "perm", "inv", "tiles", "num_tiles")]
+
+
+_vp, _sz, _i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+_P = ctypes.POINTER(moe_problem)
+_SIGS = {
+    "moe_route": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp]),
+    "moe_shuffle_workspace_size": (_sz, [_i, _i, _i]),
+    "moe_shuffle": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_tile_map": (_i, [_vp, _i, _i, _vp, _vp, _i, _vp, _sz, _vp]),
+    "moe_select_path": (_i, [_P]),
+    "moe_workspace_size": (_sz, [_P]),
+    "moe_forward": (_i, [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_forward_views": (_i, [_P, _vp, _sz, ctypes.POINTER(moe_views)]),
+    "moe_read_device_status": (_i, [_vp, _vp]),
+    "moe_status_string": (ctypes.c_char_p, [_i]),
+}
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with mixture_experts_layer_index_gb300.build.build() "
+                "(the CUDA library is the only implementation)")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(handle, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = handle
+    return _lib
+
+
+EXPORTED = tuple(_SIGS)
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {moe_status_string(status)} (status {status})")
+
+
+def moe_status_string(status: int) -> str:
+    return lib().moe_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != MOE_OK:
+        raise MoeError(status, where)
+
+
+def _ptr(t) -> Optional[int]:
+    """Device pointer of a contiguous CUDA tensor (None -> NULL; ints pass through)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("device tensor expected")
+    if not t.is_contiguous():
+        raise ValueError("contiguous tensor expected")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def problem(T: int, E: int, k: int, H: int, I: int, quant=MOE_BF16, path=MOE_PATH_AUTO) -> moe_problem:
+    if isinstance(quant, str):
+        quant = QUANT_BY_NAME[quant]
+    return moe_problem(T, E, k, H, I, int(quant), int(path))
+
+
+def moe_route(scores, T, E, k, ids, w, stream=None) -> None:
+    _check(lib().moe_route(_ptr(scores), T, E, k, _ptr(ids), _ptr(w), _stream(stream)), "moe_route")
+
+
+def moe_shuffle_workspace_size(T, E, k) -> int:
+    return int(lib().moe_shuffle_workspace_size(T, E, k))
+
+
+def moe_shuffle(ids, T, E, k, counts, offsets, perm, inv, ws, ws_bytes=None, stream=None) -> None:
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(lib().moe_shuffle(_ptr(ids), T, E, k, _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv), _ptr(ws), nb,
+                            _stream(stream)), "moe_shuffle")
+
+
+def moe_tile_map(counts, E, BM, tiles, num_tiles, max_tiles, ws, ws_bytes=None, stream=None) -> None:
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(lib().moe_tile_map(_ptr(counts), E, BM, _ptr(tiles), _ptr(num_tiles), max_tiles, _ptr(ws), nb,
+                             _stream(stream)), "moe_tile_map")
+
+
+def moe_select_path(p: moe_problem) -> int:
+    return int(lib().moe_select_path(ctypes.byref(p)))
+
+
+def moe_workspace_size(p: moe_problem) -> int:
+    return int(lib().moe_workspace_size(ctypes.byref(p)))
+
+
+def moe_forward(p: moe_problem, x, scores, w1, w2, w1_scale, w2_scale, y, ws, ws_bytes=None, stream=None) -> None:
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(lib().moe_forward(ctypes.byref(p), _ptr(x), _ptr(scores), _ptr(w1), _ptr(w2), _ptr(w1_scale),
+                            _ptr(w2_scale), _ptr(y), _ptr(ws), nb, _stream(stream)), "moe_forward")
+
+
+def moe_forward_views(p: moe_problem, ws, ws_bytes=None) -> moe_views:
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    v = moe_views()
+    _check(lib().moe_forward_views(ctypes.byref(p), _ptr(ws), nb, ctypes.byref(v)), "moe_forward_views")
+    return v
+
+
+def moe_read_device_status(ws, stream=None) -> int:
+    return int(lib().moe_read_device_status(_ptr(ws), _stream(stream)))
+
+
+def raw_status(fn_name: str, *args) -> int:
+    """Call an entry point with raw arguments and return its status code
+    (used by boundary tests that pass NULL or misaligned pointers)."""
+    return int(getattr(lib(), fn_name)(*args))

@@ -1,0 +1,418 @@
+// Grouped GEMMs of the grouped (prefill) path on the 5th-generation tensor
+// cores ("perf: add small-batch route MMA for MoE", Motivation: Gate/Up grouped
+// GEMM -> activation -> Down grouped GEMM; the "gather" step is fused into the
+// Gate/Up GEMM's TMA loads).
+//
+// One persistent CTA per SM walks work units (row tile, N tile) of a task map
+// built on the device (tile count read from device memory, no host sync).
+// Warp roles (256 threads):
+//   warp 0      TMA producer: A (activations) and B (weights) K-slices into a
+//               4-stage shared-memory ring, 128-byte swizzled.
+//   warp 1      one thread issues tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32)
+//               into one of two TMEM accumulators (2 x 256 columns).
+//   warp 2      allocates / frees the 512 TMEM columns.
+//   warps 4-7   epilogue: tcgen05.ld the accumulator (one row per thread),
+//               apply the fused epilogue, store to global memory.
+//
+// Gate/Up (MODE_GATEUP): A rows are gathered straight from x with TMA
+//   tile::gather4 (row = token of sorted route p = perm[p] / k), so the
+//   expert-sorted activation matrix is never materialised.  B = the expert's
+//   gate rows [n0, n0+128) and up rows [I+n0, I+n0+128) of W1, so one 128x256
+//   accumulator holds matching gate and up columns; the epilogue writes
+//   h = bf16(silu(g) * u) for sorted rows, columns [n0, n0+128).
+// Down (MODE_DOWN): A = h rows of the tile (contiguous, plain TMA tile loads),
+//   B = 256 rows of W2[e]; the epilogue writes bf16 o for sorted row p to
+//   route slot perm[p], so the combine reads each token's k rows contiguously.
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace gg {
+
+constexpr int BM = kGemmBM;  // 128
+constexpr int BK = 64;       // bf16 elements per stage row = 128 bytes
+constexpr int BN = 256;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 512;
+constexpr int THREADS = 256;
+constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
+constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+
+constexpr int MODE_GATEUP = 0;
+constexpr int MODE_DOWN = 1;
+
+struct Params {
+  const int32_t* tiles;
+  const int32_t* num_tiles;
+  int max_tiles;
+  const int32_t* perm;
+  int k;
+  int nN;                // N tiles per row tile
+  int K;                 // reduction length
+  int b_rows_per_expert; // rows of W per expert (2I or H)
+  int up_offset;         // I (Gate/Up)
+  int n_valid;           // valid output columns (I or H)
+  int out_ld;
+  __nv_bfloat16* out;
+  DeviceHeader* hdr;
+};
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
+  uint4 r;
+  uint32_t* w = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t*>(&b);
+  }
+  return r;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                             const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
+  const uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
+  const uint32_t mma_done = smem_u32(bars + 2 * STAGES + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 128);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int ntiles = min(*p.num_tiles, p.max_tiles);
+  const int total = ntiles * p.nN;
+  const int nk = (p.K + BK - 1) / BK;
+  const int4* tiles = reinterpret_cast<const int4*>(p.tiles);
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    uint32_t stage = 0, phase = 0;
+    int issued = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const int tile = u / p.nN, n = u - (u / p.nN) * p.nN;
+      const int4 tl = tiles[tile];
+      const int e = tl.x, row0 = tl.y, nrows = tl.z;
+      int tok[4] = {0, 0, 0, 0};
+      if (MODE == MODE_GATEUP) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int pr = row0 + min(lane * 4 + i, nrows - 1);
+          tok[i] = __ldg(p.perm + pr) / p.k;
+        }
+      }
+      const int brow = e * p.b_rows_per_expert + n * (MODE == MODE_GATEUP ? BN / 2 : BN);
+      for (int kb = 0; kb < nk; ++kb) {
+        int good = 1;
+        if (lane == 0) good = mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.hdr, 0x10000u | MODE);
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) {
+          ok = false;
+          break;
+        }
+        const uint32_t full = full0 + 8 * stage;
+        if (lane == 0) mbar_arrive_expect_tx(full, STAGE_BYTES);
+        __syncwarp();
+        const uint32_t a_dst = smem_u32(smem + stage * STAGE_BYTES);
+        const uint32_t b_dst = a_dst + A_BYTES;
+        const int kc = kb * BK;
+        if (MODE == MODE_GATEUP) {
+          tma_gather4(a_dst + lane * 4 * 128, &tmA, kc, tok[0], tok[1], tok[2], tok[3], full);
+          if (lane == 0) {
+            tma_load_2d(b_dst, &tmB, kc, brow, full);
+            tma_load_2d(b_dst + B_BYTES / 2, &tmB, kc, brow + p.up_offset, full);
+          }
+        } else {
+          if (lane == 0) {
+            tma_load_2d(a_dst, &tmA, kc, row0, full);
+            tma_load_2d(b_dst, &tmB, kc, brow, full);
+          }
+        }
+        ++issued;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      // aborted: let the copies already issued land before shared memory is released
+      for (int i = 0; i < min(issued, STAGES); ++i) {
+        stage = (stage + STAGES - 1) % STAGES;
+        if (stage == STAGES - 1) phase ^= 1;
+        mbar_wait_quiet(full0 + 8 * stage, phase, 50000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = make_idesc(1, 1, BM, BN);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, p.hdr, 0x20000u | MODE)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.hdr, 0x30000u | MODE)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_f16(d_tmem, sw128_kmajor_desc(a_addr + kk * 32), sw128_kmajor_desc(b_addr + kk * 32), idesc,
+                    (kb | kk) != 0);
+          mma_commit(empty0 + 8 * stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(tfull0 + 8 * acc);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      // every MMA issued by this thread has completed once mma_done fires
+      mma_commit(mma_done);
+      mbar_wait_quiet(mma_done, 0, 1000000000ull);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp - 4;  // TMEM lanes [32q, 32q+32)
+    const int row = q * 32 + lane;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const int tile = u / p.nN, n = u - (u / p.nN) * p.nN;
+      const int4 tl = tiles[tile];
+      const int row0 = tl.y, nrows = tl.z;
+      int good = 1;
+      if (lane == 0) good = mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, p.hdr, 0x40000u | MODE);
+      good = __shfl_sync(0xffffffffu, good, 0);
+      if (!good) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      if (MODE == MODE_GATEUP) {
+        __nv_bfloat16* out_row = p.out + static_cast<size_t>(row0 + row) * p.out_ld;
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 32) {
+          float g[32], up[32];
+          tmem_ld32(tbase + c, g);
+          tmem_ld32(tbase + BN / 2 + c, up);
+          tmem_ld_wait();
+          const int col = n * (BN / 2) + c;
+          if (row < nrows && col < p.n_valid) {
+            float hv[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) hv[i] = silu_mul(g[i], up[i]);
+            uint4* dst = reinterpret_cast<uint4*>(out_row + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = pack_bf16x8(hv + 8 * i);
+          }
+        }
+      } else {
+        const int slot = row < nrows ? __ldg(p.perm + row0 + row) : 0;
+        __nv_bfloat16* out_row = p.out + static_cast<size_t>(slot) * p.out_ld;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tmem_ld32(tbase + c, v);
+          tmem_ld_wait();
+          const int col = n * BN + c;
+          if (row < nrows && col < p.n_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(out_row + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = pack_bf16x8(v + 8 * i);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty0 + 8 * acc);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+static bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                      uint32_t box_outer) {
+  EncodeTiledFn fn = get_encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int MODE>
+static cudaError_t set_smem_attr() {
+  static cudaError_t st = cudaFuncSetAttribute(grouped_gemm_bf16_kernel<MODE>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+  return st;
+}
+
+}  // namespace gg
+
+cudaError_t launch_grouped_bf16(const GroupedArgs& a, cudaStream_t s) {
+  using namespace gg;
+  if (a.R <= 0) return cudaSuccess;
+  cudaError_t e0 = set_smem_attr<MODE_GATEUP>();
+  cudaError_t e1 = set_smem_attr<MODE_DOWN>();
+  if (e0 != cudaSuccess) return e0;
+  if (e1 != cudaSuccess) return e1;
+  const int sms = num_sms();
+  if (sms <= 0) return cudaErrorNoDevice;
+
+  CUtensorMap tmx, tmw1, tmh, tmw2;
+  if (!encode_2d(&tmx, a.x, a.H, a.T, BK, 1) ||
+      !encode_2d(&tmw1, a.w1, a.H, static_cast<uint64_t>(a.E) * 2 * a.I, BK, BN / 2) ||
+      !encode_2d(&tmh, a.h, a.I, a.R, BK, BM) ||
+      !encode_2d(&tmw2, a.w2, a.I, static_cast<uint64_t>(a.E) * a.H, BK, BN))
+    return cudaErrorInvalidValue;
+
+  Params p{};
+  p.tiles = a.tiles;
+  p.num_tiles = a.num_tiles;
+  p.max_tiles = a.max_tiles;
+  p.perm = a.perm;
+  p.k = a.k;
+  p.hdr = a.hdr;
+
+  // Gate/Up: N tiles of 128 h columns (gate 128 + up 128 accumulator columns)
+  p.nN = (a.I + BN / 2 - 1) / (BN / 2);
+  p.K = a.H;
+  p.b_rows_per_expert = 2 * a.I;
+  p.up_offset = a.I;
+  p.n_valid = a.I;
+  p.out_ld = a.I;
+  p.out = static_cast<__nv_bfloat16*>(a.h);
+  long long units = static_cast<long long>(a.max_tiles) * p.nN;
+  int grid = static_cast<int>(units < sms ? units : sms);
+  grouped_gemm_bf16_kernel<MODE_GATEUP><<<grid, THREADS, SMEM_BYTES, s>>>(tmx, tmw1, p);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+
+  // Down: N tiles of 256 output columns of H
+  p.nN = (a.H + BN - 1) / BN;
+  p.K = a.I;
+  p.b_rows_per_expert = a.H;
+  p.up_offset = 0;
+  p.n_valid = a.H;
+  p.out_ld = a.H;
+  p.out = static_cast<__nv_bfloat16*>(a.o);
+  units = static_cast<long long>(a.max_tiles) * p.nN;
+  grid = static_cast<int>(units < sms ? units : sms);
+  grouped_gemm_bf16_kernel<MODE_DOWN><<<grid, THREADS, SMEM_BYTES, s>>>(tmh, tmw2, p);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ combine
+// y[t, c] = bf16( sum_{j < k} w[t, j] * o[t*k + j, c] ), fp32, j ascending
+// (scatter/top-k reduction of the route-MMA page's Motivation; contiguous
+// route-order rows, as in its Code changes for reduce.cu).  Deterministic: no
+// atomics, fixed summation order.
+template <typename OT>
+__global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ o, const float* __restrict__ w, int T,
+                                                      int k, int H, __nv_bfloat16* __restrict__ y) {
+  const int cpt = H / 8;
+  const size_t total = static_cast<size_t>(T) * cpt;
+  for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(idx / cpt);
+    const int c = static_cast<int>(idx - static_cast<size_t>(t) * cpt) * 8;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      const size_t r = static_cast<size_t>(t) * k + j;
+      const float wj = __ldg(w + r);
+      float v[8];
+      if (sizeof(OT) == 2) {
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(o + r * H + c));
+        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(b[i]);
+          v[2 * i] = f.x;
+          v[2 * i + 1] = f.y;
+        }
+      } else {
+        const float4 f0 = __ldg(reinterpret_cast<const float4*>(o + r * H + c));
+        const float4 f1 = __ldg(reinterpret_cast<const float4*>(o + r * H + c) + 1);
+        v[0] = f0.x; v[1] = f0.y; v[2] = f0.z; v[3] = f0.w;
+        v[4] = f1.x; v[5] = f1.y; v[6] = f1.z; v[7] = f1.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
+    }
+    *reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * H + c) = gg::pack_bf16x8(acc);
+  }
+}
+
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
+  if (a.T <= 0) return cudaSuccess;
+  const size_t total = static_cast<size_t>(a.T) * (a.H / 8);
+  const int sms = num_sms();
+  size_t blocks = (total + 255) / 256;
+  const size_t cap = static_cast<size_t>(sms > 0 ? sms : 148) * 8;
+  if (blocks > cap) blocks = cap;
+  if (a.o_is_f32)
+    combine_kernel<float><<<static_cast<int>(blocks), 256, 0, s>>>(static_cast<const float*>(a.o), a.w, a.T, a.k,
+                                                                   a.H, static_cast<__nv_bfloat16*>(a.y));
+  else
+    combine_kernel<__nv_bfloat16><<<static_cast<int>(blocks), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(a.o), a.w, a.T, a.k, a.H, static_cast<__nv_bfloat16*>(a.y));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

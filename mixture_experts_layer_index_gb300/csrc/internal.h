@@ -1,0 +1,131 @@
+// Internal (non-ABI) declarations: workspace layout and kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+struct DeviceHeader;
+
+constexpr int kGemmBM = 128;          // rows (sorted routes) per grouped-GEMM tile
+constexpr int kRouteThreads = 256;    // threads of the route/rank kernel
+constexpr int kMaxRoutesPerBlock = 1024;
+constexpr int kMaxE = 512;
+constexpr int kMaxK = 32;
+constexpr int kRouteDirectMaxRoutes = 1024;
+
+// Tokens handled by one block of the route/rank kernel (its routes are that times k).
+inline int route_tokens_per_block(int k) { return k >= kMaxRoutesPerBlock ? 1 : kMaxRoutesPerBlock / k; }
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Byte offsets of the regions of a workspace (every region 256-byte aligned).
+struct ShuffleLayout {
+  size_t header = 0;
+  size_t lrank = 0;        // [R] int32: rank of a route among same-expert routes of its block
+  size_t blockcounts = 0;  // [nblk, E] int32 (then per-block base rows after the scan)
+  size_t tile_scratch = 0; // [E + 1] int32 (tile prefix of the scan kernel)
+  size_t total = 0;
+  int nblk = 0;
+};
+
+ShuffleLayout plan_shuffle(int T, int E, int k, size_t base);
+
+struct ForwardLayout {
+  moe_path path = MOE_PATH_AUTO;
+  size_t header = 0;
+  size_t ids = 0, w = 0;
+  ShuffleLayout shuf;
+  size_t counts = 0, offsets = 0, perm = 0, inv = 0;
+  size_t tiles = 0, num_tiles = 0;
+  int max_tiles = 0;
+  size_t h = 0;       // grouped: [R, I] bf16 (sorted order)
+  size_t o = 0;       // grouped: [R, H] bf16 (route order); route-direct: [R, H] fp32
+  // route-direct
+  size_t xq = 0;      // [T, H] e4m3
+  size_t sx = 0;      // [T, H/128] fp32 (blockwise) or [1] fp32 (per-tensor)
+  size_t uniq = 0;    // unique-expert table (see decode.cu)
+  size_t part = 0;    // [S, R, 2I] fp32 split-K partials of Gate/Up
+  size_t act = 0;     // per-tensor: [R, I] fp32 a;  blockwise: [R, I] e4m3 h
+  size_t sh = 0;      // blockwise: [R, I/128] fp32 scales of h
+  int splits = 1;
+  size_t total = 0;
+};
+
+bool plan_forward(const moe_problem& p, ForwardLayout* out);
+
+// ------------------------------------------------------------------ launchers
+// All return cudaSuccess or the launch error; none synchronises.
+cudaError_t launch_route_rank(const float* scores, const int32_t* ids_in, int T, int E, int k, int32_t* ids_out,
+                              float* w_out, int32_t* lrank, int32_t* blockcounts, DeviceHeader* hdr, bool route,
+                              bool rank, cudaStream_t s);
+cudaError_t launch_scan_tiles(int32_t* blockcounts, int nblk, int E, int32_t* counts, int32_t* offsets,
+                              int32_t* tiles, int32_t* num_tiles, int max_tiles, int BM, int32_t* tile_scratch,
+                              DeviceHeader* hdr, cudaStream_t s);
+cudaError_t launch_scatter(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E, int k,
+                           int32_t* perm, int32_t* inv, cudaStream_t s);
+cudaError_t launch_tile_map(const int32_t* counts, int E, int BM, int32_t* tiles, int32_t* num_tiles,
+                            int max_tiles, int32_t* tile_scratch, DeviceHeader* hdr, cudaStream_t s);
+cudaError_t launch_reset_header(DeviceHeader* hdr, cudaStream_t s);
+
+struct GroupedArgs {
+  int T, E, k, H, I, R;
+  const void* x;
+  const void* w1;
+  const void* w2;
+  const int32_t* perm;
+  const int32_t* tiles;
+  const int32_t* num_tiles;
+  int max_tiles;
+  void* h;
+  void* o;
+  DeviceHeader* hdr;
+};
+cudaError_t launch_grouped_bf16(const GroupedArgs& a, cudaStream_t s);
+
+struct CombineArgs {
+  int T, k, H;
+  const void* o;       // [R, H] route order
+  bool o_is_f32;
+  const float* w;      // [R]
+  void* y;             // [T, H] bf16
+};
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
+
+struct DecodeArgs {
+  int T, E, k, H, I, R;
+  moe_quant quant;
+  const void* x;
+  const float* scores;
+  const uint8_t* w1;
+  const uint8_t* w2;
+  const float* w1_scale;
+  const float* w2_scale;
+  int32_t* ids;
+  float* w;
+  uint8_t* xq;
+  float* sx;
+  int32_t* uniq;
+  float* part;
+  void* act;
+  float* sh;
+  float* o;
+  int splits;
+  DeviceHeader* hdr;
+};
+cudaError_t launch_route_direct(const DecodeArgs& a, cudaStream_t s);
+size_t route_direct_uniq_bytes(int T, int E, int k);
+
+// Driver entry point for cuTensorMapEncodeTiled (resolved once through the runtime).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn get_encode_tiled();
+int num_sms();
+
+}  // namespace moe

@@ -1,0 +1,357 @@
+// C ABI (include/moe.h): argument validation, workspace planning, path choice
+// and the ordered, sync-free launch sequence of each entry point.  Mirrors the
+// entry layer of "perf: add small-batch route MMA for MoE" (Code changes:
+// small-batch dispatch, split selection, contiguous workspace, input/output
+// shape and contiguity validation, preallocated output).
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ device queries
+EncodeTiledFn get_encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = v;
+  }
+  return cache[dev];
+}
+
+// ------------------------------------------------------------------ planning
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+ShuffleLayout plan_shuffle(int T, int E, int k, size_t base) {
+  ShuffleLayout L;
+  const size_t R = static_cast<size_t>(T) * k;
+  const int TB = route_tokens_per_block(k);
+  L.nblk = T > 0 ? (T + TB - 1) / TB : 0;
+  size_t off = base;
+  L.lrank = off;
+  off = align_up(off + R * 4, 256);
+  L.blockcounts = off;
+  off = align_up(off + static_cast<size_t>(L.nblk) * E * 4, 256);
+  L.tile_scratch = off;
+  off = align_up(off + static_cast<size_t>(E + 1) * 4, 256);
+  L.total = off;
+  return L;
+}
+
+static moe_path resolve_path(const moe_problem& p) {
+  if (p.path != MOE_PATH_AUTO) return p.path;
+  return p.quant == MOE_BF16 ? MOE_PATH_GROUPED : MOE_PATH_ROUTE_DIRECT;
+}
+
+// Number of K splits of the route-direct Gate/Up: enough CTAs to cover about
+// two waves of 148 SMs, each split a multiple of one 128-wide scale block and
+// at least 256 columns long.  Depends only on the shape, so the workspace size
+// is a pure function of the problem.
+static int route_direct_splits(const moe_problem& p) {
+  const int R = p.T * p.k;
+  const int maxU = R < p.E ? R : p.E;
+  const long long ctas = static_cast<long long>(maxU) * (2 * p.I / 64);
+  int s = 1;
+  while (ctas * s < 296 && (p.H / (2 * s)) % 128 == 0 && p.H / (2 * s) >= 256) s *= 2;
+  return s;
+}
+
+static moe_status validate_shape(const moe_problem& p) {
+  if (p.T < 0 || p.E < 1 || p.k < 1 || p.H < 1 || p.I < 1) return MOE_ERR_INVALID_ARG;
+  if (p.k > p.E) return MOE_ERR_INVALID_ARG;
+  if (p.quant != MOE_BF16 && p.quant != MOE_FP8_PER_TENSOR && p.quant != MOE_FP8_BLOCK128) return MOE_ERR_INVALID_ARG;
+  if (p.path != MOE_PATH_AUTO && p.path != MOE_PATH_GROUPED && p.path != MOE_PATH_ROUTE_DIRECT)
+    return MOE_ERR_INVALID_ARG;
+  if (p.E > kMaxE || p.k > kMaxK) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(p.T) * p.k >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(p.E) * 2 * p.I >= (1ll << 31) || static_cast<long long>(p.E) * p.H >= (1ll << 31))
+    return MOE_ERR_UNSUPPORTED;
+  if (p.quant == MOE_BF16) {
+    if (p.H % 64 || p.I % 64) return MOE_ERR_UNSUPPORTED;
+  } else if (p.quant == MOE_FP8_PER_TENSOR) {
+    if (p.H % 128 || p.I % 64) return MOE_ERR_UNSUPPORTED;
+  } else {
+    if (p.H % 128 || p.I % 128) return MOE_ERR_UNSUPPORTED;
+  }
+  const moe_path path = resolve_path(p);
+  if (path == MOE_PATH_GROUPED && p.quant != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (path == MOE_PATH_ROUTE_DIRECT) {
+    if (p.quant == MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (static_cast<long long>(p.T) * p.k > kRouteDirectMaxRoutes) return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+bool plan_forward(const moe_problem& p, ForwardLayout* out) {
+  if (validate_shape(p) != MOE_OK) return false;
+  ForwardLayout L;
+  L.path = resolve_path(p);
+  const size_t T = p.T, E = p.E, k = p.k, H = p.H, I = p.I, R = T * k;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  L.header = take(sizeof(DeviceHeader));
+  L.ids = take(R * 4);
+  L.w = take(R * 4);
+  if (L.path == MOE_PATH_GROUPED) {
+    L.shuf = plan_shuffle(p.T, p.E, p.k, off);
+    off = L.shuf.total;
+    L.counts = take(E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.perm = take(R * 4);
+    L.inv = take(R * 4);
+    L.max_tiles = static_cast<int>(R / kGemmBM + E);
+    L.tiles = take(static_cast<size_t>(L.max_tiles) * 16);
+    L.num_tiles = take(16);
+    L.h = take(R * I * 2);
+    L.o = take(R * H * 2);
+  } else {
+    L.splits = route_direct_splits(p);
+    L.xq = take(T * H);
+    L.sx = take(p.quant == MOE_FP8_BLOCK128 ? T * (H / 128) * 4 : 16);
+    L.uniq = take(route_direct_uniq_bytes(p.T, p.E, p.k));
+    L.part = take(static_cast<size_t>(L.splits) * R * 2 * I * 4);
+    L.act = take(R * I * 4);
+    L.sh = take(p.quant == MOE_FP8_BLOCK128 ? R * (I / 128) * 4 : 16);
+    L.o = take(R * H * 4);
+  }
+  L.total = off;
+  *out = L;
+  return true;
+}
+
+template <typename Ptr>
+static Ptr at(void* ws, size_t off) {
+  return reinterpret_cast<Ptr>(static_cast<uint8_t*>(ws) + off);
+}
+
+static moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported problem (outside this build's limits)";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device-side bounded wait timed out";
+    case MOE_ERR_DEVICE_BOUNDS: return "device-side index out of range";
+  }
+  return "unknown status";
+}
+
+moe_status moe_route(const float* scores, int T, int E, int k, int32_t* ids, float* w, moe_stream_t stream) {
+  if (T < 0 || E < 1 || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE || k > kMaxK || static_cast<long long>(T) * k >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!scores || !ids || !w || !aligned(scores, 4) || !aligned(ids, 4) || !aligned(w, 4)) return MOE_ERR_INVALID_ARG;
+  return from_cuda(launch_route_rank(scores, nullptr, T, E, k, ids, w, nullptr, nullptr, nullptr, true, false,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_shuffle_workspace_size(int T, int E, int k) {
+  if (T < 0 || E < 1 || k < 1 || E > kMaxE || k > kMaxK) return 0;
+  return plan_shuffle(T, E, k, align_up(sizeof(DeviceHeader), 256)).total;
+}
+
+moe_status moe_shuffle(const int32_t* ids, int T, int E, int k, int32_t* counts, int32_t* offsets, int32_t* perm,
+                       int32_t* inv, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (T < 0 || E < 1 || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE || k > kMaxK || static_cast<long long>(T) * k >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !offsets || !aligned(counts, 4) || !aligned(offsets, 4)) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!ids || !perm || !inv || !aligned(ids, 4) || !aligned(perm, 4) || !aligned(inv, 4)))
+    return MOE_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 16)) return MOE_ERR_WORKSPACE;
+  const ShuffleLayout L = plan_shuffle(T, E, k, align_up(sizeof(DeviceHeader), 256));
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DeviceHeader* hdr = at<DeviceHeader*>(ws, 0);
+  cudaError_t e = launch_reset_header(hdr, s);
+  if (e == cudaSuccess && T == 0) {
+    e = cudaMemsetAsync(counts, 0, static_cast<size_t>(E) * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(offsets, 0, static_cast<size_t>(E + 1) * 4, s);
+    return from_cuda(e);
+  }
+  int32_t* lrank = at<int32_t*>(ws, L.lrank);
+  int32_t* bc = at<int32_t*>(ws, L.blockcounts);
+  if (e == cudaSuccess)
+    e = launch_route_rank(nullptr, ids, T, E, k, nullptr, nullptr, lrank, bc, hdr, false, true, s);
+  if (e == cudaSuccess)
+    e = launch_scan_tiles(bc, L.nblk, E, counts, offsets, nullptr, nullptr, 0, kGemmBM, nullptr, hdr, s);
+  if (e == cudaSuccess) e = launch_scatter(ids, lrank, bc, T, E, k, perm, inv, s);
+  return from_cuda(e);
+}
+
+moe_status moe_tile_map(const int32_t* counts, int E, int BM, int32_t* tiles, int32_t* num_tiles, int max_tiles,
+                        void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (E < 1 || BM < 1 || BM > 1024 || max_tiles < 0) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !num_tiles || (max_tiles > 0 && !tiles) || !aligned(counts, 4) || !aligned(num_tiles, 4) ||
+      !aligned(tiles, 16))
+    return MOE_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 16)) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < moe_shuffle_workspace_size(0, E, 1)) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DeviceHeader* hdr = at<DeviceHeader*>(ws, 0);
+  cudaError_t e = launch_reset_header(hdr, s);
+  if (e == cudaSuccess) e = launch_tile_map(counts, E, BM, tiles, num_tiles, max_tiles, nullptr, hdr, s);
+  return from_cuda(e);
+}
+
+moe_path moe_select_path(const moe_problem* p) {
+  if (!p) return MOE_PATH_AUTO;
+  return resolve_path(*p);
+}
+
+size_t moe_workspace_size(const moe_problem* p) {
+  if (!p) return 0;
+  ForwardLayout L;
+  if (!plan_forward(*p, &L)) return 0;
+  return L.total;
+}
+
+moe_status moe_forward(const moe_problem* pp, const void* x, const float* scores, const void* w1, const void* w2,
+                       const float* w1_scale, const float* w2_scale, void* y, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
+  if (!pp) return MOE_ERR_INVALID_ARG;
+  const moe_problem p = *pp;
+  const moe_status vs = validate_shape(p);
+  if (vs != MOE_OK) return vs;
+  if (p.T == 0) return MOE_OK;
+  if (!x || !scores || !w1 || !w2 || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w1, 16) || !aligned(w2, 16) || !aligned(y, 16) || !aligned(scores, 4))
+    return MOE_ERR_INVALID_ARG;
+  if (p.quant == MOE_BF16) {
+    if (w1_scale || w2_scale) return MOE_ERR_INVALID_ARG;
+  } else {
+    if (!w1_scale || !w2_scale || !aligned(w1_scale, 4) || !aligned(w2_scale, 4)) return MOE_ERR_INVALID_ARG;
+  }
+  ForwardLayout L;
+  if (!plan_forward(p, &L)) return MOE_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DeviceHeader* hdr = at<DeviceHeader*>(ws, L.header);
+  int32_t* ids = at<int32_t*>(ws, L.ids);
+  float* w = at<float*>(ws, L.w);
+  cudaError_t e = cudaSuccess;
+  if (L.path == MOE_PATH_GROUPED) {
+    int32_t* lrank = at<int32_t*>(ws, L.shuf.lrank);
+    int32_t* bc = at<int32_t*>(ws, L.shuf.blockcounts);
+    int32_t* counts = at<int32_t*>(ws, L.counts);
+    int32_t* offsets = at<int32_t*>(ws, L.offsets);
+    int32_t* perm = at<int32_t*>(ws, L.perm);
+    int32_t* inv = at<int32_t*>(ws, L.inv);
+    int32_t* tiles = at<int32_t*>(ws, L.tiles);
+    int32_t* num_tiles = at<int32_t*>(ws, L.num_tiles);
+    e = launch_reset_header(hdr, s);
+    if (e == cudaSuccess)
+      e = launch_route_rank(scores, nullptr, p.T, p.E, p.k, ids, w, lrank, bc, hdr, true, true, s);
+    if (e == cudaSuccess)
+      e = launch_scan_tiles(bc, L.shuf.nblk, p.E, counts, offsets, tiles, num_tiles, L.max_tiles, kGemmBM, nullptr,
+                            hdr, s);
+    if (e == cudaSuccess) e = launch_scatter(ids, lrank, bc, p.T, p.E, p.k, perm, inv, s);
+    if (e == cudaSuccess) {
+      GroupedArgs g{};
+      g.T = p.T; g.E = p.E; g.k = p.k; g.H = p.H; g.I = p.I; g.R = p.T * p.k;
+      g.x = x; g.w1 = w1; g.w2 = w2;
+      g.perm = perm; g.tiles = tiles; g.num_tiles = num_tiles; g.max_tiles = L.max_tiles;
+      g.h = at<void*>(ws, L.h);
+      g.o = at<void*>(ws, L.o);
+      g.hdr = hdr;
+      e = launch_grouped_bf16(g, s);
+    }
+    if (e == cudaSuccess) {
+      CombineArgs c{p.T, p.k, p.H, at<void*>(ws, L.o), false, w, y};
+      e = launch_combine(c, s);
+    }
+  } else {
+    DecodeArgs d{};
+    d.T = p.T; d.E = p.E; d.k = p.k; d.H = p.H; d.I = p.I; d.R = p.T * p.k;
+    d.quant = p.quant;
+    d.x = x; d.scores = scores;
+    d.w1 = static_cast<const uint8_t*>(w1);
+    d.w2 = static_cast<const uint8_t*>(w2);
+    d.w1_scale = w1_scale; d.w2_scale = w2_scale;
+    d.ids = ids; d.w = w;
+    d.xq = at<uint8_t*>(ws, L.xq);
+    d.sx = at<float*>(ws, L.sx);
+    d.uniq = at<int32_t*>(ws, L.uniq);
+    d.part = at<float*>(ws, L.part);
+    d.act = at<void*>(ws, L.act);
+    d.sh = at<float*>(ws, L.sh);
+    d.o = at<float*>(ws, L.o);
+    d.splits = L.splits;
+    d.hdr = hdr;
+    e = launch_route_direct(d, s);
+    if (e == cudaSuccess) {
+      CombineArgs c{p.T, p.k, p.H, d.o, true, w, y};
+      e = launch_combine(c, s);
+    }
+  }
+  return from_cuda(e);
+}
+
+moe_status moe_forward_views(const moe_problem* p, const void* ws, size_t ws_bytes, moe_views* out) {
+  if (!p || !out) return MOE_ERR_INVALID_ARG;
+  const moe_status vs = validate_shape(*p);
+  if (vs != MOE_OK) return vs;
+  ForwardLayout L;
+  if (!plan_forward(*p, &L)) return MOE_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  void* base = const_cast<void*>(ws);
+  moe_views v{};
+  v.ids = at<const int32_t*>(base, L.ids);
+  v.w = at<const float*>(base, L.w);
+  if (L.path == MOE_PATH_GROUPED) {
+    v.counts = at<const int32_t*>(base, L.counts);
+    v.offsets = at<const int32_t*>(base, L.offsets);
+    v.perm = at<const int32_t*>(base, L.perm);
+    v.inv = at<const int32_t*>(base, L.inv);
+    v.tiles = at<const int32_t*>(base, L.tiles);
+    v.num_tiles = at<const int32_t*>(base, L.num_tiles);
+  }
+  *out = v;
+  return MOE_OK;
+}
+
+moe_status moe_read_device_status(const void* ws, moe_stream_t stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  unsigned int st = 0;
+  if (cudaMemcpy(&st, ws, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (st == 0) return MOE_OK;
+  if (st == kStatusTimeout) return MOE_ERR_DEVICE_TIMEOUT;
+  if (st == kStatusBounds) return MOE_ERR_DEVICE_BOUNDS;
+  return MOE_ERR_CUDA;
+}
+
+}  // extern "C"

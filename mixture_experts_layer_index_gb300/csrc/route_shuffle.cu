@@ -1,0 +1,269 @@
+// Top-k routing, index shuffling and the grouped-GEMM tile map.
+//
+// Routing: one warp per token (routing.cuh).
+//
+// Shuffle (index_shuffling of "Port necessary FBGEMM MoE kernels"; count/sort
+// -> prefix/task map of the route-MMA page's Motivation), in three launches
+// with no device-to-host copy:
+//   1. route_rank: per block of <= 1024 consecutive routes, the rank of each
+//      route among the block's earlier routes of the same expert (warp
+//      match_any + per-warp running histograms), and the block's per-expert
+//      counts.  Ranks follow route order, which makes the sort stable.
+//   2. scan_tiles (one block): counts = column sums of the block counts,
+//      offsets = their exclusive prefix, per-block base = offsets + the
+//      exclusive prefix over earlier blocks; then the tile map.
+//   3. scatter: perm[base + rank] = r, inv[r] = base + rank.
+#include "common.cuh"
+#include "internal.h"
+#include "routing.cuh"
+
+namespace moe {
+
+template <int MAXV, bool ROUTE, bool RANK>
+__global__ void __launch_bounds__(kRouteThreads) route_rank_kernel(
+    const float* __restrict__ scores, const int32_t* __restrict__ ids_in, int T, int E, int k, int TB,
+    int32_t* __restrict__ ids_out, float* __restrict__ w_out, int32_t* __restrict__ lrank,
+    int32_t* __restrict__ blockcounts, DeviceHeader* hdr) {
+  extern __shared__ int smem[];
+  int* s_ids = smem;                          // [1024]
+  int* s_lr = smem + kMaxRoutesPerBlock;      // [1024]
+  int* hist = smem + 2 * kMaxRoutesPerBlock;  // [8][E]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int blk = blockIdx.x;
+  const int t0 = blk * TB;
+  const int nt = min(TB, T - t0);
+  const int RB = TB * k;
+  const int nr = nt * k;
+  const size_t r0 = static_cast<size_t>(t0) * k;
+
+  if (ROUTE) {
+    for (int tb = warp; tb < nt; tb += kRouteThreads / 32) {
+      const size_t t = static_cast<size_t>(t0 + tb);
+      route_one_token<MAXV>(scores + t * E, E, k, ids_out + t * k, w_out + t * k, RANK ? s_ids + tb * k : nullptr);
+    }
+  } else {
+    for (int i = tid; i < nr; i += kRouteThreads) s_ids[i] = ids_in[r0 + i];
+  }
+  if (!RANK) return;
+  for (int i = tid; i < 8 * E; i += kRouteThreads) hist[i] = 0;
+  __syncthreads();
+
+  // each warp ranks a contiguous segment of the block's routes, 32 at a time, in order
+  const int seg = (RB + 8 * 32 - 1) / (8 * 32) * 32;
+  int* my_hist = hist + warp * E;
+  for (int c = 0; c < seg; c += 32) {
+    const int rl = warp * seg + c + lane;
+    const bool valid = rl < nr;
+    const int e = valid ? s_ids[rl] : -1;
+    const bool ok = valid && e >= 0 && e < E;
+    if (valid && !ok) record_status(hdr, kStatusBounds, static_cast<unsigned int>(r0 + rl));
+    const int keyv = ok ? e : -1 - lane;  // invalid lanes match only themselves
+    const unsigned peers = __match_any_sync(0xffffffffu, keyv);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int base = ok ? my_hist[e] : 0;
+    __syncwarp();
+    if (ok && rank == 0) my_hist[e] = base + __popc(peers);
+    __syncwarp();
+    if (valid) s_lr[rl] = ok ? base + rank : -1;
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kRouteThreads) {
+    int run = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const int c = hist[w * E + e];
+      hist[w * E + e] = run;
+      run += c;
+    }
+    blockcounts[static_cast<size_t>(blk) * E + e] = run;
+  }
+  __syncthreads();
+  for (int rl = tid; rl < nr; rl += kRouteThreads) {
+    int lr = s_lr[rl];
+    if (lr >= 0) lr += hist[(rl / seg) * E + s_ids[rl]];
+    lrank[r0 + rl] = lr;
+  }
+}
+
+// Exclusive prefix of s_cnt (E <= 512) by warp 0 into s_off, and of the tile
+// counts ceil(c/BM) into s_toff; entries [E] hold the totals.
+__device__ __forceinline__ void scan_counts_warp0(const int* s_cnt, int E, int BM, int* s_off, int* s_toff) {
+  if ((threadIdx.x >> 5) != 0) return;
+  const int lane = threadIdx.x & 31;
+  const int per = (E + 31) / 32;
+  int a = 0, b = 0;
+  for (int i = 0; i < per; ++i) {
+    const int e = lane * per + i;
+    if (e < E) {
+      a += s_cnt[e];
+      b += (s_cnt[e] + BM - 1) / BM;
+    }
+  }
+  int ia = a, ib = b;  // inclusive warp scan
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int xa = __shfl_up_sync(0xffffffffu, ia, o);
+    const int xb = __shfl_up_sync(0xffffffffu, ib, o);
+    if (lane >= o) {
+      ia += xa;
+      ib += xb;
+    }
+  }
+  int ra = ia - a, rb = ib - b;
+  for (int i = 0; i < per; ++i) {
+    const int e = lane * per + i;
+    if (e < E) {
+      s_off[e] = ra;
+      s_toff[e] = rb;
+      ra += s_cnt[e];
+      rb += (s_cnt[e] + BM - 1) / BM;
+    }
+  }
+  if (lane == 31) {
+    s_off[E] = ia;
+    s_toff[E] = ib;
+  }
+}
+
+__device__ __forceinline__ void emit_tiles(const int* s_cnt, const int* s_off, const int* s_toff, int E, int BM,
+                                           int32_t* tiles, int32_t* num_tiles, int max_tiles, DeviceHeader* hdr) {
+  for (int e = threadIdx.x >> 5; e < E; e += blockDim.x >> 5) {
+    const int c = s_cnt[e];
+    const int nt = (c + BM - 1) / BM;
+    for (int j = threadIdx.x & 31; j < nt; j += 32) {
+      const int idx = s_toff[e] + j;
+      if (idx < max_tiles) {
+        int4 t;
+        t.x = e;
+        t.y = s_off[e] + j * BM;
+        t.z = min(BM, c - j * BM);
+        t.w = 0;
+        reinterpret_cast<int4*>(tiles)[idx] = t;
+      }
+    }
+  }
+  if (threadIdx.x == 0) {
+    *num_tiles = s_toff[E];
+    if (s_toff[E] > max_tiles) record_status(hdr, kStatusBounds, 0x7100000u);
+  }
+}
+
+__global__ void __launch_bounds__(1024) scan_tiles_kernel(int32_t* __restrict__ bc, int nblk, int E,
+                                                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                          int32_t* __restrict__ tiles, int32_t* __restrict__ num_tiles,
+                                                          int max_tiles, int BM, DeviceHeader* hdr) {
+  __shared__ int s_cnt[kMaxE], s_off[kMaxE + 1], s_toff[kMaxE + 1];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int b = 0; b < nblk; ++b) {
+      const int c = bc[static_cast<size_t>(b) * E + e];
+      bc[static_cast<size_t>(b) * E + e] = run;
+      run += c;
+    }
+    s_cnt[e] = run;
+  }
+  __syncthreads();
+  scan_counts_warp0(s_cnt, E, BM, s_off, s_toff);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    counts[e] = s_cnt[e];
+    offsets[e] = s_off[e];
+  }
+  if (threadIdx.x == 0) offsets[E] = s_off[E];
+  const size_t n = static_cast<size_t>(nblk) * E;
+  for (size_t i = threadIdx.x; i < n; i += blockDim.x) bc[i] += s_off[i % E];
+  if (tiles) emit_tiles(s_cnt, s_off, s_toff, E, BM, tiles, num_tiles, max_tiles, hdr);
+}
+
+__global__ void __launch_bounds__(1024) tile_map_kernel(const int32_t* __restrict__ counts, int E, int BM,
+                                                        int32_t* __restrict__ tiles, int32_t* __restrict__ num_tiles,
+                                                        int max_tiles, DeviceHeader* hdr) {
+  __shared__ int s_cnt[kMaxE], s_off[kMaxE + 1], s_toff[kMaxE + 1];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int c = counts[e];
+    if (c < 0) record_status(hdr, kStatusBounds, 0x7200000u | e);
+    s_cnt[e] = c < 0 ? 0 : c;
+  }
+  __syncthreads();
+  scan_counts_warp0(s_cnt, E, BM, s_off, s_toff);
+  __syncthreads();
+  emit_tiles(s_cnt, s_off, s_toff, E, BM, tiles, num_tiles, max_tiles, hdr);
+}
+
+__global__ void scatter_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ lrank,
+                               const int32_t* __restrict__ blockbase, int R, int E, int RB,
+                               int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= R) return;
+  const int lr = lrank[r];
+  if (lr < 0) {
+    inv[r] = -1;
+    return;
+  }
+  const int e = ids[r];
+  const int p = blockbase[static_cast<size_t>(r / RB) * E + e] + lr;
+  perm[p] = r;
+  inv[r] = p;
+}
+
+// ------------------------------------------------------------------ launchers
+template <bool ROUTE, bool RANK>
+static cudaError_t launch_rr(int maxv, dim3 grid, size_t smem, cudaStream_t s, const float* scores,
+                             const int32_t* ids_in, int T, int E, int k, int TB, int32_t* ids_out, float* w_out,
+                             int32_t* lrank, int32_t* bc, DeviceHeader* hdr) {
+#define MOE_RR(V)                                                                                         \
+  route_rank_kernel<V, ROUTE, RANK><<<grid, kRouteThreads, smem, s>>>(scores, ids_in, T, E, k, TB, ids_out, \
+                                                                     w_out, lrank, bc, hdr)
+  switch (maxv) {
+    case 1: MOE_RR(1); break;
+    case 2: MOE_RR(2); break;
+    case 4: MOE_RR(4); break;
+    case 8: MOE_RR(8); break;
+    default: MOE_RR(16); break;
+  }
+#undef MOE_RR
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_rank(const float* scores, const int32_t* ids_in, int T, int E, int k, int32_t* ids_out,
+                              float* w_out, int32_t* lrank, int32_t* blockcounts, DeviceHeader* hdr, bool route,
+                              bool rank, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  const int TB = route_tokens_per_block(k);
+  const int nblk = (T + TB - 1) / TB;
+  const size_t smem = (2 * kMaxRoutesPerBlock + 8 * E) * sizeof(int);
+  int maxv = 1;
+  while (maxv * 32 < E) maxv *= 2;
+  const dim3 grid(nblk);
+  if (route && rank) return launch_rr<true, true>(maxv, grid, smem, s, scores, ids_in, T, E, k, TB, ids_out, w_out, lrank, blockcounts, hdr);
+  if (route) return launch_rr<true, false>(maxv, grid, smem, s, scores, ids_in, T, E, k, TB, ids_out, w_out, lrank, blockcounts, hdr);
+  return launch_rr<false, true>(maxv, grid, smem, s, scores, ids_in, T, E, k, TB, ids_out, w_out, lrank, blockcounts, hdr);
+}
+
+cudaError_t launch_scan_tiles(int32_t* blockcounts, int nblk, int E, int32_t* counts, int32_t* offsets,
+                              int32_t* tiles, int32_t* num_tiles, int max_tiles, int BM, int32_t* /*tile_scratch*/,
+                              DeviceHeader* hdr, cudaStream_t s) {
+  scan_tiles_kernel<<<1, 1024, 0, s>>>(blockcounts, nblk, E, counts, offsets, tiles, num_tiles, max_tiles, BM, hdr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E, int k,
+                           int32_t* perm, int32_t* inv, cudaStream_t s) {
+  const int R = T * k;
+  if (R <= 0) return cudaSuccess;
+  const int RB = route_tokens_per_block(k) * k;
+  scatter_kernel<<<(R + 255) / 256, 256, 0, s>>>(ids, lrank, blockbase, R, E, RB, perm, inv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tile_map(const int32_t* counts, int E, int BM, int32_t* tiles, int32_t* num_tiles, int max_tiles,
+                            int32_t* /*tile_scratch*/, DeviceHeader* hdr, cudaStream_t s) {
+  tile_map_kernel<<<1, 1024, 0, s>>>(counts, E, BM, tiles, num_tiles, max_tiles, hdr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reset_header(DeviceHeader* hdr, cudaStream_t s) {
+  return cudaMemsetAsync(hdr, 0, sizeof(DeviceHeader), s);
+}
+
+}  // namespace moe
