@@ -1,0 +1,508 @@
+#!/usr/bin/env python3
+"""Benchmark of the routed MoE FFN forward on GB300.
+
+Default (``--impl ours``): one step = one moe_forward (route -> shuffle -> tile
+map -> Gate/Up grouped GEMM with fused gather + SwiGLU -> Down grouped GEMM ->
+combine) over the skewed prefill workload T=16384, E=128, top-8, H=2048,
+I=768, bf16, Zipf(1.1) routing, on every rank (independent replicas, weak
+scaling).  The JSON line also carries:
+  roofline      the Gate/Up grouped GEMM (the dominant kernel) timed live with
+                CUDA events on the launching stream over the timed region;
+  e2e           the same metric through the C ABI with host buffers, the
+                host->device copy of x and the scores and the device->host read
+                of y inside the timed region;
+  decode        the route-direct FP8 decode sweeps (per-tensor E=192 H=4096
+                I=192; blockwise E=128 H=2048 I=768 and H=4096 I=512; B=1..8),
+                us/call from CUDA-graph replays with L2 flushed between replays
+                (outside the timed events), and the HBM roofline fraction;
+  cpu_baseline  the CPU oracle timed on this host on a bounded token sample.
+
+``--impl reference`` times the CPU oracle (the reference of this library) on
+the same workload and metric, each step a bounded token sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE fwd µs/call (B=1–8) & tokens/s (T=16K); % of HBM / tensor-core roofline"
+UNIT = "tokens/s"
+PREFILL = "prefill"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Route-MMA latencies on H20 from "perf: add small-batch route MMA for MoE" (Performance
+# tables), B = 1..8: context only (other hardware).
+H20_ROUTE_MMA_US = {
+    "hunyuan": [13.243, 16.833, 22.773, 30.663, 35.983, 41.554, 47.259, 54.124],
+    "qwen3a": [17.349, 29.863, 40.708, 52.732, 62.510, 73.040, 84.419, 94.352],
+    "qwen3b": [19.779, 37.585, 52.295, 63.833, 85.218, 98.465, 111.362, 121.922],
+}
+
+
+# ----------------------------------------------------------------------------- helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each replica draws its own batch: the seed of rank r is base + 7919 r."""
+    return base + 7919 * rank
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max of a float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput(tokens_per_rank: int, world: int, steps: int, max_ms: float) -> float:
+    """Whole-job tokens/s: every rank processes tokens_per_rank per step."""
+    return tokens_per_rank * world * steps / (max_ms / 1000.0)
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+GEMM_SOURCES = ["mixture_experts_layer_index_gb300/csrc/grouped_gemm.cu",
+                "mixture_experts_layer_index_gb300/csrc/common.cuh"]
+
+
+def committed_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when the summary is missing or the kernel's source changed since it was taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+        ent = d[kernel]
+    except (OSError, ValueError, KeyError):
+        return None
+    if ent.get("source_digest") != source_digest(GEMM_SOURCES):
+        return None
+    return ent.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.25)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                pw.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {
+            "sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "power_w_max": max(pw) if pw else None,
+            "reasons": sorted(reasons),
+            "samples": len(sm),
+        }
+
+
+def gpu_id_for_smi(torch, dev_index: int) -> str:
+    try:
+        u = torch.cuda.get_device_properties(dev_index).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis and vis.split(",")[dev_index].strip().isdigit():
+            return vis.split(",")[dev_index].strip()
+        return str(dev_index)
+
+
+# ----------------------------------------------------------------------------- CPU oracle legs
+def oracle_tokens_per_s(inp, wl, n_tokens: int, seed: int = 0):
+    """Times the CPU oracle (as it stands) on n_tokens sampled tokens; -> (tokens/s, seconds)."""
+    import numpy as np
+    import torch
+
+    from oracle import moe as O
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    x, w1, w2 = bits(inp["x"]), bits(inp["w1"]), bits(inp["w2"])
+    scores = inp["scores"].numpy()
+    rng = np.random.default_rng(seed)
+    tokens = np.sort(rng.choice(wl.T, size=min(n_tokens, wl.T), replace=False))
+    t0 = time.perf_counter()
+    O.forward(x, scores, w1, w2, None, None, wl.k, wl.quant, tokens=tokens)
+    dt = time.perf_counter() - t0
+    return len(tokens) / dt, dt
+
+
+def cpu_baseline(inp, wl, budget_s: float = 15.0):
+    _, t_small = oracle_tokens_per_s(inp, wl, 64, seed=1)
+    per_tok = max(t_small / 64.0, 1e-6)
+    n = int(min(wl.T, max(64, budget_s / per_tok)))
+    v, dt = oracle_tokens_per_s(inp, wl, n, seed=2)
+    return {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} of the {wl.T} tokens (all {wl.k} routes each, full routing/shuffle of the batch), "
+                      f"numpy fp64 oracle, {dt:.1f} s",
+            "seconds": dt}
+
+
+# ----------------------------------------------------------------------------- ours
+def workload_config(wl, l2_note):
+    return {"workload": f"{wl.name}: T={wl.T} E={wl.E} top_k={wl.k} H={wl.H} I={wl.I} bf16, "
+                        "Zipf(1.1)-skewed routing with 4 empty experts",
+            "T": wl.T, "E": wl.E, "top_k": wl.k, "H": wl.H, "I": wl.I, "quant": wl.quant,
+            "path": "grouped", "l2": l2_note}
+
+
+def run_decode_sweep(m, torch, dev, peaks, reps: int):
+    import workloads as W
+
+    out = {}
+    flush = torch.empty(int(2.5 * 129e6) // 4, dtype=torch.float32, device=dev)
+    for name in W.DECODE_SWEEPS:
+        base = W.workload(name, 1)
+        w1, w2, s1, s2 = W.make_weights(base, device=dev)
+        per_b = []
+        for B in range(1, 9):
+            wl = W.workload(name, B)
+            x = W.make_x(wl).to(dev)
+            sc = W.make_scores(wl).to(dev)
+            p = m.problem(wl.T, wl.E, wl.k, wl.H, wl.I, wl.quant)
+            ws = torch.empty(m.moe_workspace_size(p), dtype=torch.uint8, device=dev)
+            y = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
+            s = torch.cuda.Stream()
+            m.moe_forward(p, x, sc, w1, w2, s1, s2, y, ws, stream=s)  # eager warm-up
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                m.moe_forward(p, x, sc, w1, w2, s1, s2, y, ws, stream=s)
+            times = []
+            with torch.cuda.stream(s):
+                for i in range(reps + 3):
+                    flush.fill_(float(i))
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(s)
+                    g.replay()
+                    b.record(s)
+                    b.synchronize()
+                    if i >= 3:
+                        times.append(a.elapsed_time(b) * 1000.0)
+            assert m.moe_read_device_status(ws) == m.MOE_OK
+            v = m.moe_forward_views(p, ws)
+            off = v.ids - ws.data_ptr()
+            ids = ws[off:off + wl.T * wl.k * 4].view(torch.int32)
+            U = int(torch.unique(ids).numel())
+            w1e = 2 * wl.I * wl.H + (0 if s1 is None else s1[0].numel() * 4)
+            w2e = wl.H * wl.I + (0 if s2 is None else s2[0].numel() * 4)
+            algo = U * (w1e + w2e) + wl.T * wl.H * 2 * 2 + wl.T * wl.E * 4
+            us = statistics.median(times)
+            per_b.append({"B": B, "us": round(us, 3), "p10_us": round(sorted(times)[len(times) // 10], 3),
+                          "p90_us": round(sorted(times)[(9 * len(times)) // 10], 3),
+                          "distinct_experts": U, "algo_bytes": algo,
+                          "hbm_gbs": round(algo / (us * 1e-6) / 1e9, 1),
+                          "hbm_frac": round(algo / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                          "h20_route_mma_us": H20_ROUTE_MMA_US[name][B - 1],
+                          "tokens_per_s": round(B / (us * 1e-6), 1)})
+            del g
+        out[name] = {"E": base.E, "H": base.H, "I": base.I, "top_k": base.k, "quant": base.quant,
+                     "path": "route_direct", "by_batch": per_b}
+        del w1, w2, s1, s2
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import mixture_experts_layer_index_gb300 as m
+    import workloads as W
+
+    peaks, peak_src = load_peaks()
+    base = W.workload(PREFILL)
+    import dataclasses
+
+    wl = dataclasses.replace(base, seed=rank_seed(base.seed, rank))
+    if args.tokens:
+        wl = dataclasses.replace(wl, T=args.tokens, name=f"{wl.name}_T{args.tokens}")
+    inp = W.make_inputs(wl)
+    d = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+    p = m.problem(wl.T, wl.E, wl.k, wl.H, wl.I, wl.quant)
+    ws = torch.empty(m.moe_workspace_size(p), dtype=torch.uint8, device=dev)
+    y = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        m.moe_forward(p, d["x"], d["scores"], d["w1"], d["w2"], None, None, y, ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if m.moe_read_device_status(ws) != m.MOE_OK:
+        raise RuntimeError("device status not OK after warm-up")
+
+    sampler = ClockSampler(gpu_id_for_smi(torch, local))
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    m.moe_profile_start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall = time.perf_counter()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    wall_s = time.perf_counter() - t_wall
+    stages = m.moe_profile_stop()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    max_ms = reduce_max(ms, world)
+    value = throughput(wl.T, world, args.steps, max_ms)
+
+    # dominant kernel: the Gate/Up grouped GEMM, 2 * R * H * 2I algorithmic FLOPs per launch
+    R = wl.T * wl.k
+    gu_ms, gu_n = stages.get("gateup_gemm", (float("nan"), 0))
+    dn_ms, dn_n = stages.get("down_gemm", (float("nan"), 0))
+    gu_flops = 4.0 * R * wl.H * wl.I
+    dn_flops = 2.0 * R * wl.H * wl.I
+    gu_avg_s = gu_ms / max(gu_n, 1) / 1000.0
+    achieved = gu_flops / gu_avg_s / 1e12
+    peak = peaks["bf16_tflops_sustained"]
+    launches = sum(n for name, (_, n) in stages.items() if name != "header_reset")
+
+    # e2e: host buffers, copies inside the timed region
+    xh = inp["x"].pin_memory()
+    sh = inp["scores"].pin_memory()
+    yh = torch.empty(wl.T, wl.H, dtype=torch.bfloat16).pin_memory()
+    for _ in range(2):
+        d["x"].copy_(xh, non_blocking=True)
+        d["scores"].copy_(sh, non_blocking=True)
+        step()
+        yh.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        d["x"].copy_(xh, non_blocking=True)
+        d["scores"].copy_(sh, non_blocking=True)
+        step()
+        yh.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1), world)
+    e2e = {"value": throughput(wl.T, world, args.steps, e2e_ms), "unit": UNIT,
+           "h2d_bytes_per_step": xh.numel() * 2 + sh.numel() * 4, "d2h_bytes_per_step": yh.numel() * 2}
+
+    decode = None
+    if not args.no_decode and rank == 0:
+        decode = run_decode_sweep(m, torch, dev, peaks, args.decode_reps)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp, wl, args.cpu_budget)
+
+    if rank != 0:
+        return
+    per_step_ms = max_ms / args.steps
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(per_step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; random-init weights, N(0,1/fan_in))",
+        "config": workload_config(wl, "inputs larger than L2: 1.2 GB of expert weights + 67 MB of x per step"),
+        "roofline": {
+            "kernel": "gateup_gemm (tcgen05 Gate/Up grouped GEMM, fused TMA gather + SwiGLU)",
+            "bound": "tensor",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_source": f"{peak_src} bf16_tflops_sustained (burst {peaks['bf16_tflops']})",
+            "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": committed_traffic("gateup_gemm"),
+            "algorithmic_flops_per_launch": gu_flops,
+            "avg_launch_ms": round(gu_avg_s * 1000.0, 5),
+        },
+        "kernels": {name: {"total_ms": round(t, 3), "launches": n, "avg_us": round(1000.0 * t / max(n, 1), 2),
+                           "share": round(t / max(sum(v[0] for v in stages.values()), 1e-9), 4)}
+                    for name, (t, n) in stages.items()},
+        "down_gemm_tflops": round(dn_flops / (dn_ms / max(dn_n, 1) / 1000.0) / 1e12, 1) if dn_n else None,
+        "whole_step_tflops": round(6.0 * R * wl.H * wl.I / (per_step_ms / 1000.0) / 1e12, 1),
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "wall_s_timed": round(wall_s, 3),
+        "decode": decode,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+
+
+# ----------------------------------------------------------------------------- reference (oracle) arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import workloads as W
+
+    wl = W.workload(PREFILL)
+    inp = W.make_inputs(wl)
+    # calibrate a per-step token sample so that warm-up + steps take about two minutes
+    _, t64 = oracle_tokens_per_s(inp, wl, 64, seed=0)
+    per_step_s = 120.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(wl.T, 64 * per_step_s / max(t64, 1e-6))))
+    for i in range(args.warmup):
+        oracle_tokens_per_s(inp, wl, n, seed=100 + i)
+    total_s = 0.0
+    for i in range(args.steps):
+        _, dt = oracle_tokens_per_s(inp, wl, n, seed=1000 + i)
+        total_s += dt
+    value = n * args.steps / total_s
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1000.0 * total_s / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded; random-init weights, N(0,1/fan_in))",
+        "config": workload_config(wl, "CPU run"),
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"{n} sampled tokens of the T={wl.T} batch per step (all routes each, "
+                                   "full routing/shuffle), numpy fp64 oracle"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-decode", action="store_true", help="skip the route-direct decode sweep")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-reps", type=int, default=40)
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override T of the prefill workload (smaller cases for profiling; not a bench line)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

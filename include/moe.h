@@ -191,6 +191,28 @@ moe_status moe_forward_views(const moe_problem* p, const void* ws, size_t ws_byt
  * word at its start. */
 moe_status moe_read_device_status(const void* ws, moe_stream_t stream);
 
+/* ---------------------------------------------------------------- stage timing
+ * While profiling is on, each kernel launch of the entry points above is
+ * bracketed by a pair of CUDA events recorded on the caller's stream (host-side
+ * records only: nothing is synchronised or allocated on the device, and
+ * launches on a stream that is being captured into a graph are not timed).
+ *
+ * moe_profile_start - clears earlier records and turns profiling on.
+ * moe_profile_stop  - waits for the recorded events, writes one entry per
+ *   kernel stage (in order of first launch) to out[0 .. max_stages-1], turns
+ *   profiling off and returns the number of stages, or -1 if waiting on an
+ *   event failed.  total_ms sums the stage's launches; launches counts them.
+ * Stage names: route_rank, scan_tiles, scatter, gateup_gemm, down_gemm,
+ * combine (grouped path); rd_prep, rd_gateup, rd_reduce, rd_down, combine
+ * (route-direct path); tile_map, header_reset. */
+typedef struct {
+  char name[32];
+  double total_ms;
+  int launches;
+} moe_stage_time;
+int moe_profile_start(void);
+int moe_profile_stop(moe_stage_time* out, int max_stages);
+
 /* moe_status_string - static, NUL-terminated description of a status code. */
 const char* moe_status_string(moe_status status);
 

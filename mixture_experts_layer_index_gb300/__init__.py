@@ -49,6 +49,10 @@ class moe_views(ctypes.Structure):
                 ("ids", "w", "counts", "offsets", "perm", "inv", "tiles", "num_tiles")]
 
 
+class moe_stage_time(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("total_ms", ctypes.c_double), ("launches", ctypes.c_int)]
+
+
 _vp, _sz, _i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
 _P = ctypes.POINTER(moe_problem)
 _SIGS = {
@@ -61,6 +65,8 @@ _SIGS = {
     "moe_forward": (_i, [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_forward_views": (_i, [_P, _vp, _sz, ctypes.POINTER(moe_views)]),
     "moe_read_device_status": (_i, [_vp, _vp]),
+    "moe_profile_start": (_i, []),
+    "moe_profile_stop": (_i, [ctypes.POINTER(moe_stage_time), _i]),
     "moe_status_string": (ctypes.c_char_p, [_i]),
 }
 _lib = None
@@ -173,6 +179,19 @@ def moe_forward_views(p: moe_problem, ws, ws_bytes=None) -> moe_views:
 
 def moe_read_device_status(ws, stream=None) -> int:
     return int(lib().moe_read_device_status(_ptr(ws), _stream(stream)))
+
+
+def moe_profile_start() -> None:
+    lib().moe_profile_start()
+
+
+def moe_profile_stop(max_stages: int = 32) -> dict:
+    """Stops stage timing; returns {stage name: (total_ms, launches)} in launch order."""
+    arr = (moe_stage_time * max_stages)()
+    n = int(lib().moe_profile_stop(arr, max_stages))
+    if n < 0:
+        raise MoeError(MOE_ERR_CUDA, "moe_profile_stop")
+    return {arr[i].name.decode(): (float(arr[i].total_ms), int(arr[i].launches)) for i in range(min(n, max_stages))}
 
 
 def raw_status(fn_name: str, *args) -> int:

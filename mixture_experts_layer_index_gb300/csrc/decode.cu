@@ -431,6 +431,7 @@ cudaError_t launch_route_direct(const DecodeArgs& a, cudaStream_t s) {
   if (a.T <= 0) return cudaSuccess;
   int maxv = 1;
   while (maxv * 32 < a.E) maxv *= 2;
+  stage_begin("rd_prep", s);
   switch (maxv) {
     case 1: rd_prep_kernel<1><<<1, 1024, 0, s>>>(a); break;
     case 2: rd_prep_kernel<2><<<1, 1024, 0, s>>>(a); break;
@@ -439,33 +440,43 @@ cudaError_t launch_route_direct(const DecodeArgs& a, cudaStream_t s) {
     default: rd_prep_kernel<16><<<1, 1024, 0, s>>>(a); break;
   }
   cudaError_t err = cudaGetLastError();
+  stage_end(s);
   if (err != cudaSuccess) return err;
 
   const int maxU = max_uniq(a.R, a.E);
   const bool bw = a.quant == MOE_FP8_BLOCK128;
   const int nMB = 2 * a.I / ROWS_PER_CTA;
   const int g1 = maxU * nMB * a.splits;
+  stage_begin("rd_gateup", s);
   if (bw)
     rd_gateup_kernel<true><<<g1, THREADS, 0, s>>>(a, nMB, a.splits);
   else
     rd_gateup_kernel<false><<<g1, THREADS, 0, s>>>(a, nMB, a.splits);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  err = cudaGetLastError();
+  stage_end(s);
+  if (err != cudaSuccess) return err;
 
+  stage_begin("rd_reduce", s);
   if (bw) {
     const int warps = a.R * (a.I / 128);
     rd_reduce_block_kernel<<<(warps * 32 + 255) / 256, 256, 0, s>>>(a);
   } else {
     rd_reduce_tensor_kernel<<<(a.R * a.I + 255) / 256, 256, 0, s>>>(a);
   }
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  err = cudaGetLastError();
+  stage_end(s);
+  if (err != cudaSuccess) return err;
 
   const int nHB = a.H / ROWS_PER_CTA;
   const size_t smem = static_cast<size_t>(8) * a.I + 8 * (a.I / 128 + 1) * sizeof(float) + 16;
+  stage_begin("rd_down", s);
   if (bw)
     rd_down_kernel<true><<<maxU * nHB, THREADS, smem, s>>>(a, nHB);
   else
     rd_down_kernel<false><<<maxU * nHB, THREADS, smem, s>>>(a, nHB);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  err = cudaGetLastError();
+  stage_end(s);
+  if (err != cudaSuccess) return err;
 
   return cudaSuccess;
 }

@@ -303,23 +303,18 @@ static cudaError_t set_smem_attr() {
 
 }  // namespace gg
 
-cudaError_t launch_grouped_bf16(const GroupedArgs& a, cudaStream_t s) {
-  using namespace gg;
-  if (a.R <= 0) return cudaSuccess;
+namespace gg {
+
+static cudaError_t prepare(const GroupedArgs& a, int* sms) {
   cudaError_t e0 = set_smem_attr<MODE_GATEUP>();
-  cudaError_t e1 = set_smem_attr<MODE_DOWN>();
   if (e0 != cudaSuccess) return e0;
+  cudaError_t e1 = set_smem_attr<MODE_DOWN>();
   if (e1 != cudaSuccess) return e1;
-  const int sms = num_sms();
-  if (sms <= 0) return cudaErrorNoDevice;
+  *sms = num_sms();
+  return *sms > 0 ? cudaSuccess : cudaErrorNoDevice;
+}
 
-  CUtensorMap tmx, tmw1, tmh, tmw2;
-  if (!encode_2d(&tmx, a.x, a.H, a.T, BK, 1) ||
-      !encode_2d(&tmw1, a.w1, a.H, static_cast<uint64_t>(a.E) * 2 * a.I, BK, BN / 2) ||
-      !encode_2d(&tmh, a.h, a.I, a.R, BK, BM) ||
-      !encode_2d(&tmw2, a.w2, a.I, static_cast<uint64_t>(a.E) * a.H, BK, BN))
-    return cudaErrorInvalidValue;
-
+static Params base_params(const GroupedArgs& a) {
   Params p{};
   p.tiles = a.tiles;
   p.num_tiles = a.num_tiles;
@@ -327,8 +322,23 @@ cudaError_t launch_grouped_bf16(const GroupedArgs& a, cudaStream_t s) {
   p.perm = a.perm;
   p.k = a.k;
   p.hdr = a.hdr;
+  return p;
+}
 
-  // Gate/Up: N tiles of 128 h columns (gate 128 + up 128 accumulator columns)
+}  // namespace gg
+
+// Gate/Up: N tiles of 128 h columns (gate 128 + up 128 accumulator columns).
+cudaError_t launch_gateup_bf16(const GroupedArgs& a, cudaStream_t s) {
+  using namespace gg;
+  if (a.R <= 0) return cudaSuccess;
+  int sms = 0;
+  cudaError_t err = prepare(a, &sms);
+  if (err != cudaSuccess) return err;
+  CUtensorMap tmx, tmw1;
+  if (!encode_2d(&tmx, a.x, a.H, a.T, BK, 1) ||
+      !encode_2d(&tmw1, a.w1, a.H, static_cast<uint64_t>(a.E) * 2 * a.I, BK, BN / 2))
+    return cudaErrorInvalidValue;
+  Params p = base_params(a);
   p.nN = (a.I + BN / 2 - 1) / (BN / 2);
   p.K = a.H;
   p.b_rows_per_expert = 2 * a.I;
@@ -336,13 +346,27 @@ cudaError_t launch_grouped_bf16(const GroupedArgs& a, cudaStream_t s) {
   p.n_valid = a.I;
   p.out_ld = a.I;
   p.out = static_cast<__nv_bfloat16*>(a.h);
-  long long units = static_cast<long long>(a.max_tiles) * p.nN;
-  int grid = static_cast<int>(units < sms ? units : sms);
+  const long long units = static_cast<long long>(a.max_tiles) * p.nN;
+  const int grid = static_cast<int>(units < sms ? units : sms);
+  stage_begin("gateup_gemm", s);
   grouped_gemm_bf16_kernel<MODE_GATEUP><<<grid, THREADS, SMEM_BYTES, s>>>(tmx, tmw1, p);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
+  err = cudaGetLastError();
+  stage_end(s);
+  return err;
+}
 
-  // Down: N tiles of 256 output columns of H
+// Down: N tiles of 256 output columns of H.
+cudaError_t launch_down_bf16(const GroupedArgs& a, cudaStream_t s) {
+  using namespace gg;
+  if (a.R <= 0) return cudaSuccess;
+  int sms = 0;
+  cudaError_t err = prepare(a, &sms);
+  if (err != cudaSuccess) return err;
+  CUtensorMap tmh, tmw2;
+  if (!encode_2d(&tmh, a.h, a.I, a.R, BK, BM) ||
+      !encode_2d(&tmw2, a.w2, a.I, static_cast<uint64_t>(a.E) * a.H, BK, BN))
+    return cudaErrorInvalidValue;
+  Params p = base_params(a);
   p.nN = (a.H + BN - 1) / BN;
   p.K = a.I;
   p.b_rows_per_expert = a.H;
@@ -350,10 +374,13 @@ cudaError_t launch_grouped_bf16(const GroupedArgs& a, cudaStream_t s) {
   p.n_valid = a.H;
   p.out_ld = a.H;
   p.out = static_cast<__nv_bfloat16*>(a.o);
-  units = static_cast<long long>(a.max_tiles) * p.nN;
-  grid = static_cast<int>(units < sms ? units : sms);
+  const long long units = static_cast<long long>(a.max_tiles) * p.nN;
+  const int grid = static_cast<int>(units < sms ? units : sms);
+  stage_begin("down_gemm", s);
   grouped_gemm_bf16_kernel<MODE_DOWN><<<grid, THREADS, SMEM_BYTES, s>>>(tmh, tmw2, p);
-  return cudaGetLastError();
+  err = cudaGetLastError();
+  stage_end(s);
+  return err;
 }
 
 // ------------------------------------------------------------------ combine
@@ -406,13 +433,16 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
   size_t blocks = (total + 255) / 256;
   const size_t cap = static_cast<size_t>(sms > 0 ? sms : 148) * 8;
   if (blocks > cap) blocks = cap;
+  stage_begin("combine", s);
   if (a.o_is_f32)
     combine_kernel<float><<<static_cast<int>(blocks), 256, 0, s>>>(static_cast<const float*>(a.o), a.w, a.T, a.k,
                                                                    a.H, static_cast<__nv_bfloat16*>(a.y));
   else
     combine_kernel<__nv_bfloat16><<<static_cast<int>(blocks), 256, 0, s>>>(
         static_cast<const __nv_bfloat16*>(a.o), a.w, a.T, a.k, a.H, static_cast<__nv_bfloat16*>(a.y));
-  return cudaGetLastError();
+  const cudaError_t err = cudaGetLastError();
+  stage_end(s);
+  return err;
 }
 
 }  // namespace moe

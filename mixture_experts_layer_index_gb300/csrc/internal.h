@@ -86,7 +86,8 @@ struct GroupedArgs {
   void* o;
   DeviceHeader* hdr;
 };
-cudaError_t launch_grouped_bf16(const GroupedArgs& a, cudaStream_t s);
+cudaError_t launch_gateup_bf16(const GroupedArgs& a, cudaStream_t s);
+cudaError_t launch_down_bf16(const GroupedArgs& a, cudaStream_t s);
 
 struct CombineArgs {
   int T, k, H;
@@ -120,6 +121,11 @@ struct DecodeArgs {
 };
 cudaError_t launch_route_direct(const DecodeArgs& a, cudaStream_t s);
 size_t route_direct_uniq_bytes(int T, int E, int k);
+
+// Stage timing (moe_profile_start/stop): every launcher brackets its kernel with
+// stage_begin/stage_end; both are no-ops unless profiling is on.
+void stage_begin(const char* name, cudaStream_t s);
+void stage_end(cudaStream_t s);
 
 // Driver entry point for cuTensorMapEncodeTiled (resolved once through the runtime).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,

@@ -3,7 +3,10 @@
 // entry layer of "perf: add small-batch route MMA for MoE" (Code changes:
 // small-batch dispatch, split selection, contiguous workspace, input/output
 // shape and contiguity validation, preallocated output).
+#include <cstring>
 #include <mutex>
+#include <string>
+#include <vector>
 
 #include "common.cuh"
 #include "internal.h"
@@ -35,6 +38,81 @@ int num_sms() {
     cache[dev] = v;
   }
   return cache[dev];
+}
+
+// ------------------------------------------------------------------ stage timing
+namespace {
+struct StageRecord {
+  int stage;
+  cudaEvent_t begin, end;
+};
+struct Profiler {
+  std::mutex mu;
+  bool on = false;
+  std::vector<std::string> names;
+  std::vector<StageRecord> records;
+  std::vector<cudaEvent_t> pool;
+  int open = -1;  // index of the record whose end is pending
+  cudaEvent_t take() {
+    if (!pool.empty()) {
+      cudaEvent_t e = pool.back();
+      pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+  }
+  void recycle() {
+    for (auto& r : records) {
+      if (r.begin) pool.push_back(r.begin);
+      if (r.end) pool.push_back(r.end);
+    }
+    records.clear();
+    names.clear();
+    open = -1;
+  }
+};
+Profiler& prof() {
+  static Profiler p;
+  return p;
+}
+bool capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &st) != cudaSuccess) return true;
+  return st != cudaStreamCaptureStatusNone;
+}
+}  // namespace
+
+void stage_begin(const char* name, cudaStream_t s) {
+  Profiler& P = prof();
+  std::lock_guard<std::mutex> lk(P.mu);
+  if (!P.on || capturing(s)) return;
+  int idx = -1;
+  for (size_t i = 0; i < P.names.size(); ++i)
+    if (P.names[i] == name) idx = static_cast<int>(i);
+  if (idx < 0) {
+    P.names.emplace_back(name);
+    idx = static_cast<int>(P.names.size()) - 1;
+  }
+  StageRecord r{idx, P.take(), P.take()};
+  if (!r.begin || !r.end || cudaEventRecord(r.begin, s) != cudaSuccess) {
+    if (r.begin) P.pool.push_back(r.begin);
+    if (r.end) P.pool.push_back(r.end);
+    return;
+  }
+  P.records.push_back(r);
+  P.open = static_cast<int>(P.records.size()) - 1;
+}
+
+void stage_end(cudaStream_t s) {
+  Profiler& P = prof();
+  std::lock_guard<std::mutex> lk(P.mu);
+  if (!P.on || P.open < 0) return;
+  if (cudaEventRecord(P.records[P.open].end, s) != cudaSuccess) {
+    P.records[P.open].stage = -1;
+  }
+  P.open = -1;
 }
 
 // ------------------------------------------------------------------ planning
@@ -287,7 +365,8 @@ moe_status moe_forward(const moe_problem* pp, const void* x, const float* scores
       g.h = at<void*>(ws, L.h);
       g.o = at<void*>(ws, L.o);
       g.hdr = hdr;
-      e = launch_grouped_bf16(g, s);
+      e = launch_gateup_bf16(g, s);
+      if (e == cudaSuccess) e = launch_down_bf16(g, s);
     }
     if (e == cudaSuccess) {
       CombineArgs c{p.T, p.k, p.H, at<void*>(ws, L.o), false, w, y};
@@ -341,6 +420,46 @@ moe_status moe_forward_views(const moe_problem* p, const void* ws, size_t ws_byt
   }
   *out = v;
   return MOE_OK;
+}
+
+int moe_profile_start(void) {
+  Profiler& P = prof();
+  std::lock_guard<std::mutex> lk(P.mu);
+  P.recycle();
+  P.on = true;
+  return 0;
+}
+
+int moe_profile_stop(moe_stage_time* out, int max_stages) {
+  Profiler& P = prof();
+  std::lock_guard<std::mutex> lk(P.mu);
+  P.on = false;
+  std::vector<double> ms(P.names.size(), 0.0);
+  std::vector<int> n(P.names.size(), 0);
+  bool ok = true;
+  for (const auto& r : P.records) {
+    if (r.stage < 0) continue;
+    if (cudaEventSynchronize(r.end) != cudaSuccess) {
+      ok = false;
+      continue;
+    }
+    float t = 0.0f;
+    if (cudaEventElapsedTime(&t, r.begin, r.end) != cudaSuccess) {
+      ok = false;
+      continue;
+    }
+    ms[r.stage] += t;
+    n[r.stage] += 1;
+  }
+  const int count = static_cast<int>(P.names.size());
+  for (int i = 0; i < count && i < max_stages && out; ++i) {
+    std::memset(out[i].name, 0, sizeof(out[i].name));
+    std::strncpy(out[i].name, P.names[i].c_str(), sizeof(out[i].name) - 1);
+    out[i].total_ms = ms[i];
+    out[i].launches = n[i];
+  }
+  P.recycle();
+  return ok ? count : -1;
 }
 
 moe_status moe_read_device_status(const void* ws, moe_stream_t stream) {

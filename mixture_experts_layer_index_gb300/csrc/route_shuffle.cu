@@ -235,16 +235,23 @@ cudaError_t launch_route_rank(const float* scores, const int32_t* ids_in, int T,
   int maxv = 1;
   while (maxv * 32 < E) maxv *= 2;
   const dim3 grid(nblk);
-  if (route && rank) return launch_rr<true, true>(maxv, grid, smem, s, scores, ids_in, T, E, k, TB, ids_out, w_out, lrank, blockcounts, hdr);
-  if (route) return launch_rr<true, false>(maxv, grid, smem, s, scores, ids_in, T, E, k, TB, ids_out, w_out, lrank, blockcounts, hdr);
-  return launch_rr<false, true>(maxv, grid, smem, s, scores, ids_in, T, E, k, TB, ids_out, w_out, lrank, blockcounts, hdr);
+  stage_begin("route_rank", s);
+  cudaError_t err;
+  if (route && rank) err = launch_rr<true, true>(maxv, grid, smem, s, scores, ids_in, T, E, k, TB, ids_out, w_out, lrank, blockcounts, hdr);
+  else if (route) err = launch_rr<true, false>(maxv, grid, smem, s, scores, ids_in, T, E, k, TB, ids_out, w_out, lrank, blockcounts, hdr);
+  else err = launch_rr<false, true>(maxv, grid, smem, s, scores, ids_in, T, E, k, TB, ids_out, w_out, lrank, blockcounts, hdr);
+  stage_end(s);
+  return err;
 }
 
 cudaError_t launch_scan_tiles(int32_t* blockcounts, int nblk, int E, int32_t* counts, int32_t* offsets,
                               int32_t* tiles, int32_t* num_tiles, int max_tiles, int BM, int32_t* /*tile_scratch*/,
                               DeviceHeader* hdr, cudaStream_t s) {
+  stage_begin("scan_tiles", s);
   scan_tiles_kernel<<<1, 1024, 0, s>>>(blockcounts, nblk, E, counts, offsets, tiles, num_tiles, max_tiles, BM, hdr);
-  return cudaGetLastError();
+  const cudaError_t err = cudaGetLastError();
+  stage_end(s);
+  return err;
 }
 
 cudaError_t launch_scatter(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E, int k,
@@ -252,18 +259,27 @@ cudaError_t launch_scatter(const int32_t* ids, const int32_t* lrank, const int32
   const int R = T * k;
   if (R <= 0) return cudaSuccess;
   const int RB = route_tokens_per_block(k) * k;
+  stage_begin("scatter", s);
   scatter_kernel<<<(R + 255) / 256, 256, 0, s>>>(ids, lrank, blockbase, R, E, RB, perm, inv);
-  return cudaGetLastError();
+  const cudaError_t err = cudaGetLastError();
+  stage_end(s);
+  return err;
 }
 
 cudaError_t launch_tile_map(const int32_t* counts, int E, int BM, int32_t* tiles, int32_t* num_tiles, int max_tiles,
                             int32_t* /*tile_scratch*/, DeviceHeader* hdr, cudaStream_t s) {
+  stage_begin("tile_map", s);
   tile_map_kernel<<<1, 1024, 0, s>>>(counts, E, BM, tiles, num_tiles, max_tiles, hdr);
-  return cudaGetLastError();
+  const cudaError_t err = cudaGetLastError();
+  stage_end(s);
+  return err;
 }
 
 cudaError_t launch_reset_header(DeviceHeader* hdr, cudaStream_t s) {
-  return cudaMemsetAsync(hdr, 0, sizeof(DeviceHeader), s);
+  stage_begin("header_reset", s);
+  const cudaError_t err = cudaMemsetAsync(hdr, 0, sizeof(DeviceHeader), s);
+  stage_end(s);
+  return err;
 }
 
 }  // namespace moe

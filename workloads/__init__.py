@@ -85,8 +85,8 @@ def workload(name: str, B: Optional[int] = None) -> Workload:
 DECODE_SWEEPS = ("hunyuan", "qwen3a", "qwen3b")
 
 
-def _gen(seed: int, stream: int) -> torch.Generator:
-    g = torch.Generator()
+def _gen(seed: int, stream: int, device="cpu") -> torch.Generator:
+    g = torch.Generator(device=device)
     g.manual_seed(seed * 16 + stream)
     return g
 
@@ -107,7 +107,7 @@ def _pack_e4m3_block128(w: torch.Tensor):
     """w [E, rows, cols] fp32 -> (codes [E,rows,cols], scale [E, ceil(rows/128), ceil(cols/128)])."""
     E, rows, cols = w.shape
     rb, cb = math.ceil(rows / 128), math.ceil(cols / 128)
-    pad = torch.zeros(E, rb * 128, cb * 128, dtype=torch.float32)
+    pad = torch.zeros(E, rb * 128, cb * 128, dtype=torch.float32, device=w.device)
     pad[:, :rows, :cols] = w
     blk = pad.view(E, rb, 128, cb, 128)
     amax = blk.abs().amax(dim=(2, 4))
@@ -139,14 +139,16 @@ def make_x(wl: Workload) -> torch.Tensor:
     return _bf16(torch.randn(wl.T, wl.H, generator=_gen(wl.seed, 0))).contiguous()
 
 
-def make_weights(wl: Workload):
+def make_weights(wl: Workload, device="cpu"):
     """Returns (w1, w2, w1_scale, w2_scale).  bf16: tensors of dtype bfloat16,
     scales None.  FP8: uint8 e4m3 codes plus fp32 scales.  The weight streams
-    do not depend on T, so every B of a decode sweep sees the same experts."""
-    g1 = _gen(wl.weight_seed, 2)
-    g2 = _gen(wl.weight_seed, 3)
-    w1 = torch.randn(wl.E, 2 * wl.I, wl.H, generator=g1) * (1.0 / math.sqrt(wl.H))
-    w2 = torch.randn(wl.E, wl.H, wl.I, generator=g2) * (1.0 / math.sqrt(wl.I))
+    do not depend on T, so every B of a decode sweep sees the same experts.
+    ``device`` selects where the seeded generator draws (a CUDA generator draws
+    a different, equally seeded stream than the CPU one)."""
+    g1 = _gen(wl.weight_seed, 2, device)
+    g2 = _gen(wl.weight_seed, 3, device)
+    w1 = torch.randn(wl.E, 2 * wl.I, wl.H, generator=g1, device=device) * (1.0 / math.sqrt(wl.H))
+    w2 = torch.randn(wl.E, wl.H, wl.I, generator=g2, device=device) * (1.0 / math.sqrt(wl.I))
     if wl.quant == QUANT_BF16:
         return _bf16(w1).contiguous(), _bf16(w2).contiguous(), None, None
     if wl.quant == QUANT_FP8_TENSOR:
