@@ -122,6 +122,31 @@ size_t moe_shuffle_workspace_size(int T, int E, int k);
 moe_status moe_shuffle(const int32_t* ids, int T, int E, int k, int32_t* counts, int32_t* offsets,
                        int32_t* perm, int32_t* inv, void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* ---------------------------------------------------------------- shuffle, no allocation
+ * moe_shuffle_noalloc - moe_shuffle without a caller-provided workspace.  The
+ * pages have no counterpart to this entry point: it exists for callers that
+ * cannot allocate device memory when they need the shuffle - code running while
+ * a stream is captured into a CUDA graph (cudaMalloc is not allowed there),
+ * plugins of a host framework that owns all device memory and provides no
+ * scratch, and serving loops that forbid allocation after start-up.
+ *   Arguments and outputs: as moe_shuffle (caller-owned device arrays).
+ *   Scratch: a fixed array of MOE_NOALLOC_SCRATCH_BYTES inside the library;
+ *   every GPU that loads the library holds it until the process exits.  Neither
+ *   this call nor the library allocates or frees anything.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ *   Every call uses the same array: calls whose work overlaps on the GPU (e.g.
+ *   on two streams) race and must be serialised by the caller.
+ *   Errors: as moe_shuffle; MOE_ERR_WORKSPACE when the problem needs more than
+ *   the fixed array (moe_shuffle_workspace_size(T, E, k) >
+ *   MOE_NOALLOC_SCRATCH_BYTES; e.g. up to 131072 routes with E = 128 fit).
+ *   An out-of-range id is skipped as in moe_shuffle; its status word is the
+ *   array's and is not exposed. */
+#define MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
+moe_status moe_shuffle_noalloc(const int32_t* ids, int T, int E, int k, int32_t* counts, int32_t* offsets,
+                               int32_t* perm, int32_t* inv, moe_stream_t stream);
+
 /* ---------------------------------------------------------------- tile map
  * moe_tile_map - the grouped GEMMs' task map ("prefix/task map" of the
  * route-MMA page's Motivation, bounded by the non-empty workload as in its

@@ -59,6 +59,7 @@ _SIGS = {
     "moe_route": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp]),
     "moe_shuffle_workspace_size": (_sz, [_i, _i, _i]),
     "moe_shuffle": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_shuffle_noalloc": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
     "moe_tile_map": (_i, [_vp, _i, _i, _vp, _vp, _i, _vp, _sz, _vp]),
     "moe_select_path": (_i, [_P]),
     "moe_workspace_size": (_sz, [_P]),
@@ -148,6 +149,13 @@ def moe_shuffle(ids, T, E, k, counts, offsets, perm, inv, ws, ws_bytes=None, str
     nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
     _check(lib().moe_shuffle(_ptr(ids), T, E, k, _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv), _ptr(ws), nb,
                             _stream(stream)), "moe_shuffle")
+
+
+def moe_shuffle_noalloc(ids, T, E, k, counts, offsets, perm, inv, stream=None) -> None:
+    """moe_shuffle with the library's fixed scratch array instead of a workspace
+    (for callers that cannot allocate device memory; see include/moe.h)."""
+    _check(lib().moe_shuffle_noalloc(_ptr(ids), T, E, k, _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv),
+                                     _stream(stream)), "moe_shuffle_noalloc")
 
 
 def moe_tile_map(counts, E, BM, tiles, num_tiles, max_tiles, ws, ws_bytes=None, stream=None) -> None:
