@@ -1,18 +1,18 @@
 /*
  * moe.h - C ABI of the GB300 (sm_103a) routed Mixture-of-Experts FFN forward.
  *
- * The library computes, on one GPU, the routed MoE FFN forward pass
- *
- *     topk routes -> count/sort -> gather -> prefix/task map
- *       -> Gate/Up grouped GEMM -> SwiGLU (+ FP8 re-quantisation)
- *       -> Down grouped GEMM -> scatter/top-k reduction
- *
- * named in "perf: add small-batch route MMA for MoE" (Motivation), with the
- * index_shuffling and scatter_add_dense_tokens steps of "Port necessary
- * FBGEMM MoE kernels", and the route-direct small-batch path of the route-MMA
- * page (Summary: reads the expert from each token/top-k route, bypasses
- * sorting, gathering, prefix sums and task maps, splits the long Gate/Up K
- * dimension, fuses split reduction + SwiGLU + Down-input quantisation).
+ * The library computes, on one GPU, the routed MoE FFN forward pass whose
+ * expert-grouped pipeline the Motivation of "perf: add small-batch route MMA
+ * for MoE" describes: top-k routing; grouping the routes by expert (counts and
+ * a stable order); gathering the rows; prefix sums and a GEMM task map; the
+ * Gate/Up grouped GEMM; SwiGLU with optional FP8 re-quantisation; the Down
+ * grouped GEMM; and the weighted reduction of each token's k expert outputs
+ * (the index_shuffling and scatter_add_dense_tokens steps of "Port necessary
+ * FBGEMM MoE kernels").  It also has the route-direct small-batch path of the
+ * route-MMA page's Summary: each route reads its expert directly, with no
+ * sort, gather, prefix sum or task map; the long Gate/Up K dimension is split
+ * for parallelism; and the split reduction, SwiGLU and the quantisation of the
+ * Down input are done in one pass.
  *
  * Definitions used throughout:
  *   T tokens, E experts, k = top_k, H hidden size, I expert intermediate size,
@@ -77,7 +77,7 @@ typedef enum {
 
 typedef enum {
   MOE_PATH_AUTO = 0,        /* library chooses (see moe_select_path) */
-  MOE_PATH_GROUPED = 1,     /* count/sort -> tiles -> grouped GEMMs -> combine */
+  MOE_PATH_GROUPED = 1,     /* group routes by expert, tile map, grouped GEMMs, combine */
   MOE_PATH_ROUTE_DIRECT = 2 /* route-order decode path, no sort / gather / tile map */
 } moe_path;
 
@@ -94,8 +94,8 @@ typedef struct {
  *   MOE_PATH_GROUPED: bf16 only;  MOE_PATH_ROUTE_DIRECT: FP8 only, T*k <= 1024. */
 
 /* ---------------------------------------------------------------- routing
- * moe_route - top-k routing ("perf: add small-batch route MMA for MoE",
- * Motivation: topk routes).
+ * moe_route - top-k routing (the routing step of "perf: add small-batch route
+ * MMA for MoE", Motivation).
  *   scores [T, E] fp32 (finite; NaN/inf are outside the contract)
  *   ids    [T, k] int32 out: selected experts in slot order (score desc, id asc)
  *   w      [T, k] fp32  out: softmax over the k selected scores
@@ -106,7 +106,8 @@ moe_status moe_route(const float* scores, int T, int E, int k, int32_t* ids, flo
 
 /* ---------------------------------------------------------------- shuffle
  * moe_shuffle - index shuffling (index_shuffling of "Port necessary FBGEMM
- * MoE kernels"; count/sort of the route-MMA page's Motivation).
+ * MoE kernels"; the counting and sorting step of the route-MMA page's
+ * Motivation).
  *   ids     [T, k] int32 in: expert of each route, each in [0, E)
  *   counts  [E]    int32 out: routes per expert
  *   offsets [E+1]  int32 out: exclusive prefix sum of counts (offsets[E] = R)
@@ -148,9 +149,9 @@ moe_status moe_shuffle_noalloc(const int32_t* ids, int T, int E, int k, int32_t*
                                int32_t* perm, int32_t* inv, moe_stream_t stream);
 
 /* ---------------------------------------------------------------- tile map
- * moe_tile_map - the grouped GEMMs' task map ("prefix/task map" of the
- * route-MMA page's Motivation, bounded by the non-empty workload as in its
- * Code changes), built on the device with no device-to-host copy.
+ * moe_tile_map - the grouped GEMMs' task map (the task-map step of the
+ * route-MMA page's Motivation, sized by the experts that actually have routes,
+ * as its Code changes do), built on the device with no device-to-host copy.
  *   counts    [E] int32 in (e.g. from moe_shuffle)
  *   BM        row-tile height (1..1024; moe_forward uses 128)
  *   tiles     [max_tiles, 4] int32 out: {expert, first sorted row, rows, 0} for

@@ -1,8 +1,9 @@
 // Route-direct small-batch path for FP8 weights ("perf: add small-batch route
-// MMA for MoE", Summary and Motivation: data stays in route order; topk routes
-// -> route Gate/Up MMA -> split reduction + SwiGLU + FP8 quantisation -> route
-// Down MMA -> contiguous top-k reduction; no expert sort, gather, prefix sum
-// or task map).
+// MMA for MoE", Summary and Motivation): the data stays in route order - each
+// route's Gate/Up product, then one fused pass that sums the K splits, applies
+// SwiGLU and quantises the Down input, then each route's Down product, then the
+// per-token reduction over contiguous rows - with no expert sort, gather,
+// prefix sum or task map.
 //
 // The work is bound by streaming the selected experts' weights from HBM, so
 // every kernel here is organised around that stream:

@@ -385,8 +385,8 @@ cudaError_t launch_down_bf16(const GroupedArgs& a, cudaStream_t s) {
 
 // ------------------------------------------------------------------ combine
 // y[t, c] = bf16( sum_{j < k} w[t, j] * o[t*k + j, c] ), fp32, j ascending
-// (scatter/top-k reduction of the route-MMA page's Motivation; contiguous
-// route-order rows, as in its Code changes for reduce.cu).  Deterministic: no
+// (the final top-k reduction of the route-MMA page's Motivation, reading
+// route-order rows contiguously as its Code changes do for reduce.cu).  Deterministic: no
 // atomics, fixed summation order.
 template <typename OT>
 __global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ o, const float* __restrict__ w, int T,

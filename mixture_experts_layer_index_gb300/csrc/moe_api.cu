@@ -1,8 +1,9 @@
 // C ABI (include/moe.h): argument validation, workspace planning, path choice
-// and the ordered, sync-free launch sequence of each entry point.  Mirrors the
-// entry layer of "perf: add small-batch route MMA for MoE" (Code changes:
-// small-batch dispatch, split selection, contiguous workspace, input/output
-// shape and contiguity validation, preallocated output).
+// and the ordered, sync-free launch sequence of each entry point.  It plays the
+// role of the entry layer described in the Code changes of "perf: add
+// small-batch route MMA for MoE": choosing the small-batch path, picking the
+// K split, laying out one workspace, checking every argument, and writing into
+// an output the caller allocated.
 #include <cstring>
 #include <mutex>
 #include <string>

@@ -2,9 +2,9 @@
 //
 // Routing: one warp per token (routing.cuh).
 //
-// Shuffle (index_shuffling of "Port necessary FBGEMM MoE kernels"; count/sort
-// -> prefix/task map of the route-MMA page's Motivation), in three launches
-// with no device-to-host copy:
+// Shuffle (index_shuffling of "Port necessary FBGEMM MoE kernels"; the
+// counting, sorting and task-map steps of the route-MMA page's Motivation), in
+// three launches with no device-to-host copy:
 //   1. route_rank: per block of <= 1024 consecutive routes, the rank of each
 //      route among the block's earlier routes of the same expert (warp
 //      match_any + per-warp running histograms), and the block's per-expert

@@ -1,8 +1,9 @@
 // Top-k selection of one token by one warp (shared by the grouped path's
 // route/rank kernel and the route-direct prep kernel).
 //
-// Rule ("perf: add small-batch route MMA for MoE", Motivation: topk routes;
-// ties to the lower expert id, softmax over the k selected scores): every lane
+// Rule (the top-k routing step of "perf: add small-batch route MMA for MoE",
+// Motivation; ties to the lower expert id, softmax over the k selected
+// scores): every lane
 // holds ceil(E/32) scores as 64-bit keys - order-preserving score bits in the
 // high word, the complemented expert id in the low word - so the largest key
 // is the largest score and, among equal scores, the lowest id.  -0.0 is

@@ -15,11 +15,13 @@ written in numpy:
                    quantisation and the full forward (bf16, per-tensor FP8,
                    128x128-blockwise FP8), and the weighted top-k combine.
 
-The pipeline it follows is the one named in "perf: add small-batch route MMA
-for MoE" (Motivation: count/sort -> gather -> prefix/task map -> Gate/Up grouped
-GEMM -> activation/quantization -> Down grouped GEMM -> scatter/top-k reduction)
-and the index_shuffling / scatter_add_dense_tokens pair of "Port necessary
-FBGEMM MoE kernels".  Accumulations run in fp64; every rounding that the method
+The steps follow the expert-grouped pipeline described in the Motivation
+section of "perf: add small-batch route MMA for MoE" (group the routes by
+expert, gather their rows, build prefix sums and a GEMM task map, run the
+Gate/Up grouped GEMM, the activation with optional re-quantisation, the Down
+grouped GEMM, and reduce the k expert outputs of each token), and the
+index_shuffling / scatter_add_dense_tokens pair of "Port necessary FBGEMM MoE
+kernels".  Accumulations run in fp64; every rounding that the method
 defines (bf16 h, e4m3 activations, fp32 scales) is applied in fp32 exactly as
 stated in the docstrings of ``moe``.
 

@@ -13,7 +13,7 @@ index_shuffling + scatter_add_dense_tokens):
               stable sort of the routes by expert (sorted position -> route
               r); inv[perm[p]] = p.
   3. tiles    for each expert with c_e > 0, ceil(c_e / BM) tiles (e, row0, nrows)
-              covering its segment of sorted positions (the "prefix/task map").
+              covering its segment of sorted positions (the GEMM task map).
   4. FFN      per route r (token t, expert e):
                  [g | u] = W1[e] x_t       (W1[e] rows 0..I-1 = gate, I..2I-1 = up)
                  a = silu(g) * u           (silu(g) = g / (1 + exp(-g)))
