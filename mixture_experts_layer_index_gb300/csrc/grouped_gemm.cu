@@ -59,6 +59,7 @@ struct Params {
   int up_offset;         // I (Gate/Up)
   int n_valid;           // valid output columns (I or H)
   int out_ld;
+  int a_gather;          // Gate/Up: 1 = A rows gathered from x by tile::gather4, 0 = sorted rows
   __nv_bfloat16* out;
   DeviceHeader* hdr;
 };
@@ -130,7 +131,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int4 tl = tiles[tile];
       const int e = tl.x, row0 = tl.y, nrows = tl.z;
       int tok[4] = {0, 0, 0, 0};
-      if (MODE == MODE_GATEUP) {
+      if (MODE == MODE_GATEUP && p.a_gather) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int pr = row0 + min(lane * 4 + i, nrows - 1);
@@ -153,8 +154,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t b_dst = a_dst + A_BYTES;
         const int kc = kb * BK;
         if (MODE == MODE_GATEUP) {
-          tma_gather4(a_dst + lane * 4 * 128, &tmA, kc, tok[0], tok[1], tok[2], tok[3], full);
+          if (p.a_gather)
+            tma_gather4(a_dst + lane * 4 * 128, &tmA, kc, tok[0], tok[1], tok[2], tok[3], full);
           if (lane == 0) {
+            if (!p.a_gather) tma_load_2d(a_dst, &tmA, kc, row0, full);
             tma_load_2d(b_dst, &tmB, kc, brow, full);
             tma_load_2d(b_dst + B_BYTES / 2, &tmB, kc, brow + p.up_offset, full);
           }
@@ -335,10 +338,12 @@ cudaError_t launch_gateup_bf16(const GroupedArgs& a, cudaStream_t s) {
   cudaError_t err = prepare(a, &sms);
   if (err != cudaSuccess) return err;
   CUtensorMap tmx, tmw1;
-  if (!encode_2d(&tmx, a.x, a.H, a.T, BK, 1) ||
+  const bool gather = a.xs == nullptr;
+  if (!(gather ? encode_2d(&tmx, a.x, a.H, a.T, BK, 1) : encode_2d(&tmx, a.xs, a.H, a.R, BK, BM)) ||
       !encode_2d(&tmw1, a.w1, a.H, static_cast<uint64_t>(a.E) * 2 * a.I, BK, BN / 2))
     return cudaErrorInvalidValue;
   Params p = base_params(a);
+  p.a_gather = gather ? 1 : 0;
   p.nN = (a.I + BN / 2 - 1) / (BN / 2);
   p.K = a.H;
   p.b_rows_per_expert = 2 * a.I;

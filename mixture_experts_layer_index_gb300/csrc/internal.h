@@ -6,7 +6,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/moe.h"
+#include "moe.h"  // include/ is on the include path (build.py)
 
 namespace moe {
 
@@ -44,6 +44,7 @@ struct ForwardLayout {
   size_t counts = 0, offsets = 0, perm = 0, inv = 0;
   size_t tiles = 0, num_tiles = 0;
   int max_tiles = 0;
+  size_t xs = 0;      // grouped: [R, H] bf16 x rows in sorted order (Gate/Up A operand)
   size_t h = 0;       // grouped: [R, I] bf16 (sorted order)
   size_t o = 0;       // grouped: [R, H] bf16 (route order); route-direct: [R, H] fp32
   // route-direct
@@ -69,6 +70,9 @@ cudaError_t launch_scan_tiles(int32_t* blockcounts, int nblk, int E, int32_t* co
                               DeviceHeader* hdr, cudaStream_t s);
 cudaError_t launch_scatter(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E, int k,
                            int32_t* perm, int32_t* inv, cudaStream_t s);
+cudaError_t launch_scatter_gather(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
+                                  int k, int H, const void* x, void* xs, int32_t* perm, int32_t* inv,
+                                  cudaStream_t s);
 cudaError_t launch_tile_map(const int32_t* counts, int E, int BM, int32_t* tiles, int32_t* num_tiles,
                             int max_tiles, int32_t* tile_scratch, DeviceHeader* hdr, cudaStream_t s);
 cudaError_t launch_reset_header(DeviceHeader* hdr, cudaStream_t s);
@@ -76,6 +80,8 @@ cudaError_t launch_reset_header(DeviceHeader* hdr, cudaStream_t s);
 struct GroupedArgs {
   int T, E, k, H, I, R;
   const void* x;
+  const void* xs;        // sorted activations [R, H]; NULL = gather x rows with TMA tile::gather4
+
   const void* w1;
   const void* w2;
   const int32_t* perm;

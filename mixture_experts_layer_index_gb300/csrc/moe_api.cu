@@ -4,6 +4,7 @@
 // small-batch route MMA for MoE": choosing the small-batch path, picking the
 // K split, laying out one workspace, checking every argument, and writing into
 // an output the caller allocated.
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -203,6 +204,7 @@ bool plan_forward(const moe_problem& p, ForwardLayout* out) {
     L.max_tiles = static_cast<int>(R / kGemmBM + E);
     L.tiles = take(static_cast<size_t>(L.max_tiles) * 16);
     L.num_tiles = take(16);
+    L.xs = take(R * H * 2);
     L.h = take(R * I * 2);
     L.o = take(R * H * 2);
   } else {
@@ -226,6 +228,20 @@ static Ptr at(void* ws, size_t off) {
 }
 
 static moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// How the Gate/Up GEMM obtains its expert-sorted activation rows.  Default: the
+// scatter kernel copies every route's x row to its sorted position and the GEMM
+// loads contiguous TMA tiles.  MOE_GATEUP_A=gather4 (environment, read once)
+// selects the fully fused variant that gathers x rows inside the GEMM with TMA
+// tile::gather4 instead; it is kept for comparison (it measured 3.2x slower per
+// K stage on GB300).
+static bool gateup_gather4() {
+  static const bool v = [] {
+    const char* e = std::getenv("MOE_GATEUP_A");
+    return e && std::strcmp(e, "gather4") == 0;
+  }();
+  return v;
+}
 
 }  // namespace moe
 
@@ -357,11 +373,19 @@ moe_status moe_forward(const moe_problem* pp, const void* x, const float* scores
     if (e == cudaSuccess)
       e = launch_scan_tiles(bc, L.shuf.nblk, p.E, counts, offsets, tiles, num_tiles, L.max_tiles, kGemmBM, nullptr,
                             hdr, s);
-    if (e == cudaSuccess) e = launch_scatter(ids, lrank, bc, p.T, p.E, p.k, perm, inv, s);
+    const bool gather4 = gateup_gather4();
+    void* xs = at<void*>(ws, L.xs);
+    if (e == cudaSuccess) {
+      if (gather4)
+        e = launch_scatter(ids, lrank, bc, p.T, p.E, p.k, perm, inv, s);
+      else
+        e = launch_scatter_gather(ids, lrank, bc, p.T, p.E, p.k, p.H, x, xs, perm, inv, s);
+    }
     if (e == cudaSuccess) {
       GroupedArgs g{};
       g.T = p.T; g.E = p.E; g.k = p.k; g.H = p.H; g.I = p.I; g.R = p.T * p.k;
       g.x = x; g.w1 = w1; g.w2 = w2;
+      g.xs = gather4 ? nullptr : xs;
       g.perm = perm; g.tiles = tiles; g.num_tiles = num_tiles; g.max_tiles = L.max_tiles;
       g.h = at<void*>(ws, L.h);
       g.o = at<void*>(ws, L.o);

@@ -19,32 +19,11 @@
 
 namespace moe {
 
-template <int MAXV, bool ROUTE, bool RANK>
-__global__ void __launch_bounds__(kRouteThreads) route_rank_kernel(
-    const float* __restrict__ scores, const int32_t* __restrict__ ids_in, int T, int E, int k, int TB,
-    int32_t* __restrict__ ids_out, float* __restrict__ w_out, int32_t* __restrict__ lrank,
-    int32_t* __restrict__ blockcounts, DeviceHeader* hdr) {
-  extern __shared__ int smem[];
-  int* s_ids = smem;                          // [1024]
-  int* s_lr = smem + kMaxRoutesPerBlock;      // [1024]
-  int* hist = smem + 2 * kMaxRoutesPerBlock;  // [8][E]
+// Ranking phase of the route/rank kernel (s_ids holds the block's nr expert ids).
+__device__ __forceinline__ void rank_block(int* s_ids, int* s_lr, int* hist, int E, int RB, int nr, size_t r0, int blk,
+                                           int32_t* __restrict__ lrank, int32_t* __restrict__ blockcounts,
+                                           DeviceHeader* hdr) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int blk = blockIdx.x;
-  const int t0 = blk * TB;
-  const int nt = min(TB, T - t0);
-  const int RB = TB * k;
-  const int nr = nt * k;
-  const size_t r0 = static_cast<size_t>(t0) * k;
-
-  if (ROUTE) {
-    for (int tb = warp; tb < nt; tb += kRouteThreads / 32) {
-      const size_t t = static_cast<size_t>(t0 + tb);
-      route_one_token<MAXV>(scores + t * E, E, k, ids_out + t * k, w_out + t * k, RANK ? s_ids + tb * k : nullptr);
-    }
-  } else {
-    for (int i = tid; i < nr; i += kRouteThreads) s_ids[i] = ids_in[r0 + i];
-  }
-  if (!RANK) return;
   for (int i = tid; i < 8 * E; i += kRouteThreads) hist[i] = 0;
   __syncthreads();
 
@@ -83,6 +62,33 @@ __global__ void __launch_bounds__(kRouteThreads) route_rank_kernel(
     if (lr >= 0) lr += hist[(rl / seg) * E + s_ids[rl]];
     lrank[r0 + rl] = lr;
   }
+}
+
+template <int MAXV, bool ROUTE, bool RANK>
+__global__ void __launch_bounds__(kRouteThreads) route_rank_kernel(
+    const float* __restrict__ scores, const int32_t* __restrict__ ids_in, int T, int E, int k, int TB,
+    int32_t* __restrict__ ids_out, float* __restrict__ w_out, int32_t* __restrict__ lrank,
+    int32_t* __restrict__ blockcounts, DeviceHeader* hdr) {
+  extern __shared__ int smem[];
+  int* s_ids = smem;                          // [1024]
+  int* s_lr = smem + kMaxRoutesPerBlock;      // [1024]
+  int* hist = smem + 2 * kMaxRoutesPerBlock;  // [8][E]
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int blk = blockIdx.x;
+  const int t0 = blk * TB;
+  const int nt = min(TB, T - t0);
+  const int nr = nt * k;
+  const size_t r0 = static_cast<size_t>(t0) * k;
+
+  if (ROUTE) {
+    for (int tb = warp; tb < nt; tb += kRouteThreads / 32) {
+      const size_t t = static_cast<size_t>(t0 + tb);
+      route_one_token<MAXV>(scores + t * E, E, k, ids_out + t * k, w_out + t * k, RANK ? s_ids + tb * k : nullptr);
+    }
+  } else {
+    for (int i = tid; i < nr; i += kRouteThreads) s_ids[i] = ids_in[r0 + i];
+  }
+  if constexpr (RANK) rank_block(s_ids, s_lr, hist, E, TB * k, nr, r0, blk, lrank, blockcounts, hdr);
 }
 
 // Exclusive prefix of s_cnt (E <= 512) by warp 0 into s_off, and of the tile
@@ -206,6 +212,44 @@ __global__ void scatter_kernel(const int32_t* __restrict__ ids, const int32_t* _
   inv[r] = p;
 }
 
+// Scatter fused with the gather of the activations: one warp per route writes
+// perm/inv like scatter_kernel and copies the route's x row (H bf16) to sorted
+// row p of xs, so the Gate/Up GEMM reads its A tiles as plain contiguous boxes.
+__global__ void __launch_bounds__(256) scatter_gather_kernel(const int32_t* __restrict__ ids,
+                                                             const int32_t* __restrict__ lrank,
+                                                             const int32_t* __restrict__ blockbase, int R, int E,
+                                                             int RB, int k, int H, const uint4* __restrict__ x,
+                                                             uint4* __restrict__ xs, int32_t* __restrict__ perm,
+                                                             int32_t* __restrict__ inv) {
+  const int lane = threadIdx.x & 31;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  const int row16 = H / 8;  // 16-byte chunks per row
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < R; r += nw) {
+    const int lr = lrank[r];
+    if (lr < 0) {
+      if (lane == 0) inv[r] = -1;
+      continue;
+    }
+    const int e = ids[r];
+    const int p = blockbase[static_cast<size_t>(r / RB) * E + e] + lr;
+    if (lane == 0) {
+      perm[p] = r;
+      inv[r] = p;
+    }
+    const uint4* src = x + static_cast<size_t>(r / k) * row16;
+    uint4* dst = xs + static_cast<size_t>(p) * row16;
+    int c = lane;
+    for (; c + 32 * 7 < row16; c += 32 * 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = __ldg(src + c + 32 * i);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dst[c + 32 * i] = v[i];
+    }
+    for (; c < row16; c += 32) dst[c] = __ldg(src + c);
+  }
+}
+
 // ------------------------------------------------------------------ launchers
 template <bool ROUTE, bool RANK>
 static cudaError_t launch_rr(int maxv, dim3 grid, size_t smem, cudaStream_t s, const float* scores,
@@ -261,6 +305,25 @@ cudaError_t launch_scatter(const int32_t* ids, const int32_t* lrank, const int32
   const int RB = route_tokens_per_block(k) * k;
   stage_begin("scatter", s);
   scatter_kernel<<<(R + 255) / 256, 256, 0, s>>>(ids, lrank, blockbase, R, E, RB, perm, inv);
+  const cudaError_t err = cudaGetLastError();
+  stage_end(s);
+  return err;
+}
+
+cudaError_t launch_scatter_gather(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
+                                  int k, int H, const void* x, void* xs, int32_t* perm, int32_t* inv,
+                                  cudaStream_t s) {
+  const int R = T * k;
+  if (R <= 0) return cudaSuccess;
+  const int RB = route_tokens_per_block(k) * k;
+  const int sms = num_sms();
+  long long blocks = (static_cast<long long>(R) + 7) / 8;
+  const long long cap = static_cast<long long>(sms > 0 ? sms : 148) * 16;
+  if (blocks > cap) blocks = cap;
+  stage_begin("scatter_gather", s);
+  scatter_gather_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(ids, lrank, blockbase, R, E, RB, k, H,
+                                                                 static_cast<const uint4*>(x),
+                                                                 static_cast<uint4*>(xs), perm, inv);
   const cudaError_t err = cudaGetLastError();
   stage_end(s);
   return err;

@@ -321,3 +321,19 @@ def test_small_workspace_rejected_without_launch(m):
 def test_fp8_grouped_is_reported_unsupported(m):
     p = m.problem(64, 32, 8, 512, 256, "fp8_tensor", m.MOE_PATH_GROUPED)
     assert m.moe_workspace_size(p) == 0
+
+
+def test_gather4_variant_matches_oracle_in_subprocess():
+    """The fused TMA tile::gather4 Gate/Up variant (selected by MOE_GATEUP_A=gather4,
+    read once per process) stays correct; run it in a fresh process."""
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("import __graft_entry__ as g, workloads as W, mixture_experts_layer_index_gb300 as m;"
+            "print(g._run_case(W.Workload('g4', 300, 6, 2, 320, 320, W.QUANT_BF16, 25), m.MOE_PATH_GROUPED));"
+            "print(g._run_case(W.workload('tiny'), m.MOE_PATH_GROUPED))")
+    env = dict(os.environ, MOE_GATEUP_A="gather4")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
