@@ -75,6 +75,12 @@ __device__ __forceinline__ void mma_k64(float (&c)[4], const uint4& A0, const ui
   mma_e4m3(c, A0.z, A1.z, A0.w, A1.w, X.z, X.w);
 }
 
+// Programmatic dependent launch: every kernel after rd_prep is launched while
+// its predecessor still runs; it waits here before touching the predecessor's
+// results, and lets its own successor launch as early as possible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ rd_prep
 template <int MAXV>
 __global__ void __launch_bounds__(1024) rd_prep_kernel(DecodeArgs a) {
@@ -86,6 +92,7 @@ __global__ void __launch_bounds__(1024) rd_prep_kernel(DecodeArgs a) {
   __shared__ float s_red[32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
   const int T = a.T, E = a.E, k = a.k, H = a.H, R = a.R;
+  pdl_trigger();
   if (tid == 0) {
     a.hdr->status = 0u;
     a.hdr->info = 0u;
@@ -99,11 +106,26 @@ __global__ void __launch_bounds__(1024) rd_prep_kernel(DecodeArgs a) {
   // 2. dynamic e4m3 quantisation of x
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.x);
   if (a.quant == MOE_FP8_PER_TENSOR) {
+    // loads go out in batches of 8 x 16 bytes per thread: one memory round trip per batch
     float m = 0.0f;
-    const int n2 = T * H / 2;
-    for (int i = tid; i < n2; i += blockDim.x) {
-      const float2 f = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(x)[i]);
-      m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+    const int n8 = T * H / 8;
+    const uint4* x8 = reinterpret_cast<const uint4*>(x);
+    for (int base = tid; base < n8; base += blockDim.x * 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = base + j * blockDim.x;
+        v[j] = i < n8 ? __ldg(x8 + i) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v[j]);
+#pragma unroll
+        for (int h2 = 0; h2 < 4; ++h2) {
+          const float2 f = __bfloat1622float2(b[h2]);
+          m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+      }
     }
     m = warp_max(m);
     if (lane == 0) s_red[warp] = m;
@@ -120,25 +142,56 @@ __global__ void __launch_bounds__(1024) rd_prep_kernel(DecodeArgs a) {
       a.sx[0] = s;
       a.hdr->amax_x = __float_as_uint(amax);
     }
-    for (int i = tid; i < n2; i += blockDim.x) {
-      const float2 f = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(x)[i]);
-      reinterpret_cast<uint16_t*>(a.xq)[i] = cvt_e4m3x2(f.x / s, f.y / s);
+    for (int base = tid; base < n8; base += blockDim.x * 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = base + j * blockDim.x;
+        v[j] = i < n8 ? __ldg(x8 + i) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = base + j * blockDim.x;
+        if (i < n8) {
+          const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v[j]);
+          uint32_t q[2];
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const float2 f0 = __bfloat1622float2(b[2 * h2]), f1 = __bfloat1622float2(b[2 * h2 + 1]);
+            q[h2] = static_cast<uint32_t>(cvt_e4m3x2(f0.x / s, f0.y / s)) |
+                    (static_cast<uint32_t>(cvt_e4m3x2(f1.x / s, f1.y / s)) << 16);
+          }
+          reinterpret_cast<uint2*>(a.xq)[i] = make_uint2(q[0], q[1]);
+        }
+      }
     }
   } else {
-    const int ng = H / 128;
-    for (int gi = warp; gi < T * ng; gi += nwarps) {
-      const int t = gi / ng, G = gi - (gi / ng) * ng;
-      const __nv_bfloat16* src = x + static_cast<size_t>(t) * H + G * 128 + lane * 4;
-      const uint2 raw = *reinterpret_cast<const uint2*>(src);
-      const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
-      const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
-      float m = fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
-      m = warp_max(m);
-      const float s = e4m3_scale(m);
-      const uint32_t q = static_cast<uint32_t>(cvt_e4m3x2(f0.x / s, f0.y / s)) |
-                         (static_cast<uint32_t>(cvt_e4m3x2(f1.x / s, f1.y / s)) << 16);
-      *reinterpret_cast<uint32_t*>(a.xq + static_cast<size_t>(t) * H + G * 128 + lane * 4) = q;
-      if (lane == 0) a.sx[static_cast<size_t>(t) * ng + G] = s;
+    const int ng = H / 128, ntask = T * ng;
+    for (int base = warp; base < ntask; base += nwarps * 8) {
+      uint2 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int gi = base + j * nwarps;
+        const int t = gi / ng, G = gi - (gi / ng) * ng;
+        v[j] = gi < ntask ? __ldg(reinterpret_cast<const uint2*>(x + static_cast<size_t>(t) * H + G * 128) + lane)
+                          : make_uint2(0, 0);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int gi = base + j * nwarps;  // warp-uniform
+        if (gi < ntask) {
+          const int t = gi / ng, G = gi - (gi / ng) * ng;
+          const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[j].x));
+          const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[j].y));
+          float m = fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
+          m = warp_max(m);
+          const float s = e4m3_scale(m);
+          const uint32_t q = static_cast<uint32_t>(cvt_e4m3x2(f0.x / s, f0.y / s)) |
+                             (static_cast<uint32_t>(cvt_e4m3x2(f1.x / s, f1.y / s)) << 16);
+          *reinterpret_cast<uint32_t*>(a.xq + static_cast<size_t>(t) * H + G * 128 + lane * 4) = q;
+          if (lane == 0) a.sx[static_cast<size_t>(t) * ng + G] = s;
+        }
+      }
     }
   }
   // 3. distinct experts in first-use order, routes of each in route order
@@ -205,6 +258,8 @@ __global__ void __launch_bounds__(1024) rd_prep_kernel(DecodeArgs a) {
 // grid = maxU * nMB * S; block = 128 threads (4 warps x 16 rows of W1[e]).
 template <bool BLOCKWISE>
 __global__ void __launch_bounds__(THREADS) rd_gateup_kernel(DecodeArgs a, int nMB, int S) {
+  pdl_trigger();
+  pdl_wait();
   const int unit = blockIdx.x;
   const int s = unit % S;
   const int mb = (unit / S) % nMB;
@@ -230,7 +285,7 @@ __global__ void __launch_bounds__(THREADS) rd_gateup_kernel(DecodeArgs a, int nM
     const uint8_t* xrow = a.xq + static_cast<size_t>(my_t) * H + 16 * tig;
     float c[4] = {0.f, 0.f, 0.f, 0.f};
     if (!BLOCKWISE) {
-#pragma unroll 4
+#pragma unroll 8
       for (int kk = k0; kk < k0 + KS; kk += 64) {
         const uint4 A0 = ld_stream(wrow0 + kk);
         const uint4 A1 = ld_stream(wrow1 + kk);
@@ -244,7 +299,7 @@ __global__ void __launch_bounds__(THREADS) rd_gateup_kernel(DecodeArgs a, int nM
       const int t0 = 2 * tig < nn ? uv.routes()[r_beg + n0 + 2 * tig] / a.k : 0;
       const int t1 = 2 * tig + 1 < nn ? uv.routes()[r_beg + n0 + 2 * tig + 1] / a.k : 0;
       const float* sw = a.w1_scale + (static_cast<size_t>(e) * (twoI / 128) + rb) * ng;
-#pragma unroll 2
+#pragma unroll 4
       for (int kk = k0; kk < k0 + KS; kk += 128) {
         float cb[4] = {0.f, 0.f, 0.f, 0.f};
         const uint4 A0 = ld_stream(wrow0 + kk), A1 = ld_stream(wrow1 + kk);
@@ -281,6 +336,8 @@ __global__ void __launch_bounds__(THREADS) rd_gateup_kernel(DecodeArgs a, int nM
 // ------------------------------------------------------------------ rd_reduce
 // per-tensor: one thread per (route, i); blockwise: one warp per (route, 128-column group).
 __global__ void __launch_bounds__(256) rd_reduce_tensor_kernel(DecodeArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   const int I = a.I, twoI = 2 * I;
   float av = 0.0f;
@@ -301,6 +358,8 @@ __global__ void __launch_bounds__(256) rd_reduce_tensor_kernel(DecodeArgs a) {
 }
 
 __global__ void __launch_bounds__(256) rd_reduce_block_kernel(DecodeArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int I = a.I, twoI = 2 * I, ngi = I / 128;
@@ -331,6 +390,8 @@ __global__ void __launch_bounds__(256) rd_reduce_block_kernel(DecodeArgs a) {
 // grid = maxU * nHB; block = 128 threads (4 warps x 16 rows of W2[e]); K = I whole.
 template <bool BLOCKWISE>
 __global__ void __launch_bounds__(THREADS) rd_down_kernel(DecodeArgs a, int nHB) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ uint8_t s_h[];  // [8][I] e4m3 of the current 8 routes, then [8][I/128] fp32 scales
   const int hb = blockIdx.x % nHB;
   const int u = blockIdx.x / nHB;
@@ -446,40 +507,51 @@ cudaError_t launch_route_direct(const DecodeArgs& a, cudaStream_t s) {
 
   const int maxU = max_uniq(a.R, a.E);
   const bool bw = a.quant == MOE_FP8_BLOCK128;
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  auto config = [&](unsigned grid, unsigned block, size_t smem) {
+    cudaLaunchConfig_t c{};
+    c.gridDim = dim3(grid);
+    c.blockDim = dim3(block);
+    c.dynamicSmemBytes = smem;
+    c.stream = s;
+    c.attrs = pdl;
+    c.numAttrs = 1;
+    return c;
+  };
+
   const int nMB = 2 * a.I / ROWS_PER_CTA;
-  const int g1 = maxU * nMB * a.splits;
   stage_begin("rd_gateup", s);
-  if (bw)
-    rd_gateup_kernel<true><<<g1, THREADS, 0, s>>>(a, nMB, a.splits);
-  else
-    rd_gateup_kernel<false><<<g1, THREADS, 0, s>>>(a, nMB, a.splits);
-  err = cudaGetLastError();
+  {
+    const cudaLaunchConfig_t c = config(maxU * nMB * a.splits, THREADS, 0);
+    err = bw ? cudaLaunchKernelEx(&c, rd_gateup_kernel<true>, a, nMB, a.splits)
+             : cudaLaunchKernelEx(&c, rd_gateup_kernel<false>, a, nMB, a.splits);
+  }
   stage_end(s);
   if (err != cudaSuccess) return err;
 
   stage_begin("rd_reduce", s);
   if (bw) {
     const int warps = a.R * (a.I / 128);
-    rd_reduce_block_kernel<<<(warps * 32 + 255) / 256, 256, 0, s>>>(a);
+    const cudaLaunchConfig_t c = config((warps * 32 + 255) / 256, 256, 0);
+    err = cudaLaunchKernelEx(&c, rd_reduce_block_kernel, a);
   } else {
-    rd_reduce_tensor_kernel<<<(a.R * a.I + 255) / 256, 256, 0, s>>>(a);
+    const cudaLaunchConfig_t c = config((a.R * a.I + 255) / 256, 256, 0);
+    err = cudaLaunchKernelEx(&c, rd_reduce_tensor_kernel, a);
   }
-  err = cudaGetLastError();
   stage_end(s);
   if (err != cudaSuccess) return err;
 
   const int nHB = a.H / ROWS_PER_CTA;
   const size_t smem = static_cast<size_t>(8) * a.I + 8 * (a.I / 128 + 1) * sizeof(float) + 16;
   stage_begin("rd_down", s);
-  if (bw)
-    rd_down_kernel<true><<<maxU * nHB, THREADS, smem, s>>>(a, nHB);
-  else
-    rd_down_kernel<false><<<maxU * nHB, THREADS, smem, s>>>(a, nHB);
-  err = cudaGetLastError();
+  {
+    const cudaLaunchConfig_t c = config(maxU * nHB, THREADS, smem);
+    err = bw ? cudaLaunchKernelEx(&c, rd_down_kernel<true>, a, nHB) : cudaLaunchKernelEx(&c, rd_down_kernel<false>, a, nHB);
+  }
   stage_end(s);
-  if (err != cudaSuccess) return err;
-
-  return cudaSuccess;
+  return err;
 }
 
 }  // namespace moe

@@ -396,6 +396,9 @@ cudaError_t launch_down_bf16(const GroupedArgs& a, cudaStream_t s) {
 template <typename OT>
 __global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ o, const float* __restrict__ w, int T,
                                                       int k, int H, __nv_bfloat16* __restrict__ y) {
+  // launched as a programmatic dependent (route-direct path): wait for the producer
+  // of o; a no-op for an ordinary launch
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int cpt = H / 8;
   const size_t total = static_cast<size_t>(T) * cpt;
   for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < total;
@@ -429,6 +432,32 @@ __global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ o, 
     }
     *reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * H + c) = gg::pack_bf16x8(acc);
   }
+}
+
+cudaError_t launch_combine_pdl(const CombineArgs& a, cudaStream_t s) {
+  if (a.T <= 0) return cudaSuccess;
+  const size_t total = static_cast<size_t>(a.T) * (a.H / 8);
+  const int sms = num_sms();
+  size_t blocks = (total + 255) / 256;
+  const size_t cap = static_cast<size_t>(sms > 0 ? sms : 148) * 8;
+  if (blocks > cap) blocks = cap;
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  stage_begin("combine", s);
+  const cudaError_t err =
+      a.o_is_f32 ? cudaLaunchKernelEx(&cfg, combine_kernel<float>, static_cast<const float*>(a.o), a.w, a.T, a.k, a.H,
+                                      static_cast<__nv_bfloat16*>(a.y))
+                 : cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, static_cast<const __nv_bfloat16*>(a.o), a.w,
+                                      a.T, a.k, a.H, static_cast<__nv_bfloat16*>(a.y));
+  stage_end(s);
+  return err;
 }
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {

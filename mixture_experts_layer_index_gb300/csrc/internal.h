@@ -103,6 +103,8 @@ struct CombineArgs {
   void* y;             // [T, H] bf16
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
+// Same, launched as a programmatic dependent of the previous kernel on the stream.
+cudaError_t launch_combine_pdl(const CombineArgs& a, cudaStream_t s);
 
 struct DecodeArgs {
   int T, E, k, H, I, R;

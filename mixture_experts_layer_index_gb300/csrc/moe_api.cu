@@ -418,7 +418,7 @@ moe_status moe_forward(const moe_problem* pp, const void* x, const float* scores
     e = launch_route_direct(d, s);
     if (e == cudaSuccess) {
       CombineArgs c{p.T, p.k, p.H, d.o, true, w, y};
-      e = launch_combine(c, s);
+      e = launch_combine_pdl(c, s);
     }
   }
   return from_cuda(e);

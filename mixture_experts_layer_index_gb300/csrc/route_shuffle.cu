@@ -19,6 +19,8 @@
 
 namespace moe {
 
+constexpr int kScanSmemBytes = 192 * 1024;  // block-count matrix staged in shared memory up to this size
+
 // Ranking phase of the route/rank kernel (s_ids holds the block's nr expert ids).
 __device__ __forceinline__ void rank_block(int* s_ids, int* s_lr, int* hist, int E, int RB, int nr, size_t r0, int blk,
                                            int32_t* __restrict__ lrank, int32_t* __restrict__ blockcounts,
@@ -81,9 +83,17 @@ __global__ void __launch_bounds__(kRouteThreads) route_rank_kernel(
   const size_t r0 = static_cast<size_t>(t0) * k;
 
   if (ROUTE) {
-    for (int tb = warp; tb < nt; tb += kRouteThreads / 32) {
+    // each warp routes every 8th token of the block; the next token's scores are
+    // loaded while the current one is being routed
+    constexpr int NW = kRouteThreads / 32;
+    float cur[MAXV], nxt[MAXV];
+    if (warp < nt) load_scores<MAXV>(scores + static_cast<size_t>(t0 + warp) * E, E, cur);
+    for (int tb = warp; tb < nt; tb += NW) {
+      if (tb + NW < nt) load_scores<MAXV>(scores + static_cast<size_t>(t0 + tb + NW) * E, E, nxt);
       const size_t t = static_cast<size_t>(t0 + tb);
-      route_one_token<MAXV>(scores + t * E, E, k, ids_out + t * k, w_out + t * k, RANK ? s_ids + tb * k : nullptr);
+      route_values<MAXV>(cur, E, k, ids_out + t * k, w_out + t * k, RANK ? s_ids + tb * k : nullptr);
+#pragma unroll
+      for (int i = 0; i < MAXV; ++i) cur[i] = nxt[i];
     }
   } else {
     for (int i = tid; i < nr; i += kRouteThreads) s_ids[i] = ids_in[r0 + i];
@@ -154,16 +164,27 @@ __device__ __forceinline__ void emit_tiles(const int* s_cnt, const int* s_off, c
   }
 }
 
+// The block-count matrix is first copied into shared memory with independent,
+// coalesced loads (when it fits), so that the per-expert column scans run on
+// shared memory instead of a chain of dependent global loads.
 __global__ void __launch_bounds__(1024) scan_tiles_kernel(int32_t* __restrict__ bc, int nblk, int E,
                                                           int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                           int32_t* __restrict__ tiles, int32_t* __restrict__ num_tiles,
-                                                          int max_tiles, int BM, DeviceHeader* hdr) {
+                                                          int max_tiles, int BM, DeviceHeader* hdr, int use_smem) {
   __shared__ int s_cnt[kMaxE], s_off[kMaxE + 1], s_toff[kMaxE + 1];
+  extern __shared__ int sbc[];
+  const int n = nblk * E;
+  int* col = use_smem ? sbc : bc;
+  if (use_smem) {
+#pragma unroll 8
+    for (int i = threadIdx.x; i < n; i += blockDim.x) sbc[i] = bc[i];
+    __syncthreads();
+  }
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = 0;
     for (int b = 0; b < nblk; ++b) {
-      const int c = bc[static_cast<size_t>(b) * E + e];
-      bc[static_cast<size_t>(b) * E + e] = run;
+      const int c = col[b * E + e];
+      col[b * E + e] = run;
       run += c;
     }
     s_cnt[e] = run;
@@ -176,8 +197,7 @@ __global__ void __launch_bounds__(1024) scan_tiles_kernel(int32_t* __restrict__ 
     offsets[e] = s_off[e];
   }
   if (threadIdx.x == 0) offsets[E] = s_off[E];
-  const size_t n = static_cast<size_t>(nblk) * E;
-  for (size_t i = threadIdx.x; i < n; i += blockDim.x) bc[i] += s_off[i % E];
+  for (int i = threadIdx.x; i < n; i += blockDim.x) bc[i] = col[i] + s_off[i % E];
   if (tiles) emit_tiles(s_cnt, s_off, s_toff, E, BM, tiles, num_tiles, max_tiles, hdr);
 }
 
@@ -291,8 +311,14 @@ cudaError_t launch_route_rank(const float* scores, const int32_t* ids_in, int T,
 cudaError_t launch_scan_tiles(int32_t* blockcounts, int nblk, int E, int32_t* counts, int32_t* offsets,
                               int32_t* tiles, int32_t* num_tiles, int max_tiles, int BM, int32_t* /*tile_scratch*/,
                               DeviceHeader* hdr, cudaStream_t s) {
+  static const cudaError_t attr = cudaFuncSetAttribute(scan_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       kScanSmemBytes);
+  if (attr != cudaSuccess) return attr;
+  const size_t need = static_cast<size_t>(nblk) * E * sizeof(int);
+  const int use_smem = need <= static_cast<size_t>(kScanSmemBytes) ? 1 : 0;
   stage_begin("scan_tiles", s);
-  scan_tiles_kernel<<<1, 1024, 0, s>>>(blockcounts, nblk, E, counts, offsets, tiles, num_tiles, max_tiles, BM, hdr);
+  scan_tiles_kernel<<<1, 1024, use_smem ? need : 0, s>>>(blockcounts, nblk, E, counts, offsets, tiles, num_tiles,
+                                                         max_tiles, BM, hdr, use_smem);
   const cudaError_t err = cudaGetLastError();
   stage_end(s);
   return err;

@@ -22,19 +22,37 @@ __device__ __forceinline__ unsigned long long score_key(float v, int e) {
   return (static_cast<unsigned long long>(u) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(e));
 }
 
-// Lane j < k writes slot j: ids_row[j], w_row[j] and (if given) s_ids_row[j].
+// Inverse of the key's score bits (the canonicalised score itself).
+__device__ __forceinline__ float key_score(unsigned long long key) {
+  const uint32_t u = static_cast<uint32_t>(key >> 32);
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
+
+// Scores of one token, ceil(E/32) per lane (expert i*32 + lane in slot i).
 template <int MAXV>
-__device__ __forceinline__ void route_one_token(const float* __restrict__ srow, int E, int k,
-                                                int32_t* __restrict__ ids_row, float* __restrict__ w_row,
-                                                int* s_ids_row) {
+__device__ __forceinline__ void load_scores(const float* __restrict__ srow, int E, float (&v)[MAXV]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int e = i * 32 + lane;
+    v[i] = e < E ? __ldg(srow + e) : 0.0f;
+  }
+}
+
+// Route one token from its scores already in registers.  Lane j < k writes
+// slot j: ids_row[j], w_row[j] and (if given) s_ids_row[j].
+template <int MAXV>
+__device__ __forceinline__ void route_values(const float (&v)[MAXV], int E, int k, int32_t* __restrict__ ids_row,
+                                             float* __restrict__ w_row, int* s_ids_row) {
   const int lane = threadIdx.x & 31;
   unsigned long long key[MAXV];
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
     const int e = i * 32 + lane;
-    key[i] = e < E ? score_key(__ldg(srow + e), e) : 0ull;  // any real key is > 0
+    key[i] = e < E ? score_key(v[i], e) : 0ull;  // any real key is > 0
   }
   int my_id = 0;
+  float my_s = 0.0f;
 #pragma unroll 1
   for (int j = 0; j < k; ++j) {
     unsigned long long best = 0ull;
@@ -49,9 +67,11 @@ __device__ __forceinline__ void route_one_token(const float* __restrict__ srow, 
 #pragma unroll
     for (int i = 0; i < MAXV; ++i)
       if (i * 32 + lane == id) key[i] = 0ull;
-    if (lane == j) my_id = id;
+    if (lane == j) {
+      my_id = id;
+      my_s = key_score(best);
+    }
   }
-  const float my_s = lane < k ? __ldg(srow + my_id) + 0.0f : 0.0f;
   const float m = __shfl_sync(0xffffffffu, my_s, 0);
   const float ev = lane < k ? expf(my_s - m) : 0.0f;
   float sum = ev;
@@ -62,6 +82,16 @@ __device__ __forceinline__ void route_one_token(const float* __restrict__ srow, 
     w_row[lane] = ev / sum;
     if (s_ids_row) s_ids_row[lane] = my_id;
   }
+}
+
+// Lane j < k writes slot j: ids_row[j], w_row[j] and (if given) s_ids_row[j].
+template <int MAXV>
+__device__ __forceinline__ void route_one_token(const float* __restrict__ srow, int E, int k,
+                                                int32_t* __restrict__ ids_row, float* __restrict__ w_row,
+                                                int* s_ids_row) {
+  float v[MAXV];
+  load_scores<MAXV>(srow, E, v);
+  route_values<MAXV>(v, E, k, ids_row, w_row, s_ids_row);
 }
 
 }  // namespace moe
