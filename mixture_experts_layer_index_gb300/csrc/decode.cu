@@ -333,6 +333,31 @@ __global__ void __launch_bounds__(THREADS) rd_gateup_kernel(DecodeArgs a, int nM
   }
 }
 
+// Sum of the K-split partials of (route r, column i) and of (r, I + i); the
+// split loads are issued 8 at a time before they are added, in split order.
+__device__ __forceinline__ void sum_splits(const float* part, int splits, int R, int twoI, int I, int r, int i,
+                                           float& g, float& u) {
+  g = 0.f;
+  u = 0.f;
+  for (int s0 = 0; s0 < splits; s0 += 8) {
+    float gv[8], uv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int s = s0 + j < splits ? s0 + j : 0;
+      const float* pp = part + (static_cast<size_t>(s) * R + r) * twoI;
+      gv[j] = pp[i];
+      uv[j] = pp[I + i];
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (s0 + j < splits) {
+        g += gv[j];
+        u += uv[j];
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ rd_reduce
 // per-tensor: one thread per (route, i); blockwise: one warp per (route, 128-column group).
 __global__ void __launch_bounds__(256) rd_reduce_tensor_kernel(DecodeArgs a) {
@@ -343,12 +368,8 @@ __global__ void __launch_bounds__(256) rd_reduce_tensor_kernel(DecodeArgs a) {
   float av = 0.0f;
   if (idx < a.R * I) {
     const int r = idx / I, i = idx - (idx / I) * I;
-    float g = 0.f, u = 0.f;
-    for (int s = 0; s < a.splits; ++s) {
-      const float* p = a.part + (static_cast<size_t>(s) * a.R + r) * twoI;
-      g += p[i];
-      u += p[I + i];
-    }
+    float g, u;
+    sum_splits(a.part, a.splits, a.R, twoI, I, r, i, g, u);
     const float sc = a.sx[0] * __ldg(a.w1_scale + a.ids[r]);
     av = silu_mul(sc * g, sc * u);
     static_cast<float*>(a.act)[idx] = av;
@@ -369,12 +390,8 @@ __global__ void __launch_bounds__(256) rd_reduce_block_kernel(DecodeArgs a) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int i = G * 128 + lane * 4 + q;
-    float g = 0.f, u = 0.f;
-    for (int s = 0; s < a.splits; ++s) {
-      const float* p = a.part + (static_cast<size_t>(s) * a.R + r) * twoI;
-      g += p[i];
-      u += p[I + i];
-    }
+    float g, u;
+    sum_splits(a.part, a.splits, a.R, twoI, I, r, i, g, u);
     av[q] = silu_mul(g, u);
   }
   float m = fmaxf(fmaxf(fabsf(av[0]), fabsf(av[1])), fmaxf(fabsf(av[2]), fabsf(av[3])));
