@@ -33,7 +33,7 @@ namespace moe {
 namespace gg {
 
 constexpr int BM = kGemmBM;  // 128
-constexpr int BK = 64;       // bf16 elements per stage row = 128 bytes
+constexpr int BK = 64;       // bf16 elements per stage row = 128 bytes (e4m3: 128 elements)
 constexpr int BN = 256;
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
@@ -62,6 +62,11 @@ struct Params {
   int a_gather;          // Gate/Up: 1 = A rows gathered from x by tile::gather4, 0 = sorted rows
   __nv_bfloat16* out;
   DeviceHeader* hdr;
+  // e4m3 inputs (per-tensor scales)
+  const float* wscale;            // [E] scale of each expert's weight matrix
+  const unsigned int* amax_in;    // fp32 bits of the amax of the A operand's source (x or a)
+  unsigned int* amax_out;         // Gate/Up: receives the amax of a
+  float* out_f32;                 // Gate/Up: a [R, I] fp32 (quantised by the next pass)
 };
 
 __device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
@@ -75,10 +80,13 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
   return r;
 }
 
-template <int MODE>
+// F8: e4m3 operands (tcgen05 kind::f8f6f4, 128 K elements per 128-byte stage
+// row, per-tensor scales applied in the epilogue); otherwise bf16 (kind::f16).
+template <int MODE, bool F8>
 __global__ void __launch_bounds__(THREADS, 1)
-    grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                             const Params p) {
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const Params p) {
+  constexpr int BKE = F8 ? 128 : BK;  // K elements per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
@@ -118,7 +126,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int ntiles = min(*p.num_tiles, p.max_tiles);
   const int total = ntiles * p.nN;
-  const int nk = (p.K + BK - 1) / BK;
+  const int nk = (p.K + BKE - 1) / BKE;
   const int4* tiles = reinterpret_cast<const int4*>(p.tiles);
 
   if (warp == 0) {
@@ -152,7 +160,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
         const uint32_t a_dst = smem_u32(smem + stage * STAGE_BYTES);
         const uint32_t b_dst = a_dst + A_BYTES;
-        const int kc = kb * BK;
+        const int kc = kb * BKE;
         if (MODE == MODE_GATEUP) {
           if (p.a_gather)
             tma_gather4(a_dst + lane * 4 * 128, &tmA, kc, tok[0], tok[1], tok[2], tok[3], full);
@@ -185,7 +193,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = make_idesc(1, 1, BM, BN);
+      const uint32_t idesc = F8 ? make_idesc(0, 0, BM, BN) : make_idesc(1, 1, BM, BN);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
@@ -201,9 +209,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            mma_f16(d_tmem, sw128_kmajor_desc(a_addr + kk * 32), sw128_kmajor_desc(b_addr + kk * 32), idesc,
-                    (kb | kk) != 0);
+          for (int kk = 0; kk < 4; ++kk) {  // 4 x 32 bytes of K per stage: K=16 bf16 or K=32 e4m3 each
+            if (F8)
+              mma_f8(d_tmem, sw128_kmajor_desc(a_addr + kk * 32), sw128_kmajor_desc(b_addr + kk * 32), idesc,
+                     (kb | kk) != 0);
+            else
+              mma_f16(d_tmem, sw128_kmajor_desc(a_addr + kk * 32), sw128_kmajor_desc(b_addr + kk * 32), idesc,
+                      (kb | kk) != 0);
+          }
           mma_commit(empty0 + 8 * stage);
           if (++stage == STAGES) {
             stage = 0;
@@ -236,7 +249,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       if (MODE == MODE_GATEUP) {
+        // F8: a = silu(sc g) * (sc u) with sc = s_x * s_w1[e], kept in fp32 for the
+        // per-tensor quantisation of h, whose amax this epilogue also records
+        const float sc = F8 ? e4m3_scale(__uint_as_float(*p.amax_in)) * __ldg(p.wscale + tl.x) : 1.0f;
+        float amax = 0.0f;
         __nv_bfloat16* out_row = p.out + static_cast<size_t>(row0 + row) * p.out_ld;
+        float* out_row_f = F8 ? p.out_f32 + static_cast<size_t>(row0 + row) * p.out_ld : nullptr;
 #pragma unroll 1
         for (int c = 0; c < BN / 2; c += 32) {
           float g[32], up[32];
@@ -247,21 +265,41 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (row < nrows && col < p.n_valid) {
             float hv[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) hv[i] = silu_mul(g[i], up[i]);
-            uint4* dst = reinterpret_cast<uint4*>(out_row + col);
+            for (int i = 0; i < 32; ++i) hv[i] = F8 ? silu_mul(sc * g[i], sc * up[i]) : silu_mul(g[i], up[i]);
+            if (F8) {
+              float4* dst = reinterpret_cast<float4*>(out_row_f + col);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = pack_bf16x8(hv + 8 * i);
+              for (int i = 0; i < 8; ++i) {
+                dst[i] = make_float4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(hv[4 * i]), fabsf(hv[4 * i + 1])),
+                                         fmaxf(fabsf(hv[4 * i + 2]), fabsf(hv[4 * i + 3]))));
+              }
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(out_row + col);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) dst[i] = pack_bf16x8(hv + 8 * i);
+            }
           }
+        }
+        if (F8) {
+          amax = warp_max(amax);
+          if (lane == 0 && amax > 0.0f) atomicMax(p.amax_out, __float_as_uint(amax));
         }
       } else {
         const int slot = row < nrows ? __ldg(p.perm + row0 + row) : 0;
         __nv_bfloat16* out_row = p.out + static_cast<size_t>(slot) * p.out_ld;
+        // F8: o = s_h * s_w2[e] * acc
+        const float post = F8 ? e4m3_scale(__uint_as_float(*p.amax_in)) * __ldg(p.wscale + tl.x) : 1.0f;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           float v[32];
           tmem_ld32(tbase + c, v);
           tmem_ld_wait();
           const int col = n * BN + c;
+          if (F8) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= post;
+          }
           if (row < nrows && col < p.n_valid) {
             uint4* dst = reinterpret_cast<uint4*>(out_row + col);
 #pragma unroll
@@ -284,22 +322,23 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 static bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-                      uint32_t box_outer) {
+                      uint32_t box_outer, bool u8 = false) {
   EncodeTiledFn fn = get_encode_tiled();
   if (!fn) return false;
   const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint64_t strides[1] = {inner * (u8 ? 1 : 2)};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = fn(map, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+                  dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <int MODE>
+template <int MODE, bool F8>
 static cudaError_t set_smem_attr() {
-  static cudaError_t st = cudaFuncSetAttribute(grouped_gemm_bf16_kernel<MODE>,
+  static cudaError_t st = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, F8>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   return st;
 }
@@ -309,10 +348,10 @@ static cudaError_t set_smem_attr() {
 namespace gg {
 
 static cudaError_t prepare(const GroupedArgs& a, int* sms) {
-  cudaError_t e0 = set_smem_attr<MODE_GATEUP>();
-  if (e0 != cudaSuccess) return e0;
-  cudaError_t e1 = set_smem_attr<MODE_DOWN>();
-  if (e1 != cudaSuccess) return e1;
+  const cudaError_t e[4] = {set_smem_attr<MODE_GATEUP, false>(), set_smem_attr<MODE_DOWN, false>(),
+                            set_smem_attr<MODE_GATEUP, true>(), set_smem_attr<MODE_DOWN, true>()};
+  for (cudaError_t x : e)
+    if (x != cudaSuccess) return x;
   *sms = num_sms();
   return *sms > 0 ? cudaSuccess : cudaErrorNoDevice;
 }
@@ -325,6 +364,7 @@ static Params base_params(const GroupedArgs& a) {
   p.perm = a.perm;
   p.k = a.k;
   p.hdr = a.hdr;
+  p.wscale = a.w1_scale;
   return p;
 }
 
@@ -338,12 +378,17 @@ cudaError_t launch_gateup_bf16(const GroupedArgs& a, cudaStream_t s) {
   cudaError_t err = prepare(a, &sms);
   if (err != cudaSuccess) return err;
   CUtensorMap tmx, tmw1;
-  const bool gather = a.xs == nullptr;
-  if (!(gather ? encode_2d(&tmx, a.x, a.H, a.T, BK, 1) : encode_2d(&tmx, a.xs, a.H, a.R, BK, BM)) ||
-      !encode_2d(&tmw1, a.w1, a.H, static_cast<uint64_t>(a.E) * 2 * a.I, BK, BN / 2))
+  const bool gather = a.xs == nullptr && !a.f8;
+  const uint32_t bke = a.f8 ? 128 : BK;
+  if (!(gather ? encode_2d(&tmx, a.x, a.H, a.T, BK, 1) : encode_2d(&tmx, a.xs, a.H, a.R, bke, BM, a.f8)) ||
+      !encode_2d(&tmw1, a.w1, a.H, static_cast<uint64_t>(a.E) * 2 * a.I, bke, BN / 2, a.f8))
     return cudaErrorInvalidValue;
   Params p = base_params(a);
   p.a_gather = gather ? 1 : 0;
+  p.wscale = a.w1_scale;
+  p.amax_in = &a.hdr->amax_x;
+  p.amax_out = &a.hdr->amax_h;
+  p.out_f32 = static_cast<float*>(a.a_f32);
   p.nN = (a.I + BN / 2 - 1) / (BN / 2);
   p.K = a.H;
   p.b_rows_per_expert = 2 * a.I;
@@ -354,7 +399,10 @@ cudaError_t launch_gateup_bf16(const GroupedArgs& a, cudaStream_t s) {
   const long long units = static_cast<long long>(a.max_tiles) * p.nN;
   const int grid = static_cast<int>(units < sms ? units : sms);
   stage_begin("gateup_gemm", s);
-  grouped_gemm_bf16_kernel<MODE_GATEUP><<<grid, THREADS, SMEM_BYTES, s>>>(tmx, tmw1, p);
+  if (a.f8)
+    grouped_gemm_kernel<MODE_GATEUP, true><<<grid, THREADS, SMEM_BYTES, s>>>(tmx, tmw1, p);
+  else
+    grouped_gemm_kernel<MODE_GATEUP, false><<<grid, THREADS, SMEM_BYTES, s>>>(tmx, tmw1, p);
   err = cudaGetLastError();
   stage_end(s);
   return err;
@@ -368,10 +416,13 @@ cudaError_t launch_down_bf16(const GroupedArgs& a, cudaStream_t s) {
   cudaError_t err = prepare(a, &sms);
   if (err != cudaSuccess) return err;
   CUtensorMap tmh, tmw2;
-  if (!encode_2d(&tmh, a.h, a.I, a.R, BK, BM) ||
-      !encode_2d(&tmw2, a.w2, a.I, static_cast<uint64_t>(a.E) * a.H, BK, BN))
+  const uint32_t bke = a.f8 ? 128 : BK;
+  if (!encode_2d(&tmh, a.h, a.I, a.R, bke, BM, a.f8) ||
+      !encode_2d(&tmw2, a.w2, a.I, static_cast<uint64_t>(a.E) * a.H, bke, BN, a.f8))
     return cudaErrorInvalidValue;
   Params p = base_params(a);
+  p.wscale = a.w2_scale;
+  p.amax_in = &a.hdr->amax_h;
   p.nN = (a.H + BN - 1) / BN;
   p.K = a.I;
   p.b_rows_per_expert = a.H;
@@ -382,7 +433,10 @@ cudaError_t launch_down_bf16(const GroupedArgs& a, cudaStream_t s) {
   const long long units = static_cast<long long>(a.max_tiles) * p.nN;
   const int grid = static_cast<int>(units < sms ? units : sms);
   stage_begin("down_gemm", s);
-  grouped_gemm_bf16_kernel<MODE_DOWN><<<grid, THREADS, SMEM_BYTES, s>>>(tmh, tmw2, p);
+  if (a.f8)
+    grouped_gemm_kernel<MODE_DOWN, true><<<grid, THREADS, SMEM_BYTES, s>>>(tmh, tmw2, p);
+  else
+    grouped_gemm_kernel<MODE_DOWN, false><<<grid, THREADS, SMEM_BYTES, s>>>(tmh, tmw2, p);
   err = cudaGetLastError();
   stage_end(s);
   return err;

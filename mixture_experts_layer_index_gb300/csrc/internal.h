@@ -44,8 +44,9 @@ struct ForwardLayout {
   size_t counts = 0, offsets = 0, perm = 0, inv = 0;
   size_t tiles = 0, num_tiles = 0;
   int max_tiles = 0;
-  size_t xs = 0;      // grouped: [R, H] bf16 x rows in sorted order (Gate/Up A operand)
-  size_t h = 0;       // grouped: [R, I] bf16 (sorted order)
+  size_t xs = 0;      // grouped: [R, H] x rows in sorted order (Gate/Up A operand; bf16 or e4m3)
+  size_t a32 = 0;     // grouped FP8: [R, I] fp32 a before its per-tensor quantisation
+  size_t h = 0;       // grouped: [R, I] h in sorted order (bf16 or e4m3)
   size_t o = 0;       // grouped: [R, H] bf16 (route order); route-direct: [R, H] fp32
   // route-direct
   size_t xq = 0;      // [T, H] e4m3
@@ -73,6 +74,12 @@ cudaError_t launch_scatter(const int32_t* ids, const int32_t* lrank, const int32
 cudaError_t launch_scatter_gather(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
                                   int k, int H, const void* x, void* xs, int32_t* perm, int32_t* inv,
                                   cudaStream_t s);
+// Per-tensor e4m3 passes of the grouped FP8 path (quant.cu).
+cudaError_t launch_x_amax(const void* x, size_t n, DeviceHeader* hdr, cudaStream_t s);
+cudaError_t launch_scatter_gather_q(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
+                                    int k, int H, const void* x, void* xs, int32_t* perm, int32_t* inv,
+                                    const DeviceHeader* hdr, cudaStream_t s);
+cudaError_t launch_quant_rows(const float* a, void* h, size_t n, const DeviceHeader* hdr, cudaStream_t s);
 cudaError_t launch_tile_map(const int32_t* counts, int E, int BM, int32_t* tiles, int32_t* num_tiles,
                             int max_tiles, int32_t* tile_scratch, DeviceHeader* hdr, cudaStream_t s);
 cudaError_t launch_reset_header(DeviceHeader* hdr, cudaStream_t s);
@@ -88,11 +95,16 @@ struct GroupedArgs {
   const int32_t* tiles;
   const int32_t* num_tiles;
   int max_tiles;
-  void* h;
+  void* h;               // Down A operand: bf16 h, or e4m3 h (f8)
   void* o;
   DeviceHeader* hdr;
+  // per-tensor FP8 (e4m3 operands): xs/h hold e4m3 codes, x's and a's amax live in hdr
+  bool f8;
+  const float* w1_scale;
+  const float* w2_scale;
+  void* a_f32;           // Gate/Up output a [R, I] fp32 (f8)
 };
-cudaError_t launch_gateup_bf16(const GroupedArgs& a, cudaStream_t s);
+cudaError_t launch_gateup_bf16(const GroupedArgs& a, cudaStream_t s);  // bf16 or e4m3 (a.f8)
 cudaError_t launch_down_bf16(const GroupedArgs& a, cudaStream_t s);
 
 struct CombineArgs {

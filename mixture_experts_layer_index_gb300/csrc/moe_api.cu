@@ -136,9 +136,15 @@ ShuffleLayout plan_shuffle(int T, int E, int k, size_t base) {
   return L;
 }
 
+// Largest T for which AUTO takes the route-direct path with per-tensor FP8
+// weights (beyond it, the grouped path).
+constexpr int kAutoRouteDirectMaxTokens = 32;
+
 static moe_path resolve_path(const moe_problem& p) {
   if (p.path != MOE_PATH_AUTO) return p.path;
-  return p.quant == MOE_BF16 ? MOE_PATH_GROUPED : MOE_PATH_ROUTE_DIRECT;
+  if (p.quant == MOE_BF16) return MOE_PATH_GROUPED;
+  if (p.quant == MOE_FP8_PER_TENSOR && p.T > kAutoRouteDirectMaxTokens) return MOE_PATH_GROUPED;
+  return MOE_PATH_ROUTE_DIRECT;
 }
 
 // Number of K splits of the route-direct Gate/Up: enough CTAs to cover about
@@ -172,7 +178,7 @@ static moe_status validate_shape(const moe_problem& p) {
     if (p.H % 128 || p.I % 128) return MOE_ERR_UNSUPPORTED;
   }
   const moe_path path = resolve_path(p);
-  if (path == MOE_PATH_GROUPED && p.quant != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (path == MOE_PATH_GROUPED && p.quant == MOE_FP8_BLOCK128) return MOE_ERR_UNSUPPORTED;
   if (path == MOE_PATH_ROUTE_DIRECT) {
     if (p.quant == MOE_BF16) return MOE_ERR_UNSUPPORTED;
     if (static_cast<long long>(p.T) * p.k > kRouteDirectMaxRoutes) return MOE_ERR_UNSUPPORTED;
@@ -204,8 +210,10 @@ bool plan_forward(const moe_problem& p, ForwardLayout* out) {
     L.max_tiles = static_cast<int>(R / kGemmBM + E);
     L.tiles = take(static_cast<size_t>(L.max_tiles) * 16);
     L.num_tiles = take(16);
-    L.xs = take(R * H * 2);
-    L.h = take(R * I * 2);
+    const size_t eb = p.quant == MOE_BF16 ? 2 : 1;  // bytes per element of the GEMM inputs
+    L.xs = take(R * H * eb);
+    if (p.quant != MOE_BF16) L.a32 = take(R * I * 4);
+    L.h = take(R * I * eb);
     L.o = take(R * H * 2);
   } else {
     L.splits = route_direct_splits(p);
@@ -373,10 +381,14 @@ moe_status moe_forward(const moe_problem* pp, const void* x, const float* scores
     if (e == cudaSuccess)
       e = launch_scan_tiles(bc, L.shuf.nblk, p.E, counts, offsets, tiles, num_tiles, L.max_tiles, kGemmBM, nullptr,
                             hdr, s);
-    const bool gather4 = gateup_gather4();
+    const bool f8 = p.quant == MOE_FP8_PER_TENSOR;
+    const bool gather4 = !f8 && gateup_gather4();
     void* xs = at<void*>(ws, L.xs);
+    if (e == cudaSuccess && f8) e = launch_x_amax(x, static_cast<size_t>(p.T) * p.H, hdr, s);
     if (e == cudaSuccess) {
-      if (gather4)
+      if (f8)
+        e = launch_scatter_gather_q(ids, lrank, bc, p.T, p.E, p.k, p.H, x, xs, perm, inv, hdr, s);
+      else if (gather4)
         e = launch_scatter(ids, lrank, bc, p.T, p.E, p.k, perm, inv, s);
       else
         e = launch_scatter_gather(ids, lrank, bc, p.T, p.E, p.k, p.H, x, xs, perm, inv, s);
@@ -385,12 +397,18 @@ moe_status moe_forward(const moe_problem* pp, const void* x, const float* scores
       GroupedArgs g{};
       g.T = p.T; g.E = p.E; g.k = p.k; g.H = p.H; g.I = p.I; g.R = p.T * p.k;
       g.x = x; g.w1 = w1; g.w2 = w2;
+      g.f8 = f8;
+      g.w1_scale = w1_scale;
+      g.w2_scale = w2_scale;
+      g.a_f32 = f8 ? at<void*>(ws, L.a32) : nullptr;
       g.xs = gather4 ? nullptr : xs;
       g.perm = perm; g.tiles = tiles; g.num_tiles = num_tiles; g.max_tiles = L.max_tiles;
       g.h = at<void*>(ws, L.h);
       g.o = at<void*>(ws, L.o);
       g.hdr = hdr;
       e = launch_gateup_bf16(g, s);
+      if (e == cudaSuccess && f8)
+        e = launch_quant_rows(static_cast<const float*>(g.a_f32), g.h, static_cast<size_t>(g.R) * p.I, hdr, s);
       if (e == cudaSuccess) e = launch_down_bf16(g, s);
     }
     if (e == cudaSuccess) {

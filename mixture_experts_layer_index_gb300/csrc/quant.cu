@@ -1,0 +1,136 @@
+// Per-tensor e4m3 quantisation passes of the grouped FP8 path ("perf: add
+// small-batch route MMA for MoE", Summary: per-tensor FP8 with dynamic
+// activation scales): the amax of x, the expert-sorted copy of x quantised with
+// s_x = amax/448, and the quantisation of a (the SwiGLU output) with its global
+// scale s_h.  Scales: amax / 448 in fp32 (1 when amax == 0); codes: round to
+// nearest even with saturation (cvt.rn.satfinite).
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// amax |x| over n bf16 values into hdr->amax_x (fp32 bits; non-negative floats
+// order like their bit patterns).  Loads go out 8 x 16 bytes per thread at a time.
+__global__ void __launch_bounds__(256) x_amax_kernel(const uint4* __restrict__ x, size_t n8, DeviceHeader* hdr) {
+  float m = 0.0f;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t base = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; base < n8; base += stride * 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const size_t i = base + j * stride;
+      v[j] = i < n8 ? __ldg(x + i) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v[j]);
+#pragma unroll
+      for (int h2 = 0; h2 < 4; ++h2) {
+        const float2 f = __bfloat1622float2(b[h2]);
+        m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+  }
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0 && m > 0.0f) atomicMax(&hdr->amax_x, __float_as_uint(m));
+}
+
+// Scatter fused with the gather and quantisation of the activations: one warp
+// per route writes perm/inv and the route's x row, quantised with s_x, to sorted
+// row p of xs (H bytes per row).
+__global__ void __launch_bounds__(256) scatter_gather_q_kernel(const int32_t* __restrict__ ids,
+                                                               const int32_t* __restrict__ lrank,
+                                                               const int32_t* __restrict__ blockbase, int R, int E,
+                                                               int RB, int k, int H, const uint4* __restrict__ x,
+                                                               uint4* __restrict__ xs, int32_t* __restrict__ perm,
+                                                               int32_t* __restrict__ inv, const DeviceHeader* hdr) {
+  const int lane = threadIdx.x & 31;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  const float s = e4m3_scale(__uint_as_float(hdr->amax_x));
+  const int row16 = H / 16;  // 16 codes (16 bytes out, 32 bytes in) per chunk
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < R; r += nw) {
+    const int lr = lrank[r];
+    if (lr < 0) {
+      if (lane == 0) inv[r] = -1;
+      continue;
+    }
+    const int e = ids[r];
+    const int p = blockbase[static_cast<size_t>(r / RB) * E + e] + lr;
+    if (lane == 0) {
+      perm[p] = r;
+      inv[r] = p;
+    }
+    const uint4* src = x + static_cast<size_t>(r / k) * (H / 8);
+    uint4* dst = xs + static_cast<size_t>(p) * row16;
+    for (int c = lane; c < row16; c += 32) {
+      const uint4 a = __ldg(src + 2 * c), b = __ldg(src + 2 * c + 1);
+      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+      uint32_t q[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const __nv_bfloat162* pp = j < 2 ? pa : pb;
+        const float2 f0 = __bfloat1622float2(pp[(j & 1) * 2]), f1 = __bfloat1622float2(pp[(j & 1) * 2 + 1]);
+        q[j] = static_cast<uint32_t>(cvt_e4m3x2(f0.x / s, f0.y / s)) |
+               (static_cast<uint32_t>(cvt_e4m3x2(f1.x / s, f1.y / s)) << 16);
+      }
+      dst[c] = make_uint4(q[0], q[1], q[2], q[3]);
+    }
+  }
+}
+
+// h = e4m3(a / s_h), s_h = e4m3_scale(amax of a); 4 values per thread-iteration.
+__global__ void __launch_bounds__(256) quant_rows_kernel(const float4* __restrict__ a, uint32_t* __restrict__ h,
+                                                         size_t n4, const DeviceHeader* hdr) {
+  const float s = e4m3_scale(__uint_as_float(hdr->amax_h));
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4; i += stride) {
+    const float4 v = __ldg(a + i);
+    h[i] = static_cast<uint32_t>(cvt_e4m3x2(v.x / s, v.y / s)) | (static_cast<uint32_t>(cvt_e4m3x2(v.z / s, v.w / s)) << 16);
+  }
+}
+
+static unsigned grid_for(size_t work, unsigned per_block) {
+  const int sms = num_sms();
+  const size_t cap = static_cast<size_t>(sms > 0 ? sms : 148) * 16;
+  size_t b = (work + per_block - 1) / per_block;
+  if (b > cap) b = cap;
+  return static_cast<unsigned>(b < 1 ? 1 : b);
+}
+
+cudaError_t launch_x_amax(const void* x, size_t n, DeviceHeader* hdr, cudaStream_t s) {
+  const size_t n8 = n / 8;
+  if (n8 == 0) return cudaSuccess;
+  stage_begin("x_amax", s);
+  x_amax_kernel<<<grid_for(n8, 256 * 8), 256, 0, s>>>(static_cast<const uint4*>(x), n8, hdr);
+  const cudaError_t err = cudaGetLastError();
+  stage_end(s);
+  return err;
+}
+
+cudaError_t launch_scatter_gather_q(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
+                                    int k, int H, const void* x, void* xs, int32_t* perm, int32_t* inv,
+                                    const DeviceHeader* hdr, cudaStream_t s) {
+  const int R = T * k;
+  if (R <= 0) return cudaSuccess;
+  const int RB = route_tokens_per_block(k) * k;
+  stage_begin("scatter_gather", s);
+  scatter_gather_q_kernel<<<grid_for(static_cast<size_t>(R) * 32, 256), 256, 0, s>>>(
+      ids, lrank, blockbase, R, E, RB, k, H, static_cast<const uint4*>(x), static_cast<uint4*>(xs), perm, inv, hdr);
+  const cudaError_t err = cudaGetLastError();
+  stage_end(s);
+  return err;
+}
+
+cudaError_t launch_quant_rows(const float* a, void* h, size_t n, const DeviceHeader* hdr, cudaStream_t s) {
+  const size_t n4 = n / 4;
+  if (n4 == 0) return cudaSuccess;
+  stage_begin("quant_h", s);
+  quant_rows_kernel<<<grid_for(n4, 256), 256, 0, s>>>(reinterpret_cast<const float4*>(a), static_cast<uint32_t*>(h),
+                                                      n4, hdr);
+  const cudaError_t err = cudaGetLastError();
+  stage_end(s);
+  return err;
+}
+
+}  // namespace moe
