@@ -91,7 +91,7 @@ typedef struct {
  *   1 <= E <= 512;  1 <= k <= min(E, 32);  0 <= T;  T*k < 2^31;
  *   H % 64 == 0, I % 64 == 0 (bf16);  H % 128 == 0, I % 64 == 0 (FP8 per-tensor);
  *   H % 128 == 0, I % 128 == 0 (FP8 blockwise);
- *   MOE_PATH_GROUPED: bf16 and per-tensor FP8;  MOE_PATH_ROUTE_DIRECT: FP8 only, T*k <= 1024. */
+ *   MOE_PATH_GROUPED: all three modes;  MOE_PATH_ROUTE_DIRECT: FP8 only, T*k <= 1024. */
 
 /* ---------------------------------------------------------------- routing
  * moe_route - top-k routing (the routing step of "perf: add small-batch route
@@ -167,8 +167,8 @@ moe_status moe_tile_map(const int32_t* counts, int E, int BM, int32_t* tiles, in
 
 /* ---------------------------------------------------------------- forward
  * moe_select_path - the path moe_forward takes for *p (AUTO resolved):
- * bf16 -> GROUPED; per-tensor FP8 -> ROUTE_DIRECT for T <= 32, else GROUPED;
- * blockwise FP8 -> ROUTE_DIRECT.  Returns p->path when it is not AUTO. */
+ * bf16 -> GROUPED; FP8 (per-tensor or blockwise) -> ROUTE_DIRECT for T <= 32,
+ * else GROUPED.  Returns p->path when it is not AUTO. */
 moe_path moe_select_path(const moe_problem* p);
 
 /* moe_workspace_size - bytes of device workspace moe_forward needs for *p

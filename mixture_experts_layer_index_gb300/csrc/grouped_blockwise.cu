@@ -1,0 +1,361 @@
+// Grouped GEMMs for 128x128-blockwise FP8 ("perf: add small-batch route MMA for
+// MoE", Summary: 128x128 blockwise FP8; the grouped path of its Motivation).
+//
+// The weights carry one fp32 scale per 128x128 block and the activations one
+// per (row, 128 columns), so every 128-wide K block has its own scale pair and
+// the products cannot be summed inside one accumulator.  Each K block is a
+// 128-byte stage of e4m3: the MMA thread writes that block's partial product
+// (tcgen05.mma kind::f8f6f4, M=128, N=128, 4 x K=32) into one of two TMEM
+// buffers, and the epilogue warps (one accumulator row per thread) read it with
+// tcgen05.ld, multiply by s_a[row, kb] * s_w[block, kb] and add it into fp32
+// registers ("promotion"), while the MMA fills the other buffer.
+//
+// Gate/Up: N = 64 gate + the matching 64 up rows of W1[e] (two 64-row TMA
+//   boxes), A = expert-sorted e4m3 x rows with their group scales; the epilogue
+//   writes a = silu(g) * u (fp32, sorted rows, 64 columns per tile); a separate
+//   pass quantises a per (row, 128 columns).
+// Down: N = 128 rows of W2[e] (one weight scale block), A = e4m3 h rows with
+//   their group scales; the epilogue writes bf16 o to route slot perm[p].
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace gb {
+
+constexpr int BM = kGemmBM;  // 128
+constexpr int BN = 128;
+constexpr int BKB = 128;  // K bytes (= e4m3 elements) per stage, one scale block
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BKB;
+constexpr int B_BYTES = BN * BKB;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 256;  // two partial buffers of 128 columns
+constexpr int THREADS = 256;
+constexpr int NUM_BARS = 2 * STAGES + 4;
+constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+
+constexpr int MODE_GATEUP = 0;
+constexpr int MODE_DOWN = 1;
+
+struct Params {
+  const int32_t* tiles;
+  const int32_t* num_tiles;
+  int max_tiles;
+  const int32_t* perm;
+  int nN;          // N tiles per row tile
+  int K;           // reduction length (bytes = elements)
+  int I, H;
+  const float* a_scale;  // [R][K/128] scales of the A rows (sorted order)
+  const float* w_scale;  // Gate/Up: [E][2I/128][H/128]; Down: [E][H/128][I/128]
+  float* out_f32;        // Gate/Up: a [R][I]
+  __nv_bfloat16* out;    // Down: o [R][H]
+  DeviceHeader* hdr;
+};
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
+  uint4 r;
+  uint32_t* w = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t*>(&b);
+  }
+  return r;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_blockwise_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                             const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
+  const uint32_t pfull0 = smem_u32(bars + 2 * STAGES), pempty0 = smem_u32(bars + 2 * STAGES + 2);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(pfull0 + 8 * b, 1);
+      mbar_init(pempty0 + 8 * b, 128);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int ntiles = min(*p.num_tiles, p.max_tiles);
+  const int total = ntiles * p.nN;
+  const int nk = (p.K + BKB - 1) / BKB;
+  const int4* tiles = reinterpret_cast<const int4*>(p.tiles);
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    uint32_t stage = 0, phase = 0;
+    int issued = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const int tile = u / p.nN, n = u - (u / p.nN) * p.nN;
+      const int4 tl = tiles[tile];
+      const int e = tl.x, row0 = tl.y;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (lane == 0) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.hdr, 0x80000u | MODE)) ok = false;
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        if (lane == 0) {
+          const uint32_t full = full0 + 8 * stage;
+          const uint32_t a_dst = smem_u32(smem + stage * STAGE_BYTES), b_dst = a_dst + A_BYTES;
+          const int kc = kb * BKB;
+          mbar_arrive_expect_tx(full, STAGE_BYTES);
+          tma_load_2d(a_dst, &tmA, kc, row0, full);
+          if (MODE == MODE_GATEUP) {
+            const int brow = e * 2 * p.I + n * (BN / 2);
+            tma_load_2d(b_dst, &tmB, kc, brow, full);                   // 64 gate rows
+            tma_load_2d(b_dst + B_BYTES / 2, &tmB, kc, brow + p.I, full);  // the matching 64 up rows
+          } else {
+            tma_load_2d(b_dst, &tmB, kc, e * p.H + n * BN, full);
+          }
+        }
+        __syncwarp();
+        ++issued;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      for (int i = 0; i < min(issued, STAGES); ++i) {
+        stage = (stage + STAGES - 1) % STAGES;
+        if (stage == STAGES - 1) phase ^= 1;
+        mbar_wait_quiet(full0 + 8 * stage, phase, 50000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = make_idesc(0, 0, BM, BN);
+      uint32_t stage = 0, phase = 0, pb = 0, pphase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.hdr, 0x81000u | MODE) ||
+              !mbar_wait(pempty0 + 8 * pb, pphase ^ 1, abort_flag, p.hdr, 0x82000u | MODE)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES), b_addr = a_addr + A_BYTES;
+          const uint32_t d_tmem = tmem_base + pb * BN;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // a fresh partial for this K block
+            mma_f8(d_tmem, sw128_kmajor_desc(a_addr + kk * 32), sw128_kmajor_desc(b_addr + kk * 32), idesc, kk != 0);
+          mma_commit(empty0 + 8 * stage);
+          mma_commit(pfull0 + 8 * pb);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+          pb ^= 1;
+          if (pb == 0) pphase ^= 1;
+        }
+      }
+      // wait for every MMA issued by this thread before TMEM is released
+      const uint32_t last = pfull0 + 8 * (pb ^ 1);
+      mbar_wait_quiet(last, pb == 0 ? (pphase ^ 1) : pphase, 1000000000ull);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- epilogue (promotion)
+    const int q = warp - 4;
+    const int row = q * 32 + lane;
+    uint32_t pb = 0, pphase = 0;
+    const int kblocks = p.K / 128;  // scale groups along K (K is a multiple of 128)
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const int tile = u / p.nN, n = u - (u / p.nN) * p.nN;
+      const int4 tl = tiles[tile];
+      const int e = tl.x, row0 = tl.y, nrows = tl.z;
+      const int arow = row0 + min(row, nrows - 1);
+      const float* sa = p.a_scale + static_cast<size_t>(arow) * kblocks;
+      // weight scale rows of this tile's columns
+      const float* swg;
+      const float* swu;
+      if (MODE == MODE_GATEUP) {
+        const int nblk = 2 * p.I / 128, hblk = p.H / 128;
+        swg = p.w_scale + (static_cast<size_t>(e) * nblk + (n * (BN / 2)) / 128) * hblk;
+        swu = p.w_scale + (static_cast<size_t>(e) * nblk + (p.I + n * (BN / 2)) / 128) * hblk;
+      } else {
+        const int hblk = p.H / 128, iblk = p.I / 128;
+        swg = p.w_scale + (static_cast<size_t>(e) * hblk + n) * iblk;
+        swu = swg;
+      }
+      float acc[BN];
+#pragma unroll
+      for (int i = 0; i < BN; ++i) acc[i] = 0.0f;
+      float sa_next = __ldg(sa), sg_next = __ldg(swg), su_next = __ldg(swu);
+      for (int kb = 0; kb < nk; ++kb) {
+        const float sak = sa_next, sgk = sg_next, suk = su_next;
+        if (kb + 1 < nk) {
+          sa_next = __ldg(sa + kb + 1);
+          sg_next = __ldg(swg + kb + 1);
+          su_next = __ldg(swu + kb + 1);
+        }
+        int good = 1;
+        if (lane == 0) good = mbar_wait(pfull0 + 8 * pb, pphase, abort_flag, p.hdr, 0x83000u | MODE);
+        if (!__shfl_sync(0xffffffffu, good, 0)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + pb * BN;
+        const float s0 = sak * sgk, s1 = sak * suk;
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(tbase + c * 32, v);
+          tmem_ld_wait();
+          const float sc = (MODE == MODE_GATEUP && c >= 2) ? s1 : s0;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(v[i], sc, acc[c * 32 + i]);
+        }
+        tc_fence_before();
+        mbar_arrive(pempty0 + 8 * pb);
+        pb ^= 1;
+        if (pb == 0) pphase ^= 1;
+      }
+      if (!ok) break;
+      if (row < nrows) {
+        if (MODE == MODE_GATEUP) {
+          float* dst = p.out_f32 + static_cast<size_t>(row0 + row) * p.I + n * (BN / 2);
+#pragma unroll
+          for (int i = 0; i < BN / 2; i += 4) {
+            const float4 a4 = make_float4(silu_mul(acc[i], acc[BN / 2 + i]), silu_mul(acc[i + 1], acc[BN / 2 + i + 1]),
+                                          silu_mul(acc[i + 2], acc[BN / 2 + i + 2]),
+                                          silu_mul(acc[i + 3], acc[BN / 2 + i + 3]));
+            if (n * (BN / 2) + i < p.I) *reinterpret_cast<float4*>(dst + i) = a4;
+          }
+        } else {
+          const int slot = __ldg(p.perm + row0 + row);
+          __nv_bfloat16* dst = p.out + static_cast<size_t>(slot) * p.H + n * BN;
+#pragma unroll
+          for (int i = 0; i < BN; i += 8)
+            if (n * BN + i < p.H) *reinterpret_cast<uint4*>(dst + i) = pack_bf16x8(acc + i);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+static bool encode_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_rows) {
+  EncodeTiledFn fn = get_encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(BKB), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE>
+static cudaError_t smem_attr() {
+  static const cudaError_t st = cudaFuncSetAttribute(grouped_blockwise_kernel<MODE>,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+  return st;
+}
+
+}  // namespace gb
+
+cudaError_t launch_gateup_blockwise(const GroupedArgs& a, const float* xs_scale, cudaStream_t s) {
+  using namespace gb;
+  if (a.R <= 0) return cudaSuccess;
+  cudaError_t err = smem_attr<MODE_GATEUP>();
+  if (err != cudaSuccess) return err;
+  const int sms = num_sms();
+  if (sms <= 0) return cudaErrorNoDevice;
+  CUtensorMap tma, tmb;
+  if (!encode_u8(&tma, a.xs, a.H, a.R, BM) || !encode_u8(&tmb, a.w1, a.H, static_cast<uint64_t>(a.E) * 2 * a.I, BN / 2))
+    return cudaErrorInvalidValue;
+  Params p{};
+  p.tiles = a.tiles;
+  p.num_tiles = a.num_tiles;
+  p.max_tiles = a.max_tiles;
+  p.perm = a.perm;
+  p.nN = a.I / (BN / 2);
+  p.K = a.H;
+  p.I = a.I;
+  p.H = a.H;
+  p.a_scale = xs_scale;
+  p.w_scale = a.w1_scale;
+  p.out_f32 = static_cast<float*>(a.a_f32);
+  p.hdr = a.hdr;
+  const long long units = static_cast<long long>(a.max_tiles) * p.nN;
+  const int grid = static_cast<int>(units < sms ? units : sms);
+  stage_begin("gateup_gemm", s);
+  grouped_blockwise_kernel<MODE_GATEUP><<<grid, THREADS, SMEM_BYTES, s>>>(tma, tmb, p);
+  err = cudaGetLastError();
+  stage_end(s);
+  return err;
+}
+
+cudaError_t launch_down_blockwise(const GroupedArgs& a, const float* h_scale, cudaStream_t s) {
+  using namespace gb;
+  if (a.R <= 0) return cudaSuccess;
+  cudaError_t err = smem_attr<MODE_DOWN>();
+  if (err != cudaSuccess) return err;
+  const int sms = num_sms();
+  if (sms <= 0) return cudaErrorNoDevice;
+  CUtensorMap tma, tmb;
+  if (!encode_u8(&tma, a.h, a.I, a.R, BM) || !encode_u8(&tmb, a.w2, a.I, static_cast<uint64_t>(a.E) * a.H, BN))
+    return cudaErrorInvalidValue;
+  Params p{};
+  p.tiles = a.tiles;
+  p.num_tiles = a.num_tiles;
+  p.max_tiles = a.max_tiles;
+  p.perm = a.perm;
+  p.nN = a.H / BN;
+  p.K = a.I;
+  p.I = a.I;
+  p.H = a.H;
+  p.a_scale = h_scale;
+  p.w_scale = a.w2_scale;
+  p.out = static_cast<__nv_bfloat16*>(a.o);
+  p.hdr = a.hdr;
+  const long long units = static_cast<long long>(a.max_tiles) * p.nN;
+  const int grid = static_cast<int>(units < sms ? units : sms);
+  stage_begin("down_gemm", s);
+  grouped_blockwise_kernel<MODE_DOWN><<<grid, THREADS, SMEM_BYTES, s>>>(tma, tmb, p);
+  err = cudaGetLastError();
+  stage_end(s);
+  return err;
+}
+
+}  // namespace moe

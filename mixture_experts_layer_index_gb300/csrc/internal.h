@@ -45,7 +45,8 @@ struct ForwardLayout {
   size_t tiles = 0, num_tiles = 0;
   int max_tiles = 0;
   size_t xs = 0;      // grouped: [R, H] x rows in sorted order (Gate/Up A operand; bf16 or e4m3)
-  size_t a32 = 0;     // grouped FP8: [R, I] fp32 a before its per-tensor quantisation
+  size_t xs_scale = 0;  // grouped blockwise FP8: [R, H/128] fp32 scales of xs
+  size_t a32 = 0;     // grouped FP8: [R, I] fp32 a before its quantisation
   size_t h = 0;       // grouped: [R, I] h in sorted order (bf16 or e4m3)
   size_t o = 0;       // grouped: [R, H] bf16 (route order); route-direct: [R, H] fp32
   // route-direct
@@ -54,7 +55,7 @@ struct ForwardLayout {
   size_t uniq = 0;    // unique-expert table (see decode.cu)
   size_t part = 0;    // [S, R, 2I] fp32 split-K partials of Gate/Up
   size_t act = 0;     // per-tensor: [R, I] fp32 a;  blockwise: [R, I] e4m3 h
-  size_t sh = 0;      // blockwise: [R, I/128] fp32 scales of h
+  size_t sh = 0;      // blockwise (both paths): [R, I/128] fp32 scales of h
   int splits = 1;
   size_t total = 0;
 };
@@ -80,6 +81,11 @@ cudaError_t launch_scatter_gather_q(const int32_t* ids, const int32_t* lrank, co
                                     int k, int H, const void* x, void* xs, int32_t* perm, int32_t* inv,
                                     const DeviceHeader* hdr, cudaStream_t s);
 cudaError_t launch_quant_rows(const float* a, void* h, size_t n, const DeviceHeader* hdr, cudaStream_t s);
+// Blockwise (one scale per row and 128 columns) passes of the grouped FP8 path (quant.cu).
+cudaError_t launch_scatter_gather_qb(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
+                                     int k, int H, const void* x, void* xs, float* xs_scale, int32_t* perm,
+                                     int32_t* inv, cudaStream_t s);
+cudaError_t launch_quant_groups(const float* a, void* h, float* sh, int rows, int cols, cudaStream_t s);
 cudaError_t launch_tile_map(const int32_t* counts, int E, int BM, int32_t* tiles, int32_t* num_tiles,
                             int max_tiles, int32_t* tile_scratch, DeviceHeader* hdr, cudaStream_t s);
 cudaError_t launch_reset_header(DeviceHeader* hdr, cudaStream_t s);
@@ -106,6 +112,10 @@ struct GroupedArgs {
 };
 cudaError_t launch_gateup_bf16(const GroupedArgs& a, cudaStream_t s);  // bf16 or e4m3 (a.f8)
 cudaError_t launch_down_bf16(const GroupedArgs& a, cudaStream_t s);
+// 128x128-blockwise FP8 grouped GEMMs (grouped_blockwise.cu): xs / h hold e4m3
+// codes, their scales [R, H/128] / [R, I/128] in sorted row order.
+cudaError_t launch_gateup_blockwise(const GroupedArgs& a, const float* xs_scale, cudaStream_t s);
+cudaError_t launch_down_blockwise(const GroupedArgs& a, const float* h_scale, cudaStream_t s);
 
 struct CombineArgs {
   int T, k, H;

@@ -143,7 +143,7 @@ constexpr int kAutoRouteDirectMaxTokens = 32;
 static moe_path resolve_path(const moe_problem& p) {
   if (p.path != MOE_PATH_AUTO) return p.path;
   if (p.quant == MOE_BF16) return MOE_PATH_GROUPED;
-  if (p.quant == MOE_FP8_PER_TENSOR && p.T > kAutoRouteDirectMaxTokens) return MOE_PATH_GROUPED;
+  if (p.T > kAutoRouteDirectMaxTokens) return MOE_PATH_GROUPED;
   return MOE_PATH_ROUTE_DIRECT;
 }
 
@@ -178,7 +178,6 @@ static moe_status validate_shape(const moe_problem& p) {
     if (p.H % 128 || p.I % 128) return MOE_ERR_UNSUPPORTED;
   }
   const moe_path path = resolve_path(p);
-  if (path == MOE_PATH_GROUPED && p.quant == MOE_FP8_BLOCK128) return MOE_ERR_UNSUPPORTED;
   if (path == MOE_PATH_ROUTE_DIRECT) {
     if (p.quant == MOE_BF16) return MOE_ERR_UNSUPPORTED;
     if (static_cast<long long>(p.T) * p.k > kRouteDirectMaxRoutes) return MOE_ERR_UNSUPPORTED;
@@ -212,8 +211,10 @@ bool plan_forward(const moe_problem& p, ForwardLayout* out) {
     L.num_tiles = take(16);
     const size_t eb = p.quant == MOE_BF16 ? 2 : 1;  // bytes per element of the GEMM inputs
     L.xs = take(R * H * eb);
+    if (p.quant == MOE_FP8_BLOCK128) L.xs_scale = take(R * (H / 128) * 4);
     if (p.quant != MOE_BF16) L.a32 = take(R * I * 4);
     L.h = take(R * I * eb);
+    if (p.quant == MOE_FP8_BLOCK128) L.sh = take(R * (I / 128) * 4);
     L.o = take(R * H * 2);
   } else {
     L.splits = route_direct_splits(p);
@@ -382,12 +383,17 @@ moe_status moe_forward(const moe_problem* pp, const void* x, const float* scores
       e = launch_scan_tiles(bc, L.shuf.nblk, p.E, counts, offsets, tiles, num_tiles, L.max_tiles, kGemmBM, nullptr,
                             hdr, s);
     const bool f8 = p.quant == MOE_FP8_PER_TENSOR;
-    const bool gather4 = !f8 && gateup_gather4();
+    const bool blockwise = p.quant == MOE_FP8_BLOCK128;
+    const bool gather4 = p.quant == MOE_BF16 && gateup_gather4();
     void* xs = at<void*>(ws, L.xs);
+    float* xs_scale = blockwise ? at<float*>(ws, L.xs_scale) : nullptr;
+    float* sh = blockwise ? at<float*>(ws, L.sh) : nullptr;
     if (e == cudaSuccess && f8) e = launch_x_amax(x, static_cast<size_t>(p.T) * p.H, hdr, s);
     if (e == cudaSuccess) {
       if (f8)
         e = launch_scatter_gather_q(ids, lrank, bc, p.T, p.E, p.k, p.H, x, xs, perm, inv, hdr, s);
+      else if (blockwise)
+        e = launch_scatter_gather_qb(ids, lrank, bc, p.T, p.E, p.k, p.H, x, xs, xs_scale, perm, inv, s);
       else if (gather4)
         e = launch_scatter(ids, lrank, bc, p.T, p.E, p.k, perm, inv, s);
       else
@@ -397,19 +403,25 @@ moe_status moe_forward(const moe_problem* pp, const void* x, const float* scores
       GroupedArgs g{};
       g.T = p.T; g.E = p.E; g.k = p.k; g.H = p.H; g.I = p.I; g.R = p.T * p.k;
       g.x = x; g.w1 = w1; g.w2 = w2;
-      g.f8 = f8;
+      g.f8 = f8 || blockwise;
       g.w1_scale = w1_scale;
       g.w2_scale = w2_scale;
-      g.a_f32 = f8 ? at<void*>(ws, L.a32) : nullptr;
+      g.a_f32 = g.f8 ? at<void*>(ws, L.a32) : nullptr;
       g.xs = gather4 ? nullptr : xs;
       g.perm = perm; g.tiles = tiles; g.num_tiles = num_tiles; g.max_tiles = L.max_tiles;
       g.h = at<void*>(ws, L.h);
       g.o = at<void*>(ws, L.o);
       g.hdr = hdr;
-      e = launch_gateup_bf16(g, s);
-      if (e == cudaSuccess && f8)
-        e = launch_quant_rows(static_cast<const float*>(g.a_f32), g.h, static_cast<size_t>(g.R) * p.I, hdr, s);
-      if (e == cudaSuccess) e = launch_down_bf16(g, s);
+      if (blockwise) {
+        e = launch_gateup_blockwise(g, xs_scale, s);
+        if (e == cudaSuccess) e = launch_quant_groups(static_cast<const float*>(g.a_f32), g.h, sh, g.R, p.I, s);
+        if (e == cudaSuccess) e = launch_down_blockwise(g, sh, s);
+      } else {
+        e = launch_gateup_bf16(g, s);
+        if (e == cudaSuccess && f8)
+          e = launch_quant_rows(static_cast<const float*>(g.a_f32), g.h, static_cast<size_t>(g.R) * p.I, hdr, s);
+        if (e == cudaSuccess) e = launch_down_bf16(g, s);
+      }
     }
     if (e == cudaSuccess) {
       CombineArgs c{p.T, p.k, p.H, at<void*>(ws, L.o), false, w, y};

@@ -90,6 +90,101 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const float4* __restric
   }
 }
 
+// Blockwise variant of the fused scatter + gather + quantisation: one warp per
+// route; every 128-column group of the route's x row gets its own scale
+// (amax / 448 over the group), written to xs_scale[p][G] beside the codes.  A
+// pass covers 512 columns: lane l holds 16 values of group 4*pass + l/8, and
+// the group amax is reduced over its 8 lanes.  H is a multiple of 128.
+__global__ void __launch_bounds__(256) scatter_gather_qb_kernel(const int32_t* __restrict__ ids,
+                                                                const int32_t* __restrict__ lrank,
+                                                                const int32_t* __restrict__ blockbase, int R, int E,
+                                                                int RB, int k, int H, const uint4* __restrict__ x,
+                                                                uint4* __restrict__ xs, float* __restrict__ xs_scale,
+                                                                int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+  const int lane = threadIdx.x & 31;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  const int row16 = H / 16;
+  const int groups = H / 128;
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < R; r += nw) {
+    const int lr = lrank[r];
+    if (lr < 0) {
+      if (lane == 0) inv[r] = -1;
+      continue;
+    }
+    const int e = ids[r];
+    const int p = blockbase[static_cast<size_t>(r / RB) * E + e] + lr;
+    if (lane == 0) {
+      perm[p] = r;
+      inv[r] = p;
+    }
+    const uint4* src = x + static_cast<size_t>(r / k) * (H / 8);
+    uint4* dst = xs + static_cast<size_t>(p) * row16;
+    for (int base = 0; base < row16; base += 32) {
+      const int c = base + lane;
+      const bool act = c < row16;  // whole 8-lane groups are active together (H % 128 == 0)
+      uint4 a = make_uint4(0, 0, 0, 0), b = a;
+      if (act) {
+        a = __ldg(src + 2 * c);
+        b = __ldg(src + 2 * c + 1);
+      }
+      float f[16];
+      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 u = __bfloat1622float2(pa[j]), v = __bfloat1622float2(pb[j]);
+        f[2 * j] = u.x;
+        f[2 * j + 1] = u.y;
+        f[8 + 2 * j] = v.x;
+        f[8 + 2 * j + 1] = v.y;
+      }
+      float m = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(f[j]));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+      const float s = e4m3_scale(m);
+      if (act) {
+        uint32_t q[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          q[j] = static_cast<uint32_t>(cvt_e4m3x2(f[4 * j] / s, f[4 * j + 1] / s)) |
+                 (static_cast<uint32_t>(cvt_e4m3x2(f[4 * j + 2] / s, f[4 * j + 3] / s)) << 16);
+        dst[c] = make_uint4(q[0], q[1], q[2], q[3]);
+        if ((lane & 7) == 0) xs_scale[static_cast<size_t>(p) * groups + c / 8] = s;
+      }
+    }
+  }
+}
+
+// h = e4m3(a / s), one scale per (row, 128 columns): one warp per group, 4
+// values per lane; rows x groups items, 4 of them in flight per warp.
+__global__ void __launch_bounds__(256) quant_groups_kernel(const float4* __restrict__ a, uint32_t* __restrict__ h,
+                                                           float* __restrict__ sh, size_t items) {
+  const int lane = threadIdx.x & 31;
+  const size_t nw = (static_cast<size_t>(gridDim.x) * blockDim.x) >> 5;
+  for (size_t g0 = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; g0 < items; g0 += 4 * nw) {
+    float4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const size_t g = g0 + j * nw;
+      v[j] = g < items ? __ldg(a + g * 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const size_t g = g0 + j * nw;
+      const float m = warp_max(fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+      const float s = e4m3_scale(m);
+      if (g < items) {
+        h[g * 32 + lane] = static_cast<uint32_t>(cvt_e4m3x2(v[j].x / s, v[j].y / s)) |
+                           (static_cast<uint32_t>(cvt_e4m3x2(v[j].z / s, v[j].w / s)) << 16);
+        if (lane == 0) sh[g] = s;
+      }
+    }
+  }
+}
+
 static unsigned grid_for(size_t work, unsigned per_block) {
   const int sms = num_sms();
   const size_t cap = static_cast<size_t>(sms > 0 ? sms : 148) * 16;
@@ -128,6 +223,32 @@ cudaError_t launch_quant_rows(const float* a, void* h, size_t n, const DeviceHea
   stage_begin("quant_h", s);
   quant_rows_kernel<<<grid_for(n4, 256), 256, 0, s>>>(reinterpret_cast<const float4*>(a), static_cast<uint32_t*>(h),
                                                       n4, hdr);
+  const cudaError_t err = cudaGetLastError();
+  stage_end(s);
+  return err;
+}
+
+cudaError_t launch_scatter_gather_qb(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
+                                     int k, int H, const void* x, void* xs, float* xs_scale, int32_t* perm,
+                                     int32_t* inv, cudaStream_t s) {
+  const int R = T * k;
+  if (R <= 0) return cudaSuccess;
+  const int RB = route_tokens_per_block(k) * k;
+  stage_begin("scatter_gather", s);
+  scatter_gather_qb_kernel<<<grid_for(static_cast<size_t>(R) * 32, 256), 256, 0, s>>>(
+      ids, lrank, blockbase, R, E, RB, k, H, static_cast<const uint4*>(x), static_cast<uint4*>(xs), xs_scale, perm,
+      inv);
+  const cudaError_t err = cudaGetLastError();
+  stage_end(s);
+  return err;
+}
+
+cudaError_t launch_quant_groups(const float* a, void* h, float* sh, int rows, int cols, cudaStream_t s) {
+  const size_t items = static_cast<size_t>(rows) * (cols / 128);
+  if (items == 0) return cudaSuccess;
+  stage_begin("quant_h", s);
+  quant_groups_kernel<<<grid_for(items * 32, 256 * 4), 256, 0, s>>>(reinterpret_cast<const float4*>(a),
+                                                                     static_cast<uint32_t*>(h), sh, items);
   const cudaError_t err = cudaGetLastError();
   stage_end(s);
   return err;

@@ -266,16 +266,18 @@ def test_forward_route_direct_shapes(m, quant, T):
     # more tokens than one MMA's 8 columns share an expert; up to the 1024-route limit
     wl = W.Workload(f"rd{T}", T, 24, 8, 256, 256, quant, 30 + T)
     inp = W.make_inputs(wl)
-    p, y, ws = run_forward(m, wl, _dev(inp))
+    p, y, ws = run_forward(m, wl, _dev(inp), path=m.MOE_PATH_ROUTE_DIRECT)
     ref = O.forward(*oracle_args(inp), wl.k, wl.quant)
     _check_routing_views(m, wl, p, ws, ref)
     _check_y(wl, y, ref["y"])
 
 
-@pytest.mark.parametrize("wl", [W.workload("tiny"), W.workload("hunyuan", 4), W.workload("qwen3a", 3)],
+@pytest.mark.parametrize("wl", [W.workload("tiny"), W.workload("hunyuan", 4), W.workload("qwen3a", 3),
+                                W.Workload("f8t_det", 200, 32, 8, 512, 256, W.QUANT_FP8_TENSOR, 61),
+                                W.Workload("f8b_det", 200, 32, 8, 512, 256, W.QUANT_FP8_BLOCK, 62)],
                          ids=lambda w: w.name)
 def test_deterministic_and_graph_replay_bitwise(m, wl):
-    if wl.quant == W.QUANT_BF16:
+    if wl.name.split("_")[0] not in W.DECODE_SWEEPS:
         inp = W.make_inputs(wl)
     else:
         w1, w2, s1, s2 = _decode_weights(wl.name.split("_")[0])
@@ -318,11 +320,6 @@ def test_small_workspace_rejected_without_launch(m):
     assert torch.all(y == 7.0)
 
 
-def test_fp8_blockwise_grouped_is_reported_unsupported(m):
-    p = m.problem(64, 32, 8, 512, 256, "fp8_block", m.MOE_PATH_GROUPED)
-    assert m.moe_workspace_size(p) == 0
-
-
 FP8_GROUPED = [
     W.Workload("f8g_small", 64, 32, 8, 512, 256, W.QUANT_FP8_TENSOR, 41),
     W.Workload("f8g_ragged", 300, 16, 4, 384, 192, W.QUANT_FP8_TENSOR, 42),  # partial N tile, Down K tail
@@ -355,6 +352,49 @@ def test_forward_grouped_fp8_hunyuan_shape_and_auto_switch(m):
 @pytest.mark.parametrize("T", [4, 24])
 def test_fp8_grouped_and_route_direct_agree(m, T):
     wl = W.Workload("f8agree", T, 48, 8, 512, 256, W.QUANT_FP8_TENSOR, 44 + T)
+    inp = W.make_inputs(wl)
+    d = _dev(inp)
+    _, yg, _ = run_forward(m, wl, d, path=m.MOE_PATH_GROUPED)
+    _, yr, _ = run_forward(m, wl, d, path=m.MOE_PATH_ROUTE_DIRECT)
+    ref = O.forward(*oracle_args(inp), wl.k, wl.quant)
+    _check_y(wl, yg, ref["y"])
+    _check_y(wl, yr, ref["y"])
+    assert rel_l2(yg.float().cpu().numpy(), yr.float().cpu().numpy()) <= 2e-2
+
+
+FP8_BLOCK_GROUPED = [
+    W.Workload("f8b_small", 64, 32, 8, 512, 256, W.QUANT_FP8_BLOCK, 51),
+    W.Workload("f8b_ragged", 300, 16, 4, 384, 384, W.QUANT_FP8_BLOCK, 52),  # 6 Gate/Up N tiles, 3 Down N tiles
+    W.Workload("f8b_tiny", 5, 8, 2, 256, 128, W.QUANT_FP8_BLOCK, 53),
+    W.Workload("f8b_onexp", 130, 1, 1, 128, 128, W.QUANT_FP8_BLOCK, 54),  # one K block each way, 2 row tiles
+]
+
+
+@pytest.mark.parametrize("wl", FP8_BLOCK_GROUPED, ids=lambda w: w.name)
+def test_forward_grouped_fp8_blockwise(m, wl):
+    inp = W.make_inputs(wl)
+    p, y, ws = run_forward(m, wl, _dev(inp), path=m.MOE_PATH_GROUPED)
+    ref = O.forward(*oracle_args(inp), wl.k, wl.quant)
+    _check_routing_views(m, wl, p, ws, ref)
+    _check_y(wl, y, ref["y"])
+
+
+def test_forward_grouped_fp8_blockwise_qwen3_shape_and_auto_switch(m):
+    wl = W.workload("qwen3a", 1).with_tokens(512)
+    w1, w2, s1, s2 = _decode_weights("qwen3a")
+    inp = {"x": W.make_x(wl), "scores": W.make_scores(wl), "w1": w1, "w2": w2, "w1_scale": s1, "w2_scale": s2}
+    p, y, ws = run_forward(m, wl, _dev(inp))
+    assert m.moe_select_path(p) == m.MOE_PATH_GROUPED
+    ref = O.forward(*oracle_args(inp), wl.k, wl.quant)
+    _check_routing_views(m, wl, p, ws, ref)
+    _check_y(wl, y, ref["y"])
+    q = m.problem(32, wl.E, wl.k, wl.H, wl.I, wl.quant)
+    assert m.moe_select_path(q) == m.MOE_PATH_ROUTE_DIRECT
+
+
+@pytest.mark.parametrize("T", [4, 24])
+def test_fp8_blockwise_grouped_and_route_direct_agree(m, T):
+    wl = W.Workload("f8bagree", T, 48, 8, 512, 256, W.QUANT_FP8_BLOCK, 55 + T)
     inp = W.make_inputs(wl)
     d = _dev(inp)
     _, yg, _ = run_forward(m, wl, d, path=m.MOE_PATH_GROUPED)
