@@ -11,10 +11,13 @@ scaling).  The JSON line also carries:
   e2e           the same metric through the C ABI with host buffers, the
                 host->device copy of x and the scores and the device->host read
                 of y inside the timed region;
-  decode        the route-direct FP8 decode sweeps (per-tensor E=192 H=4096
-                I=192; blockwise E=128 H=2048 I=768 and H=4096 I=512; B=1..8),
-                us/call from CUDA-graph replays with L2 flushed between replays
-                (outside the timed events), and the HBM roofline fraction;
+  decode        the FP8 decode sweeps (per-tensor E=192 H=4096 I=192;
+                blockwise E=128 H=2048 I=768 and H=4096 I=512; B=1..8), both
+                the route-direct and the grouped path at every B, us/call from
+                CUDA-graph replays with L2 flushed between replays (outside the
+                timed events), and the HBM roofline fraction of the AUTO path;
+  fp8_prefill   the grouped path with e4m3 operands (per-tensor, blockwise)
+                at the prefill shape, against the FP8 dense peak measured live;
   cpu_baseline  the CPU oracle timed on this host on a bounded token sample.
 
 ``--impl reference`` times the CPU oracle (the reference of this library) on
@@ -216,9 +219,13 @@ def oracle_tokens_per_s(inp, wl, n_tokens: int, seed: int = 0):
 
 
 def cpu_baseline(inp, wl, budget_s: float = 15.0):
-    _, t_small = oracle_tokens_per_s(inp, wl, 64, seed=1)
-    per_tok = max(t_small / 64.0, 1e-6)
-    n = int(min(wl.T, max(64, budget_s / per_tok)))
+    # Two-point calibration: the oracle routes and groups the whole batch whatever
+    # the sample, so its time is a fixed part plus a per-sampled-token part.
+    _, t_a = oracle_tokens_per_s(inp, wl, 64, seed=1)
+    _, t_b = oracle_tokens_per_s(inp, wl, 512, seed=1)
+    per_tok = max((t_b - t_a) / 448.0, 1e-6)
+    fixed = max(t_a - 64 * per_tok, 0.0)
+    n = int(min(wl.T, max(64, (budget_s - fixed) / per_tok)))
     v, dt = oracle_tokens_per_s(inp, wl, n, seed=2)
     return {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{n} of the {wl.T} tokens (all {wl.k} routes each, full routing/shuffle of the batch), "
@@ -234,7 +241,37 @@ def workload_config(wl, l2_note):
             "path": "grouped", "l2": l2_note}
 
 
+def graph_replay_us(m, torch, p, args, flush, reps: int, warm: int = 20):
+    """Median / p10 / p90 µs of one moe_forward captured in a CUDA graph, L2
+    flushed (a write of 2.5x its size) before every replay, outside the events."""
+    x, sc, w1, w2, s1, s2, y, ws = args
+    s = torch.cuda.Stream()
+    m.moe_forward(p, x, sc, w1, w2, s1, s2, y, ws, stream=s)  # eager warm-up
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        m.moe_forward(p, x, sc, w1, w2, s1, s2, y, ws, stream=s)
+    times = []
+    with torch.cuda.stream(s):
+        for i in range(reps + warm):
+            flush.fill_(float(i))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            g.replay()
+            b.record(s)
+            b.synchronize()
+            if i >= warm:
+                times.append(a.elapsed_time(b) * 1000.0)
+    del g
+    if m.moe_read_device_status(ws) != m.MOE_OK:
+        raise RuntimeError("device status not OK after decode replays")
+    t = sorted(times)
+    return statistics.median(t), t[len(t) // 10], t[(9 * len(t)) // 10]
+
+
 def run_decode_sweep(m, torch, dev, peaks, reps: int):
+    """Both paths at every B: the route-direct path and the grouped path (the
+    crossover that sets the AUTO dispatch), reported for the path AUTO takes."""
     import workloads as W
 
     out = {}
@@ -247,46 +284,116 @@ def run_decode_sweep(m, torch, dev, peaks, reps: int):
             wl = W.workload(name, B)
             x = W.make_x(wl).to(dev)
             sc = W.make_scores(wl).to(dev)
-            p = m.problem(wl.T, wl.E, wl.k, wl.H, wl.I, wl.quant)
-            ws = torch.empty(m.moe_workspace_size(p), dtype=torch.uint8, device=dev)
             y = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
-            s = torch.cuda.Stream()
-            m.moe_forward(p, x, sc, w1, w2, s1, s2, y, ws, stream=s)  # eager warm-up
-            torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=s):
-                m.moe_forward(p, x, sc, w1, w2, s1, s2, y, ws, stream=s)
-            times = []
-            with torch.cuda.stream(s):
-                for i in range(reps + 3):
-                    flush.fill_(float(i))
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record(s)
-                    g.replay()
-                    b.record(s)
-                    b.synchronize()
-                    if i >= 3:
-                        times.append(a.elapsed_time(b) * 1000.0)
-            assert m.moe_read_device_status(ws) == m.MOE_OK
-            v = m.moe_forward_views(p, ws)
-            off = v.ids - ws.data_ptr()
-            ids = ws[off:off + wl.T * wl.k * 4].view(torch.int32)
-            U = int(torch.unique(ids).numel())
+            res = {}
+            U = None
+            for pname, path in (("route_direct", m.MOE_PATH_ROUTE_DIRECT), ("grouped", m.MOE_PATH_GROUPED)):
+                p = m.problem(wl.T, wl.E, wl.k, wl.H, wl.I, wl.quant, path)
+                ws = torch.empty(m.moe_workspace_size(p), dtype=torch.uint8, device=dev)
+                res[pname] = graph_replay_us(m, torch, p, (x, sc, w1, w2, s1, s2, y, ws), flush, reps)
+                if U is None:
+                    v = m.moe_forward_views(p, ws)
+                    off = v.ids - ws.data_ptr()
+                    U = int(torch.unique(ws[off:off + wl.T * wl.k * 4].view(torch.int32)).numel())
+                del ws
+            auto = m.moe_select_path(m.problem(wl.T, wl.E, wl.k, wl.H, wl.I, wl.quant))
+            auto_name = "route_direct" if auto == m.MOE_PATH_ROUTE_DIRECT else "grouped"
+            us, p10, p90 = res[auto_name]
             w1e = 2 * wl.I * wl.H + (0 if s1 is None else s1[0].numel() * 4)
             w2e = wl.H * wl.I + (0 if s2 is None else s2[0].numel() * 4)
             algo = U * (w1e + w2e) + wl.T * wl.H * 2 * 2 + wl.T * wl.E * 4
-            us = statistics.median(times)
-            per_b.append({"B": B, "us": round(us, 3), "p10_us": round(sorted(times)[len(times) // 10], 3),
-                          "p90_us": round(sorted(times)[(9 * len(times)) // 10], 3),
+            per_b.append({"B": B, "auto_path": auto_name, "us": round(us, 3), "p10_us": round(p10, 3),
+                          "p90_us": round(p90, 3),
+                          "route_direct_us": round(res["route_direct"][0], 3),
+                          "grouped_us": round(res["grouped"][0], 3),
                           "distinct_experts": U, "algo_bytes": algo,
                           "hbm_gbs": round(algo / (us * 1e-6) / 1e9, 1),
                           "hbm_frac": round(algo / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
                           "h20_route_mma_us": H20_ROUTE_MMA_US[name][B - 1],
                           "tokens_per_s": round(B / (us * 1e-6), 1)})
-            del g
         out[name] = {"E": base.E, "H": base.H, "I": base.I, "top_k": base.k, "quant": base.quant,
-                     "path": "route_direct", "by_batch": per_b}
+                     "timing": f"CUDA-graph replay, median of {reps} after 20 warm-up replays, "
+                               "L2 flushed before each replay (outside the events)",
+                     "by_batch": per_b}
         del w1, w2, s1, s2
+        torch.cuda.empty_cache()
+    return out
+
+
+def measure_fp8_peak(torch, dev, n: int = 8192):
+    """Dense e4m3 GEMM throughput of the vendor library (torch._scaled_mm, bf16
+    out), best of 10 x 5 back-to-back n^3 products: the FP8 roofline peak."""
+    try:
+        a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        bt = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        one = torch.ones((), device=dev)
+        torch._scaled_mm(a, bt.t(), one, one, out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(5):
+                torch._scaled_mm(a, bt.t(), one, one, out_dtype=torch.bfloat16)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1) / 5.0)
+        del a, bt
+        return round(2.0 * n ** 3 / (best * 1e-3) / 1e12, 1)
+    except (RuntimeError, AttributeError) as exc:  # no FP8 GEMM in this torch build
+        print(f"fp8 peak not measured: {exc}", file=sys.stderr)
+        return None
+
+
+def run_fp8_prefill(m, torch, dev, fp8_peak, steps: int = 50):
+    """The grouped path with e4m3 operands at the prefill shape (per-tensor and
+    128x128 blockwise scales): per-stage device times and GEMM throughput."""
+    import dataclasses
+
+    import workloads as W
+
+    out = {"fp8_peak_tflops": fp8_peak,
+           "fp8_peak_source": "measured live: torch._scaled_mm e4m3 8192^3, best of 10"}
+    for quant in (W.QUANT_FP8_TENSOR, W.QUANT_FP8_BLOCK):
+        wl = dataclasses.replace(W.workload(PREFILL), quant=quant, name=f"{PREFILL}_{quant}")
+        w1, w2, s1, s2 = W.make_weights(wl, device=dev)  # drawn on the device (fast); seeded
+        d = {"x": W.make_x(wl).to(dev), "scores": W.make_scores(wl).to(dev), "w1": w1, "w2": w2,
+             "w1_scale": s1, "w2_scale": s2}
+        del w1, w2, s1, s2
+        p = m.problem(wl.T, wl.E, wl.k, wl.H, wl.I, wl.quant, m.MOE_PATH_GROUPED)
+        ws = torch.empty(m.moe_workspace_size(p), dtype=torch.uint8, device=dev)
+        y = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
+        args = (p, d["x"], d["scores"], d["w1"], d["w2"], d["w1_scale"], d["w2_scale"], y, ws)
+        for _ in range(5):
+            m.moe_forward(*args)
+        torch.cuda.synchronize()
+        m.moe_profile_start()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            m.moe_forward(*args)
+        e1.record()
+        torch.cuda.synchronize()
+        stages = m.moe_profile_stop()
+        if m.moe_read_device_status(ws) != m.MOE_OK:
+            raise RuntimeError("device status not OK after the FP8 prefill steps")
+        step_us = e0.elapsed_time(e1) / steps * 1000.0
+        R = wl.T * wl.k
+
+        def tflops(name, flops):
+            t, n = stages.get(name, (float("nan"), 0))
+            return round(flops / (t / max(n, 1) / 1000.0) / 1e12, 1) if n else None
+
+        gu = tflops("gateup_gemm", 4.0 * R * wl.H * wl.I)
+        dn = tflops("down_gemm", 2.0 * R * wl.H * wl.I)
+        out[quant] = {
+            "tokens_per_s": round(wl.T / (step_us * 1e-6), 1), "us_per_step": round(step_us, 1), "steps": steps,
+            "gateup_tflops": gu, "down_tflops": dn,
+            "gateup_frac_of_fp8_peak": round(gu / fp8_peak, 4) if gu and fp8_peak else None,
+            "down_frac_of_fp8_peak": round(dn / fp8_peak, 4) if dn and fp8_peak else None,
+            "stages_us": {k: round(1000.0 * t / max(n, 1), 1) for k, (t, n) in stages.items()},
+        }
+        del d, ws, y
         torch.cuda.empty_cache()
     return out
 
@@ -388,9 +495,11 @@ def run_ours(args):
     e2e = {"value": throughput(wl.T, world, args.steps, e2e_ms), "unit": UNIT,
            "h2d_bytes_per_step": xh.numel() * 2 + sh.numel() * 4, "d2h_bytes_per_step": yh.numel() * 2}
 
-    decode = None
+    decode = fp8 = None
     if not args.no_decode and rank == 0:
         decode = run_decode_sweep(m, torch, dev, peaks, args.decode_reps)
+    if not args.no_fp8 and rank == 0:
+        fp8 = run_fp8_prefill(m, torch, dev, measure_fp8_peak(torch, dev))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -435,6 +544,7 @@ def run_ours(args):
         "clocks": clocks,
         "wall_s_timed": round(wall_s, 3),
         "decode": decode,
+        "fp8_prefill": fp8,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line))
@@ -491,7 +601,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-decode", action="store_true", help="skip the route-direct decode sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--decode-reps", type=int, default=40)
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 grouped prefill leg")
+    ap.add_argument("--decode-reps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override T of the prefill workload (smaller cases for profiling; not a bench line)")

@@ -167,8 +167,9 @@ moe_status moe_tile_map(const int32_t* counts, int E, int BM, int32_t* tiles, in
 
 /* ---------------------------------------------------------------- forward
  * moe_select_path - the path moe_forward takes for *p (AUTO resolved):
- * bf16 -> GROUPED; FP8 (per-tensor or blockwise) -> ROUTE_DIRECT for T <= 32,
- * else GROUPED.  Returns p->path when it is not AUTO. */
+ * bf16 -> GROUPED; per-tensor FP8 -> ROUTE_DIRECT for T <= 32, blockwise FP8
+ * -> ROUTE_DIRECT for T <= 64 (both also need T*k <= 1024), else GROUPED: the
+ * crossovers measured on GB300.  Returns p->path when it is not AUTO. */
 moe_path moe_select_path(const moe_problem* p);
 
 /* moe_workspace_size - bytes of device workspace moe_forward needs for *p

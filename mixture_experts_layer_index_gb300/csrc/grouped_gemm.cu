@@ -1,28 +1,30 @@
 // Grouped GEMMs of the grouped (prefill) path on the 5th-generation tensor
 // cores ("perf: add small-batch route MMA for MoE", Motivation: Gate/Up grouped
-// GEMM -> activation -> Down grouped GEMM; the "gather" step is fused into the
-// Gate/Up GEMM's TMA loads).
+// GEMM -> activation -> Down grouped GEMM).
 //
 // One persistent CTA per SM walks work units (row tile, N tile) of a task map
 // built on the device (tile count read from device memory, no host sync).
 // Warp roles (256 threads):
 //   warp 0      TMA producer: A (activations) and B (weights) K-slices into a
 //               4-stage shared-memory ring, 128-byte swizzled.
-//   warp 1      one thread issues tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32)
-//               into one of two TMEM accumulators (2 x 256 columns).
+//   warp 1      one thread issues tcgen05.mma (M=128, N=256; K=16 bf16 or K=32
+//               e4m3 per instruction, fp32 accumulate) into one of two TMEM
+//               accumulators (2 x 256 columns).
 //   warp 2      allocates / frees the 512 TMEM columns.
 //   warps 4-7   epilogue: tcgen05.ld the accumulator (one row per thread),
-//               apply the fused epilogue, store to global memory.
+//               apply the fused epilogue and store (Down: staged in shared
+//               memory and written out as whole, coalesced row segments).
 //
-// Gate/Up (MODE_GATEUP): A rows are gathered straight from x with TMA
-//   tile::gather4 (row = token of sorted route p = perm[p] / k), so the
-//   expert-sorted activation matrix is never materialised.  B = the expert's
-//   gate rows [n0, n0+128) and up rows [I+n0, I+n0+128) of W1, so one 128x256
-//   accumulator holds matching gate and up columns; the epilogue writes
-//   h = bf16(silu(g) * u) for sorted rows, columns [n0, n0+128).
-// Down (MODE_DOWN): A = h rows of the tile (contiguous, plain TMA tile loads),
-//   B = 256 rows of W2[e]; the epilogue writes bf16 o for sorted row p to
-//   route slot perm[p], so the combine reads each token's k rows contiguously.
+// Gate/Up (MODE_GATEUP): A = the expert-sorted activation rows that the
+//   scatter kernel copied (plain TMA tile loads); or, as a selectable
+//   variant, rows gathered straight from x with TMA tile::gather4 (row = token
+//   of sorted route p = perm[p] / k).  B = the expert's gate rows [n0, n0+128)
+//   and up rows [I+n0, I+n0+128) of W1, so one 128x256 accumulator holds
+//   matching gate and up columns; the epilogue writes h = bf16(silu(g) * u)
+//   (or fp32 a for the FP8 path) for sorted rows, columns [n0, n0+128).
+// Down (MODE_DOWN): A = h rows of the tile, B = 256 rows of W2[e]; the
+//   epilogue writes bf16 o for sorted row p to route slot perm[p], so the
+//   combine reads each token's k rows contiguously.
 #include <cstdio>
 #include <mutex>
 
@@ -42,7 +44,10 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;
 constexpr int THREADS = 256;
 constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
-constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+// epilogue staging: 4 warps x 32 rows x 256 bytes, after the barriers
+constexpr int STAGING_OFFSET = STAGES * STAGE_BYTES + 256;
+constexpr int STAGING_BYTES = 4 * 32 * 256;
+constexpr size_t SMEM_BYTES = 1024 + STAGING_OFFSET + STAGING_BYTES;
 
 constexpr int MODE_GATEUP = 0;
 constexpr int MODE_DOWN = 1;
@@ -249,8 +254,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       if (MODE == MODE_GATEUP) {
-        // F8: a = silu(sc g) * (sc u) with sc = s_x * s_w1[e], kept in fp32 for the
-        // per-tensor quantisation of h, whose amax this epilogue also records
+        // Direct stores (each thread writes whole 64- or 128-byte pieces of its own
+        // sorted row).  F8: a = silu(sc g) * (sc u) with sc = s_x * s_w1[e], kept
+        // in fp32 for the per-tensor quantisation of h, whose amax is recorded here.
         const float sc = F8 ? e4m3_scale(__uint_as_float(*p.amax_in)) * __ldg(p.wscale + tl.x) : 1.0f;
         float amax = 0.0f;
         __nv_bfloat16* out_row = p.out + static_cast<size_t>(row0 + row) * p.out_ld;
@@ -261,6 +267,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_ld32(tbase + c, g);
           tmem_ld32(tbase + BN / 2 + c, up);
           tmem_ld_wait();
+          if (c == BN / 2 - 32) {  // last columns read: hand the accumulator back to the MMA
+            tc_fence_before();
+            mbar_arrive(tempty0 + 8 * acc);
+          }
           const int col = n * (BN / 2) + c;
           if (row < nrows && col < p.n_valid) {
             float hv[32];
@@ -286,29 +296,47 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (lane == 0 && amax > 0.0f) atomicMax(p.amax_out, __float_as_uint(amax));
         }
       } else {
-        const int slot = row < nrows ? __ldg(p.perm + row0 + row) : 0;
-        __nv_bfloat16* out_row = p.out + static_cast<size_t>(slot) * p.out_ld;
-        // F8: o = s_h * s_w2[e] * acc
+        // Down: o rows go to scattered route slots.  Each pass stages 128 bf16
+        // columns (256 bytes) of every row of the warp in shared memory (16-byte
+        // pieces XOR-swizzled by row, so both phases are bank-conflict free), then
+        // the warp writes two whole 256-byte row segments per store instruction.
+        // F8: o = s_h * s_w2[e] * acc.
+        uint4* stg = reinterpret_cast<uint4*>(smem + STAGING_OFFSET) + q * (32 * 16);
+        const int wrows = min(32, nrows - q * 32);  // valid rows of this warp (may be <= 0)
         const float post = F8 ? e4m3_scale(__uint_as_float(*p.amax_in)) * __ldg(p.wscale + tl.x) : 1.0f;
+        const int slot = row < nrows ? __ldg(p.perm + row0 + row) : 0;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          float v[32];
-          tmem_ld32(tbase + c, v);
-          tmem_ld_wait();
-          const int col = n * BN + c;
-          if (F8) {
+        for (int pass = 0; pass < 2; ++pass) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= post;
-          }
-          if (row < nrows && col < p.n_valid) {
-            uint4* dst = reinterpret_cast<uint4*>(out_row + col);
+          for (int c = 0; c < 128; c += 32) {
+            float v[32];
+            tmem_ld32(tbase + pass * 128 + c, v);
+            tmem_ld_wait();
+            if (F8) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = pack_bf16x8(v + 8 * i);
+              for (int i = 0; i < 32; ++i) v[i] *= post;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) stg[lane * 16 + (((c / 8) + i) ^ (lane & 15))] = pack_bf16x8(v + 8 * i);
           }
+          if (pass == 1) {  // every accumulator column read: hand the buffer back to the MMA
+            tc_fence_before();
+            mbar_arrive(tempty0 + 8 * acc);
+          }
+          __syncwarp();
+          const int col0 = n * BN + pass * 128;
+#pragma unroll 4
+          for (int it = 0; it < 16; ++it) {
+            const int r = it * 2 + (lane >> 4), j = lane & 15;
+            const int rslot = __shfl_sync(0xffffffffu, slot, r);
+            const int col = col0 + j * 8;
+            if (r < wrows && col < p.n_valid)
+              *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(rslot) * p.out_ld + col) =
+                  stg[r * 16 + (j ^ (r & 15))];
+          }
+          __syncwarp();
         }
       }
-      tc_fence_before();
-      mbar_arrive(tempty0 + 8 * acc);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }

@@ -136,14 +136,21 @@ ShuffleLayout plan_shuffle(int T, int E, int k, size_t base) {
   return L;
 }
 
-// Largest T for which AUTO takes the route-direct path with per-tensor FP8
-// weights (beyond it, the grouped path).
-constexpr int kAutoRouteDirectMaxTokens = 32;
+// Largest T for which AUTO takes the route-direct path (beyond it, the grouped
+// path), per FP8 mode.  Measured on GB300 with both paths captured in CUDA
+// graphs, L2 flushed between calls, k = 8: per-tensor (E=192, H=4096, I=192)
+// route-direct is faster through T=32 and the grouped path from T=48;
+// blockwise (E=128, H=2048, I=768 / H=4096, I=512) route-direct is faster
+// through T=96 / T=48 and the grouped path from T=128 / T=64.
+constexpr int kAutoRouteDirectMaxTokensPerTensor = 32;
+constexpr int kAutoRouteDirectMaxTokensBlockwise = 64;
 
 static moe_path resolve_path(const moe_problem& p) {
   if (p.path != MOE_PATH_AUTO) return p.path;
   if (p.quant == MOE_BF16) return MOE_PATH_GROUPED;
-  if (p.T > kAutoRouteDirectMaxTokens) return MOE_PATH_GROUPED;
+  const int limit = p.quant == MOE_FP8_BLOCK128 ? kAutoRouteDirectMaxTokensBlockwise
+                                                : kAutoRouteDirectMaxTokensPerTensor;
+  if (p.T > limit || static_cast<long long>(p.T) * p.k > kRouteDirectMaxRoutes) return MOE_PATH_GROUPED;
   return MOE_PATH_ROUTE_DIRECT;
 }
 

@@ -345,8 +345,8 @@ def test_forward_grouped_fp8_hunyuan_shape_and_auto_switch(m):
     ref = O.forward(*oracle_args(inp), wl.k, wl.quant)
     _check_routing_views(m, wl, p, ws, ref)
     _check_y(wl, y, ref["y"])
-    q = m.problem(32, wl.E, wl.k, wl.H, wl.I, wl.quant)
-    assert m.moe_select_path(q) == m.MOE_PATH_ROUTE_DIRECT
+    assert m.moe_select_path(m.problem(32, wl.E, wl.k, wl.H, wl.I, wl.quant)) == m.MOE_PATH_ROUTE_DIRECT
+    assert m.moe_select_path(m.problem(33, wl.E, wl.k, wl.H, wl.I, wl.quant)) == m.MOE_PATH_GROUPED
 
 
 @pytest.mark.parametrize("T", [4, 24])
@@ -388,8 +388,8 @@ def test_forward_grouped_fp8_blockwise_qwen3_shape_and_auto_switch(m):
     ref = O.forward(*oracle_args(inp), wl.k, wl.quant)
     _check_routing_views(m, wl, p, ws, ref)
     _check_y(wl, y, ref["y"])
-    q = m.problem(32, wl.E, wl.k, wl.H, wl.I, wl.quant)
-    assert m.moe_select_path(q) == m.MOE_PATH_ROUTE_DIRECT
+    assert m.moe_select_path(m.problem(64, wl.E, wl.k, wl.H, wl.I, wl.quant)) == m.MOE_PATH_ROUTE_DIRECT
+    assert m.moe_select_path(m.problem(65, wl.E, wl.k, wl.H, wl.I, wl.quant)) == m.MOE_PATH_GROUPED
 
 
 @pytest.mark.parametrize("T", [4, 24])
