@@ -284,14 +284,23 @@ __global__ void __launch_bounds__(THREADS) rd_gateup_kernel(DecodeArgs a, int nM
     const int my_t = my_r >= 0 ? my_r / a.k : 0;
     const uint8_t* xrow = a.xq + static_cast<size_t>(my_t) * H + 16 * tig;
     float c[4] = {0.f, 0.f, 0.f, 0.f};
+    const int kend = k0 + KS;
     if (!BLOCKWISE) {
-#pragma unroll 8
-      for (int kk = k0; kk < k0 + KS; kk += 64) {
-        const uint4 A0 = ld_stream(wrow0 + kk);
-        const uint4 A1 = ld_stream(wrow1 + kk);
-        uint4 X = __ldg(reinterpret_cast<const uint4*>(xrow + kk));
-        if (my_r < 0) X = make_uint4(0, 0, 0, 0);
-        mma_k64(c, A0, A1, X);
+      // the loads of NB K-steps are issued before their MMAs: NB x 32 bytes of
+      // weights in flight per thread
+      constexpr int NB = 8;
+      for (int kb0 = k0; kb0 < kend; kb0 += 64 * NB) {
+        uint4 A0[NB], A1[NB], X[NB];
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          const int kk = kb0 + 64 * i;
+          const bool in = kk < kend;
+          A0[i] = in ? ld_stream(wrow0 + kk) : make_uint4(0, 0, 0, 0);
+          A1[i] = in ? ld_stream(wrow1 + kk) : make_uint4(0, 0, 0, 0);
+          X[i] = in && my_r >= 0 ? __ldg(reinterpret_cast<const uint4*>(xrow + kk)) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < NB; ++i) mma_k64(c, A0[i], A1[i], X[i]);
       }
     } else {
       // per 128-wide K block: fresh partial, then scale by s_w1[e, row/128, kb] * s_x[t, kb]
@@ -299,24 +308,38 @@ __global__ void __launch_bounds__(THREADS) rd_gateup_kernel(DecodeArgs a, int nM
       const int t0 = 2 * tig < nn ? uv.routes()[r_beg + n0 + 2 * tig] / a.k : 0;
       const int t1 = 2 * tig + 1 < nn ? uv.routes()[r_beg + n0 + 2 * tig + 1] / a.k : 0;
       const float* sw = a.w1_scale + (static_cast<size_t>(e) * (twoI / 128) + rb) * ng;
-#pragma unroll 4
-      for (int kk = k0; kk < k0 + KS; kk += 128) {
-        float cb[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint4 A0 = ld_stream(wrow0 + kk), A1 = ld_stream(wrow1 + kk);
-        const uint4 B0 = ld_stream(wrow0 + kk + 64), B1 = ld_stream(wrow1 + kk + 64);
-        uint4 X0 = __ldg(reinterpret_cast<const uint4*>(xrow + kk));
-        uint4 X1 = __ldg(reinterpret_cast<const uint4*>(xrow + kk + 64));
-        if (my_r < 0) X0 = X1 = make_uint4(0, 0, 0, 0);
-        mma_k64(cb, A0, A1, X0);
-        mma_k64(cb, B0, B1, X1);
-        const int kb = kk / 128;
-        const float w_s = __ldg(sw + kb);
-        const float s0 = w_s * __ldg(a.sx + static_cast<size_t>(t0) * ng + kb);
-        const float s1 = w_s * __ldg(a.sx + static_cast<size_t>(t1) * ng + kb);
-        c[0] = fmaf(cb[0], s0, c[0]);
-        c[1] = fmaf(cb[1], s1, c[1]);
-        c[2] = fmaf(cb[2], s0, c[2]);
-        c[3] = fmaf(cb[3], s1, c[3]);
+      constexpr int NB = 4;  // 128-wide K blocks per batch of loads
+      for (int kb0 = k0; kb0 < kend; kb0 += 128 * NB) {
+        uint4 A0[NB], A1[NB], B0[NB], B1[NB], X0[NB], X1[NB];
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          const int kk = kb0 + 128 * i;
+          const bool in = kk < kend;
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          A0[i] = in ? ld_stream(wrow0 + kk) : z;
+          A1[i] = in ? ld_stream(wrow1 + kk) : z;
+          B0[i] = in ? ld_stream(wrow0 + kk + 64) : z;
+          B1[i] = in ? ld_stream(wrow1 + kk + 64) : z;
+          X0[i] = in && my_r >= 0 ? __ldg(reinterpret_cast<const uint4*>(xrow + kk)) : z;
+          X1[i] = in && my_r >= 0 ? __ldg(reinterpret_cast<const uint4*>(xrow + kk + 64)) : z;
+        }
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          const int kk = kb0 + 128 * i;
+          if (kk < kend) {
+            float cb[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_k64(cb, A0[i], A1[i], X0[i]);
+            mma_k64(cb, B0[i], B1[i], X1[i]);
+            const int kb = kk / 128;
+            const float w_s = __ldg(sw + kb);
+            const float s0 = w_s * __ldg(a.sx + static_cast<size_t>(t0) * ng + kb);
+            const float s1 = w_s * __ldg(a.sx + static_cast<size_t>(t1) * ng + kb);
+            c[0] = fmaf(cb[0], s0, c[0]);
+            c[1] = fmaf(cb[1], s1, c[1]);
+            c[2] = fmaf(cb[2], s0, c[2]);
+            c[3] = fmaf(cb[3], s1, c[3]);
+          }
+        }
       }
     }
     // c0: (row, col 2tig), c1: (row, col 2tig+1), c2/c3: row + 8
@@ -455,34 +478,56 @@ __global__ void __launch_bounds__(THREADS) rd_down_kernel(DecodeArgs a, int nHB)
     const uint8_t* xrow = s_h + g * I + 16 * tig;
     float c[4] = {0.f, 0.f, 0.f, 0.f};
     if (!BLOCKWISE) {
-#pragma unroll 4
-      for (int kk = 0; kk < I; kk += 64) {
-        const uint4 A0 = ld_stream(wrow0 + kk), A1 = ld_stream(wrow1 + kk);
-        const uint4 X = *reinterpret_cast<const uint4*>(xrow + kk);
-        mma_k64(c, A0, A1, X);
+      constexpr int NB = 8;  // K-steps whose weight loads are issued before their MMAs
+      for (int kb0 = 0; kb0 < I; kb0 += 64 * NB) {
+        uint4 A0[NB], A1[NB];
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          const int kk = kb0 + 64 * i;
+          A0[i] = kk < I ? ld_stream(wrow0 + kk) : make_uint4(0, 0, 0, 0);
+          A1[i] = kk < I ? ld_stream(wrow1 + kk) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          const int kk = kb0 + 64 * i;
+          if (kk < I) mma_k64(c, A0[i], A1[i], *reinterpret_cast<const uint4*>(xrow + kk));
+        }
       }
       const float sc = s_h_t * __ldg(a.w2_scale + e);
 #pragma unroll
       for (int i = 0; i < 4; ++i) c[i] *= sc;
     } else {
       const float* sw = a.w2_scale + (static_cast<size_t>(e) * (H / 128) + row / 128) * ngi;
-#pragma unroll 2
-      for (int kk = 0; kk < I; kk += 128) {
-        float cb[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint4 A0 = ld_stream(wrow0 + kk), A1 = ld_stream(wrow1 + kk);
-        const uint4 B0 = ld_stream(wrow0 + kk + 64), B1 = ld_stream(wrow1 + kk + 64);
-        const uint4 X0 = *reinterpret_cast<const uint4*>(xrow + kk);
-        const uint4 X1 = *reinterpret_cast<const uint4*>(xrow + kk + 64);
-        mma_k64(cb, A0, A1, X0);
-        mma_k64(cb, B0, B1, X1);
-        const int kb = kk / 128;
-        const float w_s = __ldg(sw + kb);
-        const float s0 = w_s * s_sc[(2 * tig) * ngi + kb];
-        const float s1 = w_s * s_sc[(2 * tig + 1) * ngi + kb];
-        c[0] = fmaf(cb[0], s0, c[0]);
-        c[1] = fmaf(cb[1], s1, c[1]);
-        c[2] = fmaf(cb[2], s0, c[2]);
-        c[3] = fmaf(cb[3], s1, c[3]);
+      constexpr int NB = 4;  // 128-wide K blocks per batch of loads
+      for (int kb0 = 0; kb0 < I; kb0 += 128 * NB) {
+        uint4 A0[NB], A1[NB], B0[NB], B1[NB];
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          const int kk = kb0 + 128 * i;
+          const bool in = kk < I;
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          A0[i] = in ? ld_stream(wrow0 + kk) : z;
+          A1[i] = in ? ld_stream(wrow1 + kk) : z;
+          B0[i] = in ? ld_stream(wrow0 + kk + 64) : z;
+          B1[i] = in ? ld_stream(wrow1 + kk + 64) : z;
+        }
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          const int kk = kb0 + 128 * i;
+          if (kk < I) {
+            float cb[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_k64(cb, A0[i], A1[i], *reinterpret_cast<const uint4*>(xrow + kk));
+            mma_k64(cb, B0[i], B1[i], *reinterpret_cast<const uint4*>(xrow + kk + 64));
+            const int kb = kk / 128;
+            const float w_s = __ldg(sw + kb);
+            const float s0 = w_s * s_sc[(2 * tig) * ngi + kb];
+            const float s1 = w_s * s_sc[(2 * tig + 1) * ngi + kb];
+            c[0] = fmaf(cb[0], s0, c[0]);
+            c[1] = fmaf(cb[1], s1, c[1]);
+            c[2] = fmaf(cb[2], s0, c[2]);
+            c[3] = fmaf(cb[3], s1, c[3]);
+          }
+        }
       }
     }
 #pragma unroll
