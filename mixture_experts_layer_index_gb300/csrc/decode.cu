@@ -8,26 +8,32 @@
 // The work is bound by streaming the selected experts' weights from HBM, so
 // every kernel here is organised around that stream:
 //   rd_prep     one block: routing of all T tokens, dynamic e4m3 quantisation
-//               of x (per tensor, or per token and 128 columns), and the table
-//               of distinct selected experts in first-use order with their
-//               routes (a route-order scan of at most 1024 routes, no sort), so
-//               an expert chosen by several tokens is streamed once.
-//   rd_gateup   one CTA per (distinct expert, 64 rows of W1[e], K split):
-//               each warp streams 16 rows of e4m3 weights with 16-byte loads
-//               straight into mma.sync m16n8k32 e4m3 fragments (weights on M,
-//               up to 8 routes of that expert on N), fp32 partials per split.
+//               of x (per tensor, or per token and 128 columns), and the table of distinct selected
+//               experts in first-use order with their routes (a route-order
+//               scan of at most 1024 routes, no sort), so an expert chosen by
+//               several tokens is streamed once, cut into column groups of up
+//               to 8 routes.
+//   rd_gateup   persistent, two CTAs per SM over work items (column group, K
+//               split, 64 rows of W1[e]): a producer warp streams the rows with
+//               TMA into a ring of shared-memory stages; four consumer warps
+//               stage the group's e4m3 x slice when the group changes and feed
+//               16 weight rows each into mma.sync m16n8k32 e4m3 (weights on M,
+//               the group's routes on N); fp32 partials per split.
 //   rd_reduce   sums the K splits, applies the scales and SwiGLU; blockwise
 //               mode quantises h per (route, 128 columns) here, per-tensor mode
 //               records the global amax of h.
-//   rd_down     one CTA per (distinct expert, 64 rows of W2[e]); h of the
-//               expert's routes is quantised (per-tensor) or copied into
-//               shared memory, weights streamed as above; fp32 o in route order.
+//   rd_down     persistent like rd_gateup over (column group, 64 rows of
+//               W2[e]); h of the group's routes is quantised (per-tensor) or
+//               copied into shared memory; fp32 o in route order.
 //   combine     the contiguous top-k reduction shared with the grouped path.
+// All but rd_prep are launched as programmatic dependents of their predecessor.
 //
 // K permutation: a dot product does not depend on the order of its terms, so
 // each thread loads 16 consecutive bytes of a weight row and of x and feeds
 // bytes 0-7 to one m16n8k32 and bytes 8-15 to the next; A and B use the same
 // assignment, which is what makes it exact.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 #include "routing.cuh"
@@ -35,19 +41,35 @@
 namespace moe {
 namespace rd {
 
-constexpr int ROWS_PER_CTA = 64;  // 4 warps x 16 rows
-constexpr int THREADS = 128;
+constexpr int ROWS_PER_CTA = 64;  // weight rows per work item: 4 consumer warps x 16 rows
+constexpr int CONSUMERS = 4;      // consumer warps (warps 0-3); warp 4 is the copy producer
+constexpr int THREADS = 32 * (CONSUMERS + 1);
+constexpr int NS = 3;             // weight stages in flight per CTA (96 KB; two CTAs per SM)
+constexpr int CK = 512;           // K bytes of one stage (the last stage of an item may be shorter)
+constexpr int BOXK = 128;         // K bytes of one TMA box (64 rows x 128 bytes = 8 KB, 128-byte swizzle)
+constexpr int BOX_BYTES = ROWS_PER_CTA * BOXK;
+constexpr int STAGE_BYTES = ROWS_PER_CTA * CK;  // CK / BOXK boxes, each [64 rows][128 bytes]
+constexpr int GROUP = 8;          // routes per MMA column group (m16n8k32: N = 8)
+constexpr double kW2PrefetchBytes = 64.0 * 1024 * 1024;  // W2 prefetched into L2 during Gate/Up
 
 // Table of distinct experts, in int32 words:
 //   [0] U;  [1 .. 1+maxU) expert of u;  [1+maxU .. 2+2maxU) CSR offsets of u;
-//   [2+2maxU .. 2+2maxU+R) routes of u, in route order.
+//   [2+2maxU .. 2+2maxU+R) routes of u, in route order;
+//   [2+2maxU+R] G = number of column groups (up to 8 routes of one expert);
+//   then maxG entries: u of group g, and maxG entries: first route index of g
+//   within u's list.
 struct UniqView {
   int32_t* base;
   int maxU;
+  int R;
   __host__ __device__ int32_t* U() const { return base; }
   __host__ __device__ int32_t* expert() const { return base + 1; }
   __host__ __device__ int32_t* off() const { return base + 1 + maxU; }
   __host__ __device__ int32_t* routes() const { return base + 2 + 2 * maxU; }
+  __host__ __device__ int32_t* G() const { return base + 2 + 2 * maxU + R; }
+  __host__ __device__ int maxG() const { return maxU + R / GROUP + 1; }
+  __host__ __device__ int32_t* gu() const { return base + 3 + 2 * maxU + R; }
+  __host__ __device__ int32_t* gn0() const { return gu() + maxG(); }
 };
 
 __host__ __device__ inline int max_uniq(int R, int E) { return R < E ? R : E; }
@@ -89,6 +111,7 @@ __global__ void __launch_bounds__(1024) rd_prep_kernel(DecodeArgs a) {
   __shared__ int s_isfirst[kRouteDirectMaxRoutes];
   __shared__ int s_pos[kRouteDirectMaxRoutes];
   __shared__ int s_cnt[kRouteDirectMaxRoutes];
+  __shared__ int s_off[kRouteDirectMaxRoutes];
   __shared__ float s_red[32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
   const int T = a.T, E = a.E, k = a.k, H = a.H, R = a.R;
@@ -99,27 +122,39 @@ __global__ void __launch_bounds__(1024) rd_prep_kernel(DecodeArgs a) {
     a.hdr->amax_x = 0u;
     a.hdr->amax_h = 0u;
   }
-  // 1. routing
+  // 1. routing, with the loads of the first batch of x issued before it so that
+  //    both memory round trips overlap
+  const int n8 = T * H / 8;  // 16-byte pieces of x (8 values each)
+  const uint4* x8 = static_cast<const uint4*>(a.x);
+  constexpr int XB = 4;      // pieces per thread per batch
+  uint4 xv[XB];
+#pragma unroll
+  for (int j = 0; j < XB; ++j) {
+    const int i = tid + j * blockDim.x;
+    xv[j] = i < n8 ? __ldg(x8 + i) : make_uint4(0, 0, 0, 0);
+  }
   for (int t = warp; t < T; t += nwarps)
     route_one_token<MAXV>(a.scores + static_cast<size_t>(t) * E, E, k, a.ids + static_cast<size_t>(t) * k,
                            a.w + static_cast<size_t>(t) * k, s_ids + t * k);
-  // 2. dynamic e4m3 quantisation of x
-  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.x);
+  // 2. dynamic e4m3 quantisation of x: per tensor (s_x = amax / 448 over all of
+  //    x), or per (token, 128 columns) - piece i holds values [8i, 8i + 8), so 16
+  //    consecutive threads hold one 128-column group.  When x fits one batch
+  //    (T * H <= 8 * XB * 1024) it is read once, into registers.
+  const bool one_batch = n8 <= XB * static_cast<int>(blockDim.x);
+  float s_t = 1.0f;
   if (a.quant == MOE_FP8_PER_TENSOR) {
-    // loads go out in batches of 8 x 16 bytes per thread: one memory round trip per batch
     float m = 0.0f;
-    const int n8 = T * H / 8;
-    const uint4* x8 = reinterpret_cast<const uint4*>(x);
-    for (int base = tid; base < n8; base += blockDim.x * 8) {
-      uint4 v[8];
+    for (int base = 0; base < n8; base += XB * blockDim.x) {
+      if (base > 0) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = base + j * blockDim.x;
-        v[j] = i < n8 ? __ldg(x8 + i) : make_uint4(0, 0, 0, 0);
+        for (int j = 0; j < XB; ++j) {
+          const int i = base + tid + j * blockDim.x;
+          xv[j] = i < n8 ? __ldg(x8 + i) : make_uint4(0, 0, 0, 0);
+        }
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v[j]);
+      for (int j = 0; j < XB; ++j) {
+        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&xv[j]);
 #pragma unroll
         for (int h2 = 0; h2 < 4; ++h2) {
           const float2 f = __bfloat1622float2(b[h2]);
@@ -136,61 +171,47 @@ __global__ void __launch_bounds__(1024) rd_prep_kernel(DecodeArgs a) {
       if (lane == 0) s_red[0] = v;
     }
     __syncthreads();
-    const float amax = s_red[0];
-    const float s = e4m3_scale(amax);
+    s_t = e4m3_scale(s_red[0]);
     if (tid == 0) {
-      a.sx[0] = s;
-      a.hdr->amax_x = __float_as_uint(amax);
+      a.sx[0] = s_t;
+      a.hdr->amax_x = __float_as_uint(s_red[0]);
     }
-    for (int base = tid; base < n8; base += blockDim.x * 8) {
-      uint4 v[8];
+  }
+  for (int base = 0; base < n8; base += XB * blockDim.x) {
+    if (!(one_batch || (base == 0 && a.quant != MOE_FP8_PER_TENSOR))) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = base + j * blockDim.x;
-        v[j] = i < n8 ? __ldg(x8 + i) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = base + j * blockDim.x;
-        if (i < n8) {
-          const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v[j]);
-          uint32_t q[2];
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const float2 f0 = __bfloat1622float2(b[2 * h2]), f1 = __bfloat1622float2(b[2 * h2 + 1]);
-            q[h2] = static_cast<uint32_t>(cvt_e4m3x2(f0.x / s, f0.y / s)) |
-                    (static_cast<uint32_t>(cvt_e4m3x2(f1.x / s, f1.y / s)) << 16);
-          }
-          reinterpret_cast<uint2*>(a.xq)[i] = make_uint2(q[0], q[1]);
-        }
+      for (int j = 0; j < XB; ++j) {
+        const int i = base + tid + j * blockDim.x;
+        xv[j] = i < n8 ? __ldg(x8 + i) : make_uint4(0, 0, 0, 0);
       }
     }
-  } else {
-    const int ng = H / 128, ntask = T * ng;
-    for (int base = warp; base < ntask; base += nwarps * 8) {
-      uint2 v[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int gi = base + j * nwarps;
-        const int t = gi / ng, G = gi - (gi / ng) * ng;
-        v[j] = gi < ntask ? __ldg(reinterpret_cast<const uint2*>(x + static_cast<size_t>(t) * H + G * 128) + lane)
-                          : make_uint2(0, 0);
+    for (int j = 0; j < XB; ++j) {
+      const int i = base + tid + j * blockDim.x;  // i < n8 for all 16 threads of a group or none
+      float f[8];
+      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&xv[j]);
+#pragma unroll
+      for (int h2 = 0; h2 < 4; ++h2) {
+        const float2 v = __bfloat1622float2(b[h2]);
+        f[2 * h2] = v.x;
+        f[2 * h2 + 1] = v.y;
       }
+      float sc = s_t;
+      if (a.quant == MOE_FP8_BLOCK128) {
+        float mx = 0.0f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int gi = base + j * nwarps;  // warp-uniform
-        if (gi < ntask) {
-          const int t = gi / ng, G = gi - (gi / ng) * ng;
-          const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[j].x));
-          const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[j].y));
-          float m = fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
-          m = warp_max(m);
-          const float s = e4m3_scale(m);
-          const uint32_t q = static_cast<uint32_t>(cvt_e4m3x2(f0.x / s, f0.y / s)) |
-                             (static_cast<uint32_t>(cvt_e4m3x2(f1.x / s, f1.y / s)) << 16);
-          *reinterpret_cast<uint32_t*>(a.xq + static_cast<size_t>(t) * H + G * 128 + lane * 4) = q;
-          if (lane == 0) a.sx[static_cast<size_t>(t) * ng + G] = s;
-        }
+        for (int q = 0; q < 8; ++q) mx = fmaxf(mx, fabsf(f[q]));
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        sc = e4m3_scale(mx);
+        if (i < n8 && (i & 15) == 0) a.sx[i / 16] = sc;
+      }
+      if (i < n8) {
+        const uint32_t q0 = static_cast<uint32_t>(cvt_e4m3x2(f[0] / sc, f[1] / sc)) |
+                            (static_cast<uint32_t>(cvt_e4m3x2(f[2] / sc, f[3] / sc)) << 16);
+        const uint32_t q1 = static_cast<uint32_t>(cvt_e4m3x2(f[4] / sc, f[5] / sc)) |
+                            (static_cast<uint32_t>(cvt_e4m3x2(f[6] / sc, f[7] / sc)) << 16);
+        reinterpret_cast<uint2*>(a.xq)[i] = make_uint2(q0, q1);
       }
     }
   }
@@ -232,128 +253,327 @@ __global__ void __launch_bounds__(1024) rd_prep_kernel(DecodeArgs a) {
       if (r < R) s_pos[r] = base + rank;
     }
     __syncwarp();
-    if (lane == 0) {
-      UniqView uv{a.uniq, max_uniq(R, E)};
-      uv.U()[0] = run;
-      int acc = 0;
-      for (int u = 0; u < run; ++u) {
-        uv.off()[u] = acc;
-        acc += s_cnt[u];
+    // CSR offsets of the distinct experts and the table of column groups (up to
+    // 8 routes of one expert each), by warp-wide exclusive scans
+    UniqView uv{a.uniq, max_uniq(R, E), R};
+    int acc = 0, gacc = 0;
+    for (int c = 0; c < run; c += 32) {
+      const int u = c + lane;
+      const int cnt = u < run ? s_cnt[u] : 0;
+      const int ng = (cnt + GROUP - 1) / GROUP;
+      int incl = cnt, gincl = ng;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        const int gv = __shfl_up_sync(0xffffffffu, gincl, o);
+        if (lane >= o) {
+          incl += v;
+          gincl += gv;
+        }
       }
+      if (u < run) {
+        const int off = acc + incl - cnt, g0 = gacc + gincl - ng;
+        s_off[u] = off;
+        uv.off()[u] = off;
+        for (int q = 0; q < ng; ++q) {
+          uv.gu()[g0 + q] = u;
+          uv.gn0()[g0 + q] = q * GROUP;
+        }
+      }
+      acc += __shfl_sync(0xffffffffu, incl, 31);
+      gacc += __shfl_sync(0xffffffffu, gincl, 31);
+    }
+    if (lane == 0) {
+      uv.U()[0] = run;
       uv.off()[run] = acc;
+      uv.G()[0] = gacc;
     }
   }
   __syncthreads();
   {
-    UniqView uv{a.uniq, max_uniq(R, E)};
+    UniqView uv{a.uniq, max_uniq(R, E), R};
     for (int r = tid; r < R; r += blockDim.x) {
       const int u = s_isfirst[s_first[s_ids[r]]];
       if (s_first[s_ids[r]] == r) uv.expert()[u] = s_ids[r];
-      uv.routes()[uv.off()[u] + s_pos[r]] = r;
+      uv.routes()[s_off[u] + s_pos[r]] = r;
     }
   }
 }
 
-// ------------------------------------------------------------------ rd_gateup
-// grid = maxU * nMB * S; block = 128 threads (4 warps x 16 rows of W1[e]).
-template <bool BLOCKWISE>
-__global__ void __launch_bounds__(THREADS) rd_gateup_kernel(DecodeArgs a, int nMB, int S) {
-  pdl_trigger();
-  pdl_wait();
-  const int unit = blockIdx.x;
-  const int s = unit % S;
-  const int mb = (unit / S) % nMB;
-  const int u = unit / (S * nMB);
-  UniqView uv{a.uniq, max_uniq(a.R, a.E)};
-  if (u >= uv.U()[0]) return;
-  const int e = uv.expert()[u];
-  const int r_beg = uv.off()[u], cnt = uv.off()[u + 1] - r_beg;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, tig = lane & 3;
-  const int twoI = 2 * a.I, H = a.H;
-  const int row = mb * ROWS_PER_CTA + warp * 16 + g;  // rows row and row+8 of W1[e]
-  const int KS = H / S;
-  const int k0 = s * KS;
-  const uint8_t* wrow0 = a.w1 + (static_cast<size_t>(e) * twoI + row) * H + 16 * tig;
-  const uint8_t* wrow1 = wrow0 + static_cast<size_t>(8) * H;
-  const int ng = H / 128;
+// ------------------------------------------------------------------ weight streaming
+// Shared layout of rd_gateup / rd_down (dynamic shared memory):
+//   [NS weight stages: CK/128 TMA boxes of 64 rows x 128 bytes]
+//   [operand: 8 rows x pitch][operand scales: 8 x K/128 fp32]
+//   [full[NS], empty[NS] mbarriers][abort flag]
+// Boxes are written with the 128-byte swizzle: 16-byte chunk c of row r sits
+// at chunk c ^ (r & 7).  MMA row g of a warp's 16-row slab is weight row
+// swz_row(g) = g/2 + 4 (g & 1), so the two rows read in one phase of a
+// 16-byte fragment load differ in bit 2 and their chunks never share a bank.
+// A staged operand row's pitch is 64 (mod 128) bytes, which does the same for
+// rows g and g + 1 of the operand.
+__host__ __device__ constexpr int swz_row(int g) { return (g >> 1) + 4 * (g & 1); }
 
-  for (int n0 = 0; n0 < cnt; n0 += 8) {
-    const int nn = min(8, cnt - n0);
-    const int my_r = g < nn ? uv.routes()[r_beg + n0 + g] : -1;  // route of token column g
-    const int my_t = my_r >= 0 ? my_r / a.k : 0;
-    const uint8_t* xrow = a.xq + static_cast<size_t>(my_t) * H + 16 * tig;
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
-    const int kend = k0 + KS;
-    if (!BLOCKWISE) {
-      // the loads of NB K-steps are issued before their MMAs: NB x 32 bytes of
-      // weights in flight per thread
-      constexpr int NB = 8;
-      for (int kb0 = k0; kb0 < kend; kb0 += 64 * NB) {
-        uint4 A0[NB], A1[NB], X[NB];
-#pragma unroll
-        for (int i = 0; i < NB; ++i) {
-          const int kk = kb0 + 64 * i;
-          const bool in = kk < kend;
-          A0[i] = in ? ld_stream(wrow0 + kk) : make_uint4(0, 0, 0, 0);
-          A1[i] = in ? ld_stream(wrow1 + kk) : make_uint4(0, 0, 0, 0);
-          X[i] = in && my_r >= 0 ? __ldg(reinterpret_cast<const uint4*>(xrow + kk)) : make_uint4(0, 0, 0, 0);
+// Address of the 16-byte fragment of weight row r (0..63), K bytes [kb, kb + 16)
+// of a stage (kb a multiple of 16).
+__device__ __forceinline__ const uint4* wfrag(const uint8_t* stage, int r, int kb) {
+  const int box = kb / BOXK, c = (kb % BOXK) / 16;
+  return reinterpret_cast<const uint4*>(stage + box * BOX_BYTES + r * BOXK + ((c ^ (r & 7)) * 16));
+}
+struct StreamSmem {
+  uint8_t* stages;
+  uint8_t* opnd;
+  float* osc;
+  uint64_t* full;
+  uint64_t* empty;
+  volatile int* abort_flag;
+};
+
+// Pitch of a staged operand row of K bytes: 64 (mod 128).
+__host__ __device__ inline int opnd_pitch(int K) { return (K + 127) / 128 * 128 + 64; }
+
+__host__ __device__ inline size_t stream_smem_bytes(int K) {
+  const size_t opnd = static_cast<size_t>(GROUP) * opnd_pitch(K);
+  const size_t osc = static_cast<size_t>(GROUP) * (K / 128) * 4;
+  return 1024 + static_cast<size_t>(NS) * STAGE_BYTES + opnd + ((osc + 15) / 16) * 16 + 2 * NS * 8 + 16;
+}
+
+__device__ __forceinline__ StreamSmem stream_smem(uint8_t* raw, int K) {
+  StreamSmem m;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  m.stages = base;  // swizzled TMA box destinations: 1024-byte aligned
+  m.opnd = base + NS * STAGE_BYTES;
+  m.osc = reinterpret_cast<float*>(m.opnd + GROUP * opnd_pitch(K));
+  const size_t osc = static_cast<size_t>(GROUP) * (K / 128) * 4;
+  m.full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(m.osc) + ((osc + 15) / 16) * 16);
+  m.empty = m.full + NS;
+  m.abort_flag = reinterpret_cast<volatile int*>(m.empty + NS);
+  return m;
+}
+
+// Producer side of the ring: streams the 64 rows [row0, row0 + 64) of the
+// weight matrix behind `map` (K bytes innermost), columns [k0, k0 + nbytes),
+// into successive stages, CK bytes (CK / 64 boxes) per stage.  Returns false
+// after an abort.
+__device__ __forceinline__ bool produce_rows(const StreamSmem& m, const CUtensorMap* map, int k0, int row0,
+                                             int nbytes, uint32_t& stage, uint32_t& phase, DeviceHeader* hdr,
+                                             unsigned int where) {
+  const int lane = threadIdx.x & 31;
+  for (int c = 0; c < nbytes; c += CK) {
+    const int bytes = min(CK, nbytes - c);
+    int good = 1;
+    if (lane == 0) good = mbar_wait(smem_u32(m.empty + stage), phase ^ 1, m.abort_flag, hdr, where);
+    if (!__shfl_sync(0xffffffffu, good, 0)) return false;
+    const uint32_t full = smem_u32(m.full + stage);
+    if (lane == 0) {
+      // whole boxes (a box past the end of a row is zero-filled by the TMA unit and
+      // its columns are never read); weights are read once: evict them from L2 first
+      const int nbox = (bytes + BOXK - 1) / BOXK;
+      mbar_arrive_expect_tx(full, static_cast<uint32_t>(nbox) * BOX_BYTES);
+      const uint32_t dst = smem_u32(m.stages + stage * STAGE_BYTES);
+      const uint64_t pol = l2_evict_first_policy();
+      for (int j = 0; j < nbox; ++j) tma_load_2d_hint(dst + j * BOX_BYTES, map, k0 + c + j * BOXK, row0, full, pol);
+    }
+    __syncwarp();
+    if (++stage == NS) {
+      stage = 0;
+      phase ^= 1;
+    }
+  }
+  return true;
+}
+
+// Ring setup by thread 0 (full: 1 arrival + bytes; empty: one arrival per consumer warp).
+__device__ __forceinline__ void init_ring(const StreamSmem& m) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(smem_u32(m.full + i), 1);
+      mbar_init(smem_u32(m.empty + i), CONSUMERS);
+    }
+    *m.abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+}
+
+// After an abort: let the producer's copies that are still in flight land
+// before the CTA exits (bounded).
+__device__ __forceinline__ void drain_ring(const StreamSmem& m, uint32_t stage, uint32_t phase, int issued) {
+  for (int i = 0; i < min(issued, NS); ++i) {
+    stage = (stage + NS - 1) % NS;
+    if (stage == NS - 1) phase ^= 1;
+    mbar_wait_quiet(smem_u32(m.full + stage), phase, 50000000ull);
+  }
+}
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * CONSUMERS) : "memory"); }
+
+// ------------------------------------------------------------------ rd_gateup
+// Persistent: two CTAs per SM, each walking a contiguous range of work items
+// (column group g, K split s, 64 rows mb of W1[e]) ordered so that consecutive
+// items share (g, s) and with it the staged x slice.  Per item the warps
+// compute a [64 rows x 8 routes] partial over the K slice [s*KS, (s+1)*KS).
+template <bool BLOCKWISE>
+__global__ void __launch_bounds__(THREADS, 2) rd_gateup_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmw2, DecodeArgs a,
+                     int nMB, int S, int KS, int down_grid) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  pdl_trigger();
+  const StreamSmem m = stream_smem(smem_raw, KS);
+  init_ring(m);
+  pdl_wait();
+  const UniqView uv{a.uniq, max_uniq(a.R, a.E), a.R};
+  const int G = *uv.G();
+  const int per_g = S * nMB;
+  const int N = G * per_g;
+  const int it0 = static_cast<int>(static_cast<long long>(N) * blockIdx.x / gridDim.x);
+  const int it1 = static_cast<int>(static_cast<long long>(N) * (blockIdx.x + 1) / gridDim.x);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int twoI = 2 * a.I, H = a.H;
+  const int xpitch = opnd_pitch(KS);
+
+  if (warp == CONSUMERS) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tensormap(&tmw);
+      prefetch_tensormap(&tmw2);
+    }
+    uint32_t stage = 0, phase = 0;
+    int issued = 0;
+    bool ok = true;
+    for (int it = it0; it < it1 && ok; ++it) {
+      const int g = it / per_g, rest = it - g * per_g, s = rest / nMB, mb = rest - s * nMB;
+      const int e = uv.expert()[uv.gu()[g]];
+      ok = produce_rows(m, &tmw, s * KS, e * twoI + mb * ROWS_PER_CTA, KS, stage, phase, a.hdr, 0x90000u);
+      issued += (KS + CK - 1) / CK;
+    }
+    if (!ok && lane == 0) drain_ring(m, stage, phase, issued);
+    // With its W1 boxes issued, the producer prefetches W2 into L2 for the Down
+    // kernel that follows: for each Down CTA d it serves, the first items of d's
+    // work range (the same split rd_down makes), up to kW2PrefetchBytes in all,
+    // so that the Down GEMV starts from L2 while this kernel's tail still runs.
+    if (ok) {
+      const int nHB = H / ROWS_PER_CTA, nbx = (a.I + BOXK - 1) / BOXK;
+      const long long Nd = static_cast<long long>(G) * nHB;
+      const double frac = fmin(1.0, static_cast<double>(kW2PrefetchBytes) / (static_cast<double>(Nd) * ROWS_PER_CTA * a.I));
+      for (int d = blockIdx.x; d < down_grid; d += gridDim.x) {
+        const long long i0 = Nd * d / down_grid, i1 = Nd * (d + 1) / down_grid;
+        const long long iend = i0 + static_cast<long long>(ceil(frac * static_cast<double>(i1 - i0)));
+        for (long long q = i0 * nbx + lane; q < iend * nbx; q += 32) {
+          const long long item = q / nbx;
+          const int bx = static_cast<int>(q - item * nbx);
+          const int g = static_cast<int>(item / nHB), hb = static_cast<int>(item - static_cast<long long>(g) * nHB);
+          tma_prefetch_2d(&tmw2, bx * BOXK, uv.expert()[uv.gu()[g]] * H + hb * ROWS_PER_CTA);
         }
-#pragma unroll
-        for (int i = 0; i < NB; ++i) mma_k64(c, A0[i], A1[i], X[i]);
       }
-    } else {
-      // per 128-wide K block: fresh partial, then scale by s_w1[e, row/128, kb] * s_x[t, kb]
-      const int rb = row / 128;
-      const int t0 = 2 * tig < nn ? uv.routes()[r_beg + n0 + 2 * tig] / a.k : 0;
-      const int t1 = 2 * tig + 1 < nn ? uv.routes()[r_beg + n0 + 2 * tig + 1] / a.k : 0;
-      const float* sw = a.w1_scale + (static_cast<size_t>(e) * (twoI / 128) + rb) * ng;
-      constexpr int NB = 4;  // 128-wide K blocks per batch of loads
-      for (int kb0 = k0; kb0 < kend; kb0 += 128 * NB) {
-        uint4 A0[NB], A1[NB], B0[NB], B1[NB], X0[NB], X1[NB];
+    }
+  } else {
+    // ---------------------------------------------------------------- consumers
+    const int g8 = lane >> 2, tig = lane & 3;
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    int cur = -1;  // (g, s) of the staged x slice
+    int u = 0, e = 0, r_beg = 0, nn = 0;
+    for (int it = it0; it < it1; ++it) {
+      const int g = it / per_g, rest = it - g * per_g, s = rest / nMB, mb = rest - s * nMB;
+      const int k0 = s * KS;
+      if (g * S + s != cur) {
+        // stage x of this group's tokens, K slice [k0, k0 + KS) (zeros for absent columns)
+        cur = g * S + s;
+        u = uv.gu()[g];
+        e = uv.expert()[u];
+        r_beg = uv.off()[u] + uv.gn0()[g];
+        nn = min(GROUP, uv.off()[u + 1] - r_beg);
+        consumer_sync();
+        // copy this group's e4m3 x rows, K slice [k0, k0 + KS), and their scales
+        // (zeros for absent columns); loads issued 8 at a time
+        const int c16 = KS / 16;
+        for (int base = 0; base < GROUP * c16; base += 8 * 32 * CONSUMERS) {
+          uint4 v[8];
 #pragma unroll
-        for (int i = 0; i < NB; ++i) {
-          const int kk = kb0 + 128 * i;
-          const bool in = kk < kend;
-          const uint4 z = make_uint4(0, 0, 0, 0);
-          A0[i] = in ? ld_stream(wrow0 + kk) : z;
-          A1[i] = in ? ld_stream(wrow1 + kk) : z;
-          B0[i] = in ? ld_stream(wrow0 + kk + 64) : z;
-          B1[i] = in ? ld_stream(wrow1 + kk + 64) : z;
-          X0[i] = in && my_r >= 0 ? __ldg(reinterpret_cast<const uint4*>(xrow + kk)) : z;
-          X1[i] = in && my_r >= 0 ? __ldg(reinterpret_cast<const uint4*>(xrow + kk + 64)) : z;
+          for (int j = 0; j < 8; ++j) {
+            const int i = base + threadIdx.x + j * 32 * CONSUMERS;
+            const int n = i / c16, c = i - n * c16;
+            v[j] = make_uint4(0, 0, 0, 0);
+            if (n < nn) {
+              const int t = uv.routes()[r_beg + n] / a.k;
+              v[j] = __ldg(reinterpret_cast<const uint4*>(a.xq + static_cast<size_t>(t) * H + k0) + c);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int i = base + threadIdx.x + j * 32 * CONSUMERS;
+            const int n = i / c16, c = i - n * c16;
+            if (n < GROUP) *reinterpret_cast<uint4*>(m.opnd + n * xpitch + c * 16) = v[j];
+          }
         }
+        if (BLOCKWISE) {
+          const int ng = H / 128, kb0 = k0 / 128, nkb = KS / 128;
+          for (int i = threadIdx.x; i < GROUP * nkb; i += 32 * CONSUMERS) {
+            const int n = i / nkb, q = i - n * nkb;
+            m.osc[i] = n < nn ? __ldg(a.sx + static_cast<size_t>(uv.routes()[r_beg + n] / a.k) * ng + kb0 + q) : 0.0f;
+          }
+        }
+        consumer_sync();
+      }
+      const int wr = warp * 16 + swz_row(g8);              // slab rows wr and wr + 8 of this item
+      const int row = mb * ROWS_PER_CTA + wr;               // rows row and row + 8 of W1[e]
+      const uint8_t* xs = m.opnd + g8 * xpitch + 16 * tig;
+      const float* sw = BLOCKWISE ? a.w1_scale + (static_cast<size_t>(e) * (twoI / 128) + row / 128) * (H / 128) : nullptr;
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int cc = 0; cc < KS; cc += CK) {
+        const int bytes = min(CK, KS - cc);
+        // every lane observes the stage's completion; the outcome is made
+        // warp-uniform before the (warp-synchronous) MMAs
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(m.full + stage), phase, m.abort_flag, a.hdr, 0x91000u));
+        if (ok) {
+          const uint8_t* st = m.stages + stage * STAGE_BYTES;
+          if (!BLOCKWISE) {
+            for (int kk = 0; kk < bytes; kk += 64) {
+              const uint4 A0 = *wfrag(st, wr, kk + 16 * tig);
+              const uint4 A1 = *wfrag(st, wr + 8, kk + 16 * tig);
+              const uint4 X = *reinterpret_cast<const uint4*>(xs + cc + kk);
+              mma_k64(c, A0, A1, X);
+            }
+          } else {
+            for (int kk = 0; kk < bytes; kk += 128) {
+              float cb[4] = {0.f, 0.f, 0.f, 0.f};
+              mma_k64(cb, *wfrag(st, wr, kk + 16 * tig), *wfrag(st, wr + 8, kk + 16 * tig),
+                      *reinterpret_cast<const uint4*>(xs + cc + kk));
+              mma_k64(cb, *wfrag(st, wr, kk + 64 + 16 * tig), *wfrag(st, wr + 8, kk + 64 + 16 * tig),
+                      *reinterpret_cast<const uint4*>(xs + cc + kk + 64));
+              const int q = (cc + kk) / 128;
+              const float w_s = __ldg(sw + k0 / 128 + q);
+              const float s0 = w_s * m.osc[(2 * tig) * (KS / 128) + q];
+              const float s1 = w_s * m.osc[(2 * tig + 1) * (KS / 128) + q];
+              c[0] = fmaf(cb[0], s0, c[0]);
+              c[1] = fmaf(cb[1], s1, c[1]);
+              c[2] = fmaf(cb[2], s0, c[2]);
+              c[3] = fmaf(cb[3], s1, c[3]);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(m.empty + stage));
+        if (++stage == NS) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      // c0: (row, col 2tig), c1: (row, col 2tig+1), c2/c3: row + 8
+      if (ok) {
+        float* part = a.part + static_cast<size_t>(s) * a.R * twoI;
 #pragma unroll
-        for (int i = 0; i < NB; ++i) {
-          const int kk = kb0 + 128 * i;
-          if (kk < kend) {
-            float cb[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_k64(cb, A0[i], A1[i], X0[i]);
-            mma_k64(cb, B0[i], B1[i], X1[i]);
-            const int kb = kk / 128;
-            const float w_s = __ldg(sw + kb);
-            const float s0 = w_s * __ldg(a.sx + static_cast<size_t>(t0) * ng + kb);
-            const float s1 = w_s * __ldg(a.sx + static_cast<size_t>(t1) * ng + kb);
-            c[0] = fmaf(cb[0], s0, c[0]);
-            c[1] = fmaf(cb[1], s1, c[1]);
-            c[2] = fmaf(cb[2], s0, c[2]);
-            c[3] = fmaf(cb[3], s1, c[3]);
+        for (int i = 0; i < 2; ++i) {
+          const int col = 2 * tig + i;
+          if (col < nn) {
+            const int r = uv.routes()[r_beg + col];
+            part[static_cast<size_t>(r) * twoI + row] = c[i];
+            part[static_cast<size_t>(r) * twoI + row + 8] = c[2 + i];
           }
         }
       }
     }
-    // c0: (row, col 2tig), c1: (row, col 2tig+1), c2/c3: row + 8
-    float* part = a.part + static_cast<size_t>(s) * a.R * twoI;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int col = 2 * tig + i;
-      if (col < nn) {
-        const int r = uv.routes()[r_beg + n0 + col];
-        part[static_cast<size_t>(r) * twoI + row] = c[i];
-        part[static_cast<size_t>(r) * twoI + row + 8] = c[2 + i];
-      }
-    }
   }
+  __syncthreads();
 }
 
 // Sum of the K-split partials of (route r, column i) and of (r, I + i); the
@@ -427,119 +647,135 @@ __global__ void __launch_bounds__(256) rd_reduce_block_kernel(DecodeArgs a) {
 }
 
 // ------------------------------------------------------------------ rd_down
-// grid = maxU * nHB; block = 128 threads (4 warps x 16 rows of W2[e]); K = I whole.
+// Persistent like rd_gateup: work items (column group g, 64 rows hb of W2[e]),
+// consecutive items share g and with it the staged h rows; K = I whole.
 template <bool BLOCKWISE>
-__global__ void __launch_bounds__(THREADS) rd_down_kernel(DecodeArgs a, int nHB) {
+__global__ void __launch_bounds__(THREADS, 2) rd_down_kernel(const __grid_constant__ CUtensorMap tmw, DecodeArgs a, int nHB) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
   pdl_trigger();
-  pdl_wait();
-  extern __shared__ uint8_t s_h[];  // [8][I] e4m3 of the current 8 routes, then [8][I/128] fp32 scales
-  const int hb = blockIdx.x % nHB;
-  const int u = blockIdx.x / nHB;
-  UniqView uv{a.uniq, max_uniq(a.R, a.E)};
-  if (u >= uv.U()[0]) return;
-  const int e = uv.expert()[u];
-  const int r_beg = uv.off()[u], cnt = uv.off()[u + 1] - r_beg;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, tig = lane & 3;
   const int I = a.I, H = a.H, ngi = I / 128;
-  float* s_sc = reinterpret_cast<float*>(s_h + 8 * I);
-  const int row = hb * ROWS_PER_CTA + warp * 16 + g;  // rows row and row+8 of W2[e] (output columns)
-  const uint8_t* wrow0 = a.w2 + (static_cast<size_t>(e) * H + row) * I + 16 * tig;
-  const uint8_t* wrow1 = wrow0 + static_cast<size_t>(8) * I;
-  const float amax_h = __uint_as_float(a.hdr->amax_h);
-  const float s_h_t = e4m3_scale(amax_h);
+  const StreamSmem m = stream_smem(smem_raw, I);
+  init_ring(m);
+  pdl_wait();
+  const UniqView uv{a.uniq, max_uniq(a.R, a.E), a.R};
+  const int G = *uv.G();
+  const int N = G * nHB;
+  const int it0 = static_cast<int>(static_cast<long long>(N) * blockIdx.x / gridDim.x);
+  const int it1 = static_cast<int>(static_cast<long long>(N) * (blockIdx.x + 1) / gridDim.x);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hpitch = opnd_pitch(I);
 
-  for (int n0 = 0; n0 < cnt; n0 += 8) {
-    const int nn = min(8, cnt - n0);
-    __syncthreads();
-    // stage the e4m3 h of these routes (zero rows for unused columns)
-    for (int i = threadIdx.x; i < 8 * I / 4; i += THREADS) {
-      const int n = (i * 4) / I, c = (i * 4) - n * I;
-      uint32_t q = 0;
-      if (n < nn) {
-        const int r = uv.routes()[r_beg + n0 + n];
+  if (warp == CONSUMERS) {
+    if (lane == 0) prefetch_tensormap(&tmw);
+    uint32_t stage = 0, phase = 0;
+    int issued = 0;
+    bool ok = true;
+    for (int it = it0; it < it1 && ok; ++it) {
+      const int g = it / nHB, hb = it - g * nHB;
+      const int e = uv.expert()[uv.gu()[g]];
+      ok = produce_rows(m, &tmw, 0, e * H + hb * ROWS_PER_CTA, I, stage, phase, a.hdr, 0x92000u);
+      issued += (I + CK - 1) / CK;
+    }
+    if (!ok && lane == 0) drain_ring(m, stage, phase, issued);
+  } else {
+    const int g8 = lane >> 2, tig = lane & 3;
+    const float s_h_t = BLOCKWISE ? 1.0f : e4m3_scale(__uint_as_float(a.hdr->amax_h));
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    int cur = -1;
+    int e = 0, r_beg = 0, nn = 0;
+    for (int it = it0; it < it1; ++it) {
+      const int g = it / nHB, hb = it - g * nHB;
+      if (g != cur) {
+        // stage the e4m3 h rows of this group's routes (zeros for absent columns)
+        cur = g;
+        const int u = uv.gu()[g];
+        e = uv.expert()[u];
+        r_beg = uv.off()[u] + uv.gn0()[g];
+        nn = min(GROUP, uv.off()[u + 1] - r_beg);
+        consumer_sync();
+        const int c4 = I / 4;
+        for (int i = threadIdx.x; i < GROUP * c4; i += 32 * CONSUMERS) {
+          const int n = i / c4, c = (i - n * c4) * 4;
+          uint32_t q = 0;
+          if (n < nn) {
+            const int r = uv.routes()[r_beg + n];
+            if (BLOCKWISE) {
+              q = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(a.act) + static_cast<size_t>(r) * I + c));
+            } else {
+              const float4 v = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(a.act) + static_cast<size_t>(r) * I + c));
+              q = static_cast<uint32_t>(cvt_e4m3x2(v.x / s_h_t, v.y / s_h_t)) |
+                  (static_cast<uint32_t>(cvt_e4m3x2(v.z / s_h_t, v.w / s_h_t)) << 16);
+            }
+          }
+          *reinterpret_cast<uint32_t*>(m.opnd + n * hpitch + c) = q;
+        }
         if (BLOCKWISE) {
-          q = *reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(a.act) + static_cast<size_t>(r) * I + c);
-        } else {
-          const float4 v = *reinterpret_cast<const float4*>(static_cast<const float*>(a.act) + static_cast<size_t>(r) * I + c);
-          q = static_cast<uint32_t>(cvt_e4m3x2(v.x / s_h_t, v.y / s_h_t)) |
-              (static_cast<uint32_t>(cvt_e4m3x2(v.z / s_h_t, v.w / s_h_t)) << 16);
+          for (int i = threadIdx.x; i < GROUP * ngi; i += 32 * CONSUMERS) {
+            const int n = i / ngi, q = i - n * ngi;
+            m.osc[i] = n < nn ? __ldg(a.sh + static_cast<size_t>(uv.routes()[r_beg + n]) * ngi + q) : 0.0f;
+          }
+        }
+        consumer_sync();
+      }
+      const int wr = warp * 16 + swz_row(g8);              // slab rows wr and wr + 8 of this item
+      const int row = hb * ROWS_PER_CTA + wr;               // rows row and row + 8 of W2[e]
+      const uint8_t* hs = m.opnd + g8 * hpitch + 16 * tig;
+      const float* sw = BLOCKWISE ? a.w2_scale + (static_cast<size_t>(e) * (H / 128) + row / 128) * ngi : nullptr;
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int cc = 0; cc < I; cc += CK) {
+        const int bytes = min(CK, I - cc);
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(m.full + stage), phase, m.abort_flag, a.hdr, 0x93000u));
+        if (ok) {
+          const uint8_t* st = m.stages + stage * STAGE_BYTES;
+          if (!BLOCKWISE) {
+            for (int kk = 0; kk < bytes; kk += 64)
+              mma_k64(c, *wfrag(st, wr, kk + 16 * tig), *wfrag(st, wr + 8, kk + 16 * tig),
+                      *reinterpret_cast<const uint4*>(hs + cc + kk));
+          } else {
+            for (int kk = 0; kk < bytes; kk += 128) {
+              float cb[4] = {0.f, 0.f, 0.f, 0.f};
+              mma_k64(cb, *wfrag(st, wr, kk + 16 * tig), *wfrag(st, wr + 8, kk + 16 * tig),
+                      *reinterpret_cast<const uint4*>(hs + cc + kk));
+              mma_k64(cb, *wfrag(st, wr, kk + 64 + 16 * tig), *wfrag(st, wr + 8, kk + 64 + 16 * tig),
+                      *reinterpret_cast<const uint4*>(hs + cc + kk + 64));
+              const int q = (cc + kk) / 128;
+              const float w_s = __ldg(sw + q);
+              const float s0 = w_s * m.osc[(2 * tig) * ngi + q];
+              const float s1 = w_s * m.osc[(2 * tig + 1) * ngi + q];
+              c[0] = fmaf(cb[0], s0, c[0]);
+              c[1] = fmaf(cb[1], s1, c[1]);
+              c[2] = fmaf(cb[2], s0, c[2]);
+              c[3] = fmaf(cb[3], s1, c[3]);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(m.empty + stage));
+        if (++stage == NS) {
+          stage = 0;
+          phase ^= 1;
         }
       }
-      *reinterpret_cast<uint32_t*>(s_h + n * I + c) = q;
-    }
-    if (BLOCKWISE) {
-      for (int i = threadIdx.x; i < 8 * ngi; i += THREADS) {
-        const int n = i / ngi, G = i - (i / ngi) * ngi;
-        s_sc[i] = n < nn ? a.sh[static_cast<size_t>(uv.routes()[r_beg + n0 + n]) * ngi + G] : 0.0f;
-      }
-    }
-    __syncthreads();
-    const uint8_t* xrow = s_h + g * I + 16 * tig;
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
-    if (!BLOCKWISE) {
-      constexpr int NB = 8;  // K-steps whose weight loads are issued before their MMAs
-      for (int kb0 = 0; kb0 < I; kb0 += 64 * NB) {
-        uint4 A0[NB], A1[NB];
+      if (ok) {
+        if (!BLOCKWISE) {
+          const float sc = s_h_t * __ldg(a.w2_scale + e);
 #pragma unroll
-        for (int i = 0; i < NB; ++i) {
-          const int kk = kb0 + 64 * i;
-          A0[i] = kk < I ? ld_stream(wrow0 + kk) : make_uint4(0, 0, 0, 0);
-          A1[i] = kk < I ? ld_stream(wrow1 + kk) : make_uint4(0, 0, 0, 0);
+          for (int i = 0; i < 4; ++i) c[i] *= sc;
         }
 #pragma unroll
-        for (int i = 0; i < NB; ++i) {
-          const int kk = kb0 + 64 * i;
-          if (kk < I) mma_k64(c, A0[i], A1[i], *reinterpret_cast<const uint4*>(xrow + kk));
-        }
-      }
-      const float sc = s_h_t * __ldg(a.w2_scale + e);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) c[i] *= sc;
-    } else {
-      const float* sw = a.w2_scale + (static_cast<size_t>(e) * (H / 128) + row / 128) * ngi;
-      constexpr int NB = 4;  // 128-wide K blocks per batch of loads
-      for (int kb0 = 0; kb0 < I; kb0 += 128 * NB) {
-        uint4 A0[NB], A1[NB], B0[NB], B1[NB];
-#pragma unroll
-        for (int i = 0; i < NB; ++i) {
-          const int kk = kb0 + 128 * i;
-          const bool in = kk < I;
-          const uint4 z = make_uint4(0, 0, 0, 0);
-          A0[i] = in ? ld_stream(wrow0 + kk) : z;
-          A1[i] = in ? ld_stream(wrow1 + kk) : z;
-          B0[i] = in ? ld_stream(wrow0 + kk + 64) : z;
-          B1[i] = in ? ld_stream(wrow1 + kk + 64) : z;
-        }
-#pragma unroll
-        for (int i = 0; i < NB; ++i) {
-          const int kk = kb0 + 128 * i;
-          if (kk < I) {
-            float cb[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_k64(cb, A0[i], A1[i], *reinterpret_cast<const uint4*>(xrow + kk));
-            mma_k64(cb, B0[i], B1[i], *reinterpret_cast<const uint4*>(xrow + kk + 64));
-            const int kb = kk / 128;
-            const float w_s = __ldg(sw + kb);
-            const float s0 = w_s * s_sc[(2 * tig) * ngi + kb];
-            const float s1 = w_s * s_sc[(2 * tig + 1) * ngi + kb];
-            c[0] = fmaf(cb[0], s0, c[0]);
-            c[1] = fmaf(cb[1], s1, c[1]);
-            c[2] = fmaf(cb[2], s0, c[2]);
-            c[3] = fmaf(cb[3], s1, c[3]);
+        for (int i = 0; i < 2; ++i) {
+          const int col = 2 * tig + i;
+          if (col < nn) {
+            const int r = uv.routes()[r_beg + col];
+            a.o[static_cast<size_t>(r) * H + row] = c[i];
+            a.o[static_cast<size_t>(r) * H + row + 8] = c[2 + i];
           }
         }
       }
     }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int col = 2 * tig + i;
-      if (col < nn) {
-        const int r = uv.routes()[r_beg + n0 + col];
-        a.o[static_cast<size_t>(r) * H + row] = c[i];
-        a.o[static_cast<size_t>(r) * H + row + 8] = c[2 + i];
-      }
-    }
   }
+  __syncthreads();
 }
 
 }  // namespace rd
@@ -547,7 +783,8 @@ __global__ void __launch_bounds__(THREADS) rd_down_kernel(DecodeArgs a, int nHB)
 size_t route_direct_uniq_bytes(int T, int E, int k) {
   const int R = T * k;
   const int mu = rd::max_uniq(R, E);
-  return static_cast<size_t>(2 + 2 * mu + R) * sizeof(int32_t);
+  const int mg = mu + R / rd::GROUP + 1;
+  return static_cast<size_t>(3 + 2 * mu + R + 2 * mg) * sizeof(int32_t);
 }
 
 cudaError_t launch_route_direct(const DecodeArgs& a, cudaStream_t s) {
@@ -584,11 +821,58 @@ cudaError_t launch_route_direct(const DecodeArgs& a, cudaStream_t s) {
   };
 
   const int nMB = 2 * a.I / ROWS_PER_CTA;
+  const int nHB = a.H / ROWS_PER_CTA;
+  const int KS = a.H / a.splits;
+  const int maxG = maxU + a.R / GROUP + 1;
+  const int sms = 2 * num_sms();  // two persistent CTAs per SM
+  if (sms <= 0) return cudaErrorNoDevice;
+  const size_t smem_gu = stream_smem_bytes(KS), smem_dn = stream_smem_bytes(a.I);
+  {
+    // raise the dynamic shared-memory limit once per instantiation to the largest size used
+    static size_t set_gu[2] = {0, 0}, set_dn[2] = {0, 0};
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lk(mu);
+    if (smem_gu > set_gu[bw]) {
+      err = bw ? cudaFuncSetAttribute(rd_gateup_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_gu)
+               : cudaFuncSetAttribute(rd_gateup_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_gu);
+      if (err != cudaSuccess) return err;
+      set_gu[bw] = smem_gu;
+    }
+    if (smem_dn > set_dn[bw]) {
+      err = bw ? cudaFuncSetAttribute(rd_down_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_dn)
+               : cudaFuncSetAttribute(rd_down_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_dn);
+      if (err != cudaSuccess) return err;
+      set_dn[bw] = smem_dn;
+    }
+  }
+
+  // weight matrices as 2D u8 tensors [rows][K bytes], boxes of 64 rows x 128 bytes, 128-byte swizzle
+  CUtensorMap tm1, tm2;
+  {
+    EncodeTiledFn fn = get_encode_tiled();
+    if (!fn) return cudaErrorInvalidValue;
+    auto enc = [&](CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows) {
+      const cuuint64_t dims[2] = {inner, rows};
+      const cuuint64_t strides[1] = {inner};
+      const cuuint32_t box[2] = {static_cast<cuuint32_t>(BOXK), static_cast<cuuint32_t>(ROWS_PER_CTA)};
+      const cuuint32_t estr[2] = {1, 1};
+      return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    if (!enc(&tm1, a.w1, a.H, static_cast<uint64_t>(a.E) * 2 * a.I) ||
+        !enc(&tm2, a.w2, a.I, static_cast<uint64_t>(a.E) * a.H))
+      return cudaErrorInvalidValue;
+  }
+
+  const long long dn_items = static_cast<long long>(maxG) * nHB;
+  const int down_grid = static_cast<int>(dn_items < sms ? dn_items : sms);
   stage_begin("rd_gateup", s);
   {
-    const cudaLaunchConfig_t c = config(maxU * nMB * a.splits, THREADS, 0);
-    err = bw ? cudaLaunchKernelEx(&c, rd_gateup_kernel<true>, a, nMB, a.splits)
-             : cudaLaunchKernelEx(&c, rd_gateup_kernel<false>, a, nMB, a.splits);
+    const long long items = static_cast<long long>(maxG) * nMB * a.splits;
+    const cudaLaunchConfig_t c = config(static_cast<unsigned>(items < sms ? items : sms), THREADS, smem_gu);
+    err = bw ? cudaLaunchKernelEx(&c, rd_gateup_kernel<true>, tm1, tm2, a, nMB, a.splits, KS, down_grid)
+             : cudaLaunchKernelEx(&c, rd_gateup_kernel<false>, tm1, tm2, a, nMB, a.splits, KS, down_grid);
   }
   stage_end(s);
   if (err != cudaSuccess) return err;
@@ -605,12 +889,11 @@ cudaError_t launch_route_direct(const DecodeArgs& a, cudaStream_t s) {
   stage_end(s);
   if (err != cudaSuccess) return err;
 
-  const int nHB = a.H / ROWS_PER_CTA;
-  const size_t smem = static_cast<size_t>(8) * a.I + 8 * (a.I / 128 + 1) * sizeof(float) + 16;
   stage_begin("rd_down", s);
   {
-    const cudaLaunchConfig_t c = config(maxU * nHB, THREADS, smem);
-    err = bw ? cudaLaunchKernelEx(&c, rd_down_kernel<true>, a, nHB) : cudaLaunchKernelEx(&c, rd_down_kernel<false>, a, nHB);
+    const cudaLaunchConfig_t c = config(static_cast<unsigned>(down_grid), THREADS, smem_dn);
+    err = bw ? cudaLaunchKernelEx(&c, rd_down_kernel<true>, tm2, a, nHB)
+             : cudaLaunchKernelEx(&c, rd_down_kernel<false>, tm2, a, nHB);
   }
   stage_end(s);
   return err;

@@ -50,8 +50,8 @@ struct ForwardLayout {
   size_t h = 0;       // grouped: [R, I] h in sorted order (bf16 or e4m3)
   size_t o = 0;       // grouped: [R, H] bf16 (route order); route-direct: [R, H] fp32
   // route-direct
-  size_t xq = 0;      // [T, H] e4m3
-  size_t sx = 0;      // [T, H/128] fp32 (blockwise) or [1] fp32 (per-tensor)
+  size_t xq = 0;      // [T, H] e4m3 x
+  size_t sx = 0;      // [T, H/128] fp32 (blockwise) or [1] fp32 (per-tensor) scales of x
   size_t uniq = 0;    // unique-expert table (see decode.cu)
   size_t part = 0;    // [S, R, 2I] fp32 split-K partials of Gate/Up
   size_t act = 0;     // per-tensor: [R, I] fp32 a;  blockwise: [R, I] e4m3 h

@@ -154,16 +154,20 @@ static moe_path resolve_path(const moe_problem& p) {
   return MOE_PATH_ROUTE_DIRECT;
 }
 
-// Number of K splits of the route-direct Gate/Up: enough CTAs to cover about
-// two waves of 148 SMs, each split a multiple of one 128-wide scale block and
-// at least 256 columns long.  Depends only on the shape, so the workspace size
-// is a pure function of the problem.
+// Number of K splits of the route-direct Gate/Up: the K slice of one work item
+// (H / splits bytes, a multiple of 128) at most 1024 bytes, so that two CTAs'
+// weight stages and 8-token x slices fit in one SM's shared memory, then
+// doubled while the items (distinct experts x 64-row blocks x splits, at most)
+// number fewer than three per SM of a 152-SM part and the slice stays at least
+// 512 bytes long.  Depends only on the shape, so the workspace size is a pure
+// function of the problem.
 static int route_direct_splits(const moe_problem& p) {
   const int R = p.T * p.k;
   const int maxU = R < p.E ? R : p.E;
-  const long long ctas = static_cast<long long>(maxU) * (2 * p.I / 64);
+  const long long items = static_cast<long long>(maxU) * (2 * p.I / 64);
   int s = 1;
-  while (ctas * s < 296 && (p.H / (2 * s)) % 128 == 0 && p.H / (2 * s) >= 256) s *= 2;
+  while (p.H / s > 1024 && (p.H / (2 * s)) % 128 == 0) s *= 2;
+  while (items * s < 3 * 152 && (p.H / (2 * s)) % 128 == 0 && p.H / (2 * s) >= 512) s *= 2;
   return s;
 }
 
@@ -188,6 +192,8 @@ static moe_status validate_shape(const moe_problem& p) {
   if (path == MOE_PATH_ROUTE_DIRECT) {
     if (p.quant == MOE_BF16) return MOE_ERR_UNSUPPORTED;
     if (static_cast<long long>(p.T) * p.k > kRouteDirectMaxRoutes) return MOE_ERR_UNSUPPORTED;
+    // shared-memory staging of one work item's operand rows
+    if (p.I > 4096 || p.H / route_direct_splits(p) > 4096) return MOE_ERR_UNSUPPORTED;
   }
   return MOE_OK;
 }
