@@ -550,6 +550,57 @@ def run_ours(args):
     print(json.dumps(line))
 
 
+# ----------------------------------------------------------------------------- single case (profiling)
+def run_case(args):
+    """One workload only, `--warmup` untimed then `--steps` timed calls, for
+    profiler captures: prefill | prefill_fp8_tensor | prefill_fp8_block (T from
+    --tokens, default 16384) or <decode sweep>:<B> (e.g. hunyuan:8).  Prints one
+    short JSON line (not a bench line)."""
+    import dataclasses
+
+    import torch
+
+    dev = torch.device("cuda", 0)
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import mixture_experts_layer_index_gb300 as m
+    import workloads as W
+
+    name = args.case
+    if ":" in name:
+        sweep, B = name.split(":")
+        wl = W.workload(sweep, int(B))
+        w1, w2, s1, s2 = W.make_weights(W.workload(sweep, 1), device=dev)
+    else:
+        quant = {"prefill": W.QUANT_BF16, "prefill_fp8_tensor": W.QUANT_FP8_TENSOR,
+                 "prefill_fp8_block": W.QUANT_FP8_BLOCK}[name]
+        wl = dataclasses.replace(W.workload(PREFILL), quant=quant, T=args.tokens or W.workload(PREFILL).T)
+        w1, w2, s1, s2 = W.make_weights(wl, device=dev)
+    x, sc = W.make_x(wl).to(dev), W.make_scores(wl).to(dev)
+    p = m.problem(wl.T, wl.E, wl.k, wl.H, wl.I, wl.quant)
+    ws = torch.empty(m.moe_workspace_size(p), dtype=torch.uint8, device=dev)
+    y = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(int(2.5 * 129e6) // 4, dtype=torch.float32, device=dev)
+    for i in range(args.warmup):
+        m.moe_forward(p, x, sc, w1, w2, s1, s2, y, ws)
+    torch.cuda.synchronize()
+    times = []
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        m.moe_forward(p, x, sc, w1, w2, s1, s2, y, ws)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) * 1000.0)
+    if m.moe_read_device_status(ws) != m.MOE_OK:
+        raise RuntimeError("device status not OK")
+    path = "route_direct" if m.moe_select_path(p) == m.MOE_PATH_ROUTE_DIRECT else "grouped"
+    print(json.dumps({"case": name, "T": wl.T, "quant": wl.quant, "path": path,
+                      "us_median_eager": round(statistics.median(times), 2), "steps": args.steps}))
+
+
 # ----------------------------------------------------------------------------- reference (oracle) arm
 def run_reference(args):
     rank, world, _ = dist_env()
@@ -606,10 +657,15 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override T of the prefill workload (smaller cases for profiling; not a bench line)")
+    ap.add_argument("--case", default="",
+                    help="run one workload only, for profiler captures: prefill, prefill_fp8_tensor, "
+                         "prefill_fp8_block (T from --tokens) or <decode sweep>:<B>; not a bench line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.impl == "reference":
+    if args.case:
+        run_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
