@@ -5,15 +5,18 @@
 // per (row, 128 columns), so every 128-wide K block has its own scale pair and
 // the products cannot be summed inside one accumulator.  Each K block is a
 // 128-byte stage of e4m3: the MMA thread writes that block's partial product
-// (tcgen05.mma kind::f8f6f4, M=128, N=128, 4 x K=32) into one of two TMEM
-// buffers, and the epilogue warps (one accumulator row per thread) read it with
-// tcgen05.ld, multiply by s_a[row, kb] * s_w[block, kb] and add it into fp32
-// registers ("promotion"), while the MMA fills the other buffer.
+// (tcgen05.mma kind::f8f6f4, M=128, N=128, 4 x K=32) into one of four TMEM
+// buffers, and eight epilogue warps read it with tcgen05.ld, multiply by
+// s_a[row, kb] * s_w[block, kb] and add it into fp32 registers ("promotion")
+// while the MMA fills the next buffers.  Two warps share each 32-lane TMEM
+// quadrant (one accumulator row per thread), each holding 64 of the 128
+// columns, so the loads of one warp overlap the FMAs of the other.
 //
 // Gate/Up: N = 64 gate + the matching 64 up rows of W1[e] (two 64-row TMA
-//   boxes), A = expert-sorted e4m3 x rows with their group scales; the epilogue
-//   writes a = silu(g) * u (fp32, sorted rows, 64 columns per tile); a separate
-//   pass quantises a per (row, 128 columns).
+//   boxes), A = expert-sorted e4m3 x rows with their group scales; a warp holds
+//   32 gate and the matching 32 up columns and writes a = silu(g) * u (fp32,
+//   sorted rows, 64 columns per tile); a separate pass quantises a per (row,
+//   128 columns).
 // Down: N = 128 rows of W2[e] (one weight scale block), A = e4m3 h rows with
 //   their group scales; the epilogue writes bf16 o to route slot perm[p].
 #include "common.cuh"
@@ -25,14 +28,24 @@ namespace gb {
 constexpr int BM = kGemmBM;  // 128
 constexpr int BN = 128;
 constexpr int BKB = 128;  // K bytes (= e4m3 elements) per stage, one scale block
-constexpr int STAGES = 6;
+constexpr int MAX_STAGES = 6;
+// Gate/Up: 6 stages, direct stores (each thread's 32 fp32 outputs are one
+// contiguous 128-byte piece); Down: 5 stages and 32 KB of output staging.
+__host__ __device__ constexpr int stages_of(int mode) { return mode == 0 ? 6 : 5; }
 constexpr int A_BYTES = BM * BKB;
 constexpr int B_BYTES = BN * BKB;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int TMEM_COLS = 256;  // two partial buffers of 128 columns
-constexpr int THREADS = 256;
-constexpr int NUM_BARS = 2 * STAGES + 4;
-constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+constexpr int NBUF = 4;           // TMEM partial buffers of 128 columns
+constexpr int TMEM_COLS = NBUF * BN;
+constexpr int EPI_WARPS = 8;      // warps 4..11
+constexpr int THREADS = 32 * (4 + EPI_WARPS);
+constexpr int NUM_BARS = 2 * MAX_STAGES + 2 * NBUF;
+// Down output staging: 32 rows x 128 bytes per epilogue warp, after the barriers
+__host__ __device__ constexpr int staging_offset(int mode) { return stages_of(mode) * STAGE_BYTES + 256; }
+constexpr int STAGING_BYTES = EPI_WARPS * 32 * 128;
+__host__ __device__ constexpr size_t smem_bytes(int mode) {
+  return 1024 + staging_offset(mode) + (mode == 0 ? 0 : STAGING_BYTES);
+}
 
 constexpr int MODE_GATEUP = 0;
 constexpr int MODE_DOWN = 1;
@@ -67,6 +80,7 @@ template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_blockwise_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const Params p) {
+  constexpr int STAGES = stages_of(MODE);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
@@ -75,16 +89,16 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
-  const uint32_t pfull0 = smem_u32(bars + 2 * STAGES), pempty0 = smem_u32(bars + 2 * STAGES + 2);
+  const uint32_t pfull0 = smem_u32(bars + 2 * STAGES), pempty0 = smem_u32(bars + 2 * STAGES + NBUF);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NBUF; ++b) {
       mbar_init(pfull0 + 8 * b, 1);
-      mbar_init(pempty0 + 8 * b, 128);
+      mbar_init(pempty0 + 8 * b, EPI_WARPS);  // one arrival per epilogue warp
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -176,19 +190,28 @@ __global__ void __launch_bounds__(THREADS, 1)
             stage = 0;
             phase ^= 1;
           }
-          pb ^= 1;
-          if (pb == 0) pphase ^= 1;
+          if (++pb == NBUF) {
+            pb = 0;
+            pphase ^= 1;
+          }
         }
       }
-      // wait for every MMA issued by this thread before TMEM is released
-      const uint32_t last = pfull0 + 8 * (pb ^ 1);
-      mbar_wait_quiet(last, pb == 0 ? (pphase ^ 1) : pphase, 1000000000ull);
+      // wait for every MMA issued by this thread before TMEM is released (the last
+      // committed buffer; a fresh barrier passes at once when nothing was issued)
+      const uint32_t lb = (pb + NBUF - 1) % NBUF;
+      mbar_wait_quiet(pfull0 + 8 * lb, pb == 0 ? (pphase ^ 1) : pphase, 1000000000ull);
     }
     __syncwarp();
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- epilogue (promotion)
-    const int q = warp - 4;
+    const int e8 = warp - 4;
+    const int q = e8 & 3;   // TMEM lane quadrant (warp % 4)
+    const int ch = e8 >> 2; // which 64 of the 128 columns
     const int row = q * 32 + lane;
+    // Gate/Up: gate columns [32ch, 32ch+32) and the matching up columns 64 + [32ch, ...);
+    // Down: columns [64ch, 64ch+64)
+    const int c0 = MODE == MODE_GATEUP ? ch * 32 : ch * 64;
+    const int c1 = MODE == MODE_GATEUP ? BN / 2 + ch * 32 : ch * 64 + 32;
     uint32_t pb = 0, pphase = 0;
     const int kblocks = p.K / 128;  // scale groups along K (K is a multiple of 128)
     bool ok = true;
@@ -198,7 +221,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int e = tl.x, row0 = tl.y, nrows = tl.z;
       const int arow = row0 + min(row, nrows - 1);
       const float* sa = p.a_scale + static_cast<size_t>(arow) * kblocks;
-      // weight scale rows of this tile's columns
+      // weight scale rows of this tile's columns (both halves in one block for Down)
       const float* swg;
       const float* swu;
       if (MODE == MODE_GATEUP) {
@@ -210,9 +233,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         swg = p.w_scale + (static_cast<size_t>(e) * hblk + n) * iblk;
         swu = swg;
       }
-      float acc[BN];
+      float acc[64];
 #pragma unroll
-      for (int i = 0; i < BN; ++i) acc[i] = 0.0f;
+      for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
       float sa_next = __ldg(sa), sg_next = __ldg(swg), su_next = __ldg(swu);
       for (int kb = 0; kb < nk; ++kb) {
         const float sak = sa_next, sgk = sg_next, suk = su_next;
@@ -229,39 +252,55 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         tc_fence_after();
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + pb * BN;
-        const float s0 = sak * sgk, s1 = sak * suk;
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_ld32(tbase + c * 32, v);
-          tmem_ld_wait();
-          const float sc = (MODE == MODE_GATEUP && c >= 2) ? s1 : s0;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(v[i], sc, acc[c * 32 + i]);
-        }
+        float v0[32], v1[32];
+        tmem_ld32(tbase + c0, v0);
+        tmem_ld32(tbase + c1, v1);
+        tmem_ld_wait();
+        // both column ranges are in registers: hand the buffer back before the FMAs
         tc_fence_before();
-        mbar_arrive(pempty0 + 8 * pb);
-        pb ^= 1;
-        if (pb == 0) pphase ^= 1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pempty0 + 8 * pb);
+        const float s0 = sak * sgk, s1 = sak * (MODE == MODE_GATEUP ? suk : sgk);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          acc[i] = fmaf(v0[i], s0, acc[i]);
+          acc[32 + i] = fmaf(v1[i], s1, acc[32 + i]);
+        }
+        if (++pb == NBUF) {
+          pb = 0;
+          pphase ^= 1;
+        }
       }
       if (!ok) break;
-      if (row < nrows) {
-        if (MODE == MODE_GATEUP) {
-          float* dst = p.out_f32 + static_cast<size_t>(row0 + row) * p.I + n * (BN / 2);
+      if (MODE == MODE_GATEUP) {
+        // each thread's 32 fp32 outputs are one contiguous 128-byte piece of its row
+        if (row < nrows) {
+          float* dst = p.out_f32 + static_cast<size_t>(row0 + row) * p.I + n * (BN / 2) + ch * 32;
 #pragma unroll
-          for (int i = 0; i < BN / 2; i += 4) {
-            const float4 a4 = make_float4(silu_mul(acc[i], acc[BN / 2 + i]), silu_mul(acc[i + 1], acc[BN / 2 + i + 1]),
-                                          silu_mul(acc[i + 2], acc[BN / 2 + i + 2]),
-                                          silu_mul(acc[i + 3], acc[BN / 2 + i + 3]));
-            if (n * (BN / 2) + i < p.I) *reinterpret_cast<float4*>(dst + i) = a4;
-          }
-        } else {
-          const int slot = __ldg(p.perm + row0 + row);
-          __nv_bfloat16* dst = p.out + static_cast<size_t>(slot) * p.H + n * BN;
-#pragma unroll
-          for (int i = 0; i < BN; i += 8)
-            if (n * BN + i < p.H) *reinterpret_cast<uint4*>(dst + i) = pack_bf16x8(acc + i);
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(dst + i) =
+                make_float4(silu_mul(acc[i], acc[32 + i]), silu_mul(acc[i + 1], acc[33 + i]),
+                            silu_mul(acc[i + 2], acc[34 + i]), silu_mul(acc[i + 3], acc[35 + i]));
         }
+      } else {
+        // Down rows go to scattered route slots: each thread's 64 bf16 outputs are
+        // staged in shared memory (16-byte pieces XOR-swizzled by row) and the warp
+        // writes four whole 128-byte row segments per store instruction.
+        uint4* stg = reinterpret_cast<uint4*>(smem + staging_offset(MODE)) + e8 * (32 * 8);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) stg[lane * 8 + (i ^ (lane & 7))] = pack_bf16x8(acc + 8 * i);
+        __syncwarp();
+        const int wrows = min(32, nrows - q * 32);  // valid rows of this warp (may be <= 0)
+        const int slot = row < nrows ? __ldg(p.perm + row0 + row) : 0;
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int r = it * 4 + (lane >> 3), j = lane & 7;
+          const int rslot = __shfl_sync(0xffffffffu, slot, r);
+          if (r < wrows)
+            *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(rslot) * p.H + n * BN + ch * 64 + j * 8) =
+                stg[r * 8 + (j ^ (r & 7))];
+        }
+        __syncwarp();
       }
     }
   }
@@ -288,7 +327,7 @@ static bool encode_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64
 template <int MODE>
 static cudaError_t smem_attr() {
   static const cudaError_t st = cudaFuncSetAttribute(grouped_blockwise_kernel<MODE>,
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes(MODE));
   return st;
 }
 
@@ -320,7 +359,7 @@ cudaError_t launch_gateup_blockwise(const GroupedArgs& a, const float* xs_scale,
   const long long units = static_cast<long long>(a.max_tiles) * p.nN;
   const int grid = static_cast<int>(units < sms ? units : sms);
   stage_begin("gateup_gemm", s);
-  grouped_blockwise_kernel<MODE_GATEUP><<<grid, THREADS, SMEM_BYTES, s>>>(tma, tmb, p);
+  grouped_blockwise_kernel<MODE_GATEUP><<<grid, THREADS, smem_bytes(MODE_GATEUP), s>>>(tma, tmb, p);
   err = cudaGetLastError();
   stage_end(s);
   return err;
@@ -352,7 +391,7 @@ cudaError_t launch_down_blockwise(const GroupedArgs& a, const float* h_scale, cu
   const long long units = static_cast<long long>(a.max_tiles) * p.nN;
   const int grid = static_cast<int>(units < sms ? units : sms);
   stage_begin("down_gemm", s);
-  grouped_blockwise_kernel<MODE_DOWN><<<grid, THREADS, SMEM_BYTES, s>>>(tma, tmb, p);
+  grouped_blockwise_kernel<MODE_DOWN><<<grid, THREADS, smem_bytes(MODE_DOWN), s>>>(tma, tmb, p);
   err = cudaGetLastError();
   stage_end(s);
   return err;

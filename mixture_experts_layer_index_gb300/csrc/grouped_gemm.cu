@@ -4,16 +4,18 @@
 //
 // One persistent CTA per SM walks work units (row tile, N tile) of a task map
 // built on the device (tile count read from device memory, no host sync).
-// Warp roles (256 threads):
+// Warp roles (256 threads; 384 for the FP8 Gate/Up):
 //   warp 0      TMA producer: A (activations) and B (weights) K-slices into a
 //               4-stage shared-memory ring, 128-byte swizzled.
 //   warp 1      one thread issues tcgen05.mma (M=128, N=256; K=16 bf16 or K=32
 //               e4m3 per instruction, fp32 accumulate) into one of two TMEM
 //               accumulators (2 x 256 columns).
 //   warp 2      allocates / frees the 512 TMEM columns.
-//   warps 4-7   epilogue: tcgen05.ld the accumulator (one row per thread),
-//               apply the fused epilogue and store (Down: staged in shared
-//               memory and written out as whole, coalesced row segments).
+//   warps 4+    epilogue, one warp per 32-lane TMEM quadrant (two for the FP8
+//               Gate/Up, each draining half of the accumulator's columns):
+//               tcgen05.ld (one row per thread), the fused epilogue, stores
+//               (Down: staged in shared memory and written out as whole,
+//               coalesced row segments).
 //
 // Gate/Up (MODE_GATEUP): A = the expert-sorted activation rows that the
 //   scatter kernel copied (plain TMA tile loads); or, as a selectable
@@ -42,11 +44,15 @@ constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;
-constexpr int THREADS = 256;
+// Epilogue warps (from warp 4): one or two per 32-lane TMEM quadrant.  Two, each
+// draining half of the accumulator's columns, pay off where the mainloop of a
+// tile is short next to its epilogue (FP8 Gate/Up: 16 K stages and fp32 output).
+__host__ __device__ constexpr int epi_warps(int mode, bool f8) { return (mode == 0 && f8) ? 8 : 4; }
+__host__ __device__ constexpr int threads_of(int mode, bool f8) { return 32 * (4 + epi_warps(mode, f8)); }
 constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
 // epilogue staging: 4 warps x 32 rows x 256 bytes, after the barriers
 constexpr int STAGING_OFFSET = STAGES * STAGE_BYTES + 256;
-constexpr int STAGING_BYTES = 4 * 32 * 256;
+constexpr int STAGING_BYTES = 4 * 32 * 256;  // Down: 32 rows x 256 bytes per epilogue warp
 constexpr size_t SMEM_BYTES = 1024 + STAGING_OFFSET + STAGING_BYTES;
 
 constexpr int MODE_GATEUP = 0;
@@ -88,7 +94,7 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
 // F8: e4m3 operands (tcgen05 kind::f8f6f4, 128 K elements per 128-byte stage
 // row, per-tensor scales applied in the epilogue); otherwise bf16 (kind::f16).
 template <int MODE, bool F8>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(threads_of(MODE, F8), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const Params p) {
   constexpr int BKE = F8 ? 128 : BK;  // K elements per stage
@@ -110,7 +116,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 128);
+      mbar_init(tempty0 + 8 * a, epi_warps(MODE, F8));  // one arrival per epilogue warp
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -240,7 +246,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- epilogue
-    const int q = warp - 4;  // TMEM lanes [32q, 32q+32)
+    // NH warps per 32-lane TMEM quadrant q; warp h of a quadrant drains 1/NH of
+    // the accumulator's columns (Gate/Up: its gate columns with the matching up
+    // columns; Down: a contiguous range of output columns).
+    constexpr int NH = epi_warps(MODE, F8) / 4;  // warps per TMEM quadrant
+    const int e8 = warp - 4;
+    const int q = e8 & 3, h = e8 >> 2;
     const int row = q * 32 + lane;
     uint32_t acc = 0, acc_phase = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
@@ -261,15 +272,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         float amax = 0.0f;
         __nv_bfloat16* out_row = p.out + static_cast<size_t>(row0 + row) * p.out_ld;
         float* out_row_f = F8 ? p.out_f32 + static_cast<size_t>(row0 + row) * p.out_ld : nullptr;
+        constexpr int GC = BN / 2 / NH;  // gate columns of this warp (and as many up columns)
 #pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 32) {
+        for (int c = h * GC; c < h * GC + GC; c += 32) {
           float g[32], up[32];
           tmem_ld32(tbase + c, g);
           tmem_ld32(tbase + BN / 2 + c, up);
           tmem_ld_wait();
-          if (c == BN / 2 - 32) {  // last columns read: hand the accumulator back to the MMA
+          if (c == h * GC + GC - 32) {  // this warp's last columns read: release the accumulator
             tc_fence_before();
-            mbar_arrive(tempty0 + 8 * acc);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
           }
           const int col = n * (BN / 2) + c;
           if (row < nrows && col < p.n_valid) {
@@ -301,6 +314,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // pieces XOR-swizzled by row, so both phases are bank-conflict free), then
         // the warp writes two whole 256-byte row segments per store instruction.
         // F8: o = s_h * s_w2[e] * acc.
+        static_assert(MODE == MODE_GATEUP || epi_warps(MODE, F8) == 4, "Down epilogue: one warp per TMEM quadrant");
         uint4* stg = reinterpret_cast<uint4*>(smem + STAGING_OFFSET) + q * (32 * 16);
         const int wrows = min(32, nrows - q * 32);  // valid rows of this warp (may be <= 0)
         const float post = F8 ? e4m3_scale(__uint_as_float(*p.amax_in)) * __ldg(p.wscale + tl.x) : 1.0f;
@@ -321,7 +335,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           if (pass == 1) {  // every accumulator column read: hand the buffer back to the MMA
             tc_fence_before();
-            mbar_arrive(tempty0 + 8 * acc);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * acc);  // one arrival per warp
           }
           __syncwarp();
           const int col0 = n * BN + pass * 128;
@@ -428,9 +443,9 @@ cudaError_t launch_gateup_bf16(const GroupedArgs& a, cudaStream_t s) {
   const int grid = static_cast<int>(units < sms ? units : sms);
   stage_begin("gateup_gemm", s);
   if (a.f8)
-    grouped_gemm_kernel<MODE_GATEUP, true><<<grid, THREADS, SMEM_BYTES, s>>>(tmx, tmw1, p);
+    grouped_gemm_kernel<MODE_GATEUP, true><<<grid, threads_of(MODE_GATEUP, true), SMEM_BYTES, s>>>(tmx, tmw1, p);
   else
-    grouped_gemm_kernel<MODE_GATEUP, false><<<grid, THREADS, SMEM_BYTES, s>>>(tmx, tmw1, p);
+    grouped_gemm_kernel<MODE_GATEUP, false><<<grid, threads_of(MODE_GATEUP, false), SMEM_BYTES, s>>>(tmx, tmw1, p);
   err = cudaGetLastError();
   stage_end(s);
   return err;
@@ -462,9 +477,9 @@ cudaError_t launch_down_bf16(const GroupedArgs& a, cudaStream_t s) {
   const int grid = static_cast<int>(units < sms ? units : sms);
   stage_begin("down_gemm", s);
   if (a.f8)
-    grouped_gemm_kernel<MODE_DOWN, true><<<grid, THREADS, SMEM_BYTES, s>>>(tmh, tmw2, p);
+    grouped_gemm_kernel<MODE_DOWN, true><<<grid, threads_of(MODE_DOWN, true), SMEM_BYTES, s>>>(tmh, tmw2, p);
   else
-    grouped_gemm_kernel<MODE_DOWN, false><<<grid, THREADS, SMEM_BYTES, s>>>(tmh, tmw2, p);
+    grouped_gemm_kernel<MODE_DOWN, false><<<grid, threads_of(MODE_DOWN, false), SMEM_BYTES, s>>>(tmh, tmw2, p);
   err = cudaGetLastError();
   stage_end(s);
   return err;
