@@ -26,11 +26,12 @@ __device__ __forceinline__ void rank_block(int* s_ids, int* s_lr, int* hist, int
                                            int32_t* __restrict__ lrank, int32_t* __restrict__ blockcounts,
                                            DeviceHeader* hdr) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int i = tid; i < 8 * E; i += kRouteThreads) hist[i] = 0;
+  constexpr int NW = kRouteThreads / 32;
+  for (int i = tid; i < NW * E; i += kRouteThreads) hist[i] = 0;
   __syncthreads();
 
   // each warp ranks a contiguous segment of the block's routes, 32 at a time, in order
-  const int seg = (RB + 8 * 32 - 1) / (8 * 32) * 32;
+  const int seg = (RB + NW * 32 - 1) / (NW * 32) * 32;
   int* my_hist = hist + warp * E;
   for (int c = 0; c < seg; c += 32) {
     const int rl = warp * seg + c + lane;
@@ -51,7 +52,7 @@ __device__ __forceinline__ void rank_block(int* s_ids, int* s_lr, int* hist, int
   for (int e = tid; e < E; e += kRouteThreads) {
     int run = 0;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
+    for (int w = 0; w < NW; ++w) {
       const int c = hist[w * E + e];
       hist[w * E + e] = run;
       run += c;
@@ -74,7 +75,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_rank_kernel(
   extern __shared__ int smem[];
   int* s_ids = smem;                          // [1024]
   int* s_lr = smem + kMaxRoutesPerBlock;      // [1024]
-  int* hist = smem + 2 * kMaxRoutesPerBlock;  // [8][E]
+  int* hist = smem + 2 * kMaxRoutesPerBlock;  // [warps][E]
   const int tid = threadIdx.x, warp = tid >> 5;
   const int blk = blockIdx.x;
   const int t0 = blk * TB;
@@ -83,7 +84,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_rank_kernel(
   const size_t r0 = static_cast<size_t>(t0) * k;
 
   if (ROUTE) {
-    // each warp routes every 8th token of the block; the next token's scores are
+    // each warp routes every NW-th token of the block; the next token's scores are
     // loaded while the current one is being routed
     constexpr int NW = kRouteThreads / 32;
     float cur[MAXV], nxt[MAXV];
@@ -295,7 +296,7 @@ cudaError_t launch_route_rank(const float* scores, const int32_t* ids_in, int T,
   if (T <= 0) return cudaSuccess;
   const int TB = route_tokens_per_block(k);
   const int nblk = (T + TB - 1) / TB;
-  const size_t smem = (2 * kMaxRoutesPerBlock + 8 * E) * sizeof(int);
+  const size_t smem = (2 * kMaxRoutesPerBlock + (kRouteThreads / 32) * E) * sizeof(int);
   int maxv = 1;
   while (maxv * 32 < E) maxv *= 2;
   const dim3 grid(nblk);
