@@ -107,11 +107,12 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 template <int MAXV>
 __global__ void __launch_bounds__(1024) rd_prep_kernel(DecodeArgs a) {
   __shared__ int s_ids[kRouteDirectMaxRoutes];
-  __shared__ int s_first[kMaxE];
-  __shared__ int s_isfirst[kRouteDirectMaxRoutes];
-  __shared__ int s_pos[kRouteDirectMaxRoutes];
-  __shared__ int s_cnt[kRouteDirectMaxRoutes];
+  __shared__ int s_u[kRouteDirectMaxRoutes];    // distinct-expert index of each route
+  __shared__ int s_pos[kRouteDirectMaxRoutes];  // position of each route in its expert's list
+  __shared__ int s_cnt[kRouteDirectMaxRoutes];  // routes per distinct expert
   __shared__ int s_off[kRouteDirectMaxRoutes];
+  __shared__ int s_e2u[kMaxE];
+  __shared__ unsigned s_seen[kMaxE / 32];
   __shared__ float s_red[32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
   const int T = a.T, E = a.E, k = a.k, H = a.H, R = a.R;
@@ -122,140 +123,65 @@ __global__ void __launch_bounds__(1024) rd_prep_kernel(DecodeArgs a) {
     a.hdr->amax_x = 0u;
     a.hdr->amax_h = 0u;
   }
-  // 1. routing, with the loads of the first batch of x issued before it so that
-  //    both memory round trips overlap
+  // x is quantised by warps 1..31 (NQ threads) while warp 0 builds the expert
+  // table; their first batch of x loads goes out before the routing so that both
+  // memory round trips overlap.
+  constexpr int NQ = 1024 - 32;
+  const int tq = tid - 32;
   const int n8 = T * H / 8;  // 16-byte pieces of x (8 values each)
   const uint4* x8 = static_cast<const uint4*>(a.x);
-  constexpr int XB = 4;      // pieces per thread per batch
+  constexpr int XB = 5;      // pieces per thread per batch
   uint4 xv[XB];
+  if (warp > 0) {
 #pragma unroll
-  for (int j = 0; j < XB; ++j) {
-    const int i = tid + j * blockDim.x;
-    xv[j] = i < n8 ? __ldg(x8 + i) : make_uint4(0, 0, 0, 0);
+    for (int j = 0; j < XB; ++j) {
+      const int i = tq + j * NQ;
+      xv[j] = i < n8 ? __ldg(x8 + i) : make_uint4(0, 0, 0, 0);
+    }
   }
+  // 1. routing: one warp per token
   for (int t = warp; t < T; t += nwarps)
     route_one_token<MAXV>(a.scores + static_cast<size_t>(t) * E, E, k, a.ids + static_cast<size_t>(t) * k,
                            a.w + static_cast<size_t>(t) * k, s_ids + t * k);
-  // 2. dynamic e4m3 quantisation of x: per tensor (s_x = amax / 448 over all of
-  //    x), or per (token, 128 columns) - piece i holds values [8i, 8i + 8), so 16
-  //    consecutive threads hold one 128-column group.  When x fits one batch
-  //    (T * H <= 8 * XB * 1024) it is read once, into registers.
-  const bool one_batch = n8 <= XB * static_cast<int>(blockDim.x);
-  float s_t = 1.0f;
-  if (a.quant == MOE_FP8_PER_TENSOR) {
-    float m = 0.0f;
-    for (int base = 0; base < n8; base += XB * blockDim.x) {
-      if (base > 0) {
-#pragma unroll
-        for (int j = 0; j < XB; ++j) {
-          const int i = base + tid + j * blockDim.x;
-          xv[j] = i < n8 ? __ldg(x8 + i) : make_uint4(0, 0, 0, 0);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < XB; ++j) {
-        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&xv[j]);
-#pragma unroll
-        for (int h2 = 0; h2 < 4; ++h2) {
-          const float2 f = __bfloat1622float2(b[h2]);
-          m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
-        }
-      }
-    }
-    m = warp_max(m);
-    if (lane == 0) s_red[warp] = m;
-    __syncthreads();
-    if (warp == 0) {
-      float v = lane < nwarps ? s_red[lane] : 0.0f;
-      v = warp_max(v);
-      if (lane == 0) s_red[0] = v;
-    }
-    __syncthreads();
-    s_t = e4m3_scale(s_red[0]);
-    if (tid == 0) {
-      a.sx[0] = s_t;
-      a.hdr->amax_x = __float_as_uint(s_red[0]);
-    }
-  }
-  for (int base = 0; base < n8; base += XB * blockDim.x) {
-    if (!(one_batch || (base == 0 && a.quant != MOE_FP8_PER_TENSOR))) {
-#pragma unroll
-      for (int j = 0; j < XB; ++j) {
-        const int i = base + tid + j * blockDim.x;
-        xv[j] = i < n8 ? __ldg(x8 + i) : make_uint4(0, 0, 0, 0);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < XB; ++j) {
-      const int i = base + tid + j * blockDim.x;  // i < n8 for all 16 threads of a group or none
-      float f[8];
-      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&xv[j]);
-#pragma unroll
-      for (int h2 = 0; h2 < 4; ++h2) {
-        const float2 v = __bfloat1622float2(b[h2]);
-        f[2 * h2] = v.x;
-        f[2 * h2 + 1] = v.y;
-      }
-      float sc = s_t;
-      if (a.quant == MOE_FP8_BLOCK128) {
-        float mx = 0.0f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) mx = fmaxf(mx, fabsf(f[q]));
-#pragma unroll
-        for (int o = 1; o < 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        sc = e4m3_scale(mx);
-        if (i < n8 && (i & 15) == 0) a.sx[i / 16] = sc;
-      }
-      if (i < n8) {
-        const uint32_t q0 = static_cast<uint32_t>(cvt_e4m3x2(f[0] / sc, f[1] / sc)) |
-                            (static_cast<uint32_t>(cvt_e4m3x2(f[2] / sc, f[3] / sc)) << 16);
-        const uint32_t q1 = static_cast<uint32_t>(cvt_e4m3x2(f[4] / sc, f[5] / sc)) |
-                            (static_cast<uint32_t>(cvt_e4m3x2(f[6] / sc, f[7] / sc)) << 16);
-        reinterpret_cast<uint2*>(a.xq)[i] = make_uint2(q0, q1);
-      }
-    }
-  }
-  // 3. distinct experts in first-use order, routes of each in route order
-  for (int e = tid; e < E; e += blockDim.x) s_first[e] = 0x7fffffff;
-  __syncthreads();
-  for (int r = tid; r < R; r += blockDim.x) atomicMin(&s_first[s_ids[r]], r);
-  __syncthreads();
-  for (int r = tid; r < R; r += blockDim.x) s_isfirst[r] = s_first[s_ids[r]] == r ? 1 : 0;
   __syncthreads();
   if (warp == 0) {
-    // exclusive scan of s_isfirst (first-use index of each distinct expert), and the
-    // position of every route within its expert's list, walking routes in order
+    // 2a. distinct experts in first-use order and the routes of each in route
+    //     order, by one warp walking the routes 32 at a time: a route is the first
+    //     use of its expert if it is the lowest lane of its expert in the chunk and
+    //     the expert was not seen in an earlier chunk.
+    UniqView uv{a.uniq, max_uniq(R, E), R};
+    for (int i = lane; i < kMaxE / 32; i += 32) s_seen[i] = 0u;
+    __syncwarp();
     int run = 0;
     for (int c = 0; c < R; c += 32) {
       const int r = c + lane;
-      const int f = r < R ? s_isfirst[r] : 0;
-      int incl = f;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
+      const bool valid = r < R;
+      const int e = valid ? s_ids[r] : 0;
+      const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1 - lane);
+      const int leader = __ffs(peers) - 1;
+      const bool first = valid && lane == leader && !((s_seen[e >> 5] >> (e & 31)) & 1u);
+      const unsigned fb = __ballot_sync(0xffffffffu, first);
+      if (first) {
+        const int un = run + __popc(fb & ((1u << lane) - 1u));
+        s_e2u[e] = un;
+        s_cnt[un] = 0;
+        uv.expert()[un] = e;
+        atomicOr(&s_seen[e >> 5], 1u << (e & 31));
       }
-      if (r < R) s_isfirst[r] = f ? run + incl - 1 : -1;  // u index for first routes
-      run += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    __syncwarp();
-    for (int u = lane; u < run; u += 32) s_cnt[u] = 0;
-    __syncwarp();
-    for (int c = 0; c < R; c += 32) {
-      const int r = c + lane;
-      const int u = r < R ? s_isfirst[s_first[s_ids[r]]] : -1 - lane;
-      const unsigned peers = __match_any_sync(0xffffffffu, u);
-      const int rank = __popc(peers & ((1u << lane) - 1u));
-      const int base = r < R ? s_cnt[u] : 0;
+      run += __popc(fb);
       __syncwarp();
-      if (r < R && rank == 0) s_cnt[u] = base + __popc(peers);
+      const int u = valid ? s_e2u[e] : 0;
+      const int base = valid ? s_cnt[u] : 0;
       __syncwarp();
-      if (r < R) s_pos[r] = base + rank;
+      if (valid && lane == leader) s_cnt[u] = base + __popc(peers);
+      if (valid) {
+        s_u[r] = u;
+        s_pos[r] = base + __popc(peers & ((1u << lane) - 1u));
+      }
+      __syncwarp();
     }
-    __syncwarp();
-    // CSR offsets of the distinct experts and the table of column groups (up to
-    // 8 routes of one expert each), by warp-wide exclusive scans
-    UniqView uv{a.uniq, max_uniq(R, E), R};
+    // 2b. CSR offsets of the distinct experts and the table of column groups (up
+    //     to 8 routes of one expert each), by warp-wide exclusive scans
     int acc = 0, gacc = 0;
     for (int c = 0; c < run; c += 32) {
       const int u = c + lane;
@@ -283,19 +209,92 @@ __global__ void __launch_bounds__(1024) rd_prep_kernel(DecodeArgs a) {
       acc += __shfl_sync(0xffffffffu, incl, 31);
       gacc += __shfl_sync(0xffffffffu, gincl, 31);
     }
+    __syncwarp();
+    for (int r = lane; r < R; r += 32) uv.routes()[s_off[s_u[r]] + s_pos[r]] = r;
     if (lane == 0) {
       uv.U()[0] = run;
       uv.off()[run] = acc;
       uv.G()[0] = gacc;
     }
-  }
-  __syncthreads();
-  {
-    UniqView uv{a.uniq, max_uniq(R, E), R};
-    for (int r = tid; r < R; r += blockDim.x) {
-      const int u = s_isfirst[s_first[s_ids[r]]];
-      if (s_first[s_ids[r]] == r) uv.expert()[u] = s_ids[r];
-      uv.routes()[s_off[u] + s_pos[r]] = r;
+  } else {
+    // 2c. dynamic e4m3 quantisation of x: per tensor (s_x = amax / 448 over all of
+    //     x), or per (token, 128 columns) - piece i holds values [8i, 8i + 8), so 16
+    //     consecutive threads hold one 128-column group.  When x fits one batch
+    //     (T * H <= 8 * XB * NQ) it is read once, into registers.
+    const bool one_batch = n8 <= XB * NQ;
+    float s_t = 1.0f;
+    if (a.quant == MOE_FP8_PER_TENSOR) {
+      float m = 0.0f;
+      for (int base = 0; base < n8; base += XB * NQ) {
+        if (base > 0) {
+#pragma unroll
+          for (int j = 0; j < XB; ++j) {
+            const int i = base + tq + j * NQ;
+            xv[j] = i < n8 ? __ldg(x8 + i) : make_uint4(0, 0, 0, 0);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < XB; ++j) {
+          const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&xv[j]);
+#pragma unroll
+          for (int h2 = 0; h2 < 4; ++h2) {
+            const float2 f = __bfloat1622float2(b[h2]);
+            m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+          }
+        }
+      }
+      m = warp_max(m);
+      if (lane == 0) s_red[warp] = m;
+      asm volatile("bar.sync 1, %0;" ::"n"(NQ) : "memory");
+      if (warp == 1) {
+        float v = lane > 0 ? s_red[lane] : 0.0f;  // warps 1..31
+        v = warp_max(v);
+        if (lane == 0) s_red[0] = v;
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(NQ) : "memory");
+      s_t = e4m3_scale(s_red[0]);
+      if (tq == 0) {
+        a.sx[0] = s_t;
+        a.hdr->amax_x = __float_as_uint(s_red[0]);
+      }
+    }
+    for (int base = 0; base < n8; base += XB * NQ) {
+      if (!(one_batch || (base == 0 && a.quant != MOE_FP8_PER_TENSOR))) {
+#pragma unroll
+        for (int j = 0; j < XB; ++j) {
+          const int i = base + tq + j * NQ;
+          xv[j] = i < n8 ? __ldg(x8 + i) : make_uint4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < XB; ++j) {
+        const int i = base + tq + j * NQ;  // i < n8 for all 16 threads of a group or none
+        float f[8];
+        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&xv[j]);
+#pragma unroll
+        for (int h2 = 0; h2 < 4; ++h2) {
+          const float2 v = __bfloat1622float2(b[h2]);
+          f[2 * h2] = v.x;
+          f[2 * h2 + 1] = v.y;
+        }
+        float sc = s_t;
+        if (a.quant == MOE_FP8_BLOCK128) {
+          float mx = 0.0f;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) mx = fmaxf(mx, fabsf(f[q]));
+#pragma unroll
+          for (int o = 1; o < 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          sc = e4m3_scale(mx);
+          if (i < n8 && (i & 15) == 0) a.sx[i / 16] = sc;
+        }
+        if (i < n8) {
+          const uint32_t q0 = static_cast<uint32_t>(cvt_e4m3x2(f[0] / sc, f[1] / sc)) |
+                              (static_cast<uint32_t>(cvt_e4m3x2(f[2] / sc, f[3] / sc)) << 16);
+          const uint32_t q1 = static_cast<uint32_t>(cvt_e4m3x2(f[4] / sc, f[5] / sc)) |
+                              (static_cast<uint32_t>(cvt_e4m3x2(f[6] / sc, f[7] / sc)) << 16);
+          reinterpret_cast<uint2*>(a.xq)[i] = make_uint2(q0, q1);
+        }
+      }
     }
   }
 }
