@@ -31,24 +31,68 @@ __global__ void __launch_bounds__(256) x_amax_kernel(const uint4* __restrict__ x
       }
     }
   }
+  __shared__ float s_m[8];
   m = warp_max(m);
-  if ((threadIdx.x & 31) == 0 && m > 0.0f) atomicMax(&hdr->amax_x, __float_as_uint(m));
+  if ((threadIdx.x & 31) == 0) s_m[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    m = threadIdx.x < (blockDim.x >> 5) ? s_m[threadIdx.x] : 0.0f;
+    m = warp_max(m);
+    if (threadIdx.x == 0 && m > 0.0f) atomicMax(&hdr->amax_x, __float_as_uint(m));  // one atomic per block
+  }
 }
 
-// Scatter fused with the gather and quantisation of the activations: one warp
-// per route writes perm/inv and the route's x row, quantised with s_x, to sorted
-// row p of xs (H bytes per row).
-__global__ void __launch_bounds__(256) scatter_gather_q_kernel(const int32_t* __restrict__ ids,
-                                                               const int32_t* __restrict__ lrank,
-                                                               const int32_t* __restrict__ blockbase, int R, int E,
-                                                               int RB, int k, int H, const uint4* __restrict__ x,
-                                                               uint4* __restrict__ xs, int32_t* __restrict__ perm,
-                                                               int32_t* __restrict__ inv, const DeviceHeader* hdr) {
-  const int lane = threadIdx.x & 31;
-  const int nw = (gridDim.x * blockDim.x) >> 5;
-  const float s = e4m3_scale(__uint_as_float(hdr->amax_x));
-  const int row16 = H / 16;  // 16 codes (16 bytes out, 32 bytes in) per chunk
-  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < R; r += nw) {
+// Scatter fused with the gather and quantisation of the activations, one block
+// per token: the block quantises the token's x row once into shared memory (with
+// s_x, or per 128 columns with a scale of its own: 16 consecutive threads hold a
+// group, 8 values each, and reduce its amax), then one warp per route writes
+// perm / inv and copies the e4m3 row (and its scales) to sorted row p of xs.
+template <bool BLOCKWISE>
+__global__ void __launch_bounds__(256) scatter_gather_tok_q_kernel(
+    const int32_t* __restrict__ ids, const int32_t* __restrict__ lrank, const int32_t* __restrict__ blockbase, int E,
+    int RB, int k, int H, const uint4* __restrict__ x, uint4* __restrict__ xs, float* __restrict__ xs_scale,
+    int32_t* __restrict__ perm, int32_t* __restrict__ inv, const DeviceHeader* hdr) {
+  extern __shared__ __align__(16) uint8_t s_row[];  // [H] e4m3, then [H/128] fp32 scales
+  float* s_sc = reinterpret_cast<float*>(s_row + H);
+  const int t = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n8 = H / 8;  // 8-value pieces of the row
+  const float st = BLOCKWISE ? 1.0f : e4m3_scale(__uint_as_float(hdr->amax_x));
+  const uint4* src = x + static_cast<size_t>(t) * n8;
+  for (int base = 0; base < n8; base += blockDim.x) {
+    const int c = base + tid;
+    const bool act = c < n8;  // whole 16-thread groups are active together (H % 128 == 0)
+    const uint4 v = act ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+    float f[8];
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 u = __bfloat1622float2(b[j]);
+      f[2 * j] = u.x;
+      f[2 * j + 1] = u.y;
+    }
+    float sc = st;
+    if (BLOCKWISE) {
+      float m = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      sc = e4m3_scale(m);
+      if (act && (c & 15) == 0) s_sc[c / 16] = sc;
+    }
+    if (act) {
+      const uint32_t q0 = static_cast<uint32_t>(cvt_e4m3x2(f[0] / sc, f[1] / sc)) |
+                          (static_cast<uint32_t>(cvt_e4m3x2(f[2] / sc, f[3] / sc)) << 16);
+      const uint32_t q1 = static_cast<uint32_t>(cvt_e4m3x2(f[4] / sc, f[5] / sc)) |
+                          (static_cast<uint32_t>(cvt_e4m3x2(f[6] / sc, f[7] / sc)) << 16);
+      *reinterpret_cast<uint2*>(s_row + 8 * c) = make_uint2(q0, q1);
+    }
+  }
+  __syncthreads();
+  const int row16 = H / 16, groups = H / 128;
+  for (int j = warp; j < k; j += blockDim.x >> 5) {
+    const int r = t * k + j;
     const int lr = lrank[r];
     if (lr < 0) {
       if (lane == 0) inv[r] = -1;
@@ -60,22 +104,10 @@ __global__ void __launch_bounds__(256) scatter_gather_q_kernel(const int32_t* __
       perm[p] = r;
       inv[r] = p;
     }
-    const uint4* src = x + static_cast<size_t>(r / k) * (H / 8);
     uint4* dst = xs + static_cast<size_t>(p) * row16;
-    for (int c = lane; c < row16; c += 32) {
-      const uint4 a = __ldg(src + 2 * c), b = __ldg(src + 2 * c + 1);
-      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
-      uint32_t q[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const __nv_bfloat162* pp = j < 2 ? pa : pb;
-        const float2 f0 = __bfloat1622float2(pp[(j & 1) * 2]), f1 = __bfloat1622float2(pp[(j & 1) * 2 + 1]);
-        q[j] = static_cast<uint32_t>(cvt_e4m3x2(f0.x / s, f0.y / s)) |
-               (static_cast<uint32_t>(cvt_e4m3x2(f1.x / s, f1.y / s)) << 16);
-      }
-      dst[c] = make_uint4(q[0], q[1], q[2], q[3]);
-    }
+    for (int c = lane; c < row16; c += 32) dst[c] = reinterpret_cast<const uint4*>(s_row)[c];
+    if (BLOCKWISE)
+      for (int g = lane; g < groups; g += 32) xs_scale[static_cast<size_t>(p) * groups + g] = s_sc[g];
   }
 }
 
@@ -87,74 +119,6 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const float4* __restric
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4; i += stride) {
     const float4 v = __ldg(a + i);
     h[i] = static_cast<uint32_t>(cvt_e4m3x2(v.x / s, v.y / s)) | (static_cast<uint32_t>(cvt_e4m3x2(v.z / s, v.w / s)) << 16);
-  }
-}
-
-// Blockwise variant of the fused scatter + gather + quantisation: one warp per
-// route; every 128-column group of the route's x row gets its own scale
-// (amax / 448 over the group), written to xs_scale[p][G] beside the codes.  A
-// pass covers 512 columns: lane l holds 16 values of group 4*pass + l/8, and
-// the group amax is reduced over its 8 lanes.  H is a multiple of 128.
-__global__ void __launch_bounds__(256) scatter_gather_qb_kernel(const int32_t* __restrict__ ids,
-                                                                const int32_t* __restrict__ lrank,
-                                                                const int32_t* __restrict__ blockbase, int R, int E,
-                                                                int RB, int k, int H, const uint4* __restrict__ x,
-                                                                uint4* __restrict__ xs, float* __restrict__ xs_scale,
-                                                                int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
-  const int lane = threadIdx.x & 31;
-  const int nw = (gridDim.x * blockDim.x) >> 5;
-  const int row16 = H / 16;
-  const int groups = H / 128;
-  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < R; r += nw) {
-    const int lr = lrank[r];
-    if (lr < 0) {
-      if (lane == 0) inv[r] = -1;
-      continue;
-    }
-    const int e = ids[r];
-    const int p = blockbase[static_cast<size_t>(r / RB) * E + e] + lr;
-    if (lane == 0) {
-      perm[p] = r;
-      inv[r] = p;
-    }
-    const uint4* src = x + static_cast<size_t>(r / k) * (H / 8);
-    uint4* dst = xs + static_cast<size_t>(p) * row16;
-    for (int base = 0; base < row16; base += 32) {
-      const int c = base + lane;
-      const bool act = c < row16;  // whole 8-lane groups are active together (H % 128 == 0)
-      uint4 a = make_uint4(0, 0, 0, 0), b = a;
-      if (act) {
-        a = __ldg(src + 2 * c);
-        b = __ldg(src + 2 * c + 1);
-      }
-      float f[16];
-      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 u = __bfloat1622float2(pa[j]), v = __bfloat1622float2(pb[j]);
-        f[2 * j] = u.x;
-        f[2 * j + 1] = u.y;
-        f[8 + 2 * j] = v.x;
-        f[8 + 2 * j + 1] = v.y;
-      }
-      float m = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(f[j]));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-      const float s = e4m3_scale(m);
-      if (act) {
-        uint32_t q[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          q[j] = static_cast<uint32_t>(cvt_e4m3x2(f[4 * j] / s, f[4 * j + 1] / s)) |
-                 (static_cast<uint32_t>(cvt_e4m3x2(f[4 * j + 2] / s, f[4 * j + 3] / s)) << 16);
-        dst[c] = make_uint4(q[0], q[1], q[2], q[3]);
-        if ((lane & 7) == 0) xs_scale[static_cast<size_t>(p) * groups + c / 8] = s;
-      }
-    }
   }
 }
 
@@ -203,18 +167,31 @@ cudaError_t launch_x_amax(const void* x, size_t n, DeviceHeader* hdr, cudaStream
   return err;
 }
 
-cudaError_t launch_scatter_gather_q(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
-                                    int k, int H, const void* x, void* xs, int32_t* perm, int32_t* inv,
-                                    const DeviceHeader* hdr, cudaStream_t s) {
-  const int R = T * k;
-  if (R <= 0) return cudaSuccess;
+static cudaError_t launch_tok_q(bool blockwise, const int32_t* ids, const int32_t* lrank, const int32_t* blockbase,
+                                int T, int E, int k, int H, const void* x, void* xs, float* xs_scale, int32_t* perm,
+                                int32_t* inv, const DeviceHeader* hdr, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
   const int RB = route_tokens_per_block(k) * k;
+  const size_t smem = static_cast<size_t>(H) + static_cast<size_t>(H / 128) * sizeof(float);
+  if (smem > 48 * 1024) return cudaErrorInvalidValue;  // H <= 47K: far above any supported shape
   stage_begin("scatter_gather", s);
-  scatter_gather_q_kernel<<<grid_for(static_cast<size_t>(R) * 32, 256), 256, 0, s>>>(
-      ids, lrank, blockbase, R, E, RB, k, H, static_cast<const uint4*>(x), static_cast<uint4*>(xs), perm, inv, hdr);
+  if (blockwise)
+    scatter_gather_tok_q_kernel<true><<<T, 256, smem, s>>>(ids, lrank, blockbase, E, RB, k, H,
+                                                           static_cast<const uint4*>(x), static_cast<uint4*>(xs),
+                                                           xs_scale, perm, inv, hdr);
+  else
+    scatter_gather_tok_q_kernel<false><<<T, 256, smem, s>>>(ids, lrank, blockbase, E, RB, k, H,
+                                                            static_cast<const uint4*>(x), static_cast<uint4*>(xs),
+                                                            nullptr, perm, inv, hdr);
   const cudaError_t err = cudaGetLastError();
   stage_end(s);
   return err;
+}
+
+cudaError_t launch_scatter_gather_q(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
+                                    int k, int H, const void* x, void* xs, int32_t* perm, int32_t* inv,
+                                    const DeviceHeader* hdr, cudaStream_t s) {
+  return launch_tok_q(false, ids, lrank, blockbase, T, E, k, H, x, xs, nullptr, perm, inv, hdr, s);
 }
 
 cudaError_t launch_quant_rows(const float* a, void* h, size_t n, const DeviceHeader* hdr, cudaStream_t s) {
@@ -231,16 +208,7 @@ cudaError_t launch_quant_rows(const float* a, void* h, size_t n, const DeviceHea
 cudaError_t launch_scatter_gather_qb(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
                                      int k, int H, const void* x, void* xs, float* xs_scale, int32_t* perm,
                                      int32_t* inv, cudaStream_t s) {
-  const int R = T * k;
-  if (R <= 0) return cudaSuccess;
-  const int RB = route_tokens_per_block(k) * k;
-  stage_begin("scatter_gather", s);
-  scatter_gather_qb_kernel<<<grid_for(static_cast<size_t>(R) * 32, 256), 256, 0, s>>>(
-      ids, lrank, blockbase, R, E, RB, k, H, static_cast<const uint4*>(x), static_cast<uint4*>(xs), xs_scale, perm,
-      inv);
-  const cudaError_t err = cudaGetLastError();
-  stage_end(s);
-  return err;
+  return launch_tok_q(true, ids, lrank, blockbase, T, E, k, H, x, xs, xs_scale, perm, inv, nullptr, s);
 }
 
 cudaError_t launch_quant_groups(const float* a, void* h, float* sh, int rows, int cols, cudaStream_t s) {
