@@ -233,41 +233,39 @@ __global__ void scatter_kernel(const int32_t* __restrict__ ids, const int32_t* _
   inv[r] = p;
 }
 
-// Scatter fused with the gather of the activations: one warp per route writes
-// perm/inv like scatter_kernel and copies the route's x row (H bf16) to sorted
-// row p of xs, so the Gate/Up GEMM reads its A tiles as plain contiguous boxes.
+// Scatter fused with the gather of the activations, one block per token: the
+// block first places the token's k routes (perm/inv like scatter_kernel), then
+// reads the token's x row once, one 16-byte piece per thread and pass, and
+// stores each piece to the sorted row p of every route, so the Gate/Up GEMM
+// reads its A tiles as plain contiguous boxes and x is read from DRAM once.
 __global__ void __launch_bounds__(256) scatter_gather_kernel(const int32_t* __restrict__ ids,
                                                              const int32_t* __restrict__ lrank,
-                                                             const int32_t* __restrict__ blockbase, int R, int E,
-                                                             int RB, int k, int H, const uint4* __restrict__ x,
+                                                             const int32_t* __restrict__ blockbase, int E, int RB,
+                                                             int k, int H, const uint4* __restrict__ x,
                                                              uint4* __restrict__ xs, int32_t* __restrict__ perm,
                                                              int32_t* __restrict__ inv) {
-  const int lane = threadIdx.x & 31;
-  const int nw = (gridDim.x * blockDim.x) >> 5;
-  const int row16 = H / 8;  // 16-byte chunks per row
-  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < R; r += nw) {
+  __shared__ int s_p[kMaxK];
+  const int t = blockIdx.x;
+  for (int j = threadIdx.x; j < k; j += blockDim.x) {
+    const int r = t * k + j;
     const int lr = lrank[r];
-    if (lr < 0) {
-      if (lane == 0) inv[r] = -1;
-      continue;
-    }
-    const int e = ids[r];
-    const int p = blockbase[static_cast<size_t>(r / RB) * E + e] + lr;
-    if (lane == 0) {
+    int p = -1;
+    if (lr >= 0) {
+      p = blockbase[static_cast<size_t>(r / RB) * E + ids[r]] + lr;
       perm[p] = r;
-      inv[r] = p;
     }
-    const uint4* src = x + static_cast<size_t>(r / k) * row16;
-    uint4* dst = xs + static_cast<size_t>(p) * row16;
-    int c = lane;
-    for (; c + 32 * 7 < row16; c += 32 * 8) {
-      uint4 v[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = __ldg(src + c + 32 * i);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) dst[c + 32 * i] = v[i];
+    inv[r] = p;
+    s_p[j] = p;
+  }
+  __syncthreads();
+  const int row16 = H / 8;  // 16-byte pieces per row
+  const uint4* src = x + static_cast<size_t>(t) * row16;
+  for (int c = threadIdx.x; c < row16; c += blockDim.x) {
+    const uint4 v = __ldg(src + c);
+    for (int j = 0; j < k; ++j) {
+      const int p = s_p[j];
+      if (p >= 0) xs[static_cast<size_t>(p) * row16 + c] = v;
     }
-    for (; c < row16; c += 32) dst[c] = __ldg(src + c);
   }
 }
 
@@ -340,17 +338,11 @@ cudaError_t launch_scatter(const int32_t* ids, const int32_t* lrank, const int32
 cudaError_t launch_scatter_gather(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
                                   int k, int H, const void* x, void* xs, int32_t* perm, int32_t* inv,
                                   cudaStream_t s) {
-  const int R = T * k;
-  if (R <= 0) return cudaSuccess;
+  if (T <= 0) return cudaSuccess;
   const int RB = route_tokens_per_block(k) * k;
-  const int sms = num_sms();
-  long long blocks = (static_cast<long long>(R) + 7) / 8;
-  const long long cap = static_cast<long long>(sms > 0 ? sms : 148) * 16;
-  if (blocks > cap) blocks = cap;
   stage_begin("scatter_gather", s);
-  scatter_gather_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(ids, lrank, blockbase, R, E, RB, k, H,
-                                                                 static_cast<const uint4*>(x),
-                                                                 static_cast<uint4*>(xs), perm, inv);
+  scatter_gather_kernel<<<T, 256, 0, s>>>(ids, lrank, blockbase, E, RB, k, H, static_cast<const uint4*>(x),
+                                          static_cast<uint4*>(xs), perm, inv);
   const cudaError_t err = cudaGetLastError();
   stage_end(s);
   return err;
