@@ -490,6 +490,29 @@ cudaError_t launch_down_bf16(const GroupedArgs& a, cudaStream_t s) {
 // (the final top-k reduction of the route-MMA page's Motivation, reading
 // route-order rows contiguously as its Code changes do for reduce.cu).  Deterministic: no
 // atomics, fixed summation order.
+// Loads the 8 values of route row r at column c as fp32.
+template <typename OT>
+__device__ __forceinline__ void combine_load8(const OT* __restrict__ o, size_t r, int H, int c, float (&v)[8],
+                                              uint64_t pol) {
+  if (sizeof(OT) == 2) {
+    const uint4 raw = ld_nc_v4_hint(o + r * H + c, pol);
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(b[i]);
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  } else {
+    const float4 f0 = __ldg(reinterpret_cast<const float4*>(o + r * H + c));
+    const float4 f1 = __ldg(reinterpret_cast<const float4*>(o + r * H + c) + 1);
+    v[0] = f0.x; v[1] = f0.y; v[2] = f0.z; v[3] = f0.w;
+    v[4] = f1.x; v[5] = f1.y; v[6] = f1.z; v[7] = f1.w;
+  }
+}
+
+// The k rows of a token are loaded four at a time before any of them is summed,
+// so each thread keeps four loads in flight; the sum still runs j ascending.
 template <typename OT>
 __global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ o, const float* __restrict__ w, int T,
                                                       int k, int H, __nv_bfloat16* __restrict__ y) {
@@ -498,32 +521,32 @@ __global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ o, 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int cpt = H / 8;
   const size_t total = static_cast<size_t>(T) * cpt;
+  const uint64_t pol = l2_evict_first_policy();
   for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < total;
        idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const int t = static_cast<int>(idx / cpt);
     const int c = static_cast<int>(idx - static_cast<size_t>(t) * cpt) * 8;
+    const size_t r0 = static_cast<size_t>(t) * k;
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      const size_t r = static_cast<size_t>(t) * k + j;
-      const float wj = __ldg(w + r);
-      float v[8];
-      if (sizeof(OT) == 2) {
-        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(o + r * H + c));
-        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    int j = 0;
+    for (; j + 4 <= k; j += 4) {
+      float v[4][8], wj[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __bfloat1622float2(b[i]);
-          v[2 * i] = f.x;
-          v[2 * i + 1] = f.y;
-        }
-      } else {
-        const float4 f0 = __ldg(reinterpret_cast<const float4*>(o + r * H + c));
-        const float4 f1 = __ldg(reinterpret_cast<const float4*>(o + r * H + c) + 1);
-        v[0] = f0.x; v[1] = f0.y; v[2] = f0.z; v[3] = f0.w;
-        v[4] = f1.x; v[5] = f1.y; v[6] = f1.z; v[7] = f1.w;
+      for (int q = 0; q < 4; ++q) {
+        wj[q] = __ldg(w + r0 + j + q);
+        combine_load8(o, r0 + j + q, H, c, v[q], pol);
       }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[q], v[q][i], acc[i]);
+    }
+    for (; j < k; ++j) {
+      float v[8];
+      const float wj = __ldg(w + r0 + j);
+      combine_load8(o, r0 + j, H, c, v, pol);
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
     }
