@@ -144,6 +144,11 @@ __device__ __forceinline__ uint4 ld_nc_v4_hint(const void* p, uint64_t policy) {
   return v;
 }
 
+// Prefetch `bytes` of global memory at p into L2 (both multiples of 16 bytes).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Prefetch the box at {c0, c1} of `map` into L2 (no shared-memory destination).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(c0), "r"(c1)

@@ -51,6 +51,9 @@ constexpr int BOX_BYTES = ROWS_PER_CTA * BOXK;
 constexpr int STAGE_BYTES = ROWS_PER_CTA * CK;  // CK / BOXK boxes, each [64 rows][128 bytes]
 constexpr int GROUP = 8;          // routes per MMA column group (m16n8k32: N = 8)
 constexpr double kW2PrefetchBytes = 64.0 * 1024 * 1024;  // W2 prefetched into L2 during Gate/Up
+constexpr long long kW1PrefetchBytes = 64ll * 1024 * 1024;  // W1 prefetched into L2 by rd_prep
+constexpr uint32_t kPrefetchChunk = 64 * 1024;             // bytes per L2 prefetch instruction
+constexpr long long kPrefetchPerCta = 256 * 1024;          // W1 bytes per prefetch CTA of rd_prep
 
 // Table of distinct experts, in int32 words:
 //   [0] U;  [1 .. 1+maxU) expert of u;  [1+maxU .. 2+2maxU) CSR offsets of u;
@@ -117,6 +120,52 @@ __global__ void __launch_bounds__(1024) rd_prep_kernel(DecodeArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
   const int T = a.T, E = a.E, k = a.k, H = a.H, R = a.R;
   pdl_trigger();
+  if (blockIdx.x > 0) {
+    // W1 prefetch role (every CTA but the first): repeat the routing (scores
+    // only, no outputs), list the distinct experts in first-use order as the
+    // table below does, and start this CTA's share of their W1 matrices - whole
+    // matrices in that order, up to kW1PrefetchBytes in all - on its way into
+    // L2, so rd_gateup streams them from L2.  One SM issues bulk prefetches at
+    // a few hundred GB/s, hence the spread over many CTAs.
+    if (warp == 0)
+      for (int i = lane; i < kMaxE / 32; i += 32) s_seen[i] = 0u;
+    for (int t = warp; t < T; t += nwarps)
+      route_one_token<MAXV>(a.scores + static_cast<size_t>(t) * E, E, k, nullptr, nullptr, s_ids + t * k);
+    __syncthreads();
+    const long long w1_bytes = 2ll * a.I * H;
+    const int maxp = static_cast<int>(kW1PrefetchBytes / w1_bytes < kMaxE ? kW1PrefetchBytes / w1_bytes : kMaxE);
+    if (warp == 0) {
+      int run = 0;
+      for (int c = 0; c < R && run < maxp; c += 32) {
+        const int r = c + lane;
+        const bool valid = r < R;
+        const int e = valid ? s_ids[r] : 0;
+        const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1 - lane);
+        const bool first = valid && lane == __ffs(peers) - 1 && !((s_seen[e >> 5] >> (e & 31)) & 1u);
+        const unsigned fb = __ballot_sync(0xffffffffu, first);
+        const int n = run + __popc(fb & ((1u << lane) - 1u));
+        if (first) {
+          if (n < maxp) s_u[n] = e;
+          atomicOr(&s_seen[e >> 5], 1u << (e & 31));
+        }
+        run += __popc(fb);
+        __syncwarp();
+      }
+      if (lane == 0) s_cnt[0] = run < maxp ? run : maxp;
+    }
+    __syncthreads();
+    const int nd = s_cnt[0];
+    const long long nch = (w1_bytes + kPrefetchChunk - 1) / kPrefetchChunk;
+    const long long npf = gridDim.x - 1;
+    for (long long q = (blockIdx.x - 1) + npf * tid; q < nd * nch; q += npf * blockDim.x) {
+      const int u = static_cast<int>(q / nch);
+      const long long off = (q - u * nch) * kPrefetchChunk;
+      const long long left = w1_bytes - off;
+      bulk_prefetch_l2(a.w1 + static_cast<size_t>(s_u[u]) * w1_bytes + off,
+                       static_cast<uint32_t>(left < kPrefetchChunk ? left : kPrefetchChunk));
+    }
+    return;
+  }
   if (tid == 0) {
     a.hdr->status = 0u;
     a.hdr->info = 0u;
@@ -791,13 +840,23 @@ cudaError_t launch_route_direct(const DecodeArgs& a, cudaStream_t s) {
   if (a.T <= 0) return cudaSuccess;
   int maxv = 1;
   while (maxv * 32 < a.E) maxv *= 2;
+  // one prep CTA, plus prefetch CTAs of about kPrefetchPerCta of W1 each for the
+  // most W1 the batch can select (distinct experts <= min(T k, E)), within the budget
+  const long long w1_bytes = 2ll * a.I * a.H;
+  const long long cap = kW1PrefetchBytes / w1_bytes * w1_bytes;
+  const long long most = static_cast<long long>(max_uniq(a.R, a.E)) * w1_bytes;
+  const long long pf = most < cap ? most : cap;
+  const int nsm = num_sms();
+  long long npf = (pf + kPrefetchPerCta - 1) / kPrefetchPerCta;
+  if (npf > nsm - 1) npf = nsm > 1 ? nsm - 1 : 0;
+  const unsigned pgrid = 1u + static_cast<unsigned>(npf);
   stage_begin("rd_prep", s);
   switch (maxv) {
-    case 1: rd_prep_kernel<1><<<1, 1024, 0, s>>>(a); break;
-    case 2: rd_prep_kernel<2><<<1, 1024, 0, s>>>(a); break;
-    case 4: rd_prep_kernel<4><<<1, 1024, 0, s>>>(a); break;
-    case 8: rd_prep_kernel<8><<<1, 1024, 0, s>>>(a); break;
-    default: rd_prep_kernel<16><<<1, 1024, 0, s>>>(a); break;
+    case 1: rd_prep_kernel<1><<<pgrid, 1024, 0, s>>>(a); break;
+    case 2: rd_prep_kernel<2><<<pgrid, 1024, 0, s>>>(a); break;
+    case 4: rd_prep_kernel<4><<<pgrid, 1024, 0, s>>>(a); break;
+    case 8: rd_prep_kernel<8><<<pgrid, 1024, 0, s>>>(a); break;
+    default: rd_prep_kernel<16><<<pgrid, 1024, 0, s>>>(a); break;
   }
   cudaError_t err = cudaGetLastError();
   stage_end(s);

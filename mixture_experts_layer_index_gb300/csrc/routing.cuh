@@ -40,7 +40,7 @@ __device__ __forceinline__ void load_scores(const float* __restrict__ srow, int 
 }
 
 // Route one token from its scores already in registers.  Lane j < k writes
-// slot j: ids_row[j], w_row[j] and (if given) s_ids_row[j].
+// slot j of each output that is given: ids_row[j], w_row[j], s_ids_row[j].
 template <int MAXV>
 __device__ __forceinline__ void route_values(const float (&v)[MAXV], int E, int k, int32_t* __restrict__ ids_row,
                                              float* __restrict__ w_row, int* s_ids_row) {
@@ -78,8 +78,8 @@ __device__ __forceinline__ void route_values(const float (&v)[MAXV], int E, int 
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   if (lane < k) {
-    ids_row[lane] = my_id;
-    w_row[lane] = ev / sum;
+    if (ids_row) ids_row[lane] = my_id;
+    if (w_row) w_row[lane] = ev / sum;
     if (s_ids_row) s_ids_row[lane] = my_id;
   }
 }
