@@ -50,8 +50,8 @@ constexpr int BOXK = 128;         // K bytes of one TMA box (64 rows x 128 bytes
 constexpr int BOX_BYTES = ROWS_PER_CTA * BOXK;
 constexpr int STAGE_BYTES = ROWS_PER_CTA * CK;  // CK / BOXK boxes, each [64 rows][128 bytes]
 constexpr int GROUP = 8;          // routes per MMA column group (m16n8k32: N = 8)
-constexpr double kW2PrefetchBytes = 64.0 * 1024 * 1024;  // W2 prefetched into L2 during Gate/Up
-constexpr long long kW1PrefetchBytes = 64ll * 1024 * 1024;  // W1 prefetched into L2 by rd_prep
+constexpr double kW2PrefetchBytes = 16.0 * 1024 * 1024;  // W2 prefetched into L2 during Gate/Up
+constexpr long long kW1PrefetchBytes = 96ll * 1024 * 1024;  // W1 prefetched into L2 by rd_prep
 constexpr uint32_t kPrefetchChunk = 64 * 1024;             // bytes per L2 prefetch instruction
 constexpr long long kPrefetchPerCta = 256 * 1024;          // W1 bytes per prefetch CTA of rd_prep
 
@@ -651,6 +651,32 @@ __device__ __forceinline__ void sum_splits(const float* part, int splits, int R,
 
 // ------------------------------------------------------------------ rd_reduce
 // per-tensor: one thread per (route, i); blockwise: one warp per (route, 128-column group).
+// Four consecutive columns [i, i + 4) at once (i a multiple of 4): one 16-byte load
+// per split for g and for u, all splits of a batch in flight together; the sums
+// run over the splits in the same ascending order as sum_splits.
+__device__ __forceinline__ void sum_splits4(const float* part, int splits, int R, int twoI, int I, int r, int i,
+                                            float (&g)[4], float (&u)[4]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) g[q] = u[q] = 0.f;
+  for (int s0 = 0; s0 < splits; s0 += 8) {
+    float4 gv[8], uv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int s = s0 + j < splits ? s0 + j : 0;
+      const float* pp = part + (static_cast<size_t>(s) * R + r) * twoI;
+      gv[j] = *reinterpret_cast<const float4*>(pp + i);
+      uv[j] = *reinterpret_cast<const float4*>(pp + I + i);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (s0 + j < splits) {
+        g[0] += gv[j].x; g[1] += gv[j].y; g[2] += gv[j].z; g[3] += gv[j].w;
+        u[0] += uv[j].x; u[1] += uv[j].y; u[2] += uv[j].z; u[3] += uv[j].w;
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(256) rd_reduce_tensor_kernel(DecodeArgs a) {
   pdl_trigger();
   pdl_wait();
@@ -677,14 +703,10 @@ __global__ void __launch_bounds__(256) rd_reduce_block_kernel(DecodeArgs a) {
   const int I = a.I, twoI = 2 * I, ngi = I / 128;
   if (gw >= a.R * ngi) return;
   const int r = gw / ngi, G = gw - (gw / ngi) * ngi;
-  float av[4];
+  float av[4], g[4], u[4];
+  sum_splits4(a.part, a.splits, a.R, twoI, I, r, G * 128 + lane * 4, g, u);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int i = G * 128 + lane * 4 + q;
-    float g, u;
-    sum_splits(a.part, a.splits, a.R, twoI, I, r, i, g, u);
-    av[q] = silu_mul(g, u);
-  }
+  for (int q = 0; q < 4; ++q) av[q] = silu_mul(g[q], u[q]);
   float m = fmaxf(fmaxf(fabsf(av[0]), fabsf(av[1])), fmaxf(fabsf(av[2]), fabsf(av[3])));
   m = warp_max(m);
   const float sc = e4m3_scale(m);

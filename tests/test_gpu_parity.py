@@ -201,6 +201,9 @@ SMALL_GROUPED = [
     W.Workload("onetok", 1, 16, 8, 512, 256, W.QUANT_BF16, 23),
     W.Workload("kEqE", 20, 4, 4, 128, 64, W.QUANT_BF16, 24),
     W.Workload("tails", 300, 6, 2, 320, 320, W.QUANT_BF16, 25),   # counts not multiples of 128
+    # k = 32 (the largest top-k) and an x row of 544 16-byte pieces: more than one pass
+    # of the per-token scatter's 256 threads, and eight 4-row batches in the combine
+    W.Workload("bigk", 40, 64, 32, 4352, 256, W.QUANT_BF16, 26),
 ]
 
 
