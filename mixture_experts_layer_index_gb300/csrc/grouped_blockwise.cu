@@ -18,7 +18,7 @@
 //   sorted rows, 64 columns per tile); a separate pass quantises a per (row,
 //   128 columns).
 // Down: N = 128 rows of W2[e] (one weight scale block), A = e4m3 h rows with
-//   their group scales; the epilogue writes bf16 o to route slot perm[p].
+//   their group scales; the epilogue writes bf16 o for the tile's sorted rows.
 #include "common.cuh"
 #include "internal.h"
 
@@ -283,15 +283,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                             silu_mul(acc[i + 2], acc[34 + i]), silu_mul(acc[i + 3], acc[35 + i]));
         }
       } else {
-        // Down rows go to scattered route slots: each thread's 64 bf16 outputs are
-        // staged in shared memory (16-byte pieces XOR-swizzled by row) and the warp
-        // writes four whole 128-byte row segments per store instruction.
+        // Down rows (sorted order, like h): each thread's 64 bf16 outputs are staged
+        // in shared memory (16-byte pieces XOR-swizzled by row) and the warp writes
+        // four whole 128-byte row segments per store instruction.
         uint4* stg = reinterpret_cast<uint4*>(smem + staging_offset(MODE)) + e8 * (32 * 8);
 #pragma unroll
         for (int i = 0; i < 8; ++i) stg[lane * 8 + (i ^ (lane & 7))] = pack_bf16x8(acc + 8 * i);
         __syncwarp();
         const int wrows = min(32, nrows - q * 32);  // valid rows of this warp (may be <= 0)
-        const int slot = row < nrows ? __ldg(p.perm + row0 + row) : 0;
+        const int slot = row0 + row;
 #pragma unroll
         for (int it = 0; it < 8; ++it) {
           const int r = it * 4 + (lane >> 3), j = lane & 7;

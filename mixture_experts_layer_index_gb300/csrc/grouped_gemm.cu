@@ -25,8 +25,9 @@
 //   matching gate and up columns; the epilogue writes h = bf16(silu(g) * u)
 //   (or fp32 a for the FP8 path) for sorted rows, columns [n0, n0+128).
 // Down (MODE_DOWN): A = h rows of the tile, B = 256 rows of W2[e]; the
-//   epilogue writes bf16 o for sorted row p to route slot perm[p], so the
-//   combine reads each token's k rows contiguously.
+//   epilogue writes bf16 o in the same expert-sorted row order as h, so the
+//   8 N tiles of one row tile together fill a contiguous block of o; the
+//   combine finds route r's row at inv[r].
 #include <cstdio>
 #include <mutex>
 
@@ -309,7 +310,7 @@ __global__ void __launch_bounds__(threads_of(MODE, F8), 1)
           if (lane == 0 && amax > 0.0f) atomicMax(p.amax_out, __float_as_uint(amax));
         }
       } else {
-        // Down: o rows go to scattered route slots.  Each pass stages 128 bf16
+        // Down: o rows in sorted order.  Each pass stages 128 bf16
         // columns (256 bytes) of every row of the warp in shared memory (16-byte
         // pieces XOR-swizzled by row, so both phases are bank-conflict free), then
         // the warp writes two whole 256-byte row segments per store instruction.
@@ -318,7 +319,7 @@ __global__ void __launch_bounds__(threads_of(MODE, F8), 1)
         uint4* stg = reinterpret_cast<uint4*>(smem + STAGING_OFFSET) + q * (32 * 16);
         const int wrows = min(32, nrows - q * 32);  // valid rows of this warp (may be <= 0)
         const float post = F8 ? e4m3_scale(__uint_as_float(*p.amax_in)) * __ldg(p.wscale + tl.x) : 1.0f;
-        const int slot = row < nrows ? __ldg(p.perm + row0 + row) : 0;
+        const int slot = row0 + row;
 #pragma unroll 1
         for (int pass = 0; pass < 2; ++pass) {
 #pragma unroll
@@ -486,15 +487,19 @@ cudaError_t launch_down_bf16(const GroupedArgs& a, cudaStream_t s) {
 }
 
 // ------------------------------------------------------------------ combine
-// y[t, c] = bf16( sum_{j < k} w[t, j] * o[t*k + j, c] ), fp32, j ascending
-// (the final top-k reduction of the route-MMA page's Motivation, reading
-// route-order rows contiguously as its Code changes do for reduce.cu).  Deterministic: no
-// atomics, fixed summation order.
+// y[t, c] = bf16( sum_{j < k} w[t, j] * o[row(t*k + j), c] ), fp32, j ascending
+// (the final top-k reduction of the route-MMA page's Motivation), with
+// row(r) = inv[r] for the grouped path's expert-sorted o and row(r) = r for the
+// route-direct path's route-order o.  Deterministic: no atomics, fixed
+// summation order.
 // Loads the 8 values of route row r at column c as fp32.
 template <typename OT>
-__device__ __forceinline__ void combine_load8(const OT* __restrict__ o, size_t r, int H, int c, float (&v)[8],
+__device__ __forceinline__ void combine_load8(const OT* __restrict__ o, long long r, int H, int c, float (&v)[8],
                                               uint64_t pol) {
-  if (sizeof(OT) == 2) {
+  if (r < 0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+  } else if (sizeof(OT) == 2) {
     const uint4 raw = ld_nc_v4_hint(o + r * H + c, pol);
     const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
@@ -515,7 +520,8 @@ __device__ __forceinline__ void combine_load8(const OT* __restrict__ o, size_t r
 // so each thread keeps four loads in flight; the sum still runs j ascending.
 template <typename OT>
 __global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ o, const float* __restrict__ w, int T,
-                                                      int k, int H, __nv_bfloat16* __restrict__ y) {
+                                                      int k, int H, __nv_bfloat16* __restrict__ y,
+                                                      const int32_t* __restrict__ inv) {
   // launched as a programmatic dependent (route-direct path): wait for the producer
   // of o; a no-op for an ordinary launch
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -536,7 +542,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ o, 
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         wj[q] = __ldg(w + r0 + j + q);
-        combine_load8(o, r0 + j + q, H, c, v[q], pol);
+        combine_load8(o, inv ? __ldg(inv + r0 + j + q) : static_cast<long long>(r0 + j + q), H, c, v[q], pol);
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q)
@@ -546,7 +552,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ o, 
     for (; j < k; ++j) {
       float v[8];
       const float wj = __ldg(w + r0 + j);
-      combine_load8(o, r0 + j, H, c, v, pol);
+      combine_load8(o, inv ? __ldg(inv + r0 + j) : static_cast<long long>(r0 + j), H, c, v, pol);
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
     }
@@ -573,9 +579,9 @@ cudaError_t launch_combine_pdl(const CombineArgs& a, cudaStream_t s) {
   stage_begin("combine", s);
   const cudaError_t err =
       a.o_is_f32 ? cudaLaunchKernelEx(&cfg, combine_kernel<float>, static_cast<const float*>(a.o), a.w, a.T, a.k, a.H,
-                                      static_cast<__nv_bfloat16*>(a.y))
+                                      static_cast<__nv_bfloat16*>(a.y), a.inv)
                  : cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, static_cast<const __nv_bfloat16*>(a.o), a.w,
-                                      a.T, a.k, a.H, static_cast<__nv_bfloat16*>(a.y));
+                                      a.T, a.k, a.H, static_cast<__nv_bfloat16*>(a.y), a.inv);
   stage_end(s);
   return err;
 }
@@ -590,10 +596,10 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
   stage_begin("combine", s);
   if (a.o_is_f32)
     combine_kernel<float><<<static_cast<int>(blocks), 256, 0, s>>>(static_cast<const float*>(a.o), a.w, a.T, a.k,
-                                                                   a.H, static_cast<__nv_bfloat16*>(a.y));
+                                                                   a.H, static_cast<__nv_bfloat16*>(a.y), a.inv);
   else
     combine_kernel<__nv_bfloat16><<<static_cast<int>(blocks), 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(a.o), a.w, a.T, a.k, a.H, static_cast<__nv_bfloat16*>(a.y));
+        static_cast<const __nv_bfloat16*>(a.o), a.w, a.T, a.k, a.H, static_cast<__nv_bfloat16*>(a.y), a.inv);
   const cudaError_t err = cudaGetLastError();
   stage_end(s);
   return err;

@@ -48,7 +48,7 @@ struct ForwardLayout {
   size_t xs_scale = 0;  // grouped blockwise FP8: [R, H/128] fp32 scales of xs
   size_t a32 = 0;     // grouped FP8: [R, I] fp32 a before its quantisation
   size_t h = 0;       // grouped: [R, I] h in sorted order (bf16 or e4m3)
-  size_t o = 0;       // grouped: [R, H] bf16 (route order); route-direct: [R, H] fp32
+  size_t o = 0;       // grouped: [R, H] bf16 (sorted order); route-direct: [R, H] fp32 (route order)
   // route-direct
   size_t xq = 0;      // [T, H] e4m3 x
   size_t sx = 0;      // [T, H/128] fp32 (blockwise) or [1] fp32 (per-tensor) scales of x
@@ -119,10 +119,11 @@ cudaError_t launch_down_blockwise(const GroupedArgs& a, const float* h_scale, cu
 
 struct CombineArgs {
   int T, k, H;
-  const void* o;       // [R, H] route order
+  const void* o;       // [R, H]
   bool o_is_f32;
   const float* w;      // [R]
   void* y;             // [T, H] bf16
+  const int32_t* inv;  // row of route r in o (expert-sorted o), or null: o in route order
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
 // Same, launched as a programmatic dependent of the previous kernel on the stream.

@@ -437,7 +437,7 @@ moe_status moe_forward(const moe_problem* pp, const void* x, const float* scores
       }
     }
     if (e == cudaSuccess) {
-      CombineArgs c{p.T, p.k, p.H, at<void*>(ws, L.o), false, w, y};
+      CombineArgs c{p.T, p.k, p.H, at<void*>(ws, L.o), false, w, y, inv};
       e = launch_combine(c, s);
     }
   } else {
@@ -460,7 +460,7 @@ moe_status moe_forward(const moe_problem* pp, const void* x, const float* scores
     d.hdr = hdr;
     e = launch_route_direct(d, s);
     if (e == cudaSuccess) {
-      CombineArgs c{p.T, p.k, p.H, d.o, true, w, y};
+      CombineArgs c{p.T, p.k, p.H, d.o, true, w, y, nullptr};
       e = launch_combine_pdl(c, s);
     }
   }
