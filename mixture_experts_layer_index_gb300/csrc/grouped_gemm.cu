@@ -51,8 +51,9 @@ constexpr int TMEM_COLS = 512;
 __host__ __device__ constexpr int epi_warps(int mode, bool f8) { return (mode == 0 && f8) ? 8 : 4; }
 __host__ __device__ constexpr int threads_of(int mode, bool f8) { return 32 * (4 + epi_warps(mode, f8)); }
 constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
-// epilogue staging: 4 warps x 32 rows x 256 bytes, after the barriers
-constexpr int STAGING_OFFSET = STAGES * STAGE_BYTES + 256;
+// epilogue staging: 4 warps x 32 rows x 256 bytes, after the barriers, 1024-byte
+// aligned (the source of a 128-byte-swizzled TMA store)
+constexpr int STAGING_OFFSET = (STAGES * STAGE_BYTES + 256 + 1023) / 1024 * 1024;
 constexpr int STAGING_BYTES = 4 * 32 * 256;  // Down: 32 rows x 256 bytes per epilogue warp
 constexpr size_t SMEM_BYTES = 1024 + STAGING_OFFSET + STAGING_BYTES;
 
@@ -97,7 +98,7 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
 template <int MODE, bool F8>
 __global__ void __launch_bounds__(threads_of(MODE, F8), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const Params p) {
+                        const __grid_constant__ CUtensorMap tmO, const Params p) {
   constexpr int BKE = F8 ? 128 : BK;  // K elements per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -310,52 +311,74 @@ __global__ void __launch_bounds__(threads_of(MODE, F8), 1)
           if (lane == 0 && amax > 0.0f) atomicMax(p.amax_out, __float_as_uint(amax));
         }
       } else {
-        // Down: o rows in sorted order.  Each pass stages 128 bf16
-        // columns (256 bytes) of every row of the warp in shared memory (16-byte
-        // pieces XOR-swizzled by row, so both phases are bank-conflict free), then
-        // the warp writes two whole 256-byte row segments per store instruction.
-        // F8: o = s_h * s_w2[e] * acc.
+        // Down: o rows in sorted order.  Each pass stages 128 bf16 columns of the
+        // warp's 32 rows in shared memory as two [32 rows][128 bytes] boxes with the
+        // 128-byte swizzle (16-byte chunk c of row r at c ^ (r & 7): both the row-per-
+        // thread writes and the row-segment reads below take the minimum 4 wavefronts).
+        // A warp whose 32 rows all belong to the tile hands the boxes to TMA stores
+        // (lane 0 issues them; it waits for them to have read the staging before the
+        // next pass overwrites it); a warp of a partial tile writes its valid rows with
+        // 16-byte stores.  F8: o = s_h * s_w2[e] * acc.
         static_assert(MODE == MODE_GATEUP || epi_warps(MODE, F8) == 4, "Down epilogue: one warp per TMEM quadrant");
-        uint4* stg = reinterpret_cast<uint4*>(smem + STAGING_OFFSET) + q * (32 * 16);
+        uint8_t* stg = smem + STAGING_OFFSET + q * (32 * 256);
         const int wrows = min(32, nrows - q * 32);  // valid rows of this warp (may be <= 0)
         const float post = F8 ? e4m3_scale(__uint_as_float(*p.amax_in)) * __ldg(p.wscale + tl.x) : 1.0f;
-        const int slot = row0 + row;
+        const int wrow0 = row0 + q * 32;            // first o row of this warp
 #pragma unroll 1
         for (int pass = 0; pass < 2; ++pass) {
+          if (lane == 0) bulk_wait_group_read0();   // the staging's previous TMA stores have read it
+          __syncwarp();
 #pragma unroll
-          for (int c = 0; c < 128; c += 32) {
+          for (int c = 0; c < 4; ++c) {
             float v[32];
-            tmem_ld32(tbase + pass * 128 + c, v);
+            tmem_ld32(tbase + pass * 128 + c * 32, v);
             tmem_ld_wait();
             if (F8) {
 #pragma unroll
               for (int i = 0; i < 32; ++i) v[i] *= post;
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) stg[lane * 16 + (((c / 8) + i) ^ (lane & 15))] = pack_bf16x8(v + 8 * i);
+            for (int i = 0; i < 4; ++i) {
+              const int cc = c * 4 + i;  // 16-byte chunk of the row, 0..15
+              *reinterpret_cast<uint4*>(stg + (cc >> 3) * 4096 + lane * 128 + (((cc & 7) ^ (lane & 7)) << 4)) =
+                  pack_bf16x8(v + 8 * i);
+            }
           }
           if (pass == 1) {  // every accumulator column read: hand the buffer back to the MMA
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty0 + 8 * acc);  // one arrival per warp
           }
-          __syncwarp();
           const int col0 = n * BN + pass * 128;
+          if (wrows == 32) {
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+#pragma unroll
+              for (int b = 0; b < 2; ++b)
+                if (col0 + b * 64 < p.n_valid) tma_store_2d(&tmO, smem_u32(stg + b * 4096), col0 + b * 64, wrow0);
+              bulk_commit_group();
+            }
+            __syncwarp();
+          } else {
+            __syncwarp();
 #pragma unroll 4
-          for (int it = 0; it < 16; ++it) {
-            const int r = it * 2 + (lane >> 4), j = lane & 15;
-            const int rslot = __shfl_sync(0xffffffffu, slot, r);
-            const int col = col0 + j * 8;
-            if (r < wrows && col < p.n_valid)
-              *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(rslot) * p.out_ld + col) =
-                  stg[r * 16 + (j ^ (r & 15))];
+            for (int it = 0; it < 16; ++it) {
+              const int r = it * 2 + (lane >> 4), j = lane & 15;
+              const int col = col0 + j * 8;
+              if (r < wrows && col < p.n_valid)
+                *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(wrow0 + r) * p.out_ld + col) =
+                    *reinterpret_cast<const uint4*>(stg + (j >> 3) * 4096 + r * 128 + (((j & 7) ^ (r & 7)) << 4));
+            }
+            __syncwarp();
           }
-          __syncwarp();
         }
       }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+    if (MODE == MODE_DOWN && lane == 0) bulk_wait_group0();  // this warp's TMA stores have completed
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -444,9 +467,10 @@ cudaError_t launch_gateup_bf16(const GroupedArgs& a, cudaStream_t s) {
   const int grid = static_cast<int>(units < sms ? units : sms);
   stage_begin("gateup_gemm", s);
   if (a.f8)
-    grouped_gemm_kernel<MODE_GATEUP, true><<<grid, threads_of(MODE_GATEUP, true), SMEM_BYTES, s>>>(tmx, tmw1, p);
+    grouped_gemm_kernel<MODE_GATEUP, true><<<grid, threads_of(MODE_GATEUP, true), SMEM_BYTES, s>>>(tmx, tmw1, tmx, p);
   else
-    grouped_gemm_kernel<MODE_GATEUP, false><<<grid, threads_of(MODE_GATEUP, false), SMEM_BYTES, s>>>(tmx, tmw1, p);
+    grouped_gemm_kernel<MODE_GATEUP, false><<<grid, threads_of(MODE_GATEUP, false), SMEM_BYTES, s>>>(tmx, tmw1, tmx,
+                                                                                                    p);
   err = cudaGetLastError();
   stage_end(s);
   return err;
@@ -459,10 +483,12 @@ cudaError_t launch_down_bf16(const GroupedArgs& a, cudaStream_t s) {
   int sms = 0;
   cudaError_t err = prepare(a, &sms);
   if (err != cudaSuccess) return err;
-  CUtensorMap tmh, tmw2;
+  CUtensorMap tmh, tmw2, tmo;
   const uint32_t bke = a.f8 ? 128 : BK;
+  // o: bf16 [R rows][H], stored by the epilogue in [32 rows][64 columns] boxes
   if (!encode_2d(&tmh, a.h, a.I, a.R, bke, BM, a.f8) ||
-      !encode_2d(&tmw2, a.w2, a.I, static_cast<uint64_t>(a.E) * a.H, bke, BN, a.f8))
+      !encode_2d(&tmw2, a.w2, a.I, static_cast<uint64_t>(a.E) * a.H, bke, BN, a.f8) ||
+      !encode_2d(&tmo, a.o, a.H, a.R, 64, 32))
     return cudaErrorInvalidValue;
   Params p = base_params(a);
   p.wscale = a.w2_scale;
@@ -478,9 +504,9 @@ cudaError_t launch_down_bf16(const GroupedArgs& a, cudaStream_t s) {
   const int grid = static_cast<int>(units < sms ? units : sms);
   stage_begin("down_gemm", s);
   if (a.f8)
-    grouped_gemm_kernel<MODE_DOWN, true><<<grid, threads_of(MODE_DOWN, true), SMEM_BYTES, s>>>(tmh, tmw2, p);
+    grouped_gemm_kernel<MODE_DOWN, true><<<grid, threads_of(MODE_DOWN, true), SMEM_BYTES, s>>>(tmh, tmw2, tmo, p);
   else
-    grouped_gemm_kernel<MODE_DOWN, false><<<grid, threads_of(MODE_DOWN, false), SMEM_BYTES, s>>>(tmh, tmw2, p);
+    grouped_gemm_kernel<MODE_DOWN, false><<<grid, threads_of(MODE_DOWN, false), SMEM_BYTES, s>>>(tmh, tmw2, tmo, p);
   err = cudaGetLastError();
   stage_end(s);
   return err;
