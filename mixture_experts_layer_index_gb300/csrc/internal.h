@@ -13,7 +13,7 @@ namespace moe {
 struct DeviceHeader;
 
 constexpr int kGemmBM = 128;          // rows (sorted routes) per grouped-GEMM tile
-constexpr int kRouteThreads = 512;    // threads of the route/rank kernel (16 warps: 8 tokens each at k=8)
+constexpr int kRouteThreads = 1024;   // threads of the route/rank kernel (32 warps: 4 tokens each at k=8)
 constexpr int kMaxRoutesPerBlock = 1024;
 constexpr int kMaxE = 512;
 constexpr int kMaxK = 32;

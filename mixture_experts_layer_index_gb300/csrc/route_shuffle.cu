@@ -270,11 +270,24 @@ __global__ void __launch_bounds__(256) scatter_gather_kernel(const int32_t* __re
 }
 
 // ------------------------------------------------------------------ launchers
+// Shared memory of the route/rank kernel: the block's ids and ranks plus one
+// histogram of E counters per warp (up to 72 KB at E = 512).
+constexpr size_t kRouteSmemMax = (2 * kMaxRoutesPerBlock + (kRouteThreads / 32) * kMaxE) * sizeof(int);
+
+template <int V, bool ROUTE, bool RANK>
+static cudaError_t rr_smem_attr() {
+  static const cudaError_t st = cudaFuncSetAttribute(route_rank_kernel<V, ROUTE, RANK>,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     static_cast<int>(kRouteSmemMax));
+  return st;
+}
+
 template <bool ROUTE, bool RANK>
 static cudaError_t launch_rr(int maxv, dim3 grid, size_t smem, cudaStream_t s, const float* scores,
                              const int32_t* ids_in, int T, int E, int k, int TB, int32_t* ids_out, float* w_out,
                              int32_t* lrank, int32_t* bc, DeviceHeader* hdr) {
-#define MOE_RR(V)                                                                                         \
+#define MOE_RR(V)                                                                                          \
+  if (const cudaError_t ae = rr_smem_attr<V, ROUTE, RANK>()) return ae;                                    \
   route_rank_kernel<V, ROUTE, RANK><<<grid, kRouteThreads, smem, s>>>(scores, ids_in, T, E, k, TB, ids_out, \
                                                                      w_out, lrank, bc, hdr)
   switch (maxv) {
