@@ -3,28 +3,27 @@
 //
 // Rule (the top-k routing step of "perf: add small-batch route MMA for MoE",
 // Motivation; ties to the lower expert id, softmax over the k selected
-// scores): every lane
-// holds ceil(E/32) scores as 64-bit keys - order-preserving score bits in the
-// high word, the complemented expert id in the low word - so the largest key
-// is the largest score and, among equal scores, the lowest id.  -0.0 is
-// canonicalised to +0.0 first so that signed zeros tie.  k rounds of a
-// warp-wide max pick the experts in slot order; the softmax runs in fp32.
+// scores): every lane holds ceil(E/32) scores as order-preserving 32-bit keys
+// (expert i * 32 + lane in slot i); -0.0 is canonicalised to +0.0 first so that
+// signed zeros tie.  Each of k rounds takes the warp-wide maximum key and then
+// the lowest expert id holding it, so experts come out in slot order; the
+// softmax runs in fp32.
 #pragma once
 
 #include "common.cuh"
 
 namespace moe {
 
-__device__ __forceinline__ unsigned long long score_key(float v, int e) {
+// Order-preserving 32-bit image of a canonicalised score (-0.0 -> +0.0): the larger
+// the score, the larger the key.
+__device__ __forceinline__ uint32_t score_bits(float v) {
   v = v + 0.0f;
-  uint32_t u = __float_as_uint(v);
-  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return (static_cast<unsigned long long>(u) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(e));
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Inverse of the key's score bits (the canonicalised score itself).
-__device__ __forceinline__ float key_score(unsigned long long key) {
-  const uint32_t u = static_cast<uint32_t>(key >> 32);
+// Inverse of score_bits (the canonicalised score itself).
+__device__ __forceinline__ float key_score(uint32_t u) {
   return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
 }
 
@@ -41,32 +40,41 @@ __device__ __forceinline__ void load_scores(const float* __restrict__ srow, int 
 
 // Route one token from its scores already in registers.  Lane j < k writes
 // slot j of each output that is given: ids_row[j], w_row[j], s_ids_row[j].
+// Round j takes the warp-wide maximum of the 32-bit score keys still available
+// (one redux.sync) and then the lowest expert id holding it: slots are scanned in
+// ascending order (expert i * 32 + lane), and within a slot the lowest lane of
+// the ballot wins, so equal scores go to the lower expert id.
 template <int MAXV>
 __device__ __forceinline__ void route_values(const float (&v)[MAXV], int E, int k, int32_t* __restrict__ ids_row,
                                              float* __restrict__ w_row, int* s_ids_row) {
   const int lane = threadIdx.x & 31;
-  unsigned long long key[MAXV];
+  uint32_t key[MAXV];
+  unsigned avail = 0u;  // bit i: expert i * 32 + lane exists and is not taken yet
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
-    const int e = i * 32 + lane;
-    key[i] = e < E ? score_key(v[i], e) : 0ull;  // any real key is > 0
+    key[i] = score_bits(v[i]);
+    if (i * 32 + lane < E) avail |= 1u << i;
   }
   int my_id = 0;
   float my_s = 0.0f;
 #pragma unroll 1
   for (int j = 0; j < k; ++j) {
-    unsigned long long best = 0ull;
-#pragma unroll
-    for (int i = 0; i < MAXV; ++i) best = key[i] > best ? key[i] : best;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
-      best = other > best ? other : best;
-    }
-    const int id = static_cast<int>(~static_cast<uint32_t>(best & 0xffffffffull));
+    uint32_t best = 0u;
 #pragma unroll
     for (int i = 0; i < MAXV; ++i)
-      if (i * 32 + lane == id) key[i] = 0ull;
+      if ((avail >> i) & 1u) best = key[i] > best ? key[i] : best;
+    best = __reduce_max_sync(0xffffffffu, best);
+    int id = 0;
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+      const unsigned b = __ballot_sync(0xffffffffu, ((avail >> i) & 1u) && key[i] == best);
+      if (b) {
+        const int wl = __ffs(b) - 1;
+        id = i * 32 + wl;
+        if (lane == wl) avail &= ~(1u << i);
+        break;
+      }
+    }
     if (lane == j) {
       my_id = id;
       my_s = key_score(best);
