@@ -230,15 +230,20 @@ moe_status moe_read_device_status(const void* ws, moe_stream_t stream);
  *   kernel stage (in order of first launch) to out[0 .. max_stages-1], turns
  *   profiling off and returns the number of stages, or -1 if waiting on an
  *   event failed.  total_ms sums the stage's launches; launches counts them.
- * Stage names: route_rank, scan_tiles, scatter, gateup_gemm, down_gemm,
- * combine (grouped path); rd_prep, rd_gateup, rd_reduce, rd_down, combine
- * (route-direct path); tile_map, header_reset. */
+ * moe_profile_start_stage - the same, but only launches of the stage named
+ *   `stage` are timed (NULL or "" times every stage).  Each event pair recorded
+ *   between two kernels costs GPU time (about 2 us per stage on GB300), so a
+ *   measurement of the whole call brackets only the kernel it needs.
+ * Stage names: route_rank, scan_tiles, x_amax, scatter_gather, gateup_gemm,
+ * quant_h, down_gemm, combine (grouped path); rd_prep, rd_gateup, rd_reduce,
+ * rd_down, combine (route-direct path); scatter, tile_map, header_reset. */
 typedef struct {
   char name[32];
   double total_ms;
   int launches;
 } moe_stage_time;
 int moe_profile_start(void);
+int moe_profile_start_stage(const char* stage);
 int moe_profile_stop(moe_stage_time* out, int max_stages);
 
 /* moe_status_string - static, NUL-terminated description of a status code. */

@@ -67,6 +67,7 @@ _SIGS = {
     "moe_forward_views": (_i, [_P, _vp, _sz, ctypes.POINTER(moe_views)]),
     "moe_read_device_status": (_i, [_vp, _vp]),
     "moe_profile_start": (_i, []),
+    "moe_profile_start_stage": (_i, [ctypes.c_char_p]),
     "moe_profile_stop": (_i, [ctypes.POINTER(moe_stage_time), _i]),
     "moe_status_string": (ctypes.c_char_p, [_i]),
 }
@@ -191,6 +192,11 @@ def moe_read_device_status(ws, stream=None) -> int:
 
 def moe_profile_start() -> None:
     lib().moe_profile_start()
+
+
+def moe_profile_start_stage(stage: str) -> None:
+    """Profile only the launches of one stage (e.g. "gateup_gemm")."""
+    lib().moe_profile_start_stage(stage.encode() if stage else None)
 
 
 def moe_profile_stop(max_stages: int = 32) -> dict:

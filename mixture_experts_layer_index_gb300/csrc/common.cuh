@@ -134,6 +134,14 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return p;
 }
 
+// Programmatic dependent launch: a kernel launched with the attribute
+// (launch_dependent) is set up while its predecessor runs and released when the
+// predecessor completes; dep_wait then makes the predecessor's writes visible
+// (a no-op for a kernel launched without the attribute).  The grouped path's
+// kernels trigger no early launch: a persistent GEMM's CTAs resident during the
+// previous kernel's tail cost more than the earlier start gains.
+__device__ __forceinline__ void dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Tiled TMA store of the box at {c0, c1} of `map` from shared memory at src
 // (a bulk async-group of the issuing thread; src aligned as the map's swizzle needs).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {

@@ -122,6 +122,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  dep_wait();  // the tile map and the A rows come from the kernels before (the set-up above overlaps them)
 
   const int ntiles = min(*p.num_tiles, p.max_tiles);
   const int total = ntiles * p.nN;
@@ -366,8 +367,8 @@ cudaError_t launch_gateup_blockwise(const GroupedArgs& a, const float* xs_scale,
   const long long units = static_cast<long long>(a.max_tiles) * p.nN;
   const int grid = static_cast<int>(units < sms ? units : sms);
   stage_begin("gateup_gemm", s);
-  grouped_blockwise_kernel<MODE_GATEUP><<<grid, THREADS, smem_bytes(MODE_GATEUP), s>>>(tma, tmb, p);
-  err = cudaGetLastError();
+  err = launch_dependent(grouped_blockwise_kernel<MODE_GATEUP>, dim3(grid), dim3(THREADS), smem_bytes(MODE_GATEUP), s,
+                         tma, tmb, p);
   stage_end(s);
   return err;
 }
@@ -398,8 +399,8 @@ cudaError_t launch_down_blockwise(const GroupedArgs& a, const float* h_scale, cu
   const long long units = static_cast<long long>(a.max_tiles) * p.nN;
   const int grid = static_cast<int>(units < sms ? units : sms);
   stage_begin("down_gemm", s);
-  grouped_blockwise_kernel<MODE_DOWN><<<grid, THREADS, smem_bytes(MODE_DOWN), s>>>(tma, tmb, p);
-  err = cudaGetLastError();
+  err = launch_dependent(grouped_blockwise_kernel<MODE_DOWN>, dim3(grid), dim3(THREADS), smem_bytes(MODE_DOWN), s,
+                         tma, tmb, p);
   stage_end(s);
   return err;
 }

@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(threads_of(MODE, F8), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  dep_wait();  // the tile map and the A rows come from the kernels before (the set-up above overlaps them)
 
   const int ntiles = min(*p.num_tiles, p.max_tiles);
   const int total = ntiles * p.nN;
@@ -467,11 +468,11 @@ cudaError_t launch_gateup_bf16(const GroupedArgs& a, cudaStream_t s) {
   const int grid = static_cast<int>(units < sms ? units : sms);
   stage_begin("gateup_gemm", s);
   if (a.f8)
-    grouped_gemm_kernel<MODE_GATEUP, true><<<grid, threads_of(MODE_GATEUP, true), SMEM_BYTES, s>>>(tmx, tmw1, tmx, p);
+    err = launch_dependent(grouped_gemm_kernel<MODE_GATEUP, true>, dim3(grid), dim3(threads_of(MODE_GATEUP, true)),
+                           SMEM_BYTES, s, tmx, tmw1, tmx, p);
   else
-    grouped_gemm_kernel<MODE_GATEUP, false><<<grid, threads_of(MODE_GATEUP, false), SMEM_BYTES, s>>>(tmx, tmw1, tmx,
-                                                                                                    p);
-  err = cudaGetLastError();
+    err = launch_dependent(grouped_gemm_kernel<MODE_GATEUP, false>, dim3(grid), dim3(threads_of(MODE_GATEUP, false)),
+                           SMEM_BYTES, s, tmx, tmw1, tmx, p);
   stage_end(s);
   return err;
 }
@@ -504,10 +505,11 @@ cudaError_t launch_down_bf16(const GroupedArgs& a, cudaStream_t s) {
   const int grid = static_cast<int>(units < sms ? units : sms);
   stage_begin("down_gemm", s);
   if (a.f8)
-    grouped_gemm_kernel<MODE_DOWN, true><<<grid, threads_of(MODE_DOWN, true), SMEM_BYTES, s>>>(tmh, tmw2, tmo, p);
+    err = launch_dependent(grouped_gemm_kernel<MODE_DOWN, true>, dim3(grid), dim3(threads_of(MODE_DOWN, true)),
+                           SMEM_BYTES, s, tmh, tmw2, tmo, p);
   else
-    grouped_gemm_kernel<MODE_DOWN, false><<<grid, threads_of(MODE_DOWN, false), SMEM_BYTES, s>>>(tmh, tmw2, tmo, p);
-  err = cudaGetLastError();
+    err = launch_dependent(grouped_gemm_kernel<MODE_DOWN, false>, dim3(grid), dim3(threads_of(MODE_DOWN, false)),
+                           SMEM_BYTES, s, tmh, tmw2, tmo, p);
   stage_end(s);
   return err;
 }
@@ -612,23 +614,6 @@ cudaError_t launch_combine_pdl(const CombineArgs& a, cudaStream_t s) {
   return err;
 }
 
-cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
-  if (a.T <= 0) return cudaSuccess;
-  const size_t total = static_cast<size_t>(a.T) * (a.H / 8);
-  const int sms = num_sms();
-  size_t blocks = (total + 255) / 256;
-  const size_t cap = static_cast<size_t>(sms > 0 ? sms : 148) * 8;
-  if (blocks > cap) blocks = cap;
-  stage_begin("combine", s);
-  if (a.o_is_f32)
-    combine_kernel<float><<<static_cast<int>(blocks), 256, 0, s>>>(static_cast<const float*>(a.o), a.w, a.T, a.k,
-                                                                   a.H, static_cast<__nv_bfloat16*>(a.y), a.inv);
-  else
-    combine_kernel<__nv_bfloat16><<<static_cast<int>(blocks), 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(a.o), a.w, a.T, a.k, a.H, static_cast<__nv_bfloat16*>(a.y), a.inv);
-  const cudaError_t err = cudaGetLastError();
-  stage_end(s);
-  return err;
-}
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) { return launch_combine_pdl(a, s); }
 
 }  // namespace moe

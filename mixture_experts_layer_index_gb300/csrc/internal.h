@@ -153,6 +153,25 @@ struct DecodeArgs {
 cudaError_t launch_route_direct(const DecodeArgs& a, cudaStream_t s);
 size_t route_direct_uniq_bytes(int T, int E, int k);
 
+// Launch `kernel` as a programmatic dependent of the previous work on the stream:
+// its launch is prepared while the predecessor runs, and it waits for the
+// predecessor on the device (dep_wait) before touching its results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Stage timing (moe_profile_start/stop): every launcher brackets its kernel with
 // stage_begin/stage_end; both are no-ops unless profiling is on.
 void stage_begin(const char* name, cudaStream_t s);

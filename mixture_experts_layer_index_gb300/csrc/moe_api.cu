@@ -51,6 +51,7 @@ struct StageRecord {
 struct Profiler {
   std::mutex mu;
   bool on = false;
+  std::string only;  // time only this stage ("" = every stage)
   std::vector<std::string> names;
   std::vector<StageRecord> records;
   std::vector<cudaEvent_t> pool;
@@ -90,6 +91,7 @@ void stage_begin(const char* name, cudaStream_t s) {
   Profiler& P = prof();
   std::lock_guard<std::mutex> lk(P.mu);
   if (!P.on || capturing(s)) return;
+  if (!P.only.empty() && P.only != name) return;
   int idx = -1;
   for (size_t i = 0; i < P.names.size(); ++i)
     if (P.names[i] == name) idx = static_cast<int>(i);
@@ -490,10 +492,13 @@ moe_status moe_forward_views(const moe_problem* p, const void* ws, size_t ws_byt
   return MOE_OK;
 }
 
-int moe_profile_start(void) {
+int moe_profile_start(void) { return moe_profile_start_stage(nullptr); }
+
+int moe_profile_start_stage(const char* stage) {
   Profiler& P = prof();
   std::lock_guard<std::mutex> lk(P.mu);
   P.recycle();
+  P.only = stage ? stage : "";
   P.on = true;
   return 0;
 }

@@ -12,6 +12,7 @@ namespace moe {
 // amax |x| over n bf16 values into hdr->amax_x (fp32 bits; non-negative floats
 // order like their bit patterns).  Loads go out 8 x 16 bytes per thread at a time.
 __global__ void __launch_bounds__(256) x_amax_kernel(const uint4* __restrict__ x, size_t n8, DeviceHeader* hdr) {
+  dep_wait();
   float m = 0.0f;
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (size_t base = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; base < n8; base += stride * 8) {
@@ -53,6 +54,7 @@ __global__ void __launch_bounds__(256) scatter_gather_tok_q_kernel(
     int RB, int k, int H, const uint4* __restrict__ x, uint4* __restrict__ xs, float* __restrict__ xs_scale,
     int32_t* __restrict__ perm, int32_t* __restrict__ inv, const DeviceHeader* hdr) {
   extern __shared__ __align__(16) uint8_t s_row[];  // [H] e4m3, then [H/128] fp32 scales
+  dep_wait();  // block bases and (per tensor) the amax of x
   float* s_sc = reinterpret_cast<float*>(s_row + H);
   const int t = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -114,6 +116,7 @@ __global__ void __launch_bounds__(256) scatter_gather_tok_q_kernel(
 // h = e4m3(a / s_h), s_h = e4m3_scale(amax of a); 4 values per thread-iteration.
 __global__ void __launch_bounds__(256) quant_rows_kernel(const float4* __restrict__ a, uint32_t* __restrict__ h,
                                                          size_t n4, const DeviceHeader* hdr) {
+  dep_wait();  // a and its amax from the Gate/Up GEMM
   const float s = e4m3_scale(__uint_as_float(hdr->amax_h));
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4; i += stride) {
@@ -126,6 +129,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const float4* __restric
 // values per lane; rows x groups items, 4 of them in flight per warp.
 __global__ void __launch_bounds__(256) quant_groups_kernel(const float4* __restrict__ a, uint32_t* __restrict__ h,
                                                            float* __restrict__ sh, size_t items) {
+  dep_wait();  // a from the Gate/Up GEMM
   const int lane = threadIdx.x & 31;
   const size_t nw = (static_cast<size_t>(gridDim.x) * blockDim.x) >> 5;
   for (size_t g0 = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; g0 < items; g0 += 4 * nw) {
@@ -161,8 +165,8 @@ cudaError_t launch_x_amax(const void* x, size_t n, DeviceHeader* hdr, cudaStream
   const size_t n8 = n / 8;
   if (n8 == 0) return cudaSuccess;
   stage_begin("x_amax", s);
-  x_amax_kernel<<<grid_for(n8, 256 * 8), 256, 0, s>>>(static_cast<const uint4*>(x), n8, hdr);
-  const cudaError_t err = cudaGetLastError();
+  const cudaError_t err = launch_dependent(x_amax_kernel, dim3(grid_for(n8, 256 * 8)), dim3(256), 0, s,
+                                           static_cast<const uint4*>(x), n8, hdr);
   stage_end(s);
   return err;
 }
@@ -175,15 +179,13 @@ static cudaError_t launch_tok_q(bool blockwise, const int32_t* ids, const int32_
   const size_t smem = static_cast<size_t>(H) + static_cast<size_t>(H / 128) * sizeof(float);
   if (smem > 48 * 1024) return cudaErrorInvalidValue;  // H <= 47K: far above any supported shape
   stage_begin("scatter_gather", s);
-  if (blockwise)
-    scatter_gather_tok_q_kernel<true><<<T, 256, smem, s>>>(ids, lrank, blockbase, E, RB, k, H,
-                                                           static_cast<const uint4*>(x), static_cast<uint4*>(xs),
-                                                           xs_scale, perm, inv, hdr);
-  else
-    scatter_gather_tok_q_kernel<false><<<T, 256, smem, s>>>(ids, lrank, blockbase, E, RB, k, H,
-                                                            static_cast<const uint4*>(x), static_cast<uint4*>(xs),
-                                                            nullptr, perm, inv, hdr);
-  const cudaError_t err = cudaGetLastError();
+  const cudaError_t err =
+      blockwise ? launch_dependent(scatter_gather_tok_q_kernel<true>, dim3(T), dim3(256), smem, s, ids, lrank, blockbase,
+                                   E, RB, k, H, static_cast<const uint4*>(x), static_cast<uint4*>(xs), xs_scale, perm,
+                                   inv, hdr)
+                : launch_dependent(scatter_gather_tok_q_kernel<false>, dim3(T), dim3(256), smem, s, ids, lrank,
+                                   blockbase, E, RB, k, H, static_cast<const uint4*>(x), static_cast<uint4*>(xs),
+                                   static_cast<float*>(nullptr), perm, inv, hdr);
   stage_end(s);
   return err;
 }
@@ -198,9 +200,8 @@ cudaError_t launch_quant_rows(const float* a, void* h, size_t n, const DeviceHea
   const size_t n4 = n / 4;
   if (n4 == 0) return cudaSuccess;
   stage_begin("quant_h", s);
-  quant_rows_kernel<<<grid_for(n4, 256), 256, 0, s>>>(reinterpret_cast<const float4*>(a), static_cast<uint32_t*>(h),
-                                                      n4, hdr);
-  const cudaError_t err = cudaGetLastError();
+  const cudaError_t err = launch_dependent(quant_rows_kernel, dim3(grid_for(n4, 256)), dim3(256), 0, s,
+                                           reinterpret_cast<const float4*>(a), static_cast<uint32_t*>(h), n4, hdr);
   stage_end(s);
   return err;
 }
@@ -215,9 +216,8 @@ cudaError_t launch_quant_groups(const float* a, void* h, float* sh, int rows, in
   const size_t items = static_cast<size_t>(rows) * (cols / 128);
   if (items == 0) return cudaSuccess;
   stage_begin("quant_h", s);
-  quant_groups_kernel<<<grid_for(items * 32, 256 * 4), 256, 0, s>>>(reinterpret_cast<const float4*>(a),
-                                                                     static_cast<uint32_t*>(h), sh, items);
-  const cudaError_t err = cudaGetLastError();
+  const cudaError_t err = launch_dependent(quant_groups_kernel, dim3(grid_for(items * 32, 256 * 4)), dim3(256), 0, s,
+                                           reinterpret_cast<const float4*>(a), static_cast<uint32_t*>(h), sh, items);
   stage_end(s);
   return err;
 }

@@ -174,6 +174,7 @@ __global__ void __launch_bounds__(1024) scan_tiles_kernel(int32_t* __restrict__ 
                                                           int max_tiles, int BM, DeviceHeader* hdr, int use_smem) {
   __shared__ int s_cnt[kMaxE], s_off[kMaxE + 1], s_toff[kMaxE + 1];
   extern __shared__ int sbc[];
+  dep_wait();  // the block counts of the route/rank kernel
   const int n = nblk * E;
   int* col = use_smem ? sbc : bc;
   if (use_smem) {
@@ -245,6 +246,7 @@ __global__ void __launch_bounds__(256) scatter_gather_kernel(const int32_t* __re
                                                              uint4* __restrict__ xs, int32_t* __restrict__ perm,
                                                              int32_t* __restrict__ inv) {
   __shared__ int s_p[kMaxK];
+  dep_wait();  // ranks and block bases of the kernels before
   const int t = blockIdx.x;
   for (int j = threadIdx.x; j < k; j += blockDim.x) {
     const int r = t * k + j;
@@ -329,9 +331,8 @@ cudaError_t launch_scan_tiles(int32_t* blockcounts, int nblk, int E, int32_t* co
   const size_t need = static_cast<size_t>(nblk) * E * sizeof(int);
   const int use_smem = need <= static_cast<size_t>(kScanSmemBytes) ? 1 : 0;
   stage_begin("scan_tiles", s);
-  scan_tiles_kernel<<<1, 1024, use_smem ? need : 0, s>>>(blockcounts, nblk, E, counts, offsets, tiles, num_tiles,
-                                                         max_tiles, BM, hdr, use_smem);
-  const cudaError_t err = cudaGetLastError();
+  const cudaError_t err = launch_dependent(scan_tiles_kernel, dim3(1), dim3(1024), use_smem ? need : 0, s, blockcounts,
+                                           nblk, E, counts, offsets, tiles, num_tiles, max_tiles, BM, hdr, use_smem);
   stage_end(s);
   return err;
 }
@@ -354,9 +355,8 @@ cudaError_t launch_scatter_gather(const int32_t* ids, const int32_t* lrank, cons
   if (T <= 0) return cudaSuccess;
   const int RB = route_tokens_per_block(k) * k;
   stage_begin("scatter_gather", s);
-  scatter_gather_kernel<<<T, 256, 0, s>>>(ids, lrank, blockbase, E, RB, k, H, static_cast<const uint4*>(x),
-                                          static_cast<uint4*>(xs), perm, inv);
-  const cudaError_t err = cudaGetLastError();
+  const cudaError_t err = launch_dependent(scatter_gather_kernel, dim3(T), dim3(256), 0, s, ids, lrank, blockbase, E, RB,
+                                           k, H, static_cast<const uint4*>(x), static_cast<uint4*>(xs), perm, inv);
   stage_end(s);
   return err;
 }
