@@ -371,6 +371,7 @@ struct StreamSmem {
   uint8_t* stages;
   uint8_t* opnd;
   float* osc;
+  float* wsc;  // blockwise: the current item's weight scales, 32 per consumer warp
   uint64_t* full;
   uint64_t* empty;
   volatile int* abort_flag;
@@ -382,7 +383,8 @@ __host__ __device__ inline int opnd_pitch(int K) { return (K + 127) / 128 * 128 
 __host__ __device__ inline size_t stream_smem_bytes(int K) {
   const size_t opnd = static_cast<size_t>(GROUP) * opnd_pitch(K);
   const size_t osc = static_cast<size_t>(GROUP) * (K / 128) * 4;
-  return 1024 + static_cast<size_t>(NS) * STAGE_BYTES + opnd + ((osc + 15) / 16) * 16 + 2 * NS * 8 + 16;
+  return 1024 + static_cast<size_t>(NS) * STAGE_BYTES + opnd + ((osc + 15) / 16) * 16 + CONSUMERS * 32 * 4 +
+         2 * NS * 8 + 16;
 }
 
 __device__ __forceinline__ StreamSmem stream_smem(uint8_t* raw, int K) {
@@ -392,7 +394,8 @@ __device__ __forceinline__ StreamSmem stream_smem(uint8_t* raw, int K) {
   m.opnd = base + NS * STAGE_BYTES;
   m.osc = reinterpret_cast<float*>(m.opnd + GROUP * opnd_pitch(K));
   const size_t osc = static_cast<size_t>(GROUP) * (K / 128) * 4;
-  m.full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(m.osc) + ((osc + 15) / 16) * 16);
+  m.wsc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(m.osc) + ((osc + 15) / 16) * 16);
+  m.full = reinterpret_cast<uint64_t*>(m.wsc + CONSUMERS * 32);
   m.empty = m.full + NS;
   m.abort_flag = reinterpret_cast<volatile int*>(m.empty + NS);
   return m;
@@ -566,6 +569,13 @@ __global__ void __launch_bounds__(THREADS, 2) rd_gateup_kernel(const __grid_cons
       const int row = mb * ROWS_PER_CTA + wr;               // rows row and row + 8 of W1[e]
       const uint8_t* xs = m.opnd + g8 * xpitch + 16 * tig;
       const float* sw = BLOCKWISE ? a.w1_scale + (static_cast<size_t>(e) * (twoI / 128) + row / 128) * (H / 128) : nullptr;
+      // the item's weight scales (one per 128 K bytes, the same for all its rows):
+      // one coalesced load per warp, written to the warp's slot after the first
+      // stage wait so that the load overlaps it (KS / 128 <= 32 by validation)
+      float* wsl = m.wsc + warp * 32;
+      float wreg = 0.0f;
+      if (BLOCKWISE && lane < KS / 128) wreg = __ldg(sw + k0 / 128 + lane);
+      bool wsl_ready = !BLOCKWISE;
       float c[4] = {0.f, 0.f, 0.f, 0.f};
       for (int cc = 0; cc < KS; cc += CK) {
         const int bytes = min(CK, KS - cc);
@@ -574,6 +584,12 @@ __global__ void __launch_bounds__(THREADS, 2) rd_gateup_kernel(const __grid_cons
         ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(m.full + stage), phase, m.abort_flag, a.hdr, 0x91000u));
         if (ok) {
           const uint8_t* st = m.stages + stage * STAGE_BYTES;
+          if (!wsl_ready) {
+            __syncwarp();  // the previous item's reads of the slot are done
+            if (lane < KS / 128) wsl[lane] = wreg;
+            __syncwarp();
+            wsl_ready = true;
+          }
           if (!BLOCKWISE) {
             for (int kk = 0; kk < bytes; kk += 64) {
               const uint4 A0 = *wfrag(st, wr, kk + 16 * tig);
@@ -589,7 +605,7 @@ __global__ void __launch_bounds__(THREADS, 2) rd_gateup_kernel(const __grid_cons
               mma_k64(cb, *wfrag(st, wr, kk + 64 + 16 * tig), *wfrag(st, wr + 8, kk + 64 + 16 * tig),
                       *reinterpret_cast<const uint4*>(xs + cc + kk + 64));
               const int q = (cc + kk) / 128;
-              const float w_s = __ldg(sw + k0 / 128 + q);
+              const float w_s = wsl[q];
               const float s0 = w_s * m.osc[(2 * tig) * (KS / 128) + q];
               const float s1 = w_s * m.osc[(2 * tig + 1) * (KS / 128) + q];
               c[0] = fmaf(cb[0], s0, c[0]);
@@ -792,12 +808,23 @@ __global__ void __launch_bounds__(THREADS, 2) rd_down_kernel(const __grid_consta
       const int row = hb * ROWS_PER_CTA + wr;               // rows row and row + 8 of W2[e]
       const uint8_t* hs = m.opnd + g8 * hpitch + 16 * tig;
       const float* sw = BLOCKWISE ? a.w2_scale + (static_cast<size_t>(e) * (H / 128) + row / 128) * ngi : nullptr;
+      // the item's weight scales, staged like rd_gateup's (ngi = I / 128 <= 32)
+      float* wsl = m.wsc + warp * 32;
+      float wreg = 0.0f;
+      if (BLOCKWISE && lane < ngi) wreg = __ldg(sw + lane);
+      bool wsl_ready = !BLOCKWISE;
       float c[4] = {0.f, 0.f, 0.f, 0.f};
       for (int cc = 0; cc < I; cc += CK) {
         const int bytes = min(CK, I - cc);
         ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(m.full + stage), phase, m.abort_flag, a.hdr, 0x93000u));
         if (ok) {
           const uint8_t* st = m.stages + stage * STAGE_BYTES;
+          if (!wsl_ready) {
+            __syncwarp();  // the previous item's reads of the slot are done
+            if (lane < ngi) wsl[lane] = wreg;
+            __syncwarp();
+            wsl_ready = true;
+          }
           if (!BLOCKWISE) {
             for (int kk = 0; kk < bytes; kk += 64)
               mma_k64(c, *wfrag(st, wr, kk + 16 * tig), *wfrag(st, wr + 8, kk + 16 * tig),
@@ -810,7 +837,7 @@ __global__ void __launch_bounds__(THREADS, 2) rd_down_kernel(const __grid_consta
               mma_k64(cb, *wfrag(st, wr, kk + 64 + 16 * tig), *wfrag(st, wr + 8, kk + 64 + 16 * tig),
                       *reinterpret_cast<const uint4*>(hs + cc + kk + 64));
               const int q = (cc + kk) / 128;
-              const float w_s = __ldg(sw + q);
+              const float w_s = wsl[q];
               const float s0 = w_s * m.osc[(2 * tig) * ngi + q];
               const float s1 = w_s * m.osc[(2 * tig + 1) * ngi + q];
               c[0] = fmaf(cb[0], s0, c[0]);
