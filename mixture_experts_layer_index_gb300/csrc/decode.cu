@@ -380,37 +380,48 @@ struct StreamSmem {
 // Pitch of a staged operand row of K bytes: 64 (mod 128).
 __host__ __device__ inline int opnd_pitch(int K) { return (K + 127) / 128 * 128 + 64; }
 
+// Ring of a stream kernel whose stages hold RCK K bytes of 64 rows: as many stages
+// as fit the default ring's NS x CK bytes per row (Down uses RCK = 256 for short
+// rows, I <= 256, so that twice as many items are in flight).
+template <int RCK>
+__host__ __device__ constexpr int ring_ns() { return NS * CK / RCK; }
+template <int RCK>
+__host__ __device__ constexpr int ring_stage_bytes() { return ROWS_PER_CTA * RCK; }
+
+template <int RCK = CK>
 __host__ __device__ inline size_t stream_smem_bytes(int K) {
   const size_t opnd = static_cast<size_t>(GROUP) * opnd_pitch(K);
   const size_t osc = static_cast<size_t>(GROUP) * (K / 128) * 4;
-  return 1024 + static_cast<size_t>(NS) * STAGE_BYTES + opnd + ((osc + 15) / 16) * 16 + CONSUMERS * 32 * 4 +
-         2 * NS * 8 + 16;
+  return 1024 + static_cast<size_t>(ring_ns<RCK>()) * ring_stage_bytes<RCK>() + opnd + ((osc + 15) / 16) * 16 +
+         CONSUMERS * 32 * 4 + 2 * ring_ns<RCK>() * 8 + 16;
 }
 
+template <int RCK = CK>
 __device__ __forceinline__ StreamSmem stream_smem(uint8_t* raw, int K) {
   StreamSmem m;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   m.stages = base;  // swizzled TMA box destinations: 1024-byte aligned
-  m.opnd = base + NS * STAGE_BYTES;
+  m.opnd = base + ring_ns<RCK>() * ring_stage_bytes<RCK>();
   m.osc = reinterpret_cast<float*>(m.opnd + GROUP * opnd_pitch(K));
   const size_t osc = static_cast<size_t>(GROUP) * (K / 128) * 4;
   m.wsc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(m.osc) + ((osc + 15) / 16) * 16);
   m.full = reinterpret_cast<uint64_t*>(m.wsc + CONSUMERS * 32);
-  m.empty = m.full + NS;
-  m.abort_flag = reinterpret_cast<volatile int*>(m.empty + NS);
+  m.empty = m.full + ring_ns<RCK>();
+  m.abort_flag = reinterpret_cast<volatile int*>(m.empty + ring_ns<RCK>());
   return m;
 }
 
 // Producer side of the ring: streams the 64 rows [row0, row0 + 64) of the
 // weight matrix behind `map` (K bytes innermost), columns [k0, k0 + nbytes),
-// into successive stages, CK bytes (CK / 64 boxes) per stage.  Returns false
+// into successive stages, RCK bytes (RCK / 128 boxes) per stage.  Returns false
 // after an abort.
+template <int RCK = CK>
 __device__ __forceinline__ bool produce_rows(const StreamSmem& m, const CUtensorMap* map, int k0, int row0,
                                              int nbytes, uint32_t& stage, uint32_t& phase, DeviceHeader* hdr,
                                              unsigned int where) {
   const int lane = threadIdx.x & 31;
-  for (int c = 0; c < nbytes; c += CK) {
-    const int bytes = min(CK, nbytes - c);
+  for (int c = 0; c < nbytes; c += RCK) {
+    const int bytes = min(RCK, nbytes - c);
     int good = 1;
     if (lane == 0) good = mbar_wait(smem_u32(m.empty + stage), phase ^ 1, m.abort_flag, hdr, where);
     if (!__shfl_sync(0xffffffffu, good, 0)) return false;
@@ -420,12 +431,12 @@ __device__ __forceinline__ bool produce_rows(const StreamSmem& m, const CUtensor
       // its columns are never read); weights are read once: evict them from L2 first
       const int nbox = (bytes + BOXK - 1) / BOXK;
       mbar_arrive_expect_tx(full, static_cast<uint32_t>(nbox) * BOX_BYTES);
-      const uint32_t dst = smem_u32(m.stages + stage * STAGE_BYTES);
+      const uint32_t dst = smem_u32(m.stages + stage * ring_stage_bytes<RCK>());
       const uint64_t pol = l2_evict_first_policy();
       for (int j = 0; j < nbox; ++j) tma_load_2d_hint(dst + j * BOX_BYTES, map, k0 + c + j * BOXK, row0, full, pol);
     }
     __syncwarp();
-    if (++stage == NS) {
+    if (++stage == ring_ns<RCK>()) {
       stage = 0;
       phase ^= 1;
     }
@@ -434,9 +445,10 @@ __device__ __forceinline__ bool produce_rows(const StreamSmem& m, const CUtensor
 }
 
 // Ring setup by thread 0 (full: 1 arrival + bytes; empty: one arrival per consumer warp).
+template <int RCK = CK>
 __device__ __forceinline__ void init_ring(const StreamSmem& m) {
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NS; ++i) {
+    for (int i = 0; i < ring_ns<RCK>(); ++i) {
       mbar_init(smem_u32(m.full + i), 1);
       mbar_init(smem_u32(m.empty + i), CONSUMERS);
     }
@@ -448,10 +460,12 @@ __device__ __forceinline__ void init_ring(const StreamSmem& m) {
 
 // After an abort: let the producer's copies that are still in flight land
 // before the CTA exits (bounded).
+template <int RCK = CK>
 __device__ __forceinline__ void drain_ring(const StreamSmem& m, uint32_t stage, uint32_t phase, int issued) {
-  for (int i = 0; i < min(issued, NS); ++i) {
-    stage = (stage + NS - 1) % NS;
-    if (stage == NS - 1) phase ^= 1;
+  constexpr int ns = ring_ns<RCK>();
+  for (int i = 0; i < min(issued, ns); ++i) {
+    stage = (stage + ns - 1) % ns;
+    if (stage == ns - 1) phase ^= 1;
     mbar_wait_quiet(smem_u32(m.full + stage), phase, 50000000ull);
   }
 }
@@ -735,13 +749,13 @@ __global__ void __launch_bounds__(256) rd_reduce_block_kernel(DecodeArgs a) {
 // ------------------------------------------------------------------ rd_down
 // Persistent like rd_gateup: work items (column group g, 64 rows hb of W2[e]),
 // consecutive items share g and with it the staged h rows; K = I whole.
-template <bool BLOCKWISE>
+template <bool BLOCKWISE, int RCK>
 __global__ void __launch_bounds__(THREADS, 2) rd_down_kernel(const __grid_constant__ CUtensorMap tmw, DecodeArgs a, int nHB) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   pdl_trigger();
   const int I = a.I, H = a.H, ngi = I / 128;
-  const StreamSmem m = stream_smem(smem_raw, I);
-  init_ring(m);
+  const StreamSmem m = stream_smem<RCK>(smem_raw, I);
+  init_ring<RCK>(m);
   pdl_wait();
   const UniqView uv{a.uniq, max_uniq(a.R, a.E), a.R};
   const int G = *uv.G();
@@ -759,10 +773,10 @@ __global__ void __launch_bounds__(THREADS, 2) rd_down_kernel(const __grid_consta
     for (int it = it0; it < it1 && ok; ++it) {
       const int g = it / nHB, hb = it - g * nHB;
       const int e = uv.expert()[uv.gu()[g]];
-      ok = produce_rows(m, &tmw, 0, e * H + hb * ROWS_PER_CTA, I, stage, phase, a.hdr, 0x92000u);
-      issued += (I + CK - 1) / CK;
+      ok = produce_rows<RCK>(m, &tmw, 0, e * H + hb * ROWS_PER_CTA, I, stage, phase, a.hdr, 0x92000u);
+      issued += (I + RCK - 1) / RCK;
     }
-    if (!ok && lane == 0) drain_ring(m, stage, phase, issued);
+    if (!ok && lane == 0) drain_ring<RCK>(m, stage, phase, issued);
   } else {
     const int g8 = lane >> 2, tig = lane & 3;
     const float s_h_t = BLOCKWISE ? 1.0f : e4m3_scale(__uint_as_float(a.hdr->amax_h));
@@ -814,11 +828,11 @@ __global__ void __launch_bounds__(THREADS, 2) rd_down_kernel(const __grid_consta
       if (BLOCKWISE && lane < ngi) wreg = __ldg(sw + lane);
       bool wsl_ready = !BLOCKWISE;
       float c[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int cc = 0; cc < I; cc += CK) {
-        const int bytes = min(CK, I - cc);
+      for (int cc = 0; cc < I; cc += RCK) {
+        const int bytes = min(RCK, I - cc);
         ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(m.full + stage), phase, m.abort_flag, a.hdr, 0x93000u));
         if (ok) {
-          const uint8_t* st = m.stages + stage * STAGE_BYTES;
+          const uint8_t* st = m.stages + stage * ring_stage_bytes<RCK>();
           if (!wsl_ready) {
             __syncwarp();  // the previous item's reads of the slot are done
             if (lane < ngi) wsl[lane] = wreg;
@@ -849,7 +863,7 @@ __global__ void __launch_bounds__(THREADS, 2) rd_down_kernel(const __grid_consta
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(m.empty + stage));
-        if (++stage == NS) {
+        if (++stage == ring_ns<RCK>()) {
           stage = 0;
           phase ^= 1;
         }
@@ -933,10 +947,17 @@ cudaError_t launch_route_direct(const DecodeArgs& a, cudaStream_t s) {
   const int maxG = maxU + a.R / GROUP + 1;
   const int sms = 2 * num_sms();  // two persistent CTAs per SM
   if (sms <= 0) return cudaErrorNoDevice;
-  const size_t smem_gu = stream_smem_bytes(KS), smem_dn = stream_smem_bytes(a.I);
+  // Down rows are I bytes long: short rows (I <= 256) take 256-byte stages, twice as many
+  const bool short_rows = a.I <= 256;
+  const size_t smem_gu = stream_smem_bytes(KS);
+  const size_t smem_dn = short_rows ? stream_smem_bytes<256>(a.I) : stream_smem_bytes<CK>(a.I);
+  auto down_kernel = [&]() {
+    return bw ? (short_rows ? rd_down_kernel<true, 256> : rd_down_kernel<true, CK>)
+              : (short_rows ? rd_down_kernel<false, 256> : rd_down_kernel<false, CK>);
+  };
   {
     // raise the dynamic shared-memory limit once per instantiation to the largest size used
-    static size_t set_gu[2] = {0, 0}, set_dn[2] = {0, 0};
+    static size_t set_gu[2] = {0, 0}, set_dn[4] = {0, 0, 0, 0};
     static std::mutex mu;
     std::lock_guard<std::mutex> lk(mu);
     if (smem_gu > set_gu[bw]) {
@@ -945,11 +966,11 @@ cudaError_t launch_route_direct(const DecodeArgs& a, cudaStream_t s) {
       if (err != cudaSuccess) return err;
       set_gu[bw] = smem_gu;
     }
-    if (smem_dn > set_dn[bw]) {
-      err = bw ? cudaFuncSetAttribute(rd_down_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_dn)
-               : cudaFuncSetAttribute(rd_down_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_dn);
+    const int dk = 2 * (bw ? 1 : 0) + (short_rows ? 1 : 0);
+    if (smem_dn > set_dn[dk]) {
+      err = cudaFuncSetAttribute(down_kernel(), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_dn);
       if (err != cudaSuccess) return err;
-      set_dn[bw] = smem_dn;
+      set_dn[dk] = smem_dn;
     }
   }
 
@@ -999,8 +1020,7 @@ cudaError_t launch_route_direct(const DecodeArgs& a, cudaStream_t s) {
   stage_begin("rd_down", s);
   {
     const cudaLaunchConfig_t c = config(static_cast<unsigned>(down_grid), THREADS, smem_dn);
-    err = bw ? cudaLaunchKernelEx(&c, rd_down_kernel<true>, tm2, a, nHB)
-             : cudaLaunchKernelEx(&c, rd_down_kernel<false>, tm2, a, nHB);
+    err = cudaLaunchKernelEx(&c, down_kernel(), tm2, a, nHB);
   }
   stage_end(s);
   return err;
