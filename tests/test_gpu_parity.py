@@ -309,6 +309,22 @@ def test_empty_batch_leaves_output_untouched(m):
     m.moe_forward(p, None, None, None, None, None, None, None, None, 0)
 
 
+def test_profile_single_stage_and_all_stages(m):
+    # moe_profile_start_stage times only the named stage; moe_profile_start times all
+    wl = W.Workload("prof", 300, 16, 4, 256, 128, W.QUANT_BF16, 27)
+    d = _dev(W.make_inputs(wl))
+    m.moe_profile_start_stage("gateup_gemm")
+    for _ in range(3):
+        run_forward(m, wl, d)
+    st = m.moe_profile_stop()
+    assert set(st) == {"gateup_gemm"} and st["gateup_gemm"][1] == 3 and st["gateup_gemm"][0] > 0
+    m.moe_profile_start()
+    run_forward(m, wl, d)
+    st = m.moe_profile_stop()
+    assert {"route_rank", "scan_tiles", "scatter_gather", "gateup_gemm", "down_gemm", "combine"} <= set(st)
+    assert all(n == 1 for _, n in st.values())
+
+
 def test_small_workspace_rejected_without_launch(m):
     wl = W.workload("tiny")
     d = _dev(W.make_inputs(wl))
