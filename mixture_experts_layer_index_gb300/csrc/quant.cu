@@ -119,7 +119,23 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const float4* __restric
   dep_wait();  // a and its amax from the Gate/Up GEMM
   const float s = e4m3_scale(__uint_as_float(hdr->amax_h));
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4; i += stride) {
+  // four independent loads in flight per thread; a is read once, so its lines are
+  // evicted from L2 first and the h rows just written stay for the Down GEMM
+  const uint64_t pol = l2_evict_first_policy();
+  size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+  for (; i + 3 * stride < n4; i += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = ld_nc_v4_hint(a + i + j * stride, pol);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 f = make_float4(__uint_as_float(v[j].x), __uint_as_float(v[j].y), __uint_as_float(v[j].z),
+                                   __uint_as_float(v[j].w));
+      h[i + j * stride] = static_cast<uint32_t>(cvt_e4m3x2(f.x / s, f.y / s)) |
+                          (static_cast<uint32_t>(cvt_e4m3x2(f.z / s, f.w / s)) << 16);
+    }
+  }
+  for (; i < n4; i += stride) {
     const float4 v = __ldg(a + i);
     h[i] = static_cast<uint32_t>(cvt_e4m3x2(v.x / s, v.y / s)) | (static_cast<uint32_t>(cvt_e4m3x2(v.z / s, v.w / s)) << 16);
   }
