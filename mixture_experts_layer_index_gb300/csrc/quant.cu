@@ -148,15 +148,23 @@ __global__ void __launch_bounds__(256) quant_groups_kernel(const float4* __restr
   dep_wait();  // a from the Gate/Up GEMM
   const int lane = threadIdx.x & 31;
   const size_t nw = (static_cast<size_t>(gridDim.x) * blockDim.x) >> 5;
-  for (size_t g0 = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; g0 < items; g0 += 4 * nw) {
-    float4 v[4];
+  // eight groups per warp and pass (their loads in flight together, their amax
+  // reductions interleaved); a is read once: L2 evicts it first, keeping h for Down
+  constexpr int NG = 8;
+  const uint64_t pol = l2_evict_first_policy();
+  for (size_t g0 = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; g0 < items; g0 += NG * nw) {
+    float4 v[NG];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < NG; ++j) {
       const size_t g = g0 + j * nw;
-      v[j] = g < items ? __ldg(a + g * 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (g < items) {
+        const uint4 u = ld_nc_v4_hint(a + g * 32 + lane, pol);
+        v[j] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
+      }
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < NG; ++j) {
       const size_t g = g0 + j * nw;
       const float m = warp_max(fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
       const float s = e4m3_scale(m);
@@ -232,7 +240,7 @@ cudaError_t launch_quant_groups(const float* a, void* h, float* sh, int rows, in
   const size_t items = static_cast<size_t>(rows) * (cols / 128);
   if (items == 0) return cudaSuccess;
   stage_begin("quant_h", s);
-  const cudaError_t err = launch_dependent(quant_groups_kernel, dim3(grid_for(items * 32, 256 * 4)), dim3(256), 0, s,
+  const cudaError_t err = launch_dependent(quant_groups_kernel, dim3(grid_for(items * 32, 256 * 8)), dim3(256), 0, s,
                                            reinterpret_cast<const float4*>(a), static_cast<uint32_t*>(h), sh, items);
   stage_end(s);
   return err;
