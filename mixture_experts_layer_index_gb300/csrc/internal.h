@@ -64,9 +64,11 @@ bool plan_forward(const moe_problem& p, ForwardLayout* out);
 
 // ------------------------------------------------------------------ launchers
 // All return cudaSuccess or the launch error; none synchronises.
+// amax_x (bf16, amax_n values) non-null: the same launch also records the
+// per-tensor amax of x in hdr->amax_x (FP8 per-tensor forward).
 cudaError_t launch_route_rank(const float* scores, const int32_t* ids_in, int T, int E, int k, int32_t* ids_out,
                               float* w_out, int32_t* lrank, int32_t* blockcounts, DeviceHeader* hdr, bool route,
-                              bool rank, cudaStream_t s);
+                              bool rank, cudaStream_t s, const void* amax_x = nullptr, size_t amax_n = 0);
 cudaError_t launch_scan_tiles(int32_t* blockcounts, int nblk, int E, int32_t* counts, int32_t* offsets,
                               int32_t* tiles, int32_t* num_tiles, int max_tiles, int BM, int32_t* tile_scratch,
                               DeviceHeader* hdr, cudaStream_t s);
@@ -76,7 +78,6 @@ cudaError_t launch_scatter_gather(const int32_t* ids, const int32_t* lrank, cons
                                   int k, int H, const void* x, void* xs, int32_t* perm, int32_t* inv,
                                   cudaStream_t s);
 // Per-tensor e4m3 passes of the grouped FP8 path (quant.cu).
-cudaError_t launch_x_amax(const void* x, size_t n, DeviceHeader* hdr, cudaStream_t s);
 cudaError_t launch_scatter_gather_q(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
                                     int k, int H, const void* x, void* xs, int32_t* perm, int32_t* inv,
                                     const DeviceHeader* hdr, cudaStream_t s);

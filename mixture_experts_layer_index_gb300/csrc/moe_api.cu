@@ -393,7 +393,8 @@ moe_status moe_forward(const moe_problem* pp, const void* x, const float* scores
     int32_t* num_tiles = at<int32_t*>(ws, L.num_tiles);
     e = launch_reset_header(hdr, s);
     if (e == cudaSuccess)
-      e = launch_route_rank(scores, nullptr, p.T, p.E, p.k, ids, w, lrank, bc, hdr, true, true, s);
+      e = launch_route_rank(scores, nullptr, p.T, p.E, p.k, ids, w, lrank, bc, hdr, true, true, s,
+                            p.quant == MOE_FP8_PER_TENSOR ? x : nullptr, static_cast<size_t>(p.T) * p.H);
     if (e == cudaSuccess)
       e = launch_scan_tiles(bc, L.shuf.nblk, p.E, counts, offsets, tiles, num_tiles, L.max_tiles, kGemmBM, nullptr,
                             hdr, s);
@@ -403,7 +404,6 @@ moe_status moe_forward(const moe_problem* pp, const void* x, const float* scores
     void* xs = at<void*>(ws, L.xs);
     float* xs_scale = blockwise ? at<float*>(ws, L.xs_scale) : nullptr;
     float* sh = blockwise ? at<float*>(ws, L.sh) : nullptr;
-    if (e == cudaSuccess && f8) e = launch_x_amax(x, static_cast<size_t>(p.T) * p.H, hdr, s);
     if (e == cudaSuccess) {
       if (f8)
         e = launch_scatter_gather_q(ids, lrank, bc, p.T, p.E, p.k, p.H, x, xs, perm, inv, hdr, s);

@@ -1,47 +1,14 @@
 // Per-tensor e4m3 quantisation passes of the grouped FP8 path ("perf: add
 // small-batch route MMA for MoE", Summary: per-tensor FP8 with dynamic
-// activation scales): the amax of x, the expert-sorted copy of x quantised with
-// s_x = amax/448, and the quantisation of a (the SwiGLU output) with its global
-// scale s_h.  Scales: amax / 448 in fp32 (1 when amax == 0); codes: round to
-// nearest even with saturation (cvt.rn.satfinite).
+// activation scales): the expert-sorted copy of x quantised with s_x = amax/448
+// (the amax of x comes from extra blocks of the route/rank kernel), and the
+// quantisation of a (the SwiGLU output) with its global scale s_h; plus the
+// blockwise forms.  Scales: amax / 448 in fp32 (1 when amax == 0); codes: round
+// to nearest even with saturation (cvt.rn.satfinite).
 #include "common.cuh"
 #include "internal.h"
 
 namespace moe {
-
-// amax |x| over n bf16 values into hdr->amax_x (fp32 bits; non-negative floats
-// order like their bit patterns).  Loads go out 8 x 16 bytes per thread at a time.
-__global__ void __launch_bounds__(256) x_amax_kernel(const uint4* __restrict__ x, size_t n8, DeviceHeader* hdr) {
-  dep_wait();
-  float m = 0.0f;
-  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-  for (size_t base = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; base < n8; base += stride * 8) {
-    uint4 v[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const size_t i = base + j * stride;
-      v[j] = i < n8 ? __ldg(x + i) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v[j]);
-#pragma unroll
-      for (int h2 = 0; h2 < 4; ++h2) {
-        const float2 f = __bfloat1622float2(b[h2]);
-        m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
-      }
-    }
-  }
-  __shared__ float s_m[8];
-  m = warp_max(m);
-  if ((threadIdx.x & 31) == 0) s_m[threadIdx.x >> 5] = m;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    m = threadIdx.x < (blockDim.x >> 5) ? s_m[threadIdx.x] : 0.0f;
-    m = warp_max(m);
-    if (threadIdx.x == 0 && m > 0.0f) atomicMax(&hdr->amax_x, __float_as_uint(m));  // one atomic per block
-  }
-}
 
 // Scatter fused with the gather and quantisation of the activations, one block
 // per token: the block quantises the token's x row once into shared memory (with
@@ -183,16 +150,6 @@ static unsigned grid_for(size_t work, unsigned per_block) {
   size_t b = (work + per_block - 1) / per_block;
   if (b > cap) b = cap;
   return static_cast<unsigned>(b < 1 ? 1 : b);
-}
-
-cudaError_t launch_x_amax(const void* x, size_t n, DeviceHeader* hdr, cudaStream_t s) {
-  const size_t n8 = n / 8;
-  if (n8 == 0) return cudaSuccess;
-  stage_begin("x_amax", s);
-  const cudaError_t err = launch_dependent(x_amax_kernel, dim3(grid_for(n8, 256 * 8)), dim3(256), 0, s,
-                                           static_cast<const uint4*>(x), n8, hdr);
-  stage_end(s);
-  return err;
 }
 
 static cudaError_t launch_tok_q(bool blockwise, const int32_t* ids, const int32_t* lrank, const int32_t* blockbase,

@@ -67,11 +67,51 @@ __device__ __forceinline__ void rank_block(int* s_ids, int* s_lr, int* hist, int
   }
 }
 
+// Per-tensor amax of x (bf16, n8 pieces of 8 values) by `nb` blocks, block b of
+// them here: eight 16-byte loads in flight per thread, one atomic per block.
+__device__ void amax_blocks(const uint4* __restrict__ x, size_t n8, int b, int nb, DeviceHeader* hdr) {
+  __shared__ float s_m[kRouteThreads / 32];
+  float m = 0.0f;
+  const size_t stride = static_cast<size_t>(nb) * blockDim.x;
+  for (size_t base = b * static_cast<size_t>(blockDim.x) + threadIdx.x; base < n8; base += stride * 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const size_t i = base + j * stride;
+      v[j] = i < n8 ? __ldg(x + i) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v[j]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(h2[q]);
+        m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+  }
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0) s_m[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    m = threadIdx.x < (blockDim.x >> 5) ? s_m[threadIdx.x] : 0.0f;
+    m = warp_max(m);
+    if (threadIdx.x == 0 && m > 0.0f) atomicMax(&hdr->amax_x, __float_as_uint(m));
+  }
+}
+
 template <int MAXV, bool ROUTE, bool RANK>
 __global__ void __launch_bounds__(kRouteThreads) route_rank_kernel(
     const float* __restrict__ scores, const int32_t* __restrict__ ids_in, int T, int E, int k, int TB,
     int32_t* __restrict__ ids_out, float* __restrict__ w_out, int32_t* __restrict__ lrank,
-    int32_t* __restrict__ blockcounts, DeviceHeader* hdr) {
+    int32_t* __restrict__ blockcounts, DeviceHeader* hdr, const uint4* __restrict__ amax_x, size_t amax_n8,
+    int nblk) {
+  // blocks past the nblk routing blocks compute the per-tensor amax of x (FP8)
+  // alongside them: it depends on nothing the routing produces
+  if (static_cast<int>(blockIdx.x) >= nblk) {
+    amax_blocks(amax_x, amax_n8, static_cast<int>(blockIdx.x) - nblk, static_cast<int>(gridDim.x) - nblk, hdr);
+    return;
+  }
   extern __shared__ int smem[];
   int* s_ids = smem;                          // [1024]
   int* s_lr = smem + kMaxRoutesPerBlock;      // [1024]
@@ -287,11 +327,11 @@ static cudaError_t rr_smem_attr() {
 template <bool ROUTE, bool RANK>
 static cudaError_t launch_rr(int maxv, dim3 grid, size_t smem, cudaStream_t s, const float* scores,
                              const int32_t* ids_in, int T, int E, int k, int TB, int32_t* ids_out, float* w_out,
-                             int32_t* lrank, int32_t* bc, DeviceHeader* hdr) {
+                             int32_t* lrank, int32_t* bc, DeviceHeader* hdr, const uint4* ax, size_t an8, int nblk) {
 #define MOE_RR(V)                                                                                          \
   if (const cudaError_t ae = rr_smem_attr<V, ROUTE, RANK>()) return ae;                                    \
   route_rank_kernel<V, ROUTE, RANK><<<grid, kRouteThreads, smem, s>>>(scores, ids_in, T, E, k, TB, ids_out, \
-                                                                     w_out, lrank, bc, hdr)
+                                                                     w_out, lrank, bc, hdr, ax, an8, nblk)
   switch (maxv) {
     case 1: MOE_RR(1); break;
     case 2: MOE_RR(2); break;
@@ -305,19 +345,24 @@ static cudaError_t launch_rr(int maxv, dim3 grid, size_t smem, cudaStream_t s, c
 
 cudaError_t launch_route_rank(const float* scores, const int32_t* ids_in, int T, int E, int k, int32_t* ids_out,
                               float* w_out, int32_t* lrank, int32_t* blockcounts, DeviceHeader* hdr, bool route,
-                              bool rank, cudaStream_t s) {
+                              bool rank, cudaStream_t s, const void* amax_x, size_t amax_n) {
   if (T <= 0) return cudaSuccess;
   const int TB = route_tokens_per_block(k);
   const int nblk = (T + TB - 1) / TB;
   const size_t smem = (2 * kMaxRoutesPerBlock + (kRouteThreads / 32) * E) * sizeof(int);
   int maxv = 1;
   while (maxv * 32 < E) maxv *= 2;
-  const dim3 grid(nblk);
+  // amax of x: one extra block per SM; they start on the SMs the routing blocks
+  // leave free and take the others as the routing finishes
+  const size_t an8 = amax_x ? amax_n / 8 : 0;
+  const int nam = an8 > 0 ? (num_sms() > 0 ? num_sms() : 148) : 0;
+  const dim3 grid(nblk + nam);
+  const uint4* ax = static_cast<const uint4*>(amax_x);
   stage_begin("route_rank", s);
   cudaError_t err;
-  if (route && rank) err = launch_rr<true, true>(maxv, grid, smem, s, scores, ids_in, T, E, k, TB, ids_out, w_out, lrank, blockcounts, hdr);
-  else if (route) err = launch_rr<true, false>(maxv, grid, smem, s, scores, ids_in, T, E, k, TB, ids_out, w_out, lrank, blockcounts, hdr);
-  else err = launch_rr<false, true>(maxv, grid, smem, s, scores, ids_in, T, E, k, TB, ids_out, w_out, lrank, blockcounts, hdr);
+  if (route && rank) err = launch_rr<true, true>(maxv, grid, smem, s, scores, ids_in, T, E, k, TB, ids_out, w_out, lrank, blockcounts, hdr, ax, an8, nblk);
+  else if (route) err = launch_rr<true, false>(maxv, grid, smem, s, scores, ids_in, T, E, k, TB, ids_out, w_out, lrank, blockcounts, hdr, ax, an8, nblk);
+  else err = launch_rr<false, true>(maxv, grid, smem, s, scores, ids_in, T, E, k, TB, ids_out, w_out, lrank, blockcounts, hdr, ax, an8, nblk);
   stage_end(s);
   return err;
 }
