@@ -12,7 +12,8 @@
 //               experts in first-use order with their routes (a route-order
 //               scan of at most 1024 routes, no sort), so an expert chosen by
 //               several tokens is streamed once, cut into column groups of up
-//               to 8 routes.
+//               to 8 routes; plus prefetch CTAs that repeat the routing and
+//               start the selected experts' W1 on its way into L2.
 //   rd_gateup   persistent, two CTAs per SM over work items (column group, K
 //               split, 64 rows of W1[e]): a producer warp streams the rows with
 //               TMA into a ring of shared-memory stages; four consumer warps
@@ -23,8 +24,9 @@
 //               mode quantises h per (route, 128 columns) here, per-tensor mode
 //               records the global amax of h.
 //   rd_down     persistent like rd_gateup over (column group, 64 rows of
-//               W2[e]); h of the group's routes is quantised (per-tensor) or
-//               copied into shared memory; fp32 o in route order.
+//               W2[e]), with 256-byte stages for rows of at most 256 bytes; h of
+//               the group's routes is quantised (per-tensor) or copied into
+//               shared memory; fp32 o in route order.
 //   combine     the contiguous top-k reduction shared with the grouped path.
 // All but rd_prep are launched as programmatic dependents of their predecessor.
 //
