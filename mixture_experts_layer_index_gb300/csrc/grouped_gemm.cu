@@ -14,8 +14,10 @@
 //   warps 4+    epilogue, one warp per 32-lane TMEM quadrant (two for the FP8
 //               Gate/Up, each draining half of the accumulator's columns):
 //               tcgen05.ld (one row per thread), the fused epilogue, stores
-//               (Down: staged in shared memory and written out as whole,
-//               coalesced row segments).
+//               (Down: staged in shared memory as 128-byte-swizzled boxes and
+//               written by TMA tile stores).
+// Every launch is a programmatic dependent of the kernel before it: barrier
+// and TMEM set-up run before the wait for the predecessor's results.
 //
 // Gate/Up (MODE_GATEUP): A = the expert-sorted activation rows that the
 //   scatter kernel copied (plain TMA tile loads); or, as a selectable

@@ -1,6 +1,7 @@
 // Top-k routing, index shuffling and the grouped-GEMM tile map.
 //
-// Routing: one warp per token (routing.cuh).
+// Routing: one warp per token (routing.cuh).  For the per-tensor FP8 forward the
+// route/rank launch also carries extra blocks that record the amax of x.
 //
 // Shuffle (index_shuffling of "Port necessary FBGEMM MoE kernels"; the
 // counting, sorting and task-map steps of the route-MMA page's Motivation), in
