@@ -60,7 +60,7 @@ typedef struct CUstream_st* moe_stream_t;
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,    /* bad shape, null or misaligned pointer, inconsistent scales */
-  MOE_ERR_UNSUPPORTED = 2,    /* valid, but outside what this build implements (limits below) */
+  MOE_ERR_UNSUPPORTED = 2,    /* valid, but outside what this library implements (limits below) */
   MOE_ERR_WORKSPACE = 3,      /* workspace missing or smaller than the *_workspace_size() value */
   MOE_ERR_CUDA = 4,           /* a CUDA runtime/driver call or a launch failed, or no usable GPU */
   MOE_ERR_DEVICE_TIMEOUT = 5, /* a kernel's bounded wait expired (reported by moe_read_device_status) */
@@ -87,7 +87,7 @@ typedef struct {
   moe_path path;
 } moe_problem;
 
-/* Limits of this build (MOE_ERR_UNSUPPORTED beyond them):
+/* Limits of this library (MOE_ERR_UNSUPPORTED beyond them):
  *   1 <= E <= 512;  1 <= k <= min(E, 32);  0 <= T;  T*k < 2^31;
  *   H % 64 == 0, I % 64 == 0 (bf16);  H % 128 == 0, I % 64 == 0 (FP8 per-tensor);
  *   H % 128 == 0, I % 128 == 0 (FP8 blockwise);

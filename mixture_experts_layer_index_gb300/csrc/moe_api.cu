@@ -277,7 +277,7 @@ const char* moe_status_string(moe_status s) {
   switch (s) {
     case MOE_OK: return "ok";
     case MOE_ERR_INVALID_ARG: return "invalid argument";
-    case MOE_ERR_UNSUPPORTED: return "unsupported problem (outside this build's limits)";
+    case MOE_ERR_UNSUPPORTED: return "unsupported problem (outside this library's limits)";
     case MOE_ERR_WORKSPACE: return "workspace missing or too small";
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_DEVICE_TIMEOUT: return "device-side bounded wait timed out";
