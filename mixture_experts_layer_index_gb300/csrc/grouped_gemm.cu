@@ -270,13 +270,14 @@ __global__ void __launch_bounds__(threads_of(MODE, F8), 1)
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       if (MODE == MODE_GATEUP) {
-        // Direct stores (each thread writes whole 64- or 128-byte pieces of its own
+        // bf16: direct stores (each thread writes whole 64-byte pieces of its own
         // sorted row).  F8: a = silu(sc g) * (sc u) with sc = s_x * s_w1[e], kept
-        // in fp32 for the per-tensor quantisation of h, whose amax is recorded here.
+        // in fp32 for the per-tensor quantisation of h, whose amax is recorded here;
+        // each warp stages one [32 rows][32 fp32] box per iteration (128-byte
+        // swizzle) and stores it by TMA when all 32 rows belong to the tile.
         const float sc = F8 ? e4m3_scale(__uint_as_float(*p.amax_in)) * __ldg(p.wscale + tl.x) : 1.0f;
         float amax = 0.0f;
         __nv_bfloat16* out_row = p.out + static_cast<size_t>(row0 + row) * p.out_ld;
-        float* out_row_f = F8 ? p.out_f32 + static_cast<size_t>(row0 + row) * p.out_ld : nullptr;
         constexpr int GC = BN / 2 / NH;  // gate columns of this warp (and as many up columns)
 #pragma unroll 1
         for (int c = h * GC; c < h * GC + GC; c += 32) {
@@ -290,23 +291,49 @@ __global__ void __launch_bounds__(threads_of(MODE, F8), 1)
             if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
           }
           const int col = n * (BN / 2) + c;
-          if (row < nrows && col < p.n_valid) {
+          if (F8) {
+            uint8_t* stg = smem + STAGING_OFFSET + e8 * 4096;
+            const int wrows = min(32, nrows - q * 32), wrow0 = row0 + q * 32;
+            if (lane == 0) bulk_wait_group_read0();  // the previous box has left the staging
+            __syncwarp();
             float hv[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) hv[i] = F8 ? silu_mul(sc * g[i], sc * up[i]) : silu_mul(g[i], up[i]);
-            if (F8) {
-              float4* dst = reinterpret_cast<float4*>(out_row_f + col);
+            for (int i = 0; i < 32; ++i) hv[i] = silu_mul(sc * g[i], sc * up[i]);
+            const bool valid = row < nrows && col < p.n_valid;
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                dst[i] = make_float4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+            for (int i = 0; i < 8; ++i) {
+              *reinterpret_cast<float4*>(stg + lane * 128 + ((i ^ (lane & 7)) << 4)) =
+                  make_float4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+              if (valid)
                 amax = fmaxf(amax, fmaxf(fmaxf(fabsf(hv[4 * i]), fabsf(hv[4 * i + 1])),
                                          fmaxf(fabsf(hv[4 * i + 2]), fabsf(hv[4 * i + 3]))));
-              }
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(out_row + col);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) dst[i] = pack_bf16x8(hv + 8 * i);
             }
+            if (wrows == 32) {
+              fence_proxy_async_shared();
+              __syncwarp();
+              if (lane == 0) {
+                if (col < p.n_valid) tma_store_2d(&tmO, smem_u32(stg), col, wrow0);
+                bulk_commit_group();
+              }
+              __syncwarp();
+            } else {
+              __syncwarp();
+#pragma unroll
+              for (int it = 0; it < 8; ++it) {  // 4 rows of 32 fp32 (8 lanes each) per instruction
+                const int r = it * 4 + (lane >> 3), j = lane & 7;
+                if (r < wrows && col + 4 * j < p.n_valid)
+                  *reinterpret_cast<float4*>(p.out_f32 + static_cast<size_t>(wrow0 + r) * p.out_ld + col + 4 * j) =
+                      *reinterpret_cast<const float4*>(stg + r * 128 + ((j ^ (r & 7)) << 4));
+              }
+              __syncwarp();
+            }
+          } else if (row < nrows && col < p.n_valid) {
+            float hv[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) hv[i] = silu_mul(g[i], up[i]);
+            uint4* dst = reinterpret_cast<uint4*>(out_row + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = pack_bf16x8(hv + 8 * i);
           }
         }
         if (F8) {
@@ -380,7 +407,7 @@ __global__ void __launch_bounds__(threads_of(MODE, F8), 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
-    if (MODE == MODE_DOWN && lane == 0) bulk_wait_group0();  // this warp's TMA stores have completed
+    if ((MODE == MODE_DOWN || F8) && lane == 0) bulk_wait_group0();  // this warp's TMA stores have completed
     __syncwarp();
   }
   tc_fence_before();
@@ -404,6 +431,20 @@ static bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// fp32 [outer][inner] tensor, 128-byte swizzle (TMA stores of the FP8 Gate/Up output a)
+static bool encode_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                          uint32_t box_outer) {
+  EncodeTiledFn fn = get_encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 4};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int MODE, bool F8>
@@ -459,6 +500,8 @@ cudaError_t launch_gateup_bf16(const GroupedArgs& a, cudaStream_t s) {
   p.amax_in = &a.hdr->amax_x;
   p.amax_out = &a.hdr->amax_h;
   p.out_f32 = static_cast<float*>(a.a_f32);
+  CUtensorMap tma32 = tmx;  // F8: a [R rows][I] fp32, stored in [32 rows][32 columns] boxes
+  if (a.f8 && !encode_2d_f32(&tma32, a.a_f32, a.I, a.R, 32, 32)) return cudaErrorInvalidValue;
   p.nN = (a.I + BN / 2 - 1) / (BN / 2);
   p.K = a.H;
   p.b_rows_per_expert = 2 * a.I;
@@ -471,7 +514,7 @@ cudaError_t launch_gateup_bf16(const GroupedArgs& a, cudaStream_t s) {
   stage_begin("gateup_gemm", s);
   if (a.f8)
     err = launch_dependent(grouped_gemm_kernel<MODE_GATEUP, true>, dim3(grid), dim3(threads_of(MODE_GATEUP, true)),
-                           SMEM_BYTES, s, tmx, tmw1, tmx, p);
+                           SMEM_BYTES, s, tmx, tmw1, tma32, p);
   else
     err = launch_dependent(grouped_gemm_kernel<MODE_GATEUP, false>, dim3(grid), dim3(threads_of(MODE_GATEUP, false)),
                            SMEM_BYTES, s, tmx, tmw1, tmx, p);
