@@ -29,8 +29,8 @@ constexpr int BM = kGemmBM;  // 128
 constexpr int BN = 128;
 constexpr int BKB = 128;  // K bytes (= e4m3 elements) per stage, one scale block
 constexpr int MAX_STAGES = 6;
-// Gate/Up: 6 stages, direct stores (each thread's 32 fp32 outputs are one
-// contiguous 128-byte piece); Down: 5 stages and 32 KB of output staging.
+// Gate/Up: 6 stages and 32 KB of staging for the TMA stores of a; Down: 5 stages
+// and 32 KB of output staging.
 __host__ __device__ constexpr int stages_of(int mode) { return mode == 0 ? 6 : 5; }
 constexpr int A_BYTES = BM * BKB;
 constexpr int B_BYTES = BN * BKB;
@@ -41,10 +41,11 @@ constexpr int EPI_WARPS = 8;      // warps 4..11
 constexpr int THREADS = 32 * (4 + EPI_WARPS);
 constexpr int NUM_BARS = 2 * MAX_STAGES + 2 * NBUF;
 // Down output staging: 32 rows x 128 bytes per epilogue warp, after the barriers
-__host__ __device__ constexpr int staging_offset(int mode) { return stages_of(mode) * STAGE_BYTES + 256; }
+// (1024-byte aligned: the Gate/Up epilogue's boxes are sources of 128-byte-swizzled TMA stores)
+__host__ __device__ constexpr int staging_offset(int mode) { return (stages_of(mode) * STAGE_BYTES + 256 + 1023) / 1024 * 1024; }
 constexpr int STAGING_BYTES = EPI_WARPS * 32 * 128;
 __host__ __device__ constexpr size_t smem_bytes(int mode) {
-  return 1024 + staging_offset(mode) + (mode == 0 ? 0 : STAGING_BYTES);
+  return 1024 + staging_offset(mode) + STAGING_BYTES;
 }
 
 constexpr int MODE_GATEUP = 0;
@@ -86,6 +87,7 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_blockwise_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmO,
                              const Params p) {
   constexpr int STAGES = stages_of(MODE);
   extern __shared__ uint8_t smem_raw[];
@@ -281,14 +283,37 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (!ok) break;
       if (MODE == MODE_GATEUP) {
-        // each thread's 32 fp32 outputs are one contiguous 128-byte piece of its row
-        if (row < nrows) {
-          float* dst = p.out_f32 + static_cast<size_t>(row0 + row) * p.I + n * (BN / 2) + ch * 32;
+        // each thread's 32 fp32 outputs are one 128-byte piece of its row: the warp
+        // stages them as one [32 rows][32 fp32] box (128-byte swizzle) for a TMA tile
+        // store, or 16-byte stores for a partial tile's rows
+        uint8_t* stg = smem + staging_offset(MODE) + e8 * 4096;
+        const int wrows = min(32, nrows - q * 32), wrow0 = row0 + q * 32;
+        const int col = n * (BN / 2) + ch * 32;
+        if (lane == 0) bulk_wait_group_read0();  // the previous box has left the staging
+        __syncwarp();
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(dst + i) =
-                make_float4(silu_mul_fast(acc[i], acc[32 + i]), silu_mul_fast(acc[i + 1], acc[33 + i]),
-                            silu_mul_fast(acc[i + 2], acc[34 + i]), silu_mul_fast(acc[i + 3], acc[35 + i]));
+        for (int i = 0; i < 8; ++i)
+          *reinterpret_cast<float4*>(stg + lane * 128 + ((i ^ (lane & 7)) << 4)) =
+              make_float4(silu_mul_fast(acc[4 * i], acc[32 + 4 * i]), silu_mul_fast(acc[4 * i + 1], acc[33 + 4 * i]),
+                          silu_mul_fast(acc[4 * i + 2], acc[34 + 4 * i]), silu_mul_fast(acc[4 * i + 3], acc[35 + 4 * i]));
+        if (wrows == 32) {
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmO, smem_u32(stg), col, wrow0);
+            bulk_commit_group();
+          }
+          __syncwarp();
+        } else {
+          __syncwarp();
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {  // 4 rows of 32 fp32 (8 lanes each) per instruction
+            const int r = it * 4 + (lane >> 3), j = lane & 7;
+            if (r < wrows)
+              *reinterpret_cast<float4*>(p.out_f32 + static_cast<size_t>(wrow0 + r) * p.I + col + 4 * j) =
+                  *reinterpret_cast<const float4*>(stg + r * 128 + ((j ^ (r & 7)) << 4));
+          }
+          __syncwarp();
         }
       } else {
         // Down rows (sorted order, like h): each thread's 64 bf16 outputs are staged
@@ -311,6 +336,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
       }
     }
+    if (MODE == MODE_GATEUP && lane == 0) bulk_wait_group0();  // this warp's TMA stores have completed
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -318,6 +345,19 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
+}
+
+// fp32 [outer][inner] tensor in [32 rows][32 columns] boxes, 128-byte swizzle (a of the Gate/Up)
+static bool encode_f32_box32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer) {
+  EncodeTiledFn fn = get_encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 4};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 static bool encode_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_rows) {
@@ -348,8 +388,9 @@ cudaError_t launch_gateup_blockwise(const GroupedArgs& a, const float* xs_scale,
   if (err != cudaSuccess) return err;
   const int sms = num_sms();
   if (sms <= 0) return cudaErrorNoDevice;
-  CUtensorMap tma, tmb;
-  if (!encode_u8(&tma, a.xs, a.H, a.R, BM) || !encode_u8(&tmb, a.w1, a.H, static_cast<uint64_t>(a.E) * 2 * a.I, BN / 2))
+  CUtensorMap tma, tmb, tmo;
+  if (!encode_u8(&tma, a.xs, a.H, a.R, BM) || !encode_u8(&tmb, a.w1, a.H, static_cast<uint64_t>(a.E) * 2 * a.I, BN / 2) ||
+      !encode_f32_box32(&tmo, a.a_f32, a.I, a.R))
     return cudaErrorInvalidValue;
   Params p{};
   p.tiles = a.tiles;
@@ -368,7 +409,7 @@ cudaError_t launch_gateup_blockwise(const GroupedArgs& a, const float* xs_scale,
   const int grid = static_cast<int>(units < sms ? units : sms);
   stage_begin("gateup_gemm", s);
   err = launch_dependent(grouped_blockwise_kernel<MODE_GATEUP>, dim3(grid), dim3(THREADS), smem_bytes(MODE_GATEUP), s,
-                         tma, tmb, p);
+                         tma, tmb, tmo, p);
   stage_end(s);
   return err;
 }
@@ -400,7 +441,7 @@ cudaError_t launch_down_blockwise(const GroupedArgs& a, const float* h_scale, cu
   const int grid = static_cast<int>(units < sms ? units : sms);
   stage_begin("down_gemm", s);
   err = launch_dependent(grouped_blockwise_kernel<MODE_DOWN>, dim3(grid), dim3(THREADS), smem_bytes(MODE_DOWN), s,
-                         tma, tmb, p);
+                         tma, tmb, tma, p);
   stage_end(s);
   return err;
 }
