@@ -136,7 +136,9 @@ moe_status moe_shuffle(const int32_t* ids, int T, int E, int k, int32_t* counts,
  *   this call nor the library allocates or frees anything.
  *   The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture.
+ *   before any stream capture.  The looked-up address is cached for the life
+ *   of the process: destroying the device's context after the first call
+ *   (cudaDeviceReset) and calling again is not supported.
  *   Every call uses the same array: calls whose work overlaps on the GPU (e.g.
  *   on two streams) race and must be serialised by the caller.
  *   Errors: as moe_shuffle; MOE_ERR_WORKSPACE when the problem needs more than
@@ -193,11 +195,21 @@ moe_status moe_forward(const moe_problem* p, const void* x, const float* scores,
                        const void* w2, const float* w1_scale, const float* w2_scale, void* y,
                        void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* moe_forward_views - device pointers to the routing results moe_forward
+/* moe_forward_views - device pointers to the intermediate results moe_forward
  * leaves in the workspace (read-only diagnostics; valid after the call's
  * work on the stream completed).  Pointers not produced by the path chosen
  * for *p are set to NULL.  ids/w: [T, k]; counts [E]; offsets [E+1];
- * perm/inv [R]; tiles [*, 4] and num_tiles [1] as for moe_tile_map (BM 128). */
+ * perm/inv [R]; tiles [*, 4] and num_tiles [1] as for moe_tile_map (BM 128).
+ * The activations as the Gate/Up GEMM reads them (the quantisation of x is
+ * unique, so these can be checked bit for bit):
+ *   xs       grouped path: [R, H] rows in expert-sorted order, row p = x row
+ *            of token perm[p] / k (bf16 copies, or e4m3 codes in the FP8
+ *            modes); route-direct path: [T, H] e4m3 codes in token order.
+ *            NULL for the bf16 variant that gathers x inside the GEMM.
+ *   x_scale  blockwise FP8: fp32 scales of xs, one per row and 128 columns
+ *            ([R, H/128] sorted, or [T, H/128] route-direct); else NULL.
+ *   amax_x   per-tensor FP8: the fp32 amax of x over the whole [T, H]
+ *            (scale = amax / 448, 1 when it is 0); else NULL. */
 typedef struct {
   const int32_t* ids;
   const float* w;
@@ -207,6 +219,9 @@ typedef struct {
   const int32_t* inv;
   const int32_t* tiles;
   const int32_t* num_tiles;
+  const void* xs;
+  const float* x_scale;
+  const float* amax_x;
 } moe_views;
 moe_status moe_forward_views(const moe_problem* p, const void* ws, size_t ws_bytes, moe_views* out);
 

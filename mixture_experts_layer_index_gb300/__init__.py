@@ -46,7 +46,8 @@ class moe_problem(ctypes.Structure):
 
 class moe_views(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
-                ("ids", "w", "counts", "offsets", "perm", "inv", "tiles", "num_tiles")]
+                ("ids", "w", "counts", "offsets", "perm", "inv", "tiles", "num_tiles", "xs", "x_scale",
+                 "amax_x")]
 
 
 class moe_stage_time(ctypes.Structure):

@@ -4,6 +4,7 @@
 // small-batch route MMA for MoE": choosing the small-batch path, picking the
 // K split, laying out one workspace, checking every argument, and writing into
 // an output the caller allocated.
+#include <cstddef>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -487,6 +488,15 @@ moe_status moe_forward_views(const moe_problem* p, const void* ws, size_t ws_byt
     v.inv = at<const int32_t*>(base, L.inv);
     v.tiles = at<const int32_t*>(base, L.tiles);
     v.num_tiles = at<const int32_t*>(base, L.num_tiles);
+    if (!(p->quant == MOE_BF16 && gateup_gather4())) v.xs = at<const void*>(base, L.xs);
+    if (p->quant == MOE_FP8_BLOCK128) v.x_scale = at<const float*>(base, L.xs_scale);
+  } else {
+    v.xs = at<const void*>(base, L.xq);
+    if (p->quant == MOE_FP8_BLOCK128) v.x_scale = at<const float*>(base, L.sx);
+  }
+  if (p->quant == MOE_FP8_PER_TENSOR) {
+    static_assert(offsetof(DeviceHeader, amax_x) % 4 == 0, "amax_x is a 4-byte word");
+    v.amax_x = reinterpret_cast<const float*>(at<const uint8_t*>(base, L.header) + offsetof(DeviceHeader, amax_x));
   }
   *out = v;
   return MOE_OK;

@@ -14,7 +14,8 @@ import torch
 
 import workloads as W
 from oracle import moe as O
-from tests._util import cosine, oracle_args, rel_l2
+from oracle.formats import f32_from_bf16_bits
+from tests._util import bits16, cosine, oracle_args, rel_l2
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -179,7 +180,44 @@ def _check_y(wl, y, ref_y, tokens=None):
     return err
 
 
-def _check_routing_views(m, wl, p, ws, ref):
+def _check_quant_views(m, wl, p, ws, inp, ref):
+    """The activations the Gate/Up GEMM reads, bit for bit: x rows (bf16 copies or
+    e4m3 codes) in expert-sorted order on the grouped path, in token order on the
+    route-direct path, with their per-(row, 128) scales (blockwise) or the amax of
+    x (per tensor).  The quantisation of x is unique (IEEE division by the fp32
+    scale, round to nearest even, saturating), so nothing here has a tolerance."""
+    v = m.moe_forward_views(p, ws)
+    T, H, R = wl.T, wl.H, wl.T * wl.k
+    xb = bits16(inp["x"])
+    grouped = v.perm is not None
+    rows = ref["perm"] // wl.k if grouped else np.arange(T)
+    n = R if grouped else T
+    if wl.quant == W.QUANT_BF16:
+        if not v.xs:  # the variant that gathers x inside the GEMM keeps no sorted copy
+            return
+        got = _view(ws, v.xs, n * H, torch.int16).cpu().numpy().view(np.uint16).reshape(n, H)
+        assert np.array_equal(got, xb[rows])
+        return
+    xf = f32_from_bf16_bits(xb)
+    got = _view(ws, v.xs, n * H, torch.uint8).cpu().numpy().reshape(n, H)
+    if wl.quant == W.QUANT_FP8_TENSOR:
+        amax = np.float32(np.abs(xf).max())
+        got_amax = _view(ws, v.amax_x, 1, torch.float32).cpu().numpy()[0]
+        assert got_amax.view(np.uint32) == amax.view(np.uint32), (got_amax, amax)
+        codes, _ = O.quant_per_tensor(xf)
+        assert not v.x_scale
+    else:
+        codes, scales = O.quant_per_group(xf)
+        got_s = _view(ws, v.x_scale, n * (H // 128), torch.float32).cpu().numpy().reshape(n, H // 128)
+        assert np.array_equal(got_s.view(np.uint32), scales[rows].view(np.uint32))
+        assert not v.amax_x
+    bad = got != codes[rows]
+    assert not bad.any(), f"{int(bad.sum())} e4m3 codes differ, first at {np.argwhere(bad)[0]}"
+
+
+def _check_routing_views(m, wl, p, ws, ref, inp=None):
+    if inp is not None:
+        _check_quant_views(m, wl, p, ws, inp, ref)
     v = m.moe_forward_views(p, ws)
     R = wl.T * wl.k
     assert np.array_equal(_view(ws, v.ids, R, torch.int32).cpu().numpy().reshape(wl.T, wl.k), ref["ids"])
@@ -212,7 +250,7 @@ def test_forward_grouped_small_full(m, wl):
     inp = W.make_inputs(wl)
     p, y, ws = run_forward(m, wl, _dev(inp))
     ref = O.forward(*oracle_args(inp), wl.k, wl.quant)
-    _check_routing_views(m, wl, p, ws, ref)
+    _check_routing_views(m, wl, p, ws, ref, inp)
     _check_y(wl, y, ref["y"])
 
 
@@ -223,7 +261,7 @@ def test_forward_one_expert_takes_everything(m):
     p, y, ws = run_forward(m, wl, _dev(inp))
     ref = O.forward(*oracle_args(inp), wl.k, wl.quant)
     assert ref["counts"][3] == wl.T
-    _check_routing_views(m, wl, p, ws, ref)
+    _check_routing_views(m, wl, p, ws, ref, inp)
     _check_y(wl, y, ref["y"])
 
 
@@ -240,8 +278,87 @@ def test_forward_grouped_full_size_sampled(m, name):
     rng = np.random.default_rng(5)
     tokens = np.sort(rng.choice(wl.T, size=192, replace=False))
     ref = O.forward(*oracle_args(inp), wl.k, wl.quant, tokens=tokens)
-    _check_routing_views(m, wl, p, ws, ref)
+    _check_routing_views(m, wl, p, ws, ref, inp)
     _check_y(wl, y, ref["y"], tokens)
+
+
+@functools.lru_cache(maxsize=1)
+def _big_fp8_inputs(quant):
+    import dataclasses
+
+    wl = dataclasses.replace(W.workload("prefill"), quant=quant, name=f"prefill_{quant}")
+    return wl, W.make_inputs(wl)
+
+
+@pytest.mark.parametrize("quant", [W.QUANT_FP8_TENSOR, W.QUANT_FP8_BLOCK])
+def test_forward_grouped_fp8_full_size_sampled(m, quant):
+    """Both FP8 modes at the size their prefill throughput is quoted at (T=16384,
+    E=128, top-8, H=2048, I=768, Zipf-skewed): routing views and every quantised x
+    row bit-exact, y on 192 sampled tokens.  The oracle's per-tensor h scale is
+    taken over all routes (it computes every route's activation for that)."""
+    wl, inp = _big_fp8_inputs(quant)
+    _big_inputs.cache_clear()
+    p, y, ws = run_forward(m, wl, _dev(inp), path=m.MOE_PATH_GROUPED)
+    rng = np.random.default_rng(6)
+    tokens = np.sort(rng.choice(wl.T, size=192, replace=False))
+    ref = O.forward(*oracle_args(inp), wl.k, wl.quant, tokens=tokens)
+    _check_routing_views(m, wl, p, ws, ref, inp)
+    _check_y(wl, y, ref["y"], tokens)
+
+
+def _crafted_x(T, H, quant, seed):
+    """x whose quantisation exercises every rounding case of the e4m3 conversion:
+    each scale is a power of two (the amax of each scale group is 448 * 2^m), so
+    x / s lands exactly on every e4m3 code, on every midpoint between neighbouring
+    codes (ties to even), one bf16 step either side of each midpoint, in the
+    subnormal range, on +-0.0 and on the amax itself (448)."""
+    from oracle.formats import E4M3_VALUES
+
+    mags = np.unique(np.abs(E4M3_VALUES[:0x7F].astype(np.float64)))  # 0 .. 448, 127 magnitudes
+    mids = (mags[:-1] + mags[1:]) / 2.0
+    step = lambda v: np.ldexp(1.0, np.frexp(v)[1] - 8)  # one bf16 ulp at v (v > 0)
+    vals = np.concatenate([mags, mids, mids + step(mids), mids - step(mids)])
+    vals = np.concatenate([vals, -vals, [0.0, -0.0]])
+    rng = np.random.default_rng(seed)
+    x = np.empty((T, H), dtype=np.float64)
+    group = H if quant == W.QUANT_FP8_TENSOR else 128
+    for t in range(T):
+        order = rng.permutation(vals.size)
+        pos = 0
+        for g0 in range(0, H, group):
+            mexp = 0 if quant == W.QUANT_FP8_TENSOR else int(rng.integers(-3, 4))
+            seg = np.empty(group)
+            seg[0] = 448.0
+            take = order[pos:pos + group - 1]
+            pos += group - 1
+            if take.size < group - 1:  # wrap around when the row is longer than the value list
+                extra = rng.permutation(vals.size)[:group - 1 - take.size]
+                take = np.concatenate([take, extra])
+            seg[1:] = vals[take]
+            x[t, g0:g0 + group] = np.ldexp(seg, mexp)
+    xt = torch.from_numpy(x).float().to(torch.bfloat16)
+    assert torch.equal(xt.double(), torch.from_numpy(x))  # every crafted value is exact in bf16
+    return xt
+
+
+@pytest.mark.parametrize("path", ["grouped", "route_direct"])
+@pytest.mark.parametrize("quant", [W.QUANT_FP8_TENSOR, W.QUANT_FP8_BLOCK])
+def test_fp8_conversion_sweep_through_forward(m, quant, path):
+    """The e4m3 conversion of x (cvt.rn.satfinite) against the oracle's encoder on
+    every code, midpoint, near-midpoint, subnormal and signed zero, driven through
+    moe_forward on both paths: codes and scales bit-exact, y within tolerance."""
+    wl = W.Workload(f"cvt_{quant}_{path}", 6, 8, 2, 1024, 128, quant, 70)
+    inp = W.make_inputs(wl)
+    inp["x"] = _crafted_x(wl.T, wl.H, quant, seed=71)
+    xv = inp["x"].double().numpy()
+    # every scale group's amax is 448 * 2^m, so every scale amax / 448 is a power of two
+    amax = np.abs(xv).reshape(wl.T, -1, 128 if quant == W.QUANT_FP8_BLOCK else wl.H).max(axis=2)
+    assert np.all(np.frexp(amax / 448.0)[0] == 0.5)
+    mp = m.MOE_PATH_GROUPED if path == "grouped" else m.MOE_PATH_ROUTE_DIRECT
+    p, y, ws = run_forward(m, wl, _dev(inp), path=mp)
+    ref = O.forward(*oracle_args(inp), wl.k, wl.quant)
+    _check_routing_views(m, wl, p, ws, ref, inp)
+    _check_y(wl, y, ref["y"])
 
 
 @functools.lru_cache(maxsize=1)
@@ -259,7 +376,7 @@ def test_forward_route_direct_decode(m, name, B):
     p, y, ws = run_forward(m, wl, _dev(inp))
     assert m.moe_select_path(p) == m.MOE_PATH_ROUTE_DIRECT
     ref = O.forward(*oracle_args(inp), wl.k, wl.quant)
-    _check_routing_views(m, wl, p, ws, ref)
+    _check_routing_views(m, wl, p, ws, ref, inp)
     _check_y(wl, y, ref["y"])
 
 
@@ -271,7 +388,7 @@ def test_forward_route_direct_shapes(m, quant, T):
     inp = W.make_inputs(wl)
     p, y, ws = run_forward(m, wl, _dev(inp), path=m.MOE_PATH_ROUTE_DIRECT)
     ref = O.forward(*oracle_args(inp), wl.k, wl.quant)
-    _check_routing_views(m, wl, p, ws, ref)
+    _check_routing_views(m, wl, p, ws, ref, inp)
     _check_y(wl, y, ref["y"])
 
 
@@ -351,7 +468,7 @@ def test_forward_grouped_fp8_per_tensor(m, wl):
     inp = W.make_inputs(wl)
     p, y, ws = run_forward(m, wl, _dev(inp), path=m.MOE_PATH_GROUPED)
     ref = O.forward(*oracle_args(inp), wl.k, wl.quant)
-    _check_routing_views(m, wl, p, ws, ref)
+    _check_routing_views(m, wl, p, ws, ref, inp)
     _check_y(wl, y, ref["y"])
 
 
@@ -362,7 +479,7 @@ def test_forward_grouped_fp8_hunyuan_shape_and_auto_switch(m):
     p, y, ws = run_forward(m, wl, _dev(inp))
     assert m.moe_select_path(p) == m.MOE_PATH_GROUPED
     ref = O.forward(*oracle_args(inp), wl.k, wl.quant)
-    _check_routing_views(m, wl, p, ws, ref)
+    _check_routing_views(m, wl, p, ws, ref, inp)
     _check_y(wl, y, ref["y"])
     assert m.moe_select_path(m.problem(32, wl.E, wl.k, wl.H, wl.I, wl.quant)) == m.MOE_PATH_ROUTE_DIRECT
     assert m.moe_select_path(m.problem(33, wl.E, wl.k, wl.H, wl.I, wl.quant)) == m.MOE_PATH_GROUPED
@@ -394,7 +511,7 @@ def test_forward_grouped_fp8_blockwise(m, wl):
     inp = W.make_inputs(wl)
     p, y, ws = run_forward(m, wl, _dev(inp), path=m.MOE_PATH_GROUPED)
     ref = O.forward(*oracle_args(inp), wl.k, wl.quant)
-    _check_routing_views(m, wl, p, ws, ref)
+    _check_routing_views(m, wl, p, ws, ref, inp)
     _check_y(wl, y, ref["y"])
 
 
@@ -405,7 +522,7 @@ def test_forward_grouped_fp8_blockwise_qwen3_shape_and_auto_switch(m):
     p, y, ws = run_forward(m, wl, _dev(inp))
     assert m.moe_select_path(p) == m.MOE_PATH_GROUPED
     ref = O.forward(*oracle_args(inp), wl.k, wl.quant)
-    _check_routing_views(m, wl, p, ws, ref)
+    _check_routing_views(m, wl, p, ws, ref, inp)
     _check_y(wl, y, ref["y"])
     assert m.moe_select_path(m.problem(64, wl.E, wl.k, wl.H, wl.I, wl.quant)) == m.MOE_PATH_ROUTE_DIRECT
     assert m.moe_select_path(m.problem(65, wl.E, wl.k, wl.H, wl.I, wl.quant)) == m.MOE_PATH_GROUPED

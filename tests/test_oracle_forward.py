@@ -317,3 +317,30 @@ def test_fp8_quantisation_noise_is_percent_level(quant):
             y[t] += out["w"][t, j] * (W2[e] @ (g / (1 + np.exp(-g)) * u))
     err = rel_l2(out["y"], y)
     assert 1e-3 < err < 5e-2
+
+
+@pytest.mark.parametrize("quant", [M.BF16, M.FP8_TENSOR, M.FP8_BLOCK])
+def test_token_subset_gives_exactly_those_rows_of_the_full_forward(quant):
+    """forward(tokens=S) is what the full-size GPU parity tests, the CPU baseline
+    and the reference arm call: it must return rows S of the full forward bit for
+    bit.  The subset skips other tokens' routes, except that the per-tensor scale
+    of h still spans every route: the test checks that the subset's own routes
+    would give a different amax here, so a scale taken over the subset alone
+    would fail it."""
+    import workloads as W
+    from tests._util import oracle_args
+
+    wl = W.Workload("subset", 40, 16, 4, 256, 256, quant, 88)
+    args = oracle_args(W.make_inputs(wl))
+    full = M.forward(*args, wl.k, quant)
+    S = np.array([0, 3, 4, 17, 39])
+    sub = M.forward(*args, wl.k, quant, tokens=S)
+    assert np.array_equal(sub["y"].view(np.uint32), full["y"][S].view(np.uint32))
+    assert np.array_equal(sub["tokens"], S)
+    routes = (S[:, None] * wl.k + np.arange(wl.k)[None, :]).ravel()
+    assert np.array_equal(sub["a"][routes].view(np.uint32), full["a"][routes].view(np.uint32))
+    if quant == M.FP8_TENSOR:
+        assert np.abs(full["a"][routes]).max() < np.abs(full["a"]).max()
+    else:  # other tokens' routes were skipped
+        others = np.setdiff1d(np.arange(wl.T * wl.k), routes)
+        assert np.all(np.isnan(sub["a"][others]))
