@@ -200,6 +200,8 @@ def forward(
     k: int,
     quant: str,
     tokens: Optional[np.ndarray] = None,
+    shared: Optional[Dict[str, np.ndarray]] = None,
+    y_fp32: bool = False,
 ) -> Dict[str, np.ndarray]:
     """The full forward.
 
@@ -212,10 +214,22 @@ def forward(
     tokens   optional subset of token indices: y is computed only for those
              (all routes are still computed when a per-tensor scale of h needs
              them).
+    shared   optional shared experts (the "shared output" of the route-MMA
+             page's Summary): {"w1": [S, 2I, H], "w2": [S, H, I], "w1_scale",
+             "w2_scale"} in the routed experts' formats.  Every token passes
+             through every shared expert with weight 1.  Their rows are more
+             rows of the same intermediate tensor: x is quantised once for
+             both, and the per-tensor scale of h spans routed and shared rows.
+             y[t] = sum_j w[t, j] o_(t*k+j) + sum_s o_shared(s, t), summed in
+             that order, rounded once.
+    y_fp32   return y unrounded (fp32 of the sum): the partial output of one
+             slice of a tensor-parallel split of I, to be summed across the
+             slices and rounded once by the caller.
 
     Returns a dict with ids, w, counts, offsets, perm, inv, a (fp32 [R, I] for
-    the computed routes, NaN elsewhere), y (fp32 holding bf16 values, [T, H] or
-    [len(tokens), H])."""
+    the computed routes, NaN elsewhere; with shared experts [R + S*T, I], row
+    R + s*T + t for shared expert s and token t), y (fp32 holding bf16
+    values unless y_fp32, [T, H] or [len(tokens), H])."""
     x = f32_from_bf16_bits(x_bits)
     T, H = x.shape
     E, twoI, _ = w1.shape
@@ -224,14 +238,32 @@ def forward(
     ids, w = route(scores, k)
     counts, offsets, perm, inv = shuffle(ids, E)
     ids_flat = ids.reshape(-1)
+    S = 0 if shared is None else int(shared["w1"].shape[0])
+    if S:
+        # shared expert s is expert E + s of an extended expert set, and its rows
+        # R + s*T + t are extra routes that every token takes
+        w1 = np.concatenate([w1, shared["w1"]], axis=0)
+        w2 = np.concatenate([w2, shared["w2"]], axis=0)
+        if quant != BF16:
+            w1_scale = np.concatenate([w1_scale, shared["w1_scale"]], axis=0)
+            w2_scale = np.concatenate([w2_scale, shared["w2_scale"]], axis=0)
+        seg_of = [perm[offsets[e]:offsets[e + 1]] for e in range(E)]
+        seg_of += [R + s * T + np.arange(T) for s in range(S)]
+    else:
+        seg_of = [perm[offsets[e]:offsets[e + 1]] for e in range(E)]
+    RS = R + S * T
+
+    def token_of(rows):
+        return np.where(rows < R, rows // k, (rows - R) % T)
 
     if tokens is None:
         tokens = np.arange(T)
     tokens = np.asarray(tokens, dtype=np.int64)
-    need = np.zeros(R, dtype=bool)
+    need = np.zeros(RS, dtype=bool)
     for t in tokens:
         need[t * k:(t + 1) * k] = True
-    gate_up_need = np.ones(R, dtype=bool) if quant == FP8_TENSOR else need
+        need[R + t:RS:T] = True
+    gate_up_need = np.ones(RS, dtype=bool) if quant == FP8_TENSOR else need
 
     # activation quantisation of x
     if quant == BF16:
@@ -245,14 +277,15 @@ def forward(
     else:
         raise ValueError(quant)
 
-    a = np.full((R, I), np.nan, dtype=np.float32)
-    # Gate/Up per expert over its routes in sorted order (perm order)
-    for e in range(E):
-        seg = perm[offsets[e]:offsets[e + 1]]
+    a = np.full((RS, I), np.nan, dtype=np.float32)
+    # Gate/Up per expert over its routes in sorted order (perm order), then the
+    # shared experts over every token
+    for e in range(E + S):
+        seg = seg_of[e]
         seg = seg[gate_up_need[seg]]
         if seg.size == 0:
             continue
-        tok = seg // k
+        tok = token_of(seg)
         W1e = _decode_input(w1[e], quant).astype(np.float64)
         Xe = xv[tok]
         if quant == BF16:
@@ -274,22 +307,22 @@ def forward(
         a[seg] = silu_times(g, u).astype(np.float32)
 
     # quantisation of h (the Down GEMM's input)
-    hv = np.zeros((R, I), dtype=np.float64)
+    hv = np.zeros((RS, I), dtype=np.float64)
     if quant == BF16:
         hv[need] = bf16_round(a[need])
     elif quant == FP8_TENSOR:
         hq, sh = quant_per_tensor(a)
         hv = e4m3_decode(hq).astype(np.float64)
     else:
-        shg = np.zeros((R, -(-I // GROUP)), dtype=np.float32)
+        shg = np.zeros((RS, -(-I // GROUP)), dtype=np.float32)
         hq, shg_need = quant_per_group(a[need])
         hv[need] = e4m3_decode(hq)
         shg[need] = shg_need
 
-    # Down per expert, o in route order
-    o = np.zeros((R, H), dtype=np.float64)
-    for e in range(E):
-        seg = perm[offsets[e]:offsets[e + 1]]
+    # Down per expert (and shared expert), o in route order
+    o = np.zeros((RS, H), dtype=np.float64)
+    for e in range(E + S):
+        seg = seg_of[e]
         seg = seg[need[seg]]
         if seg.size == 0:
             continue
@@ -308,13 +341,16 @@ def forward(
                 acc += shg[seg, G].astype(np.float64)[:, None] * sw[None, :] * part
             o[seg] = acc
 
-    # combine: y[t] = bf16(sum_j w[t, j] o[t*k + j]), j ascending
+    # combine: y[t] = bf16(sum_j w[t, j] o[t*k + j] + sum_s o_shared(s, t)),
+    # j ascending, then s ascending
     y = np.empty((tokens.size, H), dtype=np.float32)
     for n, t in enumerate(tokens):
         acc = np.zeros(H, dtype=np.float64)
         for j in range(k):
             acc += np.float64(w[t, j]) * o[t * k + j]
-        y[n] = bf16_round(acc.astype(np.float32))
+        for s_ in range(S):
+            acc += o[R + s_ * T + t]
+        y[n] = acc.astype(np.float32) if y_fp32 else bf16_round(acc.astype(np.float32))
 
     return {
         "ids": ids,

@@ -344,3 +344,122 @@ def test_token_subset_gives_exactly_those_rows_of_the_full_forward(quant):
     else:  # other tokens' routes were skipped
         others = np.setdiff1d(np.arange(wl.T * wl.k), routes)
         assert np.all(np.isnan(sub["a"][others]))
+
+
+# ----------------------------------------------------------------------------- shared experts, fp32 partials
+def _zero_routed(quant, E, H, I):
+    """Routed experts whose weights are all zero: their routes add exactly 0."""
+    if quant == M.BF16:
+        return np.zeros((E, 2 * I, H), np.uint16), np.zeros((E, H, I), np.uint16), None, None
+    w1 = np.zeros((E, 2 * I, H), np.uint8)
+    w2 = np.zeros((E, H, I), np.uint8)
+    if quant == M.FP8_TENSOR:
+        return w1, w2, np.ones(E, np.float32), np.ones(E, np.float32)
+    return (w1, w2, np.ones((E, 2 * I // 128, H // 128), np.float32),
+            np.ones((E, H // 128, I // 128), np.float32))
+
+
+@pytest.mark.parametrize("quant", [M.BF16, M.FP8_TENSOR, M.FP8_BLOCK])
+def test_shared_identity_expert_closed_form(quant):
+    """A shared expert that is identity-like (one nonzero per row, as in the
+    routed closed form above) next to routed experts that contribute nothing:
+    y must be the SwiGLU closed form of the shared expert alone, for every
+    token (weight 1), in all three modes.  A shared expert that were skipped,
+    weighted by a routing weight, or read with the routed experts' scales would
+    fail it (the routed scales here are 1, the shared ones are not)."""
+    c = _identity_case(quant, E=1)
+    Er, k = 6, 2
+    rng = np.random.default_rng(3)
+    w1, w2, s1, s2 = _zero_routed(quant, Er, c["H"], c["I"])
+    scores = rng.standard_normal((c["T"], Er)).astype(np.float32)
+    shared = {"w1": c["w1"], "w2": c["w2"], "w1_scale": c["s1"], "w2_scale": c["s2"]}
+    out = M.forward(bits16(c["x"]), scores, w1, w2, s1, s2, k, quant, shared=shared)
+    assert np.array_equal(out["y"], _expected_identity(c, quant))
+
+
+def test_shared_expert_adds_a_dense_swiglu_to_the_routed_sum():
+    """bf16: forward with one shared expert = the routed-only forward's unrounded
+    y plus the shared expert's dense SwiGLU MLP (torch CPU, h rounded to bf16),
+    rounded once; checked to within one bf16 step (the two sides round the
+    routed sum at different points) and equal for nearly every element."""
+    rng = np.random.default_rng(11)
+    T, E, k, H, I = 12, 5, 2, 256, 128
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16)
+    scores = rng.standard_normal((T, E)).astype(np.float32)
+    mk = lambda *shape, fan: (torch.from_numpy(rng.standard_normal(shape).astype(np.float32)) / math.sqrt(fan)).to(torch.bfloat16)
+    w1, w2 = mk(E, 2 * I, H, fan=H), mk(E, H, I, fan=I)
+    s1, s2 = mk(1, 2 * I, H, fan=H), mk(1, H, I, fan=I)
+    routed = M.forward(bits16(x), scores, bits16(w1), bits16(w2), None, None, k, M.BF16, y_fp32=True)["y"]
+    both = M.forward(bits16(x), scores, bits16(w1), bits16(w2), None, None, k, M.BF16,
+                     shared={"w1": bits16(s1), "w2": bits16(s2), "w1_scale": None, "w2_scale": None})["y"]
+    X = x.double()
+    g = X @ s1[0, :I].double().T
+    u = X @ s1[0, I:].double().T
+    hh = (Fnn.silu(g) * u).float().to(torch.bfloat16).double()
+    dense = (hh @ s2[0].double().T).numpy()
+    ref = _t_bf16_val(routed.astype(np.float64) + dense)
+    ulp = np.abs(ref) * 2.0 ** -7 + 1e-30
+    assert np.all(np.abs(both - ref) <= ulp)
+    assert np.mean(both == ref) > 0.99
+    assert not np.array_equal(both, _t_bf16_val(routed))  # the shared term is not negligible
+
+
+@pytest.mark.parametrize("quant", [M.BF16, M.FP8_TENSOR, M.FP8_BLOCK])
+def test_fp32_partial_rounds_to_the_bf16_output(quant):
+    import workloads as W
+    from tests._util import oracle_args
+
+    wl = W.Workload("partial", 10, 8, 2, 256, 256, quant, 90)
+    args = oracle_args(W.make_inputs(wl))
+    y32 = M.forward(*args, wl.k, quant, y_fp32=True)["y"]
+    y16 = M.forward(*args, wl.k, quant)["y"]
+    assert np.array_equal(bf16_round_t(y32), y16)
+    assert not np.array_equal(y32, y16)  # the partial is not rounded
+
+
+def bf16_round_t(v):
+    return torch.from_numpy(np.asarray(v, np.float32)).to(torch.bfloat16).float().numpy()
+
+
+def tp_slice(w1, w2, s1, s2, quant, P, p):
+    """Slice p of P of a tensor-parallel split of the intermediate dimension I:
+    gate rows and up rows [p I/P, (p+1) I/P) of W1, the same columns of W2 (and
+    the matching 128 x 128 scale blocks)."""
+    I = w1.shape[1] // 2
+    n = I // P
+    rows = np.concatenate([np.arange(p * n, (p + 1) * n), I + np.arange(p * n, (p + 1) * n)])
+    w1p, w2p = w1[:, rows], w2[:, :, p * n:(p + 1) * n]
+    if quant == M.FP8_BLOCK:
+        assert n % 128 == 0
+        b = n // 128
+        brows = np.concatenate([np.arange(p * b, (p + 1) * b), I // 128 + np.arange(p * b, (p + 1) * b)])
+        return w1p, w2p, s1[:, brows], s2[:, :, p * b:(p + 1) * b]
+    return w1p, w2p, s1, s2
+
+
+@pytest.mark.parametrize("quant", [M.BF16, M.FP8_BLOCK])
+def test_tensor_parallel_slices_sum_to_the_whole(quant):
+    """Splitting I into slices (the TP8 deployment of the route-MMA page's
+    Performance section) and summing the slices' unrounded partial outputs gives
+    the unsplit forward's unrounded output: every h value and its quantisation
+    (bf16, or per 128-column group when the slices are whole groups) is the same
+    on both sides, so they differ only by fp32 summation order.  With shared
+    experts too (sliced the same way)."""
+    import workloads as W
+    from tests._util import oracle_args
+
+    wl = W.Workload("tp", 9, 8, 2, 256, 256, quant, 91)
+    x, scores, w1, w2, s1, s2 = oracle_args(W.make_inputs(wl))
+    sh = oracle_args(W.make_inputs(W.Workload("tp_sh", 9, 1, 1, 256, 256, quant, 92)))
+    shared = {"w1": sh[2], "w2": sh[3], "w1_scale": sh[4], "w2_scale": sh[5]}
+    whole = M.forward(x, scores, w1, w2, s1, s2, wl.k, quant, shared=shared, y_fp32=True)["y"]
+    P = 2
+    total = np.zeros_like(whole, dtype=np.float64)
+    for p in range(P):
+        a1, a2, b1, b2 = tp_slice(w1, w2, s1, s2, quant, P, p)
+        c1, c2, d1, d2 = tp_slice(shared["w1"], shared["w2"], shared["w1_scale"], shared["w2_scale"], quant, P, p)
+        part = M.forward(x, scores, a1, a2, b1, b2, wl.k, quant, y_fp32=True,
+                         shared={"w1": c1, "w2": c2, "w1_scale": d1, "w2_scale": d2})["y"]
+        assert np.abs(part).max() > 0.05 * np.abs(whole).max()  # each slice contributes
+        total += part
+    assert np.max(np.abs(total - whole)) <= 1e-5 * np.abs(whole).max()
