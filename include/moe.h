@@ -31,7 +31,8 @@
  *     fp32 arrays 4-byte aligned.
  *   - The caller owns and allocates every buffer, including outputs and the
  *     workspace.  The library never allocates, frees or synchronises inside
- *     moe_route / moe_shuffle / moe_tile_map / moe_forward: work is enqueued
+ *     moe_route / moe_shuffle / moe_tile_map / moe_forward / moe_forward_ex /
+ *     moe_round_bf16: work is enqueued
  *     on `stream` in order, with no device-to-host copy, so these calls can be
  *     captured in a CUDA graph.  Inputs are never written.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).
@@ -195,6 +196,56 @@ moe_status moe_forward(const moe_problem* p, const void* x, const float* scores,
                        const void* w2, const float* w1_scale, const float* w2_scale, void* y,
                        void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* ---------------------------------------------------------------- forward, extended
+ * moe_forward_ex - moe_forward with the optional parts below (opt NULL or all
+ * zero = moe_forward).
+ *
+ * Shared experts (the "shared output" that the Summary of "perf: add small-batch
+ * route MMA for MoE" lists; the page does not define it, and this library takes
+ * the common reading): n_shared = S experts, each with the routed experts'
+ * shapes and formats, that every token passes through with weight 1:
+ *   y[t] = sum_j w[t, j] * o_(t, j)  +  sum_s FFN_shared[s](x_t),
+ * summed j ascending then s ascending, rounded once.  Their rows are more rows
+ * of the same intermediate tensor: x is quantised once for both, and in
+ * per-tensor FP8 the dynamic scale of h spans the routed and the shared rows.
+ *   w1_shared        [S, 2I, H] bf16 | e4m3 (rows 0..I-1 gate, I..2I-1 up)
+ *   w2_shared        [S, H, I]
+ *   w1_shared_scale  NULL (bf16) | fp32 [S] | fp32 [S, 2I/128, H/128]
+ *   w2_shared_scale  NULL (bf16) | fp32 [S] | fp32 [S, H/128, I/128]
+ * Shared experts run on the grouped path (AUTO takes it; an explicit
+ * MOE_PATH_ROUTE_DIRECT with S > 0 is UNSUPPORTED).  0 <= S <= 16.
+ *
+ * Unrounded output (y_fp32 = 1): y is fp32 [T, H], the sum above before its
+ * rounding.  This is the partial output of one slice of a tensor-parallel
+ * split of I (the TP8 deployment in the route-MMA page's Performance section):
+ * each slice holds gate rows and up rows [p*I/P, (p+1)*I/P) of every W1[e] (and
+ * the same columns of W2[e], and for blockwise FP8 the matching scale blocks, so
+ * I/P must be a multiple of 128) and runs moe_forward_ex with I/P as its I; the
+ * caller sums the slices' partial outputs (e.g. an all-reduce) and rounds the sum
+ * with moe_round_bf16.  In bf16 and blockwise FP8 that equals the unsplit
+ * forward up to fp32 summation order; per-tensor FP8 then scales h per slice.
+ *
+ * moe_workspace_size_ex gives the workspace for (*p, *opt); moe_forward_views_ex
+ * the views of that workspace.  Errors: as moe_forward. */
+typedef struct {
+  int n_shared;
+  const void* w1_shared;
+  const void* w2_shared;
+  const float* w1_shared_scale;
+  const float* w2_shared_scale;
+  int y_fp32;
+} moe_forward_options;
+size_t moe_workspace_size_ex(const moe_problem* p, const moe_forward_options* opt);
+moe_status moe_forward_ex(const moe_problem* p, const moe_forward_options* opt, const void* x, const float* scores,
+                          const void* w1, const void* w2, const float* w1_scale, const float* w2_scale, void* y,
+                          void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* moe_round_bf16 - y[i] = bf16(y32[i]) for i < n (round to nearest even): the
+ * single rounding of a sum of partial outputs (moe_forward_ex, y_fp32 = 1).
+ * y32 fp32 [n], y bf16 [n], both 16-byte aligned, n a multiple of 8.
+ * Errors: INVALID_ARG, CUDA. */
+moe_status moe_round_bf16(const float* y32, void* y, size_t n, moe_stream_t stream);
+
 /* moe_forward_views - device pointers to the intermediate results moe_forward
  * leaves in the workspace (read-only diagnostics; valid after the call's
  * work on the stream completed).  Pointers not produced by the path chosen
@@ -224,6 +275,11 @@ typedef struct {
   const float* amax_x;
 } moe_views;
 moe_status moe_forward_views(const moe_problem* p, const void* ws, size_t ws_bytes, moe_views* out);
+/* The same for a workspace of moe_forward_ex(p, opt, ...); with shared experts
+ * xs (and x_scale) hold T*k + S*T rows, shared expert s's row of token t at
+ * T*k + s*T + t. */
+moe_status moe_forward_views_ex(const moe_problem* p, const moe_forward_options* opt, const void* ws,
+                                size_t ws_bytes, moe_views* out);
 
 /* ---------------------------------------------------------------- diagnostics
  * moe_read_device_status - synchronises `stream`, then returns the status

@@ -50,12 +50,18 @@ class moe_views(ctypes.Structure):
                  "amax_x")]
 
 
+class moe_forward_options(ctypes.Structure):
+    _fields_ = [("n_shared", ctypes.c_int), ("w1_shared", ctypes.c_void_p), ("w2_shared", ctypes.c_void_p),
+                ("w1_shared_scale", ctypes.c_void_p), ("w2_shared_scale", ctypes.c_void_p), ("y_fp32", ctypes.c_int)]
+
+
 class moe_stage_time(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 32), ("total_ms", ctypes.c_double), ("launches", ctypes.c_int)]
 
 
 _vp, _sz, _i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
 _P = ctypes.POINTER(moe_problem)
+_O = ctypes.POINTER(moe_forward_options)
 _SIGS = {
     "moe_route": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp]),
     "moe_shuffle_workspace_size": (_sz, [_i, _i, _i]),
@@ -66,6 +72,10 @@ _SIGS = {
     "moe_workspace_size": (_sz, [_P]),
     "moe_forward": (_i, [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_forward_views": (_i, [_P, _vp, _sz, ctypes.POINTER(moe_views)]),
+    "moe_workspace_size_ex": (_sz, [_P, _O]),
+    "moe_forward_ex": (_i, [_P, _O, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_forward_views_ex": (_i, [_P, _O, _vp, _sz, ctypes.POINTER(moe_views)]),
+    "moe_round_bf16": (_i, [_vp, _vp, _sz, _vp]),
     "moe_read_device_status": (_i, [_vp, _vp]),
     "moe_profile_start": (_i, []),
     "moe_profile_start_stage": (_i, [ctypes.c_char_p]),
@@ -178,6 +188,41 @@ def moe_forward(p: moe_problem, x, scores, w1, w2, w1_scale, w2_scale, y, ws, ws
     nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
     _check(lib().moe_forward(ctypes.byref(p), _ptr(x), _ptr(scores), _ptr(w1), _ptr(w2), _ptr(w1_scale),
                             _ptr(w2_scale), _ptr(y), _ptr(ws), nb, _stream(stream)), "moe_forward")
+
+
+def forward_options(n_shared=0, w1_shared=None, w2_shared=None, w1_shared_scale=None, w2_shared_scale=None,
+                    y_fp32=False) -> moe_forward_options:
+    return moe_forward_options(int(n_shared), _ptr(w1_shared), _ptr(w2_shared), _ptr(w1_shared_scale),
+                               _ptr(w2_shared_scale), 1 if y_fp32 else 0)
+
+
+def _opt_ref(opt):
+    return None if opt is None else ctypes.byref(opt)
+
+
+def moe_workspace_size_ex(p: moe_problem, opt: Optional[moe_forward_options]) -> int:
+    return int(lib().moe_workspace_size_ex(ctypes.byref(p), _opt_ref(opt)))
+
+
+def moe_forward_ex(p: moe_problem, opt: Optional[moe_forward_options], x, scores, w1, w2, w1_scale, w2_scale, y, ws,
+                   ws_bytes=None, stream=None) -> None:
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(lib().moe_forward_ex(ctypes.byref(p), _opt_ref(opt), _ptr(x), _ptr(scores), _ptr(w1), _ptr(w2),
+                               _ptr(w1_scale), _ptr(w2_scale), _ptr(y), _ptr(ws), nb, _stream(stream)),
+           "moe_forward_ex")
+
+
+def moe_forward_views_ex(p: moe_problem, opt: Optional[moe_forward_options], ws, ws_bytes=None) -> moe_views:
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    v = moe_views()
+    _check(lib().moe_forward_views_ex(ctypes.byref(p), _opt_ref(opt), _ptr(ws), nb, ctypes.byref(v)),
+           "moe_forward_views_ex")
+    return v
+
+
+def moe_round_bf16(y32, y, n=None, stream=None) -> None:
+    n = y32.numel() if n is None else n
+    _check(lib().moe_round_bf16(_ptr(y32), _ptr(y), n, _stream(stream)), "moe_round_bf16")
 
 
 def moe_forward_views(p: moe_problem, ws, ws_bytes=None) -> moe_views:

@@ -61,6 +61,8 @@ struct Params {
   int I, H;
   const float* a_scale;  // [R][K/128] scales of the A rows (sorted order)
   const float* w_scale;  // Gate/Up: [E][2I/128][H/128]; Down: [E][H/128][I/128]
+  const float* w_scale2; // the same for the S shared experts (tiles of expert E + s, weights in tmB2)
+  int E;
   float* out_f32;        // Gate/Up: a [R][I]
   __nv_bfloat16* out;    // Down: o [R][H]
   DeviceHeader* hdr;
@@ -87,7 +89,7 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_blockwise_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                             const __grid_constant__ CUtensorMap tmO,
+                             const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmB2,
                              const Params p) {
   constexpr int STAGES = stages_of(MODE);
   extern __shared__ uint8_t smem_raw[];
@@ -115,6 +117,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
+    prefetch_tensormap(&tmB2);
   }
   if (warp == 2) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -139,7 +142,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       const int tile = u / p.nN, n = u - (u / p.nN) * p.nN;
       const int4 tl = tiles[tile];
-      const int e = tl.x, row0 = tl.y;
+      const int row0 = tl.y;
+      const bool shx = tl.x >= p.E;  // a shared expert's tile: its own weight tensor
+      const int e = shx ? tl.x - p.E : tl.x;
+      const CUtensorMap* tb = shx ? &tmB2 : &tmB;
       for (int kb = 0; kb < nk; ++kb) {
         if (lane == 0) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.hdr, 0x80000u | MODE)) ok = false;
@@ -154,10 +160,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           tma_load_2d(a_dst, &tmA, kc, row0, full);
           if (MODE == MODE_GATEUP) {
             const int brow = e * 2 * p.I + n * (BN / 2);
-            tma_load_2d(b_dst, &tmB, kc, brow, full);                   // 64 gate rows
-            tma_load_2d(b_dst + B_BYTES / 2, &tmB, kc, brow + p.I, full);  // the matching 64 up rows
+            tma_load_2d(b_dst, tb, kc, brow, full);                   // 64 gate rows
+            tma_load_2d(b_dst + B_BYTES / 2, tb, kc, brow + p.I, full);  // the matching 64 up rows
           } else {
-            tma_load_2d(b_dst, &tmB, kc, e * p.H + n * BN, full);
+            tma_load_2d(b_dst, tb, kc, e * p.H + n * BN, full);
           }
         }
         __syncwarp();
@@ -228,7 +234,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       const int tile = u / p.nN, n = u - (u / p.nN) * p.nN;
       const int4 tl = tiles[tile];
-      const int e = tl.x, row0 = tl.y, nrows = tl.z;
+      const int row0 = tl.y, nrows = tl.z;
+      const bool shx = tl.x >= p.E;
+      const int e = shx ? tl.x - p.E : tl.x;
+      const float* wsc = shx ? p.w_scale2 : p.w_scale;
       const int arow = row0 + min(row, nrows - 1);
       const float* sa = p.a_scale + static_cast<size_t>(arow) * kblocks;
       // weight scale rows of this tile's columns (both halves in one block for Down)
@@ -236,11 +245,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float* swu;
       if (MODE == MODE_GATEUP) {
         const int nblk = 2 * p.I / 128, hblk = p.H / 128;
-        swg = p.w_scale + (static_cast<size_t>(e) * nblk + (n * (BN / 2)) / 128) * hblk;
-        swu = p.w_scale + (static_cast<size_t>(e) * nblk + (p.I + n * (BN / 2)) / 128) * hblk;
+        swg = wsc + (static_cast<size_t>(e) * nblk + (n * (BN / 2)) / 128) * hblk;
+        swu = wsc + (static_cast<size_t>(e) * nblk + (p.I + n * (BN / 2)) / 128) * hblk;
       } else {
         const int hblk = p.H / 128, iblk = p.I / 128;
-        swg = p.w_scale + (static_cast<size_t>(e) * hblk + n) * iblk;
+        swg = wsc + (static_cast<size_t>(e) * hblk + n) * iblk;
         swu = swg;
       }
       float acc[64];
@@ -388,9 +397,12 @@ cudaError_t launch_gateup_blockwise(const GroupedArgs& a, const float* xs_scale,
   if (err != cudaSuccess) return err;
   const int sms = num_sms();
   if (sms <= 0) return cudaErrorNoDevice;
-  CUtensorMap tma, tmb, tmo;
+  CUtensorMap tma, tmb, tmo, tmbs;
   if (!encode_u8(&tma, a.xs, a.H, a.R, BM) || !encode_u8(&tmb, a.w1, a.H, static_cast<uint64_t>(a.E) * 2 * a.I, BN / 2) ||
       !encode_f32_box32(&tmo, a.a_f32, a.I, a.R))
+    return cudaErrorInvalidValue;
+  tmbs = tmb;
+  if (a.S > 0 && !encode_u8(&tmbs, a.w1s, a.H, static_cast<uint64_t>(a.S) * 2 * a.I, BN / 2))
     return cudaErrorInvalidValue;
   Params p{};
   p.tiles = a.tiles;
@@ -403,13 +415,15 @@ cudaError_t launch_gateup_blockwise(const GroupedArgs& a, const float* xs_scale,
   p.H = a.H;
   p.a_scale = xs_scale;
   p.w_scale = a.w1_scale;
+  p.w_scale2 = a.w1s_scale;
+  p.E = a.E;
   p.out_f32 = static_cast<float*>(a.a_f32);
   p.hdr = a.hdr;
   const long long units = static_cast<long long>(a.max_tiles) * p.nN;
   const int grid = static_cast<int>(units < sms ? units : sms);
   stage_begin("gateup_gemm", s);
   err = launch_dependent(grouped_blockwise_kernel<MODE_GATEUP>, dim3(grid), dim3(THREADS), smem_bytes(MODE_GATEUP), s,
-                         tma, tmb, tmo, p);
+                         tma, tmb, tmo, tmbs, p);
   stage_end(s);
   return err;
 }
@@ -421,9 +435,11 @@ cudaError_t launch_down_blockwise(const GroupedArgs& a, const float* h_scale, cu
   if (err != cudaSuccess) return err;
   const int sms = num_sms();
   if (sms <= 0) return cudaErrorNoDevice;
-  CUtensorMap tma, tmb;
+  CUtensorMap tma, tmb, tmbs;
   if (!encode_u8(&tma, a.h, a.I, a.R, BM) || !encode_u8(&tmb, a.w2, a.I, static_cast<uint64_t>(a.E) * a.H, BN))
     return cudaErrorInvalidValue;
+  tmbs = tmb;
+  if (a.S > 0 && !encode_u8(&tmbs, a.w2s, a.I, static_cast<uint64_t>(a.S) * a.H, BN)) return cudaErrorInvalidValue;
   Params p{};
   p.tiles = a.tiles;
   p.num_tiles = a.num_tiles;
@@ -435,13 +451,15 @@ cudaError_t launch_down_blockwise(const GroupedArgs& a, const float* h_scale, cu
   p.H = a.H;
   p.a_scale = h_scale;
   p.w_scale = a.w2_scale;
+  p.w_scale2 = a.w2s_scale;
+  p.E = a.E;
   p.out = static_cast<__nv_bfloat16*>(a.o);
   p.hdr = a.hdr;
   const long long units = static_cast<long long>(a.max_tiles) * p.nN;
   const int grid = static_cast<int>(units < sms ? units : sms);
   stage_begin("down_gemm", s);
   err = launch_dependent(grouped_blockwise_kernel<MODE_DOWN>, dim3(grid), dim3(THREADS), smem_bytes(MODE_DOWN), s,
-                         tma, tmb, tma, p);
+                         tma, tmb, tma, tmbs, p);
   stage_end(s);
   return err;
 }

@@ -77,8 +77,10 @@ struct Params {
   int a_gather;          // Gate/Up: 1 = A rows gathered from x by tile::gather4, 0 = sorted rows
   __nv_bfloat16* out;
   DeviceHeader* hdr;
+  int E;                 // routed experts; tiles of expert E + s belong to shared expert s (weights in tmB2)
   // e4m3 inputs (per-tensor scales)
   const float* wscale;            // [E] scale of each expert's weight matrix
+  const float* wscale2;           // [S] scales of the shared experts' matrices
   const unsigned int* amax_in;    // fp32 bits of the amax of the A operand's source (x or a)
   unsigned int* amax_out;         // Gate/Up: receives the amax of a
   float* out_f32;                 // Gate/Up: a [R, I] fp32 (quantised by the next pass)
@@ -95,12 +97,18 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
   return r;
 }
 
+// Per-tensor weight scale of expert e (a shared expert's for e >= p.E).
+__device__ __forceinline__ float wscale_of(const Params& p, int e) {
+  return e < p.E ? __ldg(p.wscale + e) : __ldg(p.wscale2 + (e - p.E));
+}
+
 // F8: e4m3 operands (tcgen05 kind::f8f6f4, 128 K elements per 128-byte stage
 // row, per-tensor scales applied in the epilogue); otherwise bf16 (kind::f16).
 template <int MODE, bool F8>
 __global__ void __launch_bounds__(threads_of(MODE, F8), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmO, const Params p) {
+                        const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmB2,
+                        const Params p) {
   constexpr int BKE = F8 ? 128 : BK;  // K elements per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -129,6 +137,7 @@ __global__ void __launch_bounds__(threads_of(MODE, F8), 1)
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
+    prefetch_tensormap(&tmB2);
   }
   if (warp == 2) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -162,7 +171,9 @@ __global__ void __launch_bounds__(threads_of(MODE, F8), 1)
           tok[i] = __ldg(p.perm + pr) / p.k;
         }
       }
-      const int brow = e * p.b_rows_per_expert + n * (MODE == MODE_GATEUP ? BN / 2 : BN);
+      const bool shx = e >= p.E;  // a shared expert's tile: its own weight tensor
+      const CUtensorMap* tb = shx ? &tmB2 : &tmB;
+      const int brow = (shx ? e - p.E : e) * p.b_rows_per_expert + n * (MODE == MODE_GATEUP ? BN / 2 : BN);
       for (int kb = 0; kb < nk; ++kb) {
         int good = 1;
         if (lane == 0) good = mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.hdr, 0x10000u | MODE);
@@ -182,13 +193,13 @@ __global__ void __launch_bounds__(threads_of(MODE, F8), 1)
             tma_gather4(a_dst + lane * 4 * 128, &tmA, kc, tok[0], tok[1], tok[2], tok[3], full);
           if (lane == 0) {
             if (!p.a_gather) tma_load_2d(a_dst, &tmA, kc, row0, full);
-            tma_load_2d(b_dst, &tmB, kc, brow, full);
-            tma_load_2d(b_dst + B_BYTES / 2, &tmB, kc, brow + p.up_offset, full);
+            tma_load_2d(b_dst, tb, kc, brow, full);
+            tma_load_2d(b_dst + B_BYTES / 2, tb, kc, brow + p.up_offset, full);
           }
         } else {
           if (lane == 0) {
             tma_load_2d(a_dst, &tmA, kc, row0, full);
-            tma_load_2d(b_dst, &tmB, kc, brow, full);
+            tma_load_2d(b_dst, tb, kc, brow, full);
           }
         }
         ++issued;
@@ -275,7 +286,7 @@ __global__ void __launch_bounds__(threads_of(MODE, F8), 1)
         // in fp32 for the per-tensor quantisation of h, whose amax is recorded here;
         // each warp stages one [32 rows][32 fp32] box per iteration (128-byte
         // swizzle) and stores it by TMA when all 32 rows belong to the tile.
-        const float sc = F8 ? e4m3_scale(__uint_as_float(*p.amax_in)) * __ldg(p.wscale + tl.x) : 1.0f;
+        const float sc = F8 ? e4m3_scale(__uint_as_float(*p.amax_in)) * wscale_of(p, tl.x) : 1.0f;
         float amax = 0.0f;
         __nv_bfloat16* out_row = p.out + static_cast<size_t>(row0 + row) * p.out_ld;
         constexpr int GC = BN / 2 / NH;  // gate columns of this warp (and as many up columns)
@@ -352,7 +363,7 @@ __global__ void __launch_bounds__(threads_of(MODE, F8), 1)
         static_assert(MODE == MODE_GATEUP || epi_warps(MODE, F8) == 4, "Down epilogue: one warp per TMEM quadrant");
         uint8_t* stg = smem + STAGING_OFFSET + q * (32 * 256);
         const int wrows = min(32, nrows - q * 32);  // valid rows of this warp (may be <= 0)
-        const float post = F8 ? e4m3_scale(__uint_as_float(*p.amax_in)) * __ldg(p.wscale + tl.x) : 1.0f;
+        const float post = F8 ? e4m3_scale(__uint_as_float(*p.amax_in)) * wscale_of(p, tl.x) : 1.0f;
         const int wrow0 = row0 + q * 32;            // first o row of this warp
 #pragma unroll 1
         for (int pass = 0; pass < 2; ++pass) {
@@ -475,6 +486,7 @@ static Params base_params(const GroupedArgs& a) {
   p.perm = a.perm;
   p.k = a.k;
   p.hdr = a.hdr;
+  p.E = a.E;
   p.wscale = a.w1_scale;
   return p;
 }
@@ -488,15 +500,19 @@ cudaError_t launch_gateup_bf16(const GroupedArgs& a, cudaStream_t s) {
   int sms = 0;
   cudaError_t err = prepare(a, &sms);
   if (err != cudaSuccess) return err;
-  CUtensorMap tmx, tmw1;
+  CUtensorMap tmx, tmw1, tmw1s;
   const bool gather = a.xs == nullptr && !a.f8;
   const uint32_t bke = a.f8 ? 128 : BK;
   if (!(gather ? encode_2d(&tmx, a.x, a.H, a.T, BK, 1) : encode_2d(&tmx, a.xs, a.H, a.R, bke, BM, a.f8)) ||
       !encode_2d(&tmw1, a.w1, a.H, static_cast<uint64_t>(a.E) * 2 * a.I, bke, BN / 2, a.f8))
     return cudaErrorInvalidValue;
+  tmw1s = tmw1;
+  if (a.S > 0 && !encode_2d(&tmw1s, a.w1s, a.H, static_cast<uint64_t>(a.S) * 2 * a.I, bke, BN / 2, a.f8))
+    return cudaErrorInvalidValue;
   Params p = base_params(a);
   p.a_gather = gather ? 1 : 0;
   p.wscale = a.w1_scale;
+  p.wscale2 = a.w1s_scale;
   p.amax_in = &a.hdr->amax_x;
   p.amax_out = &a.hdr->amax_h;
   p.out_f32 = static_cast<float*>(a.a_f32);
@@ -514,10 +530,10 @@ cudaError_t launch_gateup_bf16(const GroupedArgs& a, cudaStream_t s) {
   stage_begin("gateup_gemm", s);
   if (a.f8)
     err = launch_dependent(grouped_gemm_kernel<MODE_GATEUP, true>, dim3(grid), dim3(threads_of(MODE_GATEUP, true)),
-                           SMEM_BYTES, s, tmx, tmw1, tma32, p);
+                           SMEM_BYTES, s, tmx, tmw1, tma32, tmw1s, p);
   else
     err = launch_dependent(grouped_gemm_kernel<MODE_GATEUP, false>, dim3(grid), dim3(threads_of(MODE_GATEUP, false)),
-                           SMEM_BYTES, s, tmx, tmw1, tmx, p);
+                           SMEM_BYTES, s, tmx, tmw1, tmx, tmw1s, p);
   stage_end(s);
   return err;
 }
@@ -529,15 +545,19 @@ cudaError_t launch_down_bf16(const GroupedArgs& a, cudaStream_t s) {
   int sms = 0;
   cudaError_t err = prepare(a, &sms);
   if (err != cudaSuccess) return err;
-  CUtensorMap tmh, tmw2, tmo;
+  CUtensorMap tmh, tmw2, tmo, tmw2s;
   const uint32_t bke = a.f8 ? 128 : BK;
   // o: bf16 [R rows][H], stored by the epilogue in [32 rows][64 columns] boxes
   if (!encode_2d(&tmh, a.h, a.I, a.R, bke, BM, a.f8) ||
       !encode_2d(&tmw2, a.w2, a.I, static_cast<uint64_t>(a.E) * a.H, bke, BN, a.f8) ||
       !encode_2d(&tmo, a.o, a.H, a.R, 64, 32))
     return cudaErrorInvalidValue;
+  tmw2s = tmw2;
+  if (a.S > 0 && !encode_2d(&tmw2s, a.w2s, a.I, static_cast<uint64_t>(a.S) * a.H, bke, BN, a.f8))
+    return cudaErrorInvalidValue;
   Params p = base_params(a);
   p.wscale = a.w2_scale;
+  p.wscale2 = a.w2s_scale;
   p.amax_in = &a.hdr->amax_h;
   p.nN = (a.H + BN - 1) / BN;
   p.K = a.I;
@@ -551,10 +571,10 @@ cudaError_t launch_down_bf16(const GroupedArgs& a, cudaStream_t s) {
   stage_begin("down_gemm", s);
   if (a.f8)
     err = launch_dependent(grouped_gemm_kernel<MODE_DOWN, true>, dim3(grid), dim3(threads_of(MODE_DOWN, true)),
-                           SMEM_BYTES, s, tmh, tmw2, tmo, p);
+                           SMEM_BYTES, s, tmh, tmw2, tmo, tmw2s, p);
   else
     err = launch_dependent(grouped_gemm_kernel<MODE_DOWN, false>, dim3(grid), dim3(threads_of(MODE_DOWN, false)),
-                           SMEM_BYTES, s, tmh, tmw2, tmo, p);
+                           SMEM_BYTES, s, tmh, tmw2, tmo, tmw2s, p);
   stage_end(s);
   return err;
 }
@@ -591,10 +611,12 @@ __device__ __forceinline__ void combine_load8(const OT* __restrict__ o, long lon
 
 // The k rows of a token are loaded four at a time before any of them is summed,
 // so each thread keeps four loads in flight; the sum still runs j ascending.
-template <typename OT>
+// Then the token's rows T*k + s*T + t of the S shared experts are added with
+// weight 1, s ascending.  YF32: y is the unrounded fp32 sum.
+template <typename OT, bool YF32>
 __global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ o, const float* __restrict__ w, int T,
-                                                      int k, int H, __nv_bfloat16* __restrict__ y,
-                                                      const int32_t* __restrict__ inv) {
+                                                      int k, int H, void* __restrict__ y,
+                                                      const int32_t* __restrict__ inv, int S) {
   // launched as a programmatic dependent (route-direct path): wait for the producer
   // of o; a no-op for an ordinary launch
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -629,8 +651,47 @@ __global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ o, 
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
     }
-    *reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * H + c) = gg::pack_bf16x8(acc);
+    for (int sx = 0; sx < S; ++sx) {
+      float v[8];
+      combine_load8(o, static_cast<long long>(T) * k + static_cast<long long>(sx) * T + t, H, c, v, pol);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += v[i];
+    }
+    if (YF32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(y) + static_cast<size_t>(t) * H + c);
+      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    } else {
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(y) + static_cast<size_t>(t) * H + c) =
+          gg::pack_bf16x8(acc);
+    }
   }
+}
+
+// y = bf16(y32): 8 values per thread and iteration.
+__global__ void __launch_bounds__(256) round_bf16_kernel(const float4* __restrict__ y32, uint4* __restrict__ y,
+                                                         size_t n8) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float4 a = __ldg(y32 + 2 * i), b = __ldg(y32 + 2 * i + 1);
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    y[i] = gg::pack_bf16x8(v);
+  }
+}
+
+cudaError_t launch_round_bf16(const float* y32, void* y, size_t n, cudaStream_t s) {
+  const size_t n8 = n / 8;
+  if (n8 == 0) return cudaSuccess;
+  const int sms = num_sms();
+  size_t blocks = (n8 + 255) / 256;
+  const size_t cap = static_cast<size_t>(sms > 0 ? sms : 148) * 8;
+  if (blocks > cap) blocks = cap;
+  stage_begin("round_bf16", s);
+  round_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(reinterpret_cast<const float4*>(y32),
+                                                                  static_cast<uint4*>(y), n8);
+  const cudaError_t err = cudaGetLastError();
+  stage_end(s);
+  return err;
 }
 
 cudaError_t launch_combine_pdl(const CombineArgs& a, cudaStream_t s) {
@@ -650,11 +711,16 @@ cudaError_t launch_combine_pdl(const CombineArgs& a, cudaStream_t s) {
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
   stage_begin("combine", s);
-  const cudaError_t err =
-      a.o_is_f32 ? cudaLaunchKernelEx(&cfg, combine_kernel<float>, static_cast<const float*>(a.o), a.w, a.T, a.k, a.H,
-                                      static_cast<__nv_bfloat16*>(a.y), a.inv)
-                 : cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, static_cast<const __nv_bfloat16*>(a.o), a.w,
-                                      a.T, a.k, a.H, static_cast<__nv_bfloat16*>(a.y), a.inv);
+  const float* of = static_cast<const float*>(a.o);
+  const __nv_bfloat16* ob = static_cast<const __nv_bfloat16*>(a.o);
+  cudaError_t err;
+  if (a.o_is_f32)
+    err = a.y_f32 ? cudaLaunchKernelEx(&cfg, combine_kernel<float, true>, of, a.w, a.T, a.k, a.H, a.y, a.inv, a.S)
+                  : cudaLaunchKernelEx(&cfg, combine_kernel<float, false>, of, a.w, a.T, a.k, a.H, a.y, a.inv, a.S);
+  else
+    err = a.y_f32
+              ? cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, true>, ob, a.w, a.T, a.k, a.H, a.y, a.inv, a.S)
+              : cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, false>, ob, a.w, a.T, a.k, a.H, a.y, a.inv, a.S);
   stage_end(s);
   return err;
 }

@@ -17,6 +17,7 @@ constexpr int kRouteThreads = 1024;   // threads of the route/rank kernel (32 wa
 constexpr int kMaxRoutesPerBlock = 1024;
 constexpr int kMaxE = 512;
 constexpr int kMaxK = 32;
+constexpr int kMaxShared = 16;        // shared experts of moe_forward_ex
 constexpr int kRouteDirectMaxRoutes = 1024;
 
 // Tokens handled by one block of the route/rank kernel (its routes are that times k).
@@ -60,7 +61,8 @@ struct ForwardLayout {
   size_t total = 0;
 };
 
-bool plan_forward(const moe_problem& p, ForwardLayout* out);
+// S shared experts (moe_forward_ex) add S*T rows to the grouped path's intermediate tensors.
+bool plan_forward(const moe_problem& p, ForwardLayout* out, int S = 0);
 
 // ------------------------------------------------------------------ launchers
 // All return cudaSuccess or the launch error; none synchronises.
@@ -69,35 +71,46 @@ bool plan_forward(const moe_problem& p, ForwardLayout* out);
 cudaError_t launch_route_rank(const float* scores, const int32_t* ids_in, int T, int E, int k, int32_t* ids_out,
                               float* w_out, int32_t* lrank, int32_t* blockcounts, DeviceHeader* hdr, bool route,
                               bool rank, cudaStream_t s, const void* amax_x = nullptr, size_t amax_n = 0);
+// With tiles: the routed experts' tiles, then (S > 0) ceil(T/BM) tiles per shared
+// expert s, numbered expert E + s, over rows [Rr + s*T, Rr + (s+1)*T) (Rr = T*k).
 cudaError_t launch_scan_tiles(int32_t* blockcounts, int nblk, int E, int32_t* counts, int32_t* offsets,
                               int32_t* tiles, int32_t* num_tiles, int max_tiles, int BM, int32_t* tile_scratch,
-                              DeviceHeader* hdr, cudaStream_t s);
+                              DeviceHeader* hdr, cudaStream_t s, int T = 0, int S = 0, int Rr = 0);
 cudaError_t launch_scatter(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E, int k,
                            int32_t* perm, int32_t* inv, cudaStream_t s);
+// The scatter-gather kernels also copy each token's row to rows R + s*T + t of
+// xs for the S shared experts.
 cudaError_t launch_scatter_gather(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
                                   int k, int H, const void* x, void* xs, int32_t* perm, int32_t* inv,
-                                  cudaStream_t s);
+                                  cudaStream_t s, int S = 0);
 // Per-tensor e4m3 passes of the grouped FP8 path (quant.cu).
 cudaError_t launch_scatter_gather_q(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
                                     int k, int H, const void* x, void* xs, int32_t* perm, int32_t* inv,
-                                    const DeviceHeader* hdr, cudaStream_t s);
+                                    const DeviceHeader* hdr, cudaStream_t s, int S = 0);
 cudaError_t launch_quant_rows(const float* a, void* h, size_t n, const DeviceHeader* hdr, cudaStream_t s);
 // Blockwise (one scale per row and 128 columns) passes of the grouped FP8 path (quant.cu).
 cudaError_t launch_scatter_gather_qb(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
                                      int k, int H, const void* x, void* xs, float* xs_scale, int32_t* perm,
-                                     int32_t* inv, cudaStream_t s);
+                                     int32_t* inv, cudaStream_t s, int S = 0);
 cudaError_t launch_quant_groups(const float* a, void* h, float* sh, int rows, int cols, cudaStream_t s);
 cudaError_t launch_tile_map(const int32_t* counts, int E, int BM, int32_t* tiles, int32_t* num_tiles,
                             int max_tiles, int32_t* tile_scratch, DeviceHeader* hdr, cudaStream_t s);
 cudaError_t launch_reset_header(DeviceHeader* hdr, cudaStream_t s);
 
 struct GroupedArgs {
-  int T, E, k, H, I, R;
+  int T, E, k, H, I;
+  int R;                 // rows of the intermediate tensors: T*k routed rows + S*T shared-expert rows
   const void* x;
   const void* xs;        // sorted activations [R, H]; NULL = gather x rows with TMA tile::gather4
 
   const void* w1;
   const void* w2;
+  // S shared experts: tiles with expert id E + s read these weights (and scales)
+  int S;
+  const void* w1s;
+  const void* w2s;
+  const float* w1s_scale;
+  const float* w2s_scale;
   const int32_t* perm;
   const int32_t* tiles;
   const int32_t* num_tiles;
@@ -120,15 +133,19 @@ cudaError_t launch_down_blockwise(const GroupedArgs& a, const float* h_scale, cu
 
 struct CombineArgs {
   int T, k, H;
-  const void* o;       // [R, H]
+  const void* o;       // [R + S*T, H]
   bool o_is_f32;
   const float* w;      // [R]
-  void* y;             // [T, H] bf16
+  void* y;             // [T, H] bf16, or fp32 when y_f32
   const int32_t* inv;  // row of route r in o (expert-sorted o), or null: o in route order
+  int S = 0;           // shared experts: rows T*k + s*T + t of o are added with weight 1
+  bool y_f32 = false;  // write the unrounded fp32 sum
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
 // Same, launched as a programmatic dependent of the previous kernel on the stream.
 cudaError_t launch_combine_pdl(const CombineArgs& a, cudaStream_t s);
+// y = bf16(y32), n values (round to nearest even).
+cudaError_t launch_round_bf16(const float* y32, void* y, size_t n, cudaStream_t s);
 
 struct DecodeArgs {
   int T, E, k, H, I, R;

@@ -148,9 +148,11 @@ ShuffleLayout plan_shuffle(int T, int E, int k, size_t base) {
 constexpr int kAutoRouteDirectMaxTokensPerTensor = 32;
 constexpr int kAutoRouteDirectMaxTokensBlockwise = 64;
 
-static moe_path resolve_path(const moe_problem& p) {
+// S shared experts run on the grouped path only (their rows join the expert-sorted
+// intermediate tensors and the tile map).
+static moe_path resolve_path(const moe_problem& p, int S = 0) {
   if (p.path != MOE_PATH_AUTO) return p.path;
-  if (p.quant == MOE_BF16) return MOE_PATH_GROUPED;
+  if (p.quant == MOE_BF16 || S > 0) return MOE_PATH_GROUPED;
   const int limit = p.quant == MOE_FP8_BLOCK128 ? kAutoRouteDirectMaxTokensBlockwise
                                                 : kAutoRouteDirectMaxTokensPerTensor;
   if (p.T > limit || static_cast<long long>(p.T) * p.k > kRouteDirectMaxRoutes) return MOE_PATH_GROUPED;
@@ -174,7 +176,7 @@ static int route_direct_splits(const moe_problem& p) {
   return s;
 }
 
-static moe_status validate_shape(const moe_problem& p) {
+static moe_status validate_shape(const moe_problem& p, int S = 0) {
   if (p.T < 0 || p.E < 1 || p.k < 1 || p.H < 1 || p.I < 1) return MOE_ERR_INVALID_ARG;
   if (p.k > p.E) return MOE_ERR_INVALID_ARG;
   if (p.quant != MOE_BF16 && p.quant != MOE_FP8_PER_TENSOR && p.quant != MOE_FP8_BLOCK128) return MOE_ERR_INVALID_ARG;
@@ -191,9 +193,12 @@ static moe_status validate_shape(const moe_problem& p) {
   } else {
     if (p.H % 128 || p.I % 128) return MOE_ERR_UNSUPPORTED;
   }
-  const moe_path path = resolve_path(p);
+  if (S < 0) return MOE_ERR_INVALID_ARG;
+  if (S > kMaxShared) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(p.T) * (p.k + S) >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  const moe_path path = resolve_path(p, S);
   if (path == MOE_PATH_ROUTE_DIRECT) {
-    if (p.quant == MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (p.quant == MOE_BF16 || S > 0) return MOE_ERR_UNSUPPORTED;
     if (static_cast<long long>(p.T) * p.k > kRouteDirectMaxRoutes) return MOE_ERR_UNSUPPORTED;
     // shared-memory staging of one work item's operand rows
     if (p.I > 4096 || p.H / route_direct_splits(p) > 4096) return MOE_ERR_UNSUPPORTED;
@@ -201,11 +206,13 @@ static moe_status validate_shape(const moe_problem& p) {
   return MOE_OK;
 }
 
-bool plan_forward(const moe_problem& p, ForwardLayout* out) {
-  if (validate_shape(p) != MOE_OK) return false;
+bool plan_forward(const moe_problem& p, ForwardLayout* out, int S) {
+  if (validate_shape(p, S) != MOE_OK) return false;
   ForwardLayout L;
-  L.path = resolve_path(p);
+  L.path = resolve_path(p, S);
   const size_t T = p.T, E = p.E, k = p.k, H = p.H, I = p.I, R = T * k;
+  // rows of the intermediate tensors: the routes, then T rows per shared expert
+  const size_t RS = R + static_cast<size_t>(S) * T;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;
@@ -222,16 +229,16 @@ bool plan_forward(const moe_problem& p, ForwardLayout* out) {
     L.offsets = take((E + 1) * 4);
     L.perm = take(R * 4);
     L.inv = take(R * 4);
-    L.max_tiles = static_cast<int>(R / kGemmBM + E);
+    L.max_tiles = static_cast<int>(R / kGemmBM + E + static_cast<size_t>(S) * ((T + kGemmBM - 1) / kGemmBM));
     L.tiles = take(static_cast<size_t>(L.max_tiles) * 16);
     L.num_tiles = take(16);
     const size_t eb = p.quant == MOE_BF16 ? 2 : 1;  // bytes per element of the GEMM inputs
-    L.xs = take(R * H * eb);
-    if (p.quant == MOE_FP8_BLOCK128) L.xs_scale = take(R * (H / 128) * 4);
-    if (p.quant != MOE_BF16) L.a32 = take(R * I * 4);
-    L.h = take(R * I * eb);
-    if (p.quant == MOE_FP8_BLOCK128) L.sh = take(R * (I / 128) * 4);
-    L.o = take(R * H * 2);
+    L.xs = take(RS * H * eb);
+    if (p.quant == MOE_FP8_BLOCK128) L.xs_scale = take(RS * (H / 128) * 4);
+    if (p.quant != MOE_BF16) L.a32 = take(RS * I * 4);
+    L.h = take(RS * I * eb);
+    if (p.quant == MOE_FP8_BLOCK128) L.sh = take(RS * (I / 128) * 4);
+    L.o = take(RS * H * 2);
   } else {
     L.splits = route_direct_splits(p);
     L.xq = take(T * H);
@@ -360,9 +367,25 @@ size_t moe_workspace_size(const moe_problem* p) {
 moe_status moe_forward(const moe_problem* pp, const void* x, const float* scores, const void* w1, const void* w2,
                        const float* w1_scale, const float* w2_scale, void* y, void* ws, size_t ws_bytes,
                        moe_stream_t stream) {
+  return moe_forward_ex(pp, nullptr, x, scores, w1, w2, w1_scale, w2_scale, y, ws, ws_bytes, stream);
+}
+
+size_t moe_workspace_size_ex(const moe_problem* p, const moe_forward_options* opt) {
+  if (!p) return 0;
+  ForwardLayout L;
+  if (!plan_forward(*p, &L, opt ? opt->n_shared : 0)) return 0;
+  return L.total;
+}
+
+moe_status moe_forward_ex(const moe_problem* pp, const moe_forward_options* opt, const void* x, const float* scores,
+                          const void* w1, const void* w2, const float* w1_scale, const float* w2_scale, void* y,
+                          void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (!pp) return MOE_ERR_INVALID_ARG;
   const moe_problem p = *pp;
-  const moe_status vs = validate_shape(p);
+  const moe_forward_options o = opt ? *opt : moe_forward_options{};
+  const int S = o.n_shared;
+  if (o.y_fp32 != 0 && o.y_fp32 != 1) return MOE_ERR_INVALID_ARG;
+  const moe_status vs = validate_shape(p, S);
   if (vs != MOE_OK) return vs;
   if (p.T == 0) return MOE_OK;
   if (!x || !scores || !w1 || !w2 || !y) return MOE_ERR_INVALID_ARG;
@@ -373,8 +396,18 @@ moe_status moe_forward(const moe_problem* pp, const void* x, const float* scores
   } else {
     if (!w1_scale || !w2_scale || !aligned(w1_scale, 4) || !aligned(w2_scale, 4)) return MOE_ERR_INVALID_ARG;
   }
+  if (S > 0) {
+    if (!o.w1_shared || !o.w2_shared || !aligned(o.w1_shared, 16) || !aligned(o.w2_shared, 16))
+      return MOE_ERR_INVALID_ARG;
+    if (p.quant == MOE_BF16) {
+      if (o.w1_shared_scale || o.w2_shared_scale) return MOE_ERR_INVALID_ARG;
+    } else if (!o.w1_shared_scale || !o.w2_shared_scale || !aligned(o.w1_shared_scale, 4) ||
+               !aligned(o.w2_shared_scale, 4)) {
+      return MOE_ERR_INVALID_ARG;
+    }
+  }
   ForwardLayout L;
-  if (!plan_forward(p, &L)) return MOE_ERR_UNSUPPORTED;
+  if (!plan_forward(p, &L, S)) return MOE_ERR_UNSUPPORTED;
   if (!ws || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
 
@@ -398,27 +431,32 @@ moe_status moe_forward(const moe_problem* pp, const void* x, const float* scores
                             p.quant == MOE_FP8_PER_TENSOR ? x : nullptr, static_cast<size_t>(p.T) * p.H);
     if (e == cudaSuccess)
       e = launch_scan_tiles(bc, L.shuf.nblk, p.E, counts, offsets, tiles, num_tiles, L.max_tiles, kGemmBM, nullptr,
-                            hdr, s);
+                            hdr, s, p.T, S, p.T * p.k);
     const bool f8 = p.quant == MOE_FP8_PER_TENSOR;
     const bool blockwise = p.quant == MOE_FP8_BLOCK128;
-    const bool gather4 = p.quant == MOE_BF16 && gateup_gather4();
+    // the variant that gathers x inside the GEMM reads routed rows only
+    const bool gather4 = p.quant == MOE_BF16 && S == 0 && gateup_gather4();
     void* xs = at<void*>(ws, L.xs);
     float* xs_scale = blockwise ? at<float*>(ws, L.xs_scale) : nullptr;
     float* sh = blockwise ? at<float*>(ws, L.sh) : nullptr;
     if (e == cudaSuccess) {
       if (f8)
-        e = launch_scatter_gather_q(ids, lrank, bc, p.T, p.E, p.k, p.H, x, xs, perm, inv, hdr, s);
+        e = launch_scatter_gather_q(ids, lrank, bc, p.T, p.E, p.k, p.H, x, xs, perm, inv, hdr, s, S);
       else if (blockwise)
-        e = launch_scatter_gather_qb(ids, lrank, bc, p.T, p.E, p.k, p.H, x, xs, xs_scale, perm, inv, s);
+        e = launch_scatter_gather_qb(ids, lrank, bc, p.T, p.E, p.k, p.H, x, xs, xs_scale, perm, inv, s, S);
       else if (gather4)
         e = launch_scatter(ids, lrank, bc, p.T, p.E, p.k, perm, inv, s);
       else
-        e = launch_scatter_gather(ids, lrank, bc, p.T, p.E, p.k, p.H, x, xs, perm, inv, s);
+        e = launch_scatter_gather(ids, lrank, bc, p.T, p.E, p.k, p.H, x, xs, perm, inv, s, S);
     }
     if (e == cudaSuccess) {
       GroupedArgs g{};
-      g.T = p.T; g.E = p.E; g.k = p.k; g.H = p.H; g.I = p.I; g.R = p.T * p.k;
+      g.T = p.T; g.E = p.E; g.k = p.k; g.H = p.H; g.I = p.I;
+      g.R = p.T * p.k + S * p.T;
       g.x = x; g.w1 = w1; g.w2 = w2;
+      g.S = S;
+      g.w1s = o.w1_shared; g.w2s = o.w2_shared;
+      g.w1s_scale = o.w1_shared_scale; g.w2s_scale = o.w2_shared_scale;
       g.f8 = f8 || blockwise;
       g.w1_scale = w1_scale;
       g.w2_scale = w2_scale;
@@ -441,6 +479,8 @@ moe_status moe_forward(const moe_problem* pp, const void* x, const float* scores
     }
     if (e == cudaSuccess) {
       CombineArgs c{p.T, p.k, p.H, at<void*>(ws, L.o), false, w, y, inv};
+      c.S = S;
+      c.y_f32 = o.y_fp32 != 0;
       e = launch_combine(c, s);
     }
   } else {
@@ -464,18 +504,31 @@ moe_status moe_forward(const moe_problem* pp, const void* x, const float* scores
     e = launch_route_direct(d, s);
     if (e == cudaSuccess) {
       CombineArgs c{p.T, p.k, p.H, d.o, true, w, y, nullptr};
+      c.y_f32 = o.y_fp32 != 0;
       e = launch_combine_pdl(c, s);
     }
   }
   return from_cuda(e);
 }
 
+moe_status moe_round_bf16(const float* y32, void* y, size_t n, moe_stream_t stream) {
+  if (n == 0) return MOE_OK;
+  if (!y32 || !y || !aligned(y32, 16) || !aligned(y, 16) || n % 8) return MOE_ERR_INVALID_ARG;
+  return from_cuda(launch_round_bf16(y32, y, n, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_forward_views(const moe_problem* p, const void* ws, size_t ws_bytes, moe_views* out) {
+  return moe_forward_views_ex(p, nullptr, ws, ws_bytes, out);
+}
+
+moe_status moe_forward_views_ex(const moe_problem* p, const moe_forward_options* opt, const void* ws,
+                                size_t ws_bytes, moe_views* out) {
   if (!p || !out) return MOE_ERR_INVALID_ARG;
-  const moe_status vs = validate_shape(*p);
+  const int S = opt ? opt->n_shared : 0;
+  const moe_status vs = validate_shape(*p, S);
   if (vs != MOE_OK) return vs;
   ForwardLayout L;
-  if (!plan_forward(*p, &L)) return MOE_ERR_UNSUPPORTED;
+  if (!plan_forward(*p, &L, S)) return MOE_ERR_UNSUPPORTED;
   if (!ws || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   void* base = const_cast<void*>(ws);
   moe_views v{};
@@ -488,7 +541,7 @@ moe_status moe_forward_views(const moe_problem* p, const void* ws, size_t ws_byt
     v.inv = at<const int32_t*>(base, L.inv);
     v.tiles = at<const int32_t*>(base, L.tiles);
     v.num_tiles = at<const int32_t*>(base, L.num_tiles);
-    if (!(p->quant == MOE_BF16 && gateup_gather4())) v.xs = at<const void*>(base, L.xs);
+    if (!(p->quant == MOE_BF16 && S == 0 && gateup_gather4())) v.xs = at<const void*>(base, L.xs);
     if (p->quant == MOE_FP8_BLOCK128) v.x_scale = at<const float*>(base, L.xs_scale);
   } else {
     v.xs = at<const void*>(base, L.xq);

@@ -19,7 +19,7 @@ template <bool BLOCKWISE>
 __global__ void __launch_bounds__(256) scatter_gather_tok_q_kernel(
     const int32_t* __restrict__ ids, const int32_t* __restrict__ lrank, const int32_t* __restrict__ blockbase, int E,
     int RB, int k, int H, const uint4* __restrict__ x, uint4* __restrict__ xs, float* __restrict__ xs_scale,
-    int32_t* __restrict__ perm, int32_t* __restrict__ inv, const DeviceHeader* hdr) {
+    int32_t* __restrict__ perm, int32_t* __restrict__ inv, const DeviceHeader* hdr, int S, int T) {
   extern __shared__ __align__(16) uint8_t s_row[];  // [H] e4m3, then [H/128] fp32 scales
   dep_wait();  // block bases and (per tensor) the amax of x
   float* s_sc = reinterpret_cast<float*>(s_row + H);
@@ -60,18 +60,24 @@ __global__ void __launch_bounds__(256) scatter_gather_tok_q_kernel(
   }
   __syncthreads();
   const int row16 = H / 16, groups = H / 128;
-  for (int j = warp; j < k; j += blockDim.x >> 5) {
-    const int r = t * k + j;
-    const int lr = lrank[r];
-    if (lr < 0) {
-      if (lane == 0) inv[r] = -1;
-      continue;
-    }
-    const int e = ids[r];
-    const int p = blockbase[static_cast<size_t>(r / RB) * E + e] + lr;
-    if (lane == 0) {
-      perm[p] = r;
-      inv[r] = p;
+  // rows of the token's k routes, then its rows T*k + s*T + t of the S shared experts
+  for (int j = warp; j < k + S; j += blockDim.x >> 5) {
+    int p;
+    if (j < k) {
+      const int r = t * k + j;
+      const int lr = lrank[r];
+      if (lr < 0) {
+        if (lane == 0) inv[r] = -1;
+        continue;
+      }
+      const int e = ids[r];
+      p = blockbase[static_cast<size_t>(r / RB) * E + e] + lr;
+      if (lane == 0) {
+        perm[p] = r;
+        inv[r] = p;
+      }
+    } else {
+      p = T * k + (j - k) * T + t;
     }
     uint4* dst = xs + static_cast<size_t>(p) * row16;
     for (int c = lane; c < row16; c += 32) dst[c] = reinterpret_cast<const uint4*>(s_row)[c];
@@ -154,7 +160,7 @@ static unsigned grid_for(size_t work, unsigned per_block) {
 
 static cudaError_t launch_tok_q(bool blockwise, const int32_t* ids, const int32_t* lrank, const int32_t* blockbase,
                                 int T, int E, int k, int H, const void* x, void* xs, float* xs_scale, int32_t* perm,
-                                int32_t* inv, const DeviceHeader* hdr, cudaStream_t s) {
+                                int32_t* inv, const DeviceHeader* hdr, cudaStream_t s, int S) {
   if (T <= 0) return cudaSuccess;
   const int RB = route_tokens_per_block(k) * k;
   const size_t smem = static_cast<size_t>(H) + static_cast<size_t>(H / 128) * sizeof(float);
@@ -163,18 +169,18 @@ static cudaError_t launch_tok_q(bool blockwise, const int32_t* ids, const int32_
   const cudaError_t err =
       blockwise ? launch_dependent(scatter_gather_tok_q_kernel<true>, dim3(T), dim3(256), smem, s, ids, lrank, blockbase,
                                    E, RB, k, H, static_cast<const uint4*>(x), static_cast<uint4*>(xs), xs_scale, perm,
-                                   inv, hdr)
+                                   inv, hdr, S, T)
                 : launch_dependent(scatter_gather_tok_q_kernel<false>, dim3(T), dim3(256), smem, s, ids, lrank,
                                    blockbase, E, RB, k, H, static_cast<const uint4*>(x), static_cast<uint4*>(xs),
-                                   static_cast<float*>(nullptr), perm, inv, hdr);
+                                   static_cast<float*>(nullptr), perm, inv, hdr, S, T);
   stage_end(s);
   return err;
 }
 
 cudaError_t launch_scatter_gather_q(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
                                     int k, int H, const void* x, void* xs, int32_t* perm, int32_t* inv,
-                                    const DeviceHeader* hdr, cudaStream_t s) {
-  return launch_tok_q(false, ids, lrank, blockbase, T, E, k, H, x, xs, nullptr, perm, inv, hdr, s);
+                                    const DeviceHeader* hdr, cudaStream_t s, int S) {
+  return launch_tok_q(false, ids, lrank, blockbase, T, E, k, H, x, xs, nullptr, perm, inv, hdr, s, S);
 }
 
 cudaError_t launch_quant_rows(const float* a, void* h, size_t n, const DeviceHeader* hdr, cudaStream_t s) {
@@ -189,8 +195,8 @@ cudaError_t launch_quant_rows(const float* a, void* h, size_t n, const DeviceHea
 
 cudaError_t launch_scatter_gather_qb(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
                                      int k, int H, const void* x, void* xs, float* xs_scale, int32_t* perm,
-                                     int32_t* inv, cudaStream_t s) {
-  return launch_tok_q(true, ids, lrank, blockbase, T, E, k, H, x, xs, xs_scale, perm, inv, nullptr, s);
+                                     int32_t* inv, cudaStream_t s, int S) {
+  return launch_tok_q(true, ids, lrank, blockbase, T, E, k, H, x, xs, xs_scale, perm, inv, nullptr, s, S);
 }
 
 cudaError_t launch_quant_groups(const float* a, void* h, float* sh, int rows, int cols, cudaStream_t s) {

@@ -183,8 +183,10 @@ __device__ __forceinline__ void scan_counts_warp0(const int* s_cnt, int E, int B
   }
 }
 
+// `extra` tiles follow the routed experts' (the shared experts' tiles, written by the caller).
 __device__ __forceinline__ void emit_tiles(const int* s_cnt, const int* s_off, const int* s_toff, int E, int BM,
-                                           int32_t* tiles, int32_t* num_tiles, int max_tiles, DeviceHeader* hdr) {
+                                           int32_t* tiles, int32_t* num_tiles, int max_tiles, DeviceHeader* hdr,
+                                           int extra = 0) {
   for (int e = threadIdx.x >> 5; e < E; e += blockDim.x >> 5) {
     const int c = s_cnt[e];
     const int nt = (c + BM - 1) / BM;
@@ -201,8 +203,8 @@ __device__ __forceinline__ void emit_tiles(const int* s_cnt, const int* s_off, c
     }
   }
   if (threadIdx.x == 0) {
-    *num_tiles = s_toff[E];
-    if (s_toff[E] > max_tiles) record_status(hdr, kStatusBounds, 0x7100000u);
+    *num_tiles = s_toff[E] + extra;
+    if (s_toff[E] + extra > max_tiles) record_status(hdr, kStatusBounds, 0x7100000u);
   }
 }
 
@@ -212,7 +214,8 @@ __device__ __forceinline__ void emit_tiles(const int* s_cnt, const int* s_off, c
 __global__ void __launch_bounds__(1024) scan_tiles_kernel(int32_t* __restrict__ bc, int nblk, int E,
                                                           int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                           int32_t* __restrict__ tiles, int32_t* __restrict__ num_tiles,
-                                                          int max_tiles, int BM, DeviceHeader* hdr, int use_smem) {
+                                                          int max_tiles, int BM, DeviceHeader* hdr, int use_smem,
+                                                          int T, int S, int Rr) {
   __shared__ int s_cnt[kMaxE], s_off[kMaxE + 1], s_toff[kMaxE + 1];
   extern __shared__ int sbc[];
   dep_wait();  // the block counts of the route/rank kernel
@@ -241,7 +244,16 @@ __global__ void __launch_bounds__(1024) scan_tiles_kernel(int32_t* __restrict__ 
   }
   if (threadIdx.x == 0) offsets[E] = s_off[E];
   for (int i = threadIdx.x; i < n; i += blockDim.x) bc[i] = col[i] + s_off[i % E];
-  if (tiles) emit_tiles(s_cnt, s_off, s_toff, E, BM, tiles, num_tiles, max_tiles, hdr);
+  if (!tiles) return;
+  // shared expert s is expert E + s of the tile map: every token, rows [Rr + s*T, Rr + (s+1)*T)
+  const int nts = (T + BM - 1) / BM;
+  emit_tiles(s_cnt, s_off, s_toff, E, BM, tiles, num_tiles, max_tiles, hdr, S * nts);
+  for (int i = threadIdx.x; i < S * nts; i += blockDim.x) {
+    const int sx = i / nts, j = i - sx * nts;
+    const int idx = s_toff[E] + i;
+    if (idx < max_tiles)
+      reinterpret_cast<int4*>(tiles)[idx] = make_int4(E + sx, Rr + sx * T + j * BM, min(BM, T - j * BM), 0);
+  }
 }
 
 __global__ void __launch_bounds__(1024) tile_map_kernel(const int32_t* __restrict__ counts, int E, int BM,
@@ -285,8 +297,8 @@ __global__ void __launch_bounds__(256) scatter_gather_kernel(const int32_t* __re
                                                              const int32_t* __restrict__ blockbase, int E, int RB,
                                                              int k, int H, const uint4* __restrict__ x,
                                                              uint4* __restrict__ xs, int32_t* __restrict__ perm,
-                                                             int32_t* __restrict__ inv) {
-  __shared__ int s_p[kMaxK];
+                                                             int32_t* __restrict__ inv, int S, int T) {
+  __shared__ int s_p[kMaxK + kMaxShared];
   dep_wait();  // ranks and block bases of the kernels before
   const int t = blockIdx.x;
   for (int j = threadIdx.x; j < k; j += blockDim.x) {
@@ -300,12 +312,15 @@ __global__ void __launch_bounds__(256) scatter_gather_kernel(const int32_t* __re
     inv[r] = p;
     s_p[j] = p;
   }
+  // the token's row of each shared expert: T*k + s*T + t
+  for (int j = threadIdx.x; j < S; j += blockDim.x) s_p[k + j] = T * k + j * T + t;
   __syncthreads();
   const int row16 = H / 8;  // 16-byte pieces per row
+  const int nrow = k + S;
   const uint4* src = x + static_cast<size_t>(t) * row16;
   for (int c = threadIdx.x; c < row16; c += blockDim.x) {
     const uint4 v = __ldg(src + c);
-    for (int j = 0; j < k; ++j) {
+    for (int j = 0; j < nrow; ++j) {
       const int p = s_p[j];
       if (p >= 0) xs[static_cast<size_t>(p) * row16 + c] = v;
     }
@@ -370,7 +385,7 @@ cudaError_t launch_route_rank(const float* scores, const int32_t* ids_in, int T,
 
 cudaError_t launch_scan_tiles(int32_t* blockcounts, int nblk, int E, int32_t* counts, int32_t* offsets,
                               int32_t* tiles, int32_t* num_tiles, int max_tiles, int BM, int32_t* /*tile_scratch*/,
-                              DeviceHeader* hdr, cudaStream_t s) {
+                              DeviceHeader* hdr, cudaStream_t s, int T, int S, int Rr) {
   static const cudaError_t attr = cudaFuncSetAttribute(scan_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                        kScanSmemBytes);
   if (attr != cudaSuccess) return attr;
@@ -378,7 +393,8 @@ cudaError_t launch_scan_tiles(int32_t* blockcounts, int nblk, int E, int32_t* co
   const int use_smem = need <= static_cast<size_t>(kScanSmemBytes) ? 1 : 0;
   stage_begin("scan_tiles", s);
   const cudaError_t err = launch_dependent(scan_tiles_kernel, dim3(1), dim3(1024), use_smem ? need : 0, s, blockcounts,
-                                           nblk, E, counts, offsets, tiles, num_tiles, max_tiles, BM, hdr, use_smem);
+                                           nblk, E, counts, offsets, tiles, num_tiles, max_tiles, BM, hdr, use_smem, T,
+                                           S, Rr);
   stage_end(s);
   return err;
 }
@@ -397,12 +413,12 @@ cudaError_t launch_scatter(const int32_t* ids, const int32_t* lrank, const int32
 
 cudaError_t launch_scatter_gather(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
                                   int k, int H, const void* x, void* xs, int32_t* perm, int32_t* inv,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, int S) {
   if (T <= 0) return cudaSuccess;
   const int RB = route_tokens_per_block(k) * k;
   stage_begin("scatter_gather", s);
   const cudaError_t err = launch_dependent(scatter_gather_kernel, dim3(T), dim3(256), 0, s, ids, lrank, blockbase, E, RB,
-                                           k, H, static_cast<const uint4*>(x), static_cast<uint4*>(xs), perm, inv);
+                                           k, H, static_cast<const uint4*>(x), static_cast<uint4*>(xs), perm, inv, S, T);
   stage_end(s);
   return err;
 }

@@ -180,18 +180,20 @@ def _check_y(wl, y, ref_y, tokens=None):
     return err
 
 
-def _check_quant_views(m, wl, p, ws, inp, ref):
+def _check_quant_views(m, wl, p, ws, inp, ref, opt=None):
     """The activations the Gate/Up GEMM reads, bit for bit: x rows (bf16 copies or
     e4m3 codes) in expert-sorted order on the grouped path, in token order on the
     route-direct path, with their per-(row, 128) scales (blockwise) or the amax of
     x (per tensor).  The quantisation of x is unique (IEEE division by the fp32
     scale, round to nearest even, saturating), so nothing here has a tolerance."""
-    v = m.moe_forward_views(p, ws)
+    v = m.moe_forward_views_ex(p, opt, ws)
     T, H, R = wl.T, wl.H, wl.T * wl.k
+    S = opt.n_shared if opt is not None else 0
     xb = bits16(inp["x"])
     grouped = v.perm is not None
-    rows = ref["perm"] // wl.k if grouped else np.arange(T)
-    n = R if grouped else T
+    # grouped: the routes' rows in sorted order, then each shared expert's T rows in token order
+    rows = np.concatenate([ref["perm"] // wl.k, np.tile(np.arange(T), S)]) if grouped else np.arange(T)
+    n = R + S * T if grouped else T
     if wl.quant == W.QUANT_BF16:
         if not v.xs:  # the variant that gathers x inside the GEMM keeps no sorted copy
             return
@@ -215,10 +217,10 @@ def _check_quant_views(m, wl, p, ws, inp, ref):
     assert not bad.any(), f"{int(bad.sum())} e4m3 codes differ, first at {np.argwhere(bad)[0]}"
 
 
-def _check_routing_views(m, wl, p, ws, ref, inp=None):
+def _check_routing_views(m, wl, p, ws, ref, inp=None, opt=None):
     if inp is not None:
-        _check_quant_views(m, wl, p, ws, inp, ref)
-    v = m.moe_forward_views(p, ws)
+        _check_quant_views(m, wl, p, ws, inp, ref, opt)
+    v = m.moe_forward_views_ex(p, opt, ws)
     R = wl.T * wl.k
     assert np.array_equal(_view(ws, v.ids, R, torch.int32).cpu().numpy().reshape(wl.T, wl.k), ref["ids"])
     assert np.max(np.abs(_view(ws, v.w, R, torch.float32).cpu().numpy().reshape(wl.T, wl.k) - ref["w"])) <= 1e-6
@@ -229,7 +231,10 @@ def _check_routing_views(m, wl, p, ws, ref, inp=None):
         assert np.array_equal(_view(ws, v.inv, R, torch.int32).cpu().numpy(), ref["inv"])
         nt = _view(ws, v.num_tiles, 1, torch.int32).item()
         tiles = _view(ws, v.tiles, nt * 4, torch.int32).cpu().numpy().reshape(nt, 4)[:, :3]
-        assert np.array_equal(tiles, O.tile_map(ref["counts"], m.GEMM_BM))
+        S = opt.n_shared if opt is not None else 0
+        # the shared experts' tiles follow the routed ones: expert E + s, rows T*k + s*T + [0, T)
+        shared_tiles = O.tile_map(np.full(S, wl.T, np.int32), m.GEMM_BM) + np.array([wl.E, R, 0], np.int32)
+        assert np.array_equal(tiles, np.concatenate([O.tile_map(ref["counts"], m.GEMM_BM), shared_tiles]))
 
 
 SMALL_GROUPED = [
@@ -555,3 +560,124 @@ def test_gather4_variant_matches_oracle_in_subprocess():
     env = dict(os.environ, MOE_GATEUP_A="gather4")
     r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout + r.stderr
+
+
+# ----------------------------------------------------------------------------- shared experts, fp32 partials
+def _shared_weights(wl, S, seed):
+    """S shared experts with the routed experts' shapes and format (own seed)."""
+    sw = W.Workload(f"{wl.name}_shared", wl.T, S, 1, wl.H, wl.I, wl.quant, seed)
+    w1, w2, s1, s2 = W.make_weights(sw)
+    return {"w1": w1, "w2": w2, "w1_scale": s1, "w2_scale": s2}
+
+
+def _oracle_shared(sh):
+    from tests._util import u8
+
+    cv = (lambda t: bits16(t)) if sh["w1"].dtype == torch.bfloat16 else (lambda t: u8(t))
+    return {"w1": cv(sh["w1"]), "w2": cv(sh["w2"]),
+            "w1_scale": None if sh["w1_scale"] is None else sh["w1_scale"].numpy(),
+            "w2_scale": None if sh["w2_scale"] is None else sh["w2_scale"].numpy()}
+
+
+def run_forward_ex(m, wl, d, shd, S, y_fp32=False, path=None):
+    path = m.MOE_PATH_AUTO if path is None else path
+    p = m.problem(wl.T, wl.E, wl.k, wl.H, wl.I, wl.quant, path)
+    opt = m.forward_options(S, shd["w1"], shd["w2"], shd["w1_scale"], shd["w2_scale"], y_fp32)
+    ws = torch.empty(m.moe_workspace_size_ex(p, opt), dtype=torch.uint8, device=DEV)
+    y = torch.full((wl.T, wl.H), float("nan"), dtype=torch.float32 if y_fp32 else torch.bfloat16, device=DEV)
+    m.moe_forward_ex(p, opt, d["x"], d["scores"], d["w1"], d["w2"], d["w1_scale"], d["w2_scale"], y, ws)
+    torch.cuda.synchronize()
+    assert m.moe_read_device_status(ws) == m.MOE_OK
+    return p, opt, y, ws
+
+
+SHARED_CASES = [
+    (W.workload("tiny"), 1, None),
+    (W.Workload("sh_ragged", 300, 6, 2, 320, 320, W.QUANT_BF16, 81), 2, None),   # partial tiles, 2 shared
+    (W.workload("world16"), 1, 192),
+    (W.workload("prefill"), 1, 192),
+    (W.Workload("sh_f8t", 200, 16, 4, 512, 256, W.QUANT_FP8_TENSOR, 82), 1, None),
+    (W.Workload("sh_f8b", 200, 16, 4, 512, 256, W.QUANT_FP8_BLOCK, 83), 2, None),
+]
+
+
+@pytest.mark.parametrize("wl,S,sample", SHARED_CASES, ids=lambda c: getattr(c, "name", str(c)))
+def test_forward_shared_experts(m, wl, S, sample):
+    """Shared experts ("shared output", route-MMA page, Summary) through
+    moe_forward_ex: every token's row of every shared expert joins the grouped
+    GEMMs as expert E + s; y = routed sum + shared outputs, rounded once."""
+    inp = _big_inputs(wl.name)[1] if wl.name in ("world16", "prefill") else W.make_inputs(wl)
+    shd = _shared_weights(wl, S, 500 + S)
+    d = _dev(inp)
+    p, opt, y, ws = run_forward_ex(m, wl, d, _dev(shd), S)
+    tokens = None
+    if sample:
+        tokens = np.sort(np.random.default_rng(8).choice(wl.T, size=sample, replace=False))
+    ref = O.forward(*oracle_args(inp), wl.k, wl.quant, tokens=tokens, shared=_oracle_shared(shd))
+    _check_routing_views(m, wl, p, ws, ref, inp, opt)
+    _check_y(wl, y, ref["y"], tokens)
+    # the shared term matters: without it the result is far from the reference
+    ref0 = O.forward(*oracle_args(inp), wl.k, wl.quant, tokens=tokens)
+    assert rel_l2(ref0["y"], ref["y"]) > 0.1
+
+
+def test_route_direct_with_shared_experts_is_rejected(m):
+    wl = W.workload("hunyuan", 2)
+    p = m.problem(wl.T, wl.E, wl.k, wl.H, wl.I, wl.quant, m.MOE_PATH_ROUTE_DIRECT)
+    opt = m.forward_options(1, 16, 16, 4, 4)  # never dereferenced: rejected before any launch
+    assert m.moe_workspace_size_ex(p, opt) == 0
+    assert m.moe_workspace_size_ex(m.problem(wl.T, wl.E, wl.k, wl.H, wl.I, wl.quant), opt) > 0
+
+
+@pytest.mark.parametrize("quant,path", [(W.QUANT_BF16, "grouped"), (W.QUANT_FP8_TENSOR, "grouped"),
+                                        (W.QUANT_FP8_BLOCK, "grouped"), (W.QUANT_FP8_TENSOR, "route_direct"),
+                                        (W.QUANT_FP8_BLOCK, "route_direct")])
+def test_fp32_partial_output_and_rounding(m, quant, path):
+    """y_fp32 = 1 writes the unrounded sum (checked against the oracle's unrounded
+    y); moe_round_bf16 of it equals the forward's own bf16 output bit for bit."""
+    wl = W.Workload(f"y32_{quant}", 24, 16, 4, 512, 256, quant, 84)
+    inp = W.make_inputs(wl)
+    d = _dev(inp)
+    mp = m.MOE_PATH_GROUPED if path == "grouped" else m.MOE_PATH_ROUTE_DIRECT
+    none = {"w1": None, "w2": None, "w1_scale": None, "w2_scale": None}
+    _, _, y32, _ = run_forward_ex(m, wl, d, none, 0, y_fp32=True, path=mp)
+    _, y16, _ = run_forward(m, wl, d, path=mp)
+    ref = O.forward(*oracle_args(inp), wl.k, wl.quant, y_fp32=True)
+    got = y32.cpu().numpy()
+    assert rel_l2(got, ref["y"]) <= (1e-2 if quant == W.QUANT_BF16 else 2e-2)
+    yr = torch.empty_like(y16)
+    m.moe_round_bf16(y32, yr)
+    torch.cuda.synchronize()
+    assert torch.equal(yr.view(torch.int16), y16.view(torch.int16))
+    assert torch.equal(yr.view(torch.int16), y32.to(torch.bfloat16).view(torch.int16))  # RNE, as torch rounds
+
+
+@pytest.mark.parametrize("quant", [W.QUANT_BF16, W.QUANT_FP8_BLOCK])
+def test_tensor_parallel_slices_on_gpu(m, quant):
+    """Two slices of a tensor-parallel split of I, each run as its own forward
+    with y_fp32 = 1 (one per rank in a TP deployment, here one after the other on
+    one GPU), summed and rounded once with moe_round_bf16: equal to the unsplit
+    forward's oracle within the usual tolerance, shared expert included."""
+    from tests.test_oracle_forward import tp_slice
+
+    wl = W.Workload(f"tp_{quant}", 200, 16, 4, 512, 256, quant, 85)
+    inp = W.make_inputs(wl)
+    shd = _shared_weights(wl, 1, 86)
+    ref = O.forward(*oracle_args(inp), wl.k, wl.quant, shared=_oracle_shared(shd))
+    P = 2
+    acc = torch.zeros(wl.T, wl.H, dtype=torch.float32, device=DEV)
+    sl = W.Workload(wl.name + "_slice", wl.T, wl.E, wl.k, wl.H, wl.I // P, quant, 85)
+    for rank in range(P):
+        w1, w2, s1, s2 = tp_slice(inp["w1"], inp["w2"], inp["w1_scale"], inp["w2_scale"], quant, P, rank)
+        c1, c2, d1, d2 = tp_slice(shd["w1"], shd["w2"], shd["w1_scale"], shd["w2_scale"], quant, P, rank)
+        part_in = {"x": inp["x"], "scores": inp["scores"], "w1": w1.contiguous(), "w2": w2.contiguous(),
+                   "w1_scale": None if s1 is None else s1.contiguous(),
+                   "w2_scale": None if s2 is None else s2.contiguous()}
+        part_sh = {"w1": c1.contiguous(), "w2": c2.contiguous(), "w1_scale": None if d1 is None else d1.contiguous(),
+                   "w2_scale": None if d2 is None else d2.contiguous()}
+        _, _, y32, _ = run_forward_ex(m, sl, _dev(part_in), _dev(part_sh), 1, y_fp32=True, path=m.MOE_PATH_GROUPED)
+        acc += y32
+    y = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=DEV)
+    m.moe_round_bf16(acc, y)
+    torch.cuda.synchronize()
+    _check_y(wl, y, ref["y"])
