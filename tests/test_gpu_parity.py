@@ -658,7 +658,7 @@ def test_tensor_parallel_slices_on_gpu(m, quant):
     with y_fp32 = 1 (one per rank in a TP deployment, here one after the other on
     one GPU), summed and rounded once with moe_round_bf16: equal to the unsplit
     forward's oracle within the usual tolerance, shared expert included."""
-    from tests.test_oracle_forward import tp_slice
+    from mixture_experts_layer_index_gb300.tp import shard_weights
 
     wl = W.Workload(f"tp_{quant}", 200, 16, 4, 512, 256, quant, 85)
     inp = W.make_inputs(wl)
@@ -668,13 +668,10 @@ def test_tensor_parallel_slices_on_gpu(m, quant):
     acc = torch.zeros(wl.T, wl.H, dtype=torch.float32, device=DEV)
     sl = W.Workload(wl.name + "_slice", wl.T, wl.E, wl.k, wl.H, wl.I // P, quant, 85)
     for rank in range(P):
-        w1, w2, s1, s2 = tp_slice(inp["w1"], inp["w2"], inp["w1_scale"], inp["w2_scale"], quant, P, rank)
-        c1, c2, d1, d2 = tp_slice(shd["w1"], shd["w2"], shd["w1_scale"], shd["w2_scale"], quant, P, rank)
-        part_in = {"x": inp["x"], "scores": inp["scores"], "w1": w1.contiguous(), "w2": w2.contiguous(),
-                   "w1_scale": None if s1 is None else s1.contiguous(),
-                   "w2_scale": None if s2 is None else s2.contiguous()}
-        part_sh = {"w1": c1.contiguous(), "w2": c2.contiguous(), "w1_scale": None if d1 is None else d1.contiguous(),
-                   "w2_scale": None if d2 is None else d2.contiguous()}
+        w1, w2, s1, s2 = shard_weights(inp["w1"], inp["w2"], inp["w1_scale"], inp["w2_scale"], quant, rank, P)
+        c1, c2, d1, d2 = shard_weights(shd["w1"], shd["w2"], shd["w1_scale"], shd["w2_scale"], quant, rank, P)
+        part_in = {"x": inp["x"], "scores": inp["scores"], "w1": w1, "w2": w2, "w1_scale": s1, "w2_scale": s2}
+        part_sh = {"w1": c1, "w2": c2, "w1_scale": d1, "w2_scale": d2}
         _, _, y32, _ = run_forward_ex(m, sl, _dev(part_in), _dev(part_sh), 1, y_fp32=True, path=m.MOE_PATH_GROUPED)
         acc += y32
     y = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=DEV)
