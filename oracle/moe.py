@@ -32,6 +32,13 @@ is used, and the same rule serves every quantised tensor):
                g = (s_x * s_w1[e]) * sum_h q_x q_w1, likewise u; h is quantised
                with one dynamic scale over all R x I values of a; o = (s_h *
                s_w2[e]) * sum_i q_h q_w2.
+  mxfp8        OCP MX with e4m3 elements (the format of "[mxfp8 moe training]
+               add per group blocked scale kernels", Summary; rule in oracle/mx.py):
+               x and h are quantised per run of 32 consecutive values along the
+               contraction dimension with a power-of-two (E8M0) scale; weights
+               arrive as e4m3 codes with E8M0 scales [E, rows, K/32]; every
+               operand is the exact product code * 2^X, so the GEMMs contract
+               the dequantised values.
   fp8 block    x scales per (token, 128-column group); weight scales per
                128 x 128 block; g_i = sum_G s_x[t, G] s_w1[e, i//128, G] *
                sum_{h in G} q_x q_w1 (the up row I+i uses block row
@@ -64,10 +71,12 @@ from .formats import (
     e4m3_encode,
     f32_from_bf16_bits,
 )
+from .mx import mx_dequantize, mx_quantize
 
 BF16 = "bf16"
 FP8_TENSOR = "fp8_tensor"
 FP8_BLOCK = "fp8_block"
+MXFP8 = "mxfp8"
 GROUP = 128  # 128-wide scale groups of the blockwise mode
 
 
@@ -209,8 +218,8 @@ def forward(
     scores   fp32   [T, E]
     w1       [E, 2I, H]           bf16 bits (uint16) or e4m3 codes (uint8)
     w2       [E, H, I]            same
-    w1_scale None | fp32 [E] | fp32 [E, ceil(2I/128), ceil(H/128)]
-    w2_scale None | fp32 [E] | fp32 [E, ceil(H/128), ceil(I/128)]
+    w1_scale None | fp32 [E] | fp32 [E, ceil(2I/128), ceil(H/128)] | E8M0 uint8 [E, 2I, H/32] (mxfp8)
+    w2_scale None | fp32 [E] | fp32 [E, ceil(H/128), ceil(I/128)] | E8M0 uint8 [E, H, I/32] (mxfp8)
     tokens   optional subset of token indices: y is computed only for those
              (all routes are still computed when a per-tensor scale of h needs
              them).
@@ -274,6 +283,9 @@ def forward(
     elif quant == FP8_BLOCK:
         xq, sxg = quant_per_group(x)
         xv = e4m3_decode(xq).astype(np.float64)
+    elif quant == MXFP8:
+        xq, sxm = mx_quantize(x)
+        xv = mx_dequantize(xq, sxm)
     else:
         raise ValueError(quant)
 
@@ -286,9 +298,12 @@ def forward(
         if seg.size == 0:
             continue
         tok = token_of(seg)
-        W1e = _decode_input(w1[e], quant).astype(np.float64)
+        if quant == MXFP8:
+            W1e = mx_dequantize(w1[e], w1_scale[e])
+        else:
+            W1e = _decode_input(w1[e], quant).astype(np.float64)
         Xe = xv[tok]
-        if quant == BF16:
+        if quant in (BF16, MXFP8):
             g = Xe @ W1e[:I].T
             u = Xe @ W1e[I:].T
         elif quant == FP8_TENSOR:
@@ -313,6 +328,9 @@ def forward(
     elif quant == FP8_TENSOR:
         hq, sh = quant_per_tensor(a)
         hv = e4m3_decode(hq).astype(np.float64)
+    elif quant == MXFP8:
+        hq, shm = mx_quantize(a[need])
+        hv[need] = mx_dequantize(hq, shm)
     else:
         shg = np.zeros((RS, -(-I // GROUP)), dtype=np.float32)
         hq, shg_need = quant_per_group(a[need])
@@ -326,9 +344,12 @@ def forward(
         seg = seg[need[seg]]
         if seg.size == 0:
             continue
-        W2e = _decode_input(w2[e], quant).astype(np.float64)
+        if quant == MXFP8:
+            W2e = mx_dequantize(w2[e], w2_scale[e])
+        else:
+            W2e = _decode_input(w2[e], quant).astype(np.float64)
         He = hv[seg]
-        if quant == BF16:
+        if quant in (BF16, MXFP8):
             o[seg] = He @ W2e.T
         elif quant == FP8_TENSOR:
             o[seg] = (np.float64(sh) * np.float64(w2_scale[e])) * (He @ W2e.T)

@@ -463,3 +463,111 @@ def test_tensor_parallel_slices_sum_to_the_whole(quant):
         assert np.abs(part).max() > 0.05 * np.abs(whole).max()  # each slice contributes
         total += part
     assert np.max(np.abs(total - whole)) <= 1e-5 * np.abs(whole).max()
+
+
+# ----------------------------------------------------------------------------- MXFP8
+def _mx_torch(v32):
+    """MX quantisation written with torch: per run of 32 along the last axis, X =
+    (frexp exponent of the run's amax) - 1 - 8 (-127 for a zero run, clamped),
+    codes by torch's float8 conversion after a clamp to +-448.  Returns the
+    dequantised values (fp64) and the exponents."""
+    t = torch.from_numpy(np.asarray(v32, np.float32))
+    rows, cols = t.shape
+    runs = t.view(rows, cols // 32, 32)
+    amax = runs.abs().amax(dim=2)
+    _, ex = torch.frexp(amax)
+    X = torch.where(amax > 0, ex.long() - 9, torch.full_like(ex.long(), -127)).clamp(-127, 127)
+    sc = torch.exp2(X.double())
+    q = (runs.double() / sc[..., None]).float().clamp(-448, 448).to(E4).double()
+    return (q * sc[..., None]).reshape(rows, cols).numpy(), X.numpy()
+
+
+def test_mx_identity_experts_closed_form():
+    """MXFP8 forward with identity-like experts (one nonzero e4m3 code per weight
+    row, random power-of-two run scales), top_k = 1: every dot product has one
+    term, so y follows from the SwiGLU formula with x and h quantised per run of
+    32 (computed here with torch's float8 conversion and frexp)."""
+    rng = np.random.default_rng(12)
+    T, E, H, I = 20, 3, 256, 128
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16)
+    scores = rng.standard_normal((T, E)).astype(np.float32)
+    sig = [rng.permutation(H)[:I] for _ in range(E)]
+    pi = [rng.permutation(I) for _ in range(E)]
+    w1 = np.zeros((E, 2 * I, H), np.uint8)
+    w2 = np.zeros((E, H, I), np.uint8)
+    s1 = (127 + rng.integers(-3, 4, size=(E, 2 * I, H // 32))).astype(np.uint8)
+    s2 = (127 + rng.integers(-3, 4, size=(E, H, I // 32))).astype(np.uint8)
+    for e in range(E):
+        w1[e, np.arange(I), sig[e]] = CODE_2
+        w1[e, I + np.arange(I), sig[e]] = CODE_1
+        w2[e, np.arange(H), pi[e][np.arange(H) % I]] = CODE_1
+    out = M.forward(bits16(x), scores, w1, w2, s1, s2, 1, M.MXFP8)
+    xq, _ = _mx_torch(x.float().numpy())
+    e_of = np.argmax(scores, axis=1)
+    a = np.zeros((T, I), np.float32)
+    for t in range(T):
+        e = e_of[t]
+        s = sig[e]
+        i = np.arange(I)
+        g = 2.0 * xq[t, s] * np.exp2(s1[e, i, s // 32].astype(np.float64) - 127)
+        u = xq[t, s] * np.exp2(s1[e, I + i, s // 32].astype(np.float64) - 127)
+        a[t] = _silu_u(g, u)
+    hq, _ = _mx_torch(a)
+    y = np.zeros((T, H))
+    for t in range(T):
+        e = e_of[t]
+        src = pi[e][np.arange(H) % I]
+        y[t] = hq[t, src] * np.exp2(s2[e, np.arange(H), src // 32].astype(np.float64) - 127)
+    assert np.array_equal(out["y"], _t_bf16_val(y))
+
+
+def test_mx_brute_force_dense_sum_over_all_experts():
+    rng = np.random.default_rng(13)
+    T, E, k, H, I = 3, 4, 2, 128, 64
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16)
+    scores = rng.standard_normal((T, E)).astype(np.float32)
+    import workloads as W
+
+    w1c, s1 = W._pack_mxfp8(torch.from_numpy(rng.standard_normal((E, 2 * I, H)) / math.sqrt(H)).float())
+    w2c, s2 = W._pack_mxfp8(torch.from_numpy(rng.standard_normal((E, H, I)) / math.sqrt(I)).float())
+    w1v = w1c.view(E4).double() * torch.exp2(s1.double() - 127).repeat_interleave(32, dim=2)
+    w2v = w2c.view(E4).double() * torch.exp2(s2.double() - 127).repeat_interleave(32, dim=2)
+    out = M.forward(bits16(x), scores, w1c.numpy(), w2c.numpy(), s1.numpy(), s2.numpy(), k, M.MXFP8)
+    xin, _ = _mx_torch(x.float().numpy())
+    y = np.zeros((T, H))
+    for t in range(T):
+        order, wts = _brute_route(scores[t], k)
+        for e, wv in zip(order, wts):
+            g = w1v[e, :I].numpy() @ xin[t]
+            u = w1v[e, I:].numpy() @ xin[t]
+            a = _silu_u(g, u).astype(np.float32)[None, :]
+            h, _ = _mx_torch(a)
+            y[t] += np.float32(wv) * (w2v[e].numpy() @ h[0])
+    ref = _t_bf16_val(y)
+    assert np.all(np.abs(out["y"] - ref) <= np.abs(ref) * 2.0 ** -7 + 1e-30)
+    assert np.mean(out["y"] == ref) > 0.97
+
+
+def test_mx_quantisation_noise_is_percent_level():
+    import workloads as W
+    from oracle.mx import mx_dequantize
+    from tests._util import oracle_args
+
+    wl = W.Workload("mxnoise", 4, 16, 4, 512, 256, W.QUANT_MXFP8, 78)
+    x, scores, w1, w2, s1, s2 = oracle_args(W.make_inputs(wl))
+    out = M.forward(x, scores, w1, w2, s1, s2, wl.k, M.MXFP8)
+    from oracle.formats import f32_from_bf16_bits
+
+    xv = f32_from_bf16_bits(x).astype(np.float64)
+    y = np.zeros((wl.T, wl.H))
+    for t in range(wl.T):
+        for j in range(wl.k):
+            e = out["ids"][t, j]
+            W1 = mx_dequantize(w1[e], s1[e])
+            g, u = W1[:wl.I] @ xv[t], W1[wl.I:] @ xv[t]
+            y[t] += out["w"][t, j] * (mx_dequantize(w2[e], s2[e]) @ (g / (1 + np.exp(-g)) * u))
+    err = rel_l2(out["y"], y)
+    # larger than the fp32-scaled forms: the OCP shared exponent floor(log2 amax) - 8
+    # leaves amax / 2^X in [256, 512), so a run whose amax has a significand of 1.75 or
+    # more (about a fifth of runs) saturates its largest values at 448, by up to 12.5%
+    assert 1e-3 < err < 1e-1

@@ -34,6 +34,7 @@ import torch
 QUANT_BF16 = "bf16"
 QUANT_FP8_TENSOR = "fp8_tensor"
 QUANT_FP8_BLOCK = "fp8_block"
+QUANT_MXFP8 = "mxfp8"
 E4M3_MAX = 448.0
 
 
@@ -117,6 +118,21 @@ def _pack_e4m3_block128(w: torch.Tensor):
     return q.to(torch.float8_e4m3fn).view(torch.uint8).contiguous(), scale.contiguous()
 
 
+def _pack_mxfp8(w: torch.Tensor):
+    """w [E, rows, cols] fp32 (cols a multiple of 32) -> (e4m3 codes [E, rows, cols],
+    E8M0 scale codes uint8 [E, rows, cols/32]): each run of 32 values along a row
+    shares 2^X with X = (exponent of the run's amax) - 8, saturating codes.  The
+    exponent comes from torch.frexp; the codes from torch's float8 conversion."""
+    E, rows, cols = w.shape
+    runs = w.view(E, rows, cols // 32, 32)
+    amax = runs.abs().amax(dim=3)
+    _, ex = torch.frexp(amax)
+    X = torch.where(amax > 0, ex.long() - 1 - 8, torch.full_like(ex.long(), -127)).clamp(-127, 127)
+    q = (runs / torch.exp2(X.double()).float()[..., None]).clamp(-E4M3_MAX, E4M3_MAX)
+    codes = q.reshape(E, rows, cols).to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+    return codes, (X + 127).to(torch.uint8).contiguous()
+
+
 def skew_bias(E: int, seed: int) -> torch.Tensor:
     """Per-expert router bias giving Zipf(s=1.1) popularity: rank r_e (a seeded
     permutation of 1..E) gets bias -1.1*ln(r_e), so exp(bias) = r_e^-1.1; the four
@@ -158,6 +174,10 @@ def make_weights(wl: Workload, device="cpu"):
     if wl.quant == QUANT_FP8_BLOCK:
         q1, s1 = _pack_e4m3_block128(w1)
         q2, s2 = _pack_e4m3_block128(w2)
+        return q1, q2, s1, s2
+    if wl.quant == QUANT_MXFP8:
+        q1, s1 = _pack_mxfp8(w1)
+        q2, s2 = _pack_mxfp8(w2)
         return q1, q2, s1, s2
     raise ValueError(wl.quant)
 
