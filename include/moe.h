@@ -72,8 +72,11 @@ typedef enum {
   MOE_BF16 = 0,           /* bf16 x, W1, W2; bf16 h; fp32 accumulation */
   MOE_FP8_PER_TENSOR = 1, /* e4m3 W1/W2 with one fp32 scale per expert matrix; x and h quantised to
                              e4m3 with one dynamic scale each (amax/448 over the whole tensor) */
-  MOE_FP8_BLOCK128 = 2    /* e4m3 W1/W2 with fp32 scales per 128x128 block; x quantised per
+  MOE_FP8_BLOCK128 = 2,   /* e4m3 W1/W2 with fp32 scales per 128x128 block; x quantised per
                              (token, 128 columns); h per (route, 128 columns) */
+  MOE_MXFP8 = 3           /* MXFP8: e4m3 W1/W2 with one E8M0 (power-of-two) scale per 32
+                             consecutive values of a row along K; x and h quantised the same
+                             way (grouped path only; see moe_forward) */
 } moe_quant;
 
 typedef enum {
@@ -91,8 +94,9 @@ typedef struct {
 /* Limits of this library (MOE_ERR_UNSUPPORTED beyond them):
  *   1 <= E <= 512;  1 <= k <= min(E, 32);  0 <= T;  T*k < 2^31;
  *   H % 64 == 0, I % 64 == 0 (bf16);  H % 128 == 0, I % 64 == 0 (FP8 per-tensor);
- *   H % 128 == 0, I % 128 == 0 (FP8 blockwise);
- *   MOE_PATH_GROUPED: all three modes;  MOE_PATH_ROUTE_DIRECT: FP8 only, T*k <= 1024. */
+ *   H % 128 == 0, I % 128 == 0 (FP8 blockwise);  H % 128 == 0, I % 64 == 0 (MXFP8);
+ *   MOE_PATH_GROUPED: all four modes;  MOE_PATH_ROUTE_DIRECT: per-tensor and blockwise FP8,
+ *   T*k <= 1024. */
 
 /* ---------------------------------------------------------------- routing
  * moe_route - top-k routing (the routing step of "perf: add small-batch route
@@ -185,12 +189,22 @@ size_t moe_workspace_size(const moe_problem* p);
  *   w1       [E, 2I, H] bf16 (MOE_BF16) or e4m3 codes (FP8 modes); rows 0..I-1 gate, I..2I-1 up
  *   w2       [E, H, I]  bf16 or e4m3
  *   w1_scale NULL (bf16) | fp32 [E] (per-tensor) | fp32 [E, 2I/128, H/128] (blockwise)
+ *            | uint8 E8M0 codes [E, 2I, H/32] (MXFP8, passed through this pointer)
  *   w2_scale NULL (bf16) | fp32 [E] (per-tensor) | fp32 [E, H/128, I/128] (blockwise)
+ *            | uint8 E8M0 codes [E, H, I/32] (MXFP8)
  *   y        [T, H]  bf16 out, preallocated by the caller (written, never read)
  *   ws       device workspace of at least moe_workspace_size(p) bytes; its
  *            contents on entry do not matter and are overwritten
  * Quantisation (FP8 modes): scale = amax/448 in fp32 (1 when amax == 0),
- * code = e4m3(v / scale) rounded to nearest even with saturation.
+ * code = e4m3(v / scale) rounded to nearest even with saturation.  MXFP8 (the
+ * OCP Microscaling format named by "[mxfp8 moe training] add per group blocked
+ * scale kernels"): each run of 32 values along the contraction dimension
+ * shares the scale 2^X, X = floor(log2(amax)) - 8 clamped to [-127, 127] (-127
+ * for a zero run), stored as the E8M0 code X + 127; code = e4m3(v / 2^X), RNE,
+ * saturating.  The MXFP8 forward converts x's, h's and the weights' scales
+ * into the blocked layout of moe_mx_blocked_scales (groups = the experts'
+ * row segments) on every call and multiplies with the tensor cores'
+ * block-scaled MMA; h is quantised in the Gate/Up epilogue.
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
 moe_status moe_forward(const moe_problem* p, const void* x, const float* scores, const void* w1,
                        const void* w2, const float* w1_scale, const float* w2_scale, void* y,
@@ -246,6 +260,35 @@ moe_status moe_forward_ex(const moe_problem* p, const moe_forward_options* opt, 
  * Errors: INVALID_ARG, CUDA. */
 moe_status moe_round_bf16(const float* y32, void* y, size_t n, moe_stream_t stream);
 
+/* ---------------------------------------------------------------- MX scale layout
+ * moe_mx_blocked_scales - the per-group blocked scale conversion of "[mxfp8 moe
+ * training] add per group blocked scale kernels" (Summary): MX scales of row
+ * groups (e.g. the expert groups of a grouped GEMM's activations) converted
+ * into the blocked, swizzled layout that block-scaled tensor-core MMAs read,
+ * each group on its own and padded to whole 128-row blocks, with every group's
+ * start row in the padded output computed on the device (no device-to-host
+ * copy).
+ *   scales        [rows, cols] uint8 (one byte per scale, row-major)
+ *   group_offsets [groups + 1] int32: group g = rows [off[g], off[g+1]),
+ *                 nondecreasing, off[groups] <= rows
+ *   out           blocked output, at least moe_mx_blocked_bytes(rows, cols,
+ *                 groups) bytes; group g's padded rows start at row
+ *                 group_starts[g] of an [*, ceil(cols/4)*4] byte matrix
+ *   group_starts  [groups + 1] int32 out: padded start rows; entry groups = total
+ *   ws            scratch of moe_mx_blocked_workspace_size(rows, groups) bytes
+ * Layout: each group's scales are zero-padded to a multiple of 128 rows and of
+ * 4 columns and cut into 128 x 4 blocks, stored block row by block row; inside
+ * a 512-byte block the scale of (row r, column c) is at byte (r % 32) * 16 +
+ * (r / 32) * 4 + c.  Output bytes past group_starts[groups] rows are not
+ * written.  A negative group size is recorded as MOE_ERR_DEVICE_BOUNDS (status
+ * word at the head of ws) and treated as empty.  1 <= groups <= 4096.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
+size_t moe_mx_blocked_bytes(int rows, int cols, int groups);
+size_t moe_mx_blocked_workspace_size(int rows, int groups);
+moe_status moe_mx_blocked_scales(const uint8_t* scales, int rows, int cols, const int32_t* group_offsets,
+                                 int groups, uint8_t* out, size_t out_bytes, int32_t* group_starts, void* ws,
+                                 size_t ws_bytes, moe_stream_t stream);
+
 /* moe_forward_views - device pointers to the intermediate results moe_forward
  * leaves in the workspace (read-only diagnostics; valid after the call's
  * work on the stream completed).  Pointers not produced by the path chosen
@@ -258,7 +301,9 @@ moe_status moe_round_bf16(const float* y32, void* y, size_t n, moe_stream_t stre
  *            modes); route-direct path: [T, H] e4m3 codes in token order.
  *            NULL for the bf16 variant that gathers x inside the GEMM.
  *   x_scale  blockwise FP8: fp32 scales of xs, one per row and 128 columns
- *            ([R, H/128] sorted, or [T, H/128] route-direct); else NULL.
+ *            ([R, H/128] sorted, or [T, H/128] route-direct); MXFP8: uint8
+ *            E8M0 codes, one per row and 32 columns ([R, H/32] sorted); else
+ *            NULL.
  *   amax_x   per-tensor FP8: the fp32 amax of x over the whole [T, H]
  *            (scale = amax / 448, 1 when it is 0); else NULL. */
 typedef struct {

@@ -30,12 +30,14 @@ MOE_ERR_DEVICE_BOUNDS = 6
 MOE_BF16 = 0
 MOE_FP8_PER_TENSOR = 1
 MOE_FP8_BLOCK128 = 2
+MOE_MXFP8 = 3
 # moe_path
 MOE_PATH_AUTO = 0
 MOE_PATH_GROUPED = 1
 MOE_PATH_ROUTE_DIRECT = 2
 
-QUANT_BY_NAME = {"bf16": MOE_BF16, "fp8_tensor": MOE_FP8_PER_TENSOR, "fp8_block": MOE_FP8_BLOCK128}
+QUANT_BY_NAME = {"bf16": MOE_BF16, "fp8_tensor": MOE_FP8_PER_TENSOR, "fp8_block": MOE_FP8_BLOCK128,
+                 "mxfp8": MOE_MXFP8}
 GEMM_BM = 128  # row-tile height of the grouped GEMMs (tile map of moe_forward)
 
 
@@ -76,6 +78,9 @@ _SIGS = {
     "moe_forward_ex": (_i, [_P, _O, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_forward_views_ex": (_i, [_P, _O, _vp, _sz, ctypes.POINTER(moe_views)]),
     "moe_round_bf16": (_i, [_vp, _vp, _sz, _vp]),
+    "moe_mx_blocked_bytes": (_sz, [_i, _i, _i]),
+    "moe_mx_blocked_workspace_size": (_sz, [_i, _i]),
+    "moe_mx_blocked_scales": (_i, [_vp, _i, _i, _vp, _i, _vp, _sz, _vp, _vp, _sz, _vp]),
     "moe_read_device_status": (_i, [_vp, _vp]),
     "moe_profile_start": (_i, []),
     "moe_profile_start_stage": (_i, [ctypes.c_char_p]),
@@ -223,6 +228,23 @@ def moe_forward_views_ex(p: moe_problem, opt: Optional[moe_forward_options], ws,
 def moe_round_bf16(y32, y, n=None, stream=None) -> None:
     n = y32.numel() if n is None else n
     _check(lib().moe_round_bf16(_ptr(y32), _ptr(y), n, _stream(stream)), "moe_round_bf16")
+
+
+def moe_mx_blocked_bytes(rows: int, cols: int, groups: int) -> int:
+    return int(lib().moe_mx_blocked_bytes(rows, cols, groups))
+
+
+def moe_mx_blocked_workspace_size(rows: int, groups: int) -> int:
+    return int(lib().moe_mx_blocked_workspace_size(rows, groups))
+
+
+def moe_mx_blocked_scales(scales, rows, cols, group_offsets, groups, out, group_starts, ws, out_bytes=None,
+                          ws_bytes=None, stream=None) -> None:
+    """Per-group blocked layout of MX scales (see include/moe.h)."""
+    ob = out.numel() * out.element_size() if out_bytes is None else out_bytes
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(lib().moe_mx_blocked_scales(_ptr(scales), rows, cols, _ptr(group_offsets), groups, _ptr(out), ob,
+                                      _ptr(group_starts), _ptr(ws), nb, _stream(stream)), "moe_mx_blocked_scales")
 
 
 def moe_forward_views(p: moe_problem, ws, ws_bytes=None) -> moe_views:

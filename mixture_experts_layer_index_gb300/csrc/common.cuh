@@ -260,6 +260,56 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t
       : "memory");
 }
 
+// Instruction descriptor for the block-scaled kind::mxf8f6f4 (e4m3 A and B, fp32
+// accumulator, E8M0 scale factors): B scale-factor id at bits 4-5, A/B type codes
+// at bits 7-9 / 10-12 (0 = e4m3), both operands K-major, N >> 3 at bits 17-22,
+// scale type at bit 23 (1 = UE8M0), M >> 4 at bits 24-28, A scale-factor id at
+// bits 29-30.  The ids pick the byte of each 32-bit TMEM scale word, i.e. which
+// 32-wide K chunk of a four-chunk scale block an instruction uses.
+__host__ __device__ constexpr uint32_t make_idesc_mx(int M, int N, uint32_t a_sf_id, uint32_t b_sf_id) {
+  return (b_sf_id << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(M >> 4) << 24) | (a_sf_id << 29);
+}
+
+// D[tmem] (+)= (A * 2^sfA) [smem] * (B * 2^sfB)[smem]^T, MXFP8 (kind::mxf8f6f4 with one
+// E8M0 scale per 32 K values of every row of A and of B, read from TMEM).
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Shared-memory descriptor of a block of scale factors for tcgen05.cp: 32 lines of
+// 16 bytes, no swizzle, 8-line groups 128 bytes apart (stride byte offset), base
+// 16-byte aligned; version 1 (bits 46-47).
+__device__ __forceinline__ uint64_t sf_desc(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  return d;
+}
+
+// Copy 32 lines x 128 bits of shared memory (sf_desc) into TMEM lanes 0-31 at
+// column taddr (four 32-bit columns per line), replicated into the other three
+// 32-lane quadrants.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Untiled bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from global memory into shared memory, completion counted on mbarrier `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // Arrive on `bar` once every tcgen05.mma issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)

@@ -57,6 +57,10 @@ struct ForwardLayout {
   size_t part = 0;    // [S, R, 2I] fp32 split-K partials of Gate/Up
   size_t act = 0;     // per-tensor: [R, I] fp32 a;  blockwise: [R, I] e4m3 h
   size_t sh = 0;      // blockwise (both paths): [R, I/128] fp32 scales of h
+  // MXFP8 (grouped): E8M0 scale codes, row-major and in the blocked layout
+  size_t xs_sc = 0, xs_sf = 0;  // x rows [R, H/32]; blocked per tile
+  size_t h_sc = 0, h_sf = 0;    // h rows [R, I/32]; blocked per tile
+  size_t w1_sf = 0, w2_sf = 0, w1s_sf = 0, w2s_sf = 0;  // blocked weight scales (routed, shared)
   int splits = 1;
   size_t total = 0;
 };
@@ -130,6 +134,29 @@ cudaError_t launch_down_bf16(const GroupedArgs& a, cudaStream_t s);
 // codes, their scales [R, H/128] / [R, I/128] in sorted row order.
 cudaError_t launch_gateup_blockwise(const GroupedArgs& a, const float* xs_scale, cudaStream_t s);
 cudaError_t launch_down_blockwise(const GroupedArgs& a, const float* h_scale, cudaStream_t s);
+
+// MXFP8 grouped path (mx.cu).  Blocked scale tensors hold (C + 3) / 4 blocks of
+// 512 bytes per 128-row block (mx_blocked_bytes).
+size_t mx_blocked_bytes(size_t blocks, int C);
+cudaError_t launch_scatter_gather_mx(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
+                                     int k, int H, const void* x, void* xs, uint8_t* xs_sc, int32_t* perm,
+                                     int32_t* inv, cudaStream_t s, int S = 0);
+// Row-major scales [rows, C] -> blocked layout, one block per tile of the tile map.
+cudaError_t launch_mx_blocked_tiles(const uint8_t* sc, int C, const int32_t* tiles, const int32_t* num_tiles,
+                                    int max_tiles, uint8_t* out, cudaStream_t s);
+// W1 scales [E, 2I, H/32] (blocks of 64 gate + the matching 64 up rows) and W2
+// scales [E, H, I/32] (blocks of 128 rows) -> blocked layouts.
+cudaError_t launch_mx_blocked_weights(const uint8_t* w1_sc, const uint8_t* w2_sc, int E, int H, int I, uint8_t* w1_sf,
+                                      uint8_t* w2_sf, cudaStream_t s);
+// Groups of rows given by offsets [G+1] -> their tile map (in ws), padded start
+// rows [G+1], and the blocked layout.
+cudaError_t launch_mx_group_blocked(const uint8_t* sc, int rows, int C, const int32_t* goff, int G, uint8_t* out,
+                                    int32_t* starts, int32_t* tiles, int32_t* num_tiles, int max_tiles,
+                                    DeviceHeader* hdr, cudaStream_t s);
+cudaError_t launch_gateup_mx(const GroupedArgs& a, const uint8_t* xs_sf, const uint8_t* w1_sf, const uint8_t* w1s_sf,
+                             uint8_t* h_sc, cudaStream_t s);
+cudaError_t launch_down_mx(const GroupedArgs& a, const uint8_t* h_sf, const uint8_t* w2_sf, const uint8_t* w2s_sf,
+                           cudaStream_t s);
 
 struct CombineArgs {
   int T, k, H;

@@ -152,7 +152,7 @@ constexpr int kAutoRouteDirectMaxTokensBlockwise = 64;
 // intermediate tensors and the tile map).
 static moe_path resolve_path(const moe_problem& p, int S = 0) {
   if (p.path != MOE_PATH_AUTO) return p.path;
-  if (p.quant == MOE_BF16 || S > 0) return MOE_PATH_GROUPED;
+  if (p.quant == MOE_BF16 || p.quant == MOE_MXFP8 || S > 0) return MOE_PATH_GROUPED;
   const int limit = p.quant == MOE_FP8_BLOCK128 ? kAutoRouteDirectMaxTokensBlockwise
                                                 : kAutoRouteDirectMaxTokensPerTensor;
   if (p.T > limit || static_cast<long long>(p.T) * p.k > kRouteDirectMaxRoutes) return MOE_PATH_GROUPED;
@@ -179,7 +179,8 @@ static int route_direct_splits(const moe_problem& p) {
 static moe_status validate_shape(const moe_problem& p, int S = 0) {
   if (p.T < 0 || p.E < 1 || p.k < 1 || p.H < 1 || p.I < 1) return MOE_ERR_INVALID_ARG;
   if (p.k > p.E) return MOE_ERR_INVALID_ARG;
-  if (p.quant != MOE_BF16 && p.quant != MOE_FP8_PER_TENSOR && p.quant != MOE_FP8_BLOCK128) return MOE_ERR_INVALID_ARG;
+  if (p.quant != MOE_BF16 && p.quant != MOE_FP8_PER_TENSOR && p.quant != MOE_FP8_BLOCK128 && p.quant != MOE_MXFP8)
+    return MOE_ERR_INVALID_ARG;
   if (p.path != MOE_PATH_AUTO && p.path != MOE_PATH_GROUPED && p.path != MOE_PATH_ROUTE_DIRECT)
     return MOE_ERR_INVALID_ARG;
   if (p.E > kMaxE || p.k > kMaxK) return MOE_ERR_UNSUPPORTED;
@@ -188,7 +189,7 @@ static moe_status validate_shape(const moe_problem& p, int S = 0) {
     return MOE_ERR_UNSUPPORTED;
   if (p.quant == MOE_BF16) {
     if (p.H % 64 || p.I % 64) return MOE_ERR_UNSUPPORTED;
-  } else if (p.quant == MOE_FP8_PER_TENSOR) {
+  } else if (p.quant == MOE_FP8_PER_TENSOR || p.quant == MOE_MXFP8) {
     if (p.H % 128 || p.I % 64) return MOE_ERR_UNSUPPORTED;
   } else {
     if (p.H % 128 || p.I % 128) return MOE_ERR_UNSUPPORTED;
@@ -198,7 +199,7 @@ static moe_status validate_shape(const moe_problem& p, int S = 0) {
   if (static_cast<long long>(p.T) * (p.k + S) >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
   const moe_path path = resolve_path(p, S);
   if (path == MOE_PATH_ROUTE_DIRECT) {
-    if (p.quant == MOE_BF16 || S > 0) return MOE_ERR_UNSUPPORTED;
+    if (p.quant == MOE_BF16 || p.quant == MOE_MXFP8 || S > 0) return MOE_ERR_UNSUPPORTED;
     if (static_cast<long long>(p.T) * p.k > kRouteDirectMaxRoutes) return MOE_ERR_UNSUPPORTED;
     // shared-memory staging of one work item's operand rows
     if (p.I > 4096 || p.H / route_direct_splits(p) > 4096) return MOE_ERR_UNSUPPORTED;
@@ -235,9 +236,22 @@ bool plan_forward(const moe_problem& p, ForwardLayout* out, int S) {
     const size_t eb = p.quant == MOE_BF16 ? 2 : 1;  // bytes per element of the GEMM inputs
     L.xs = take(RS * H * eb);
     if (p.quant == MOE_FP8_BLOCK128) L.xs_scale = take(RS * (H / 128) * 4);
-    if (p.quant != MOE_BF16) L.a32 = take(RS * I * 4);
+    if (p.quant == MOE_FP8_PER_TENSOR || p.quant == MOE_FP8_BLOCK128) L.a32 = take(RS * I * 4);
     L.h = take(RS * I * eb);
     if (p.quant == MOE_FP8_BLOCK128) L.sh = take(RS * (I / 128) * 4);
+    if (p.quant == MOE_MXFP8) {
+      const int Hc = p.H / 32, Ic = p.I / 32;
+      L.xs_sc = take(RS * Hc);
+      L.xs_sf = take(mx_blocked_bytes(L.max_tiles, Hc));
+      L.h_sc = take(RS * Ic);
+      L.h_sf = take(mx_blocked_bytes(L.max_tiles, Ic));
+      L.w1_sf = take(mx_blocked_bytes(E * (I / 64), Hc));
+      L.w2_sf = take(mx_blocked_bytes(E * (H / 128), Ic));
+      if (S > 0) {
+        L.w1s_sf = take(mx_blocked_bytes(static_cast<size_t>(S) * (I / 64), Hc));
+        L.w2s_sf = take(mx_blocked_bytes(static_cast<size_t>(S) * (H / 128), Ic));
+      }
+    }
     L.o = take(RS * H * 2);
   } else {
     L.splits = route_direct_splits(p);
@@ -434,13 +448,17 @@ moe_status moe_forward_ex(const moe_problem* pp, const moe_forward_options* opt,
                             hdr, s, p.T, S, p.T * p.k);
     const bool f8 = p.quant == MOE_FP8_PER_TENSOR;
     const bool blockwise = p.quant == MOE_FP8_BLOCK128;
+    const bool mxfp8 = p.quant == MOE_MXFP8;
     // the variant that gathers x inside the GEMM reads routed rows only
     const bool gather4 = p.quant == MOE_BF16 && S == 0 && gateup_gather4();
     void* xs = at<void*>(ws, L.xs);
     float* xs_scale = blockwise ? at<float*>(ws, L.xs_scale) : nullptr;
     float* sh = blockwise ? at<float*>(ws, L.sh) : nullptr;
     if (e == cudaSuccess) {
-      if (f8)
+      if (mxfp8)
+        e = launch_scatter_gather_mx(ids, lrank, bc, p.T, p.E, p.k, p.H, x, xs, at<uint8_t*>(ws, L.xs_sc), perm, inv,
+                                     s, S);
+      else if (f8)
         e = launch_scatter_gather_q(ids, lrank, bc, p.T, p.E, p.k, p.H, x, xs, perm, inv, hdr, s, S);
       else if (blockwise)
         e = launch_scatter_gather_qb(ids, lrank, bc, p.T, p.E, p.k, p.H, x, xs, xs_scale, perm, inv, s, S);
@@ -461,12 +479,33 @@ moe_status moe_forward_ex(const moe_problem* pp, const moe_forward_options* opt,
       g.w1_scale = w1_scale;
       g.w2_scale = w2_scale;
       g.a_f32 = g.f8 ? at<void*>(ws, L.a32) : nullptr;
+      if (mxfp8) g.f8 = true;
       g.xs = gather4 ? nullptr : xs;
       g.perm = perm; g.tiles = tiles; g.num_tiles = num_tiles; g.max_tiles = L.max_tiles;
       g.h = at<void*>(ws, L.h);
       g.o = at<void*>(ws, L.o);
       g.hdr = hdr;
-      if (blockwise) {
+      if (mxfp8) {
+        const int Hc = p.H / 32, Ic = p.I / 32;
+        uint8_t* xs_sf = at<uint8_t*>(ws, L.xs_sf);
+        uint8_t* h_sc = at<uint8_t*>(ws, L.h_sc);
+        uint8_t* h_sf = at<uint8_t*>(ws, L.h_sf);
+        uint8_t* w1_sf = at<uint8_t*>(ws, L.w1_sf);
+        uint8_t* w2_sf = at<uint8_t*>(ws, L.w2_sf);
+        uint8_t* w1s_sf = S > 0 ? at<uint8_t*>(ws, L.w1s_sf) : nullptr;
+        uint8_t* w2s_sf = S > 0 ? at<uint8_t*>(ws, L.w2s_sf) : nullptr;
+        e = launch_mx_blocked_tiles(at<uint8_t*>(ws, L.xs_sc), Hc, tiles, num_tiles, L.max_tiles, xs_sf, s);
+        if (e == cudaSuccess)
+          e = launch_mx_blocked_weights(reinterpret_cast<const uint8_t*>(w1_scale),
+                                        reinterpret_cast<const uint8_t*>(w2_scale), p.E, p.H, p.I, w1_sf, w2_sf, s);
+        if (e == cudaSuccess && S > 0)
+          e = launch_mx_blocked_weights(reinterpret_cast<const uint8_t*>(o.w1_shared_scale),
+                                        reinterpret_cast<const uint8_t*>(o.w2_shared_scale), S, p.H, p.I, w1s_sf,
+                                        w2s_sf, s);
+        if (e == cudaSuccess) e = launch_gateup_mx(g, xs_sf, w1_sf, w1s_sf, h_sc, s);
+        if (e == cudaSuccess) e = launch_mx_blocked_tiles(h_sc, Ic, tiles, num_tiles, L.max_tiles, h_sf, s);
+        if (e == cudaSuccess) e = launch_down_mx(g, h_sf, w2_sf, w2s_sf, s);
+      } else if (blockwise) {
         e = launch_gateup_blockwise(g, xs_scale, s);
         if (e == cudaSuccess) e = launch_quant_groups(static_cast<const float*>(g.a_f32), g.h, sh, g.R, p.I, s);
         if (e == cudaSuccess) e = launch_down_blockwise(g, sh, s);
@@ -511,6 +550,42 @@ moe_status moe_forward_ex(const moe_problem* pp, const moe_forward_options* opt,
   return from_cuda(e);
 }
 
+size_t moe_mx_blocked_bytes(int rows, int cols, int groups) {
+  if (rows < 0 || cols < 1 || groups < 1) return 0;
+  return mx_blocked_bytes(static_cast<size_t>(rows) / kGemmBM + groups, cols);
+}
+
+static constexpr int kMxMaxGroups = 4096;
+
+size_t moe_mx_blocked_workspace_size(int rows, int groups) {
+  if (rows < 0 || groups < 1 || groups > kMxMaxGroups) return 0;
+  const size_t max_tiles = static_cast<size_t>(rows) / kGemmBM + groups;
+  return align_up(sizeof(DeviceHeader), 256) + align_up(max_tiles * 16, 256) + 256;
+}
+
+moe_status moe_mx_blocked_scales(const uint8_t* scales, int rows, int cols, const int32_t* group_offsets, int groups,
+                                 uint8_t* out, size_t out_bytes, int32_t* group_starts, void* ws, size_t ws_bytes,
+                                 moe_stream_t stream) {
+  if (rows < 0 || cols < 1 || groups < 1) return MOE_ERR_INVALID_ARG;
+  if (groups > kMxMaxGroups || static_cast<long long>(rows) * cols >= (1ll << 40)) return MOE_ERR_UNSUPPORTED;
+  if (!group_offsets || !group_starts || !out || !aligned(group_offsets, 4) || !aligned(group_starts, 4) ||
+      !aligned(out, 16) || (rows > 0 && !scales))
+    return MOE_ERR_INVALID_ARG;
+  if (out_bytes < moe_mx_blocked_bytes(rows, cols, groups)) return MOE_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256) || ws_bytes < moe_mx_blocked_workspace_size(rows, groups)) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DeviceHeader* hdr = at<DeviceHeader*>(ws, 0);
+  const size_t toff = align_up(sizeof(DeviceHeader), 256);
+  const int max_tiles = rows / kGemmBM + groups;
+  int32_t* tiles = at<int32_t*>(ws, toff);
+  int32_t* num_tiles = at<int32_t*>(ws, toff + align_up(static_cast<size_t>(max_tiles) * 16, 256));
+  cudaError_t e = launch_reset_header(hdr, s);
+  if (e == cudaSuccess)
+    e = launch_mx_group_blocked(scales, rows, cols, group_offsets, groups, out, group_starts, tiles, num_tiles,
+                                max_tiles, hdr, s);
+  return from_cuda(e);
+}
+
 moe_status moe_round_bf16(const float* y32, void* y, size_t n, moe_stream_t stream) {
   if (n == 0) return MOE_OK;
   if (!y32 || !y || !aligned(y32, 16) || !aligned(y, 16) || n % 8) return MOE_ERR_INVALID_ARG;
@@ -543,6 +618,7 @@ moe_status moe_forward_views_ex(const moe_problem* p, const moe_forward_options*
     v.num_tiles = at<const int32_t*>(base, L.num_tiles);
     if (!(p->quant == MOE_BF16 && S == 0 && gateup_gather4())) v.xs = at<const void*>(base, L.xs);
     if (p->quant == MOE_FP8_BLOCK128) v.x_scale = at<const float*>(base, L.xs_scale);
+    if (p->quant == MOE_MXFP8) v.x_scale = at<const float*>(base, L.xs_sc);
   } else {
     v.xs = at<const void*>(base, L.xq);
     if (p->quant == MOE_FP8_BLOCK128) v.x_scale = at<const float*>(base, L.sx);

@@ -208,6 +208,13 @@ def _check_quant_views(m, wl, p, ws, inp, ref, opt=None):
         assert got_amax.view(np.uint32) == amax.view(np.uint32), (got_amax, amax)
         codes, _ = O.quant_per_tensor(xf)
         assert not v.x_scale
+    elif wl.quant == W.QUANT_MXFP8:
+        from oracle import mx as OX
+
+        codes, scales = OX.mx_quantize(xf)
+        got_s = _view(ws, v.x_scale, n * (H // 32), torch.uint8).cpu().numpy().reshape(n, H // 32)
+        assert np.array_equal(got_s, scales[rows])
+        assert not v.amax_x
     else:
         codes, scales = O.quant_per_group(xf)
         got_s = _view(ws, v.x_scale, n * (H // 128), torch.float32).cpu().numpy().reshape(n, H // 128)
@@ -326,7 +333,7 @@ def _crafted_x(T, H, quant, seed):
     vals = np.concatenate([vals, -vals, [0.0, -0.0]])
     rng = np.random.default_rng(seed)
     x = np.empty((T, H), dtype=np.float64)
-    group = H if quant == W.QUANT_FP8_TENSOR else 128
+    group = {W.QUANT_FP8_TENSOR: H, W.QUANT_MXFP8: 32}.get(quant, 128)
     for t in range(T):
         order = rng.permutation(vals.size)
         pos = 0
@@ -346,8 +353,9 @@ def _crafted_x(T, H, quant, seed):
     return xt
 
 
-@pytest.mark.parametrize("path", ["grouped", "route_direct"])
-@pytest.mark.parametrize("quant", [W.QUANT_FP8_TENSOR, W.QUANT_FP8_BLOCK])
+@pytest.mark.parametrize("quant,path", [(W.QUANT_FP8_TENSOR, "grouped"), (W.QUANT_FP8_TENSOR, "route_direct"),
+                                        (W.QUANT_FP8_BLOCK, "grouped"), (W.QUANT_FP8_BLOCK, "route_direct"),
+                                        (W.QUANT_MXFP8, "grouped")])
 def test_fp8_conversion_sweep_through_forward(m, quant, path):
     """The e4m3 conversion of x (cvt.rn.satfinite) against the oracle's encoder on
     every code, midpoint, near-midpoint, subnormal and signed zero, driven through
@@ -357,7 +365,7 @@ def test_fp8_conversion_sweep_through_forward(m, quant, path):
     inp["x"] = _crafted_x(wl.T, wl.H, quant, seed=71)
     xv = inp["x"].double().numpy()
     # every scale group's amax is 448 * 2^m, so every scale amax / 448 is a power of two
-    amax = np.abs(xv).reshape(wl.T, -1, 128 if quant == W.QUANT_FP8_BLOCK else wl.H).max(axis=2)
+    amax = np.abs(xv).reshape(wl.T, -1, {W.QUANT_FP8_TENSOR: wl.H, W.QUANT_MXFP8: 32}.get(quant, 128)).max(axis=2)
     assert np.all(np.frexp(amax / 448.0)[0] == 0.5)
     mp = m.MOE_PATH_GROUPED if path == "grouped" else m.MOE_PATH_ROUTE_DIRECT
     p, y, ws = run_forward(m, wl, _dev(inp), path=mp)
@@ -678,3 +686,99 @@ def test_tensor_parallel_slices_on_gpu(m, quant):
     m.moe_round_bf16(acc, y)
     torch.cuda.synchronize()
     _check_y(wl, y, ref["y"])
+
+
+# ----------------------------------------------------------------------------- MXFP8
+def _mx_group_case(m, rows, cols, sizes, seed):
+    from oracle import mx as OX
+
+    rng = np.random.default_rng(seed)
+    sc = rng.integers(0, 255, size=(rows, cols)).astype(np.uint8)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    assert off[-1] <= rows
+    G = len(sizes)
+    out = torch.full((m.moe_mx_blocked_bytes(rows, cols, G),), 0xAB, dtype=torch.uint8, device=DEV)
+    starts = torch.full((G + 1,), -1, dtype=torch.int32, device=DEV)
+    ws = torch.empty(m.moe_mx_blocked_workspace_size(rows, G), dtype=torch.uint8, device=DEV)
+    m.moe_mx_blocked_scales(torch.from_numpy(sc).to(DEV), rows, cols, torch.from_numpy(off).to(DEV), G, out, starts, ws)
+    assert m.moe_read_device_status(ws) == m.MOE_OK
+    ref, ref_starts = OX.per_group_blocked(sc, off)
+    assert np.array_equal(starts.cpu().numpy(), ref_starts)
+    got = out.cpu().numpy()[:ref.size].reshape(ref.shape)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("rows,cols,sizes", [
+    (16640, 160, [1040] * 16),                           # the page's benchmark shape, 16 groups
+    (700, 5, [3, 0, 130, 128, 400]),                     # ragged, an empty group, cols not a multiple of 4
+    (2048, 64, [0, 0, 2048]),
+    (131072, 24, list(np.random.default_rng(3).multinomial(131072, np.ones(128) / 128))),
+    (1, 1, [1]),
+])
+def test_mx_blocked_scales_bit_exact(m, rows, cols, sizes):
+    """The per-group blocked scale conversion ("[mxfp8 moe training] add per group
+    blocked scale kernels") against the oracle, byte for byte, with the groups'
+    padded start rows computed on the device."""
+    _mx_group_case(m, rows, cols, [int(v) for v in sizes], rows + cols)
+
+
+def test_mx_blocked_scales_reports_groups_outside_the_matrix(m):
+    rows, cols = 300, 8
+    off = torch.tensor([0, 100, 400], dtype=torch.int32, device=DEV)  # second group runs past the last row
+    out = torch.zeros(m.moe_mx_blocked_bytes(rows, cols, 2), dtype=torch.uint8, device=DEV)
+    starts = torch.zeros(3, dtype=torch.int32, device=DEV)
+    ws = torch.empty(m.moe_mx_blocked_workspace_size(rows, 2), dtype=torch.uint8, device=DEV)
+    m.moe_mx_blocked_scales(torch.zeros(rows, cols, dtype=torch.uint8, device=DEV), rows, cols, off, 2, out, starts, ws)
+    assert m.moe_read_device_status(ws) == m.MOE_ERR_DEVICE_BOUNDS
+    assert starts.cpu().tolist() == [0, 128, 128]
+
+
+MX_GROUPED = [
+    W.Workload("mx_small", 64, 32, 8, 512, 256, W.QUANT_MXFP8, 101),
+    W.Workload("mx_ragged", 300, 16, 4, 384, 192, W.QUANT_MXFP8, 102),   # I % 128 == 64: a half K stage in Down
+    W.Workload("mx_tiny", 5, 8, 2, 256, 128, W.QUANT_MXFP8, 103),
+    W.Workload("mx_dense", 130, 1, 1, 128, 64, W.QUANT_MXFP8, 104),    # E = k = 1, two row tiles, one K stage
+]
+
+
+@pytest.mark.parametrize("wl", MX_GROUPED, ids=lambda w: w.name)
+def test_forward_grouped_mxfp8(m, wl):
+    inp = W.make_inputs(wl)
+    p, y, ws = run_forward(m, wl, _dev(inp))
+    assert m.moe_select_path(p) == m.MOE_PATH_GROUPED
+    ref = O.forward(*oracle_args(inp), wl.k, wl.quant)
+    _check_routing_views(m, wl, p, ws, ref, inp)
+    _check_y(wl, y, ref["y"])
+
+
+def test_forward_mxfp8_with_shared_experts_and_fp32_partial(m):
+    wl = W.Workload("mx_shared", 200, 16, 4, 512, 256, W.QUANT_MXFP8, 105)
+    inp = W.make_inputs(wl)
+    shd = _shared_weights(wl, 2, 106)
+    d = _dev(inp)
+    p, opt, y, ws = run_forward_ex(m, wl, d, _dev(shd), 2)
+    ref = O.forward(*oracle_args(inp), wl.k, wl.quant, shared=_oracle_shared(shd))
+    _check_routing_views(m, wl, p, ws, ref, inp, opt)
+    _check_y(wl, y, ref["y"])
+    _, _, y32, _ = run_forward_ex(m, wl, d, _dev(shd), 2, y_fp32=True)
+    assert torch.equal(y32.to(torch.bfloat16).view(torch.int16), y.view(torch.int16))
+
+
+def test_forward_grouped_mxfp8_full_size_sampled(m):
+    import dataclasses
+
+    wl = dataclasses.replace(W.workload("prefill"), quant=W.QUANT_MXFP8, name="prefill_mxfp8")
+    inp = W.make_inputs(wl)
+    _big_inputs.cache_clear()
+    _big_fp8_inputs.cache_clear()
+    p, y, ws = run_forward(m, wl, _dev(inp))
+    tokens = np.sort(np.random.default_rng(7).choice(wl.T, size=192, replace=False))
+    ref = O.forward(*oracle_args(inp), wl.k, wl.quant, tokens=tokens)
+    _check_routing_views(m, wl, p, ws, ref, inp)
+    _check_y(wl, y, ref["y"], tokens)
+
+
+def test_mxfp8_route_direct_is_rejected(m):
+    p = m.problem(2, 16, 4, 256, 128, "mxfp8", m.MOE_PATH_ROUTE_DIRECT)
+    assert m.moe_workspace_size(p) == 0
+    assert m.moe_select_path(m.problem(2, 16, 4, 256, 128, "mxfp8")) == m.MOE_PATH_GROUPED
