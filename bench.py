@@ -439,8 +439,9 @@ def measure_fp8_peak(torch, dev, n: int = 8192):
 
 
 def run_fp8_prefill(m, torch, dev, fp8_peak, bf16_sustained: float, steps: int = 50):
-    """The grouped path with e4m3 operands at the prefill shape (per-tensor and
-    128x128 blockwise scales): per-stage device times and GEMM throughput."""
+    """The grouped path with e4m3 operands at the prefill shape (per-tensor,
+    128x128 blockwise and MXFP8 scales): per-stage device times and GEMM
+    throughput."""
     import dataclasses
 
     import workloads as W
@@ -449,7 +450,7 @@ def run_fp8_prefill(m, torch, dev, fp8_peak, bf16_sustained: float, steps: int =
            "fp8_peak_source": "measured live: torch._scaled_mm e4m3 8192^3, best of 10 (burst)",
            "fp8_nominal_tflops": round(2.0 * bf16_sustained, 1),
            "fp8_nominal_source": "2 x the measured sustained bf16 peak (the dense e4m3 : bf16 rate ratio)"}
-    for quant in (W.QUANT_FP8_TENSOR, W.QUANT_FP8_BLOCK):
+    for quant in (W.QUANT_FP8_TENSOR, W.QUANT_FP8_BLOCK, W.QUANT_MXFP8):
         wl = dataclasses.replace(W.workload(PREFILL), quant=quant, name=f"{PREFILL}_{quant}")
         w1, w2, s1, s2 = W.make_weights(wl, device=dev)  # drawn on the device (fast); seeded
         d = {"x": W.make_x(wl).to(dev), "scores": W.make_scores(wl).to(dev), "w1": w1, "w2": w2,
@@ -741,7 +742,7 @@ def run_case(args):
         w1, w2, s1, s2 = W.make_weights(W.workload(sweep, 1), device=dev)
     else:
         quant = {"prefill": W.QUANT_BF16, "prefill_fp8_tensor": W.QUANT_FP8_TENSOR,
-                 "prefill_fp8_block": W.QUANT_FP8_BLOCK}[name]
+                 "prefill_fp8_block": W.QUANT_FP8_BLOCK, "prefill_mxfp8": W.QUANT_MXFP8}[name]
         wl = dataclasses.replace(W.workload(PREFILL), quant=quant, T=args.tokens or W.workload(PREFILL).T)
         w1, w2, s1, s2 = W.make_weights(wl, device=dev)
     x, sc = W.make_x(wl).to(dev), W.make_scores(wl).to(dev)
@@ -827,7 +828,7 @@ def main(argv=None):
                     help="override T of the prefill workload (smaller cases for profiling; not a bench line)")
     ap.add_argument("--case", default="",
                     help="run one workload only, for profiler captures: prefill, prefill_fp8_tensor, "
-                         "prefill_fp8_block (T from --tokens) or <decode sweep>:<B>; not a bench line")
+                         "prefill_fp8_block, prefill_mxfp8 (T from --tokens) or <decode sweep>:<B>; not a bench line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
