@@ -268,7 +268,7 @@ moe_status moe_round_bf16(const float* y32, void* y, size_t n, moe_stream_t stre
  * each group on its own and padded to whole 128-row blocks, with every group's
  * start row in the padded output computed on the device (no device-to-host
  * copy).
- *   scales        [rows, cols] uint8 (one byte per scale, row-major)
+ *   scales        [rows, cols] uint8 (one byte per scale, row-major; base 4-byte aligned)
  *   group_offsets [groups + 1] int32: group g = rows [off[g], off[g+1]),
  *                 nondecreasing, off[groups] <= rows
  *   out           blocked output, at least moe_mx_blocked_bytes(rows, cols,

@@ -569,7 +569,7 @@ moe_status moe_mx_blocked_scales(const uint8_t* scales, int rows, int cols, cons
   if (rows < 0 || cols < 1 || groups < 1) return MOE_ERR_INVALID_ARG;
   if (groups > kMxMaxGroups || static_cast<long long>(rows) * cols >= (1ll << 40)) return MOE_ERR_UNSUPPORTED;
   if (!group_offsets || !group_starts || !out || !aligned(group_offsets, 4) || !aligned(group_starts, 4) ||
-      !aligned(out, 16) || (rows > 0 && !scales))
+      !aligned(out, 16) || (rows > 0 && (!scales || !aligned(scales, 4))))
     return MOE_ERR_INVALID_ARG;
   if (out_bytes < moe_mx_blocked_bytes(rows, cols, groups)) return MOE_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, 256) || ws_bytes < moe_mx_blocked_workspace_size(rows, groups)) return MOE_ERR_WORKSPACE;

@@ -73,12 +73,14 @@ __device__ __forceinline__ float pow2_exact(int x) {
   return x >= -126 ? __uint_as_float(static_cast<uint32_t>(x + 127) << 23) : __uint_as_float(0x00400000u);
 }
 
-// 8 values -> 8 e4m3 codes (IEEE division by the run's scale, RNE, saturating).
-__device__ __forceinline__ uint2 quant8(const float* f, float s) {
-  const uint32_t q0 = static_cast<uint32_t>(cvt_e4m3x2(f[0] / s, f[1] / s)) |
-                      (static_cast<uint32_t>(cvt_e4m3x2(f[2] / s, f[3] / s)) << 16);
-  const uint32_t q1 = static_cast<uint32_t>(cvt_e4m3x2(f[4] / s, f[5] / s)) |
-                      (static_cast<uint32_t>(cvt_e4m3x2(f[6] / s, f[7] / s)) << 16);
+// 8 values -> 8 e4m3 codes of v / 2^X (RNE, saturating).  inv = 2^-X is exact for X
+// in [-127, 127], so v * inv is the correctly rounded quotient v / 2^X, the same
+// value an IEEE division gives, at the cost of a multiplication.
+__device__ __forceinline__ uint2 quant8(const float* f, float inv) {
+  const uint32_t q0 = static_cast<uint32_t>(cvt_e4m3x2(f[0] * inv, f[1] * inv)) |
+                      (static_cast<uint32_t>(cvt_e4m3x2(f[2] * inv, f[3] * inv)) << 16);
+  const uint32_t q1 = static_cast<uint32_t>(cvt_e4m3x2(f[4] * inv, f[5] * inv)) |
+                      (static_cast<uint32_t>(cvt_e4m3x2(f[6] * inv, f[7] * inv)) << 16);
   return make_uint2(q0, q1);
 }
 
@@ -118,7 +120,7 @@ __global__ void __launch_bounds__(256) scatter_gather_mx_kernel(
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
     const int X = mx_exponent(m);
     if (act) {
-      *reinterpret_cast<uint2*>(s_row + 8 * c) = quant8(f, pow2_exact(X));
+      *reinterpret_cast<uint2*>(s_row + 8 * c) = quant8(f, pow2_exact(-X));
       if ((c & 3) == 0) s_sc[c / 4] = static_cast<uint8_t>(X + 127);
     }
   }
@@ -196,10 +198,14 @@ __global__ void __launch_bounds__(256) mx_blocked_kernel(const uint8_t* __restri
         src_row = row0 + r;
       uint32_t word = 0;
       if (src_row >= 0) {
+        if ((C & 3) == 0) {  // four whole scale bytes: one aligned 32-bit load
+          word = __ldg(reinterpret_cast<const uint32_t*>(sc + src_row * C + 4 * cb));
+        } else {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int col = 4 * cb + c;
-          if (col < C) word |= static_cast<uint32_t>(__ldg(sc + src_row * C + col)) << (8 * c);
+          for (int c = 0; c < 4; ++c) {
+            const int col = 4 * cb + c;
+            if (col < C) word |= static_cast<uint32_t>(__ldg(sc + src_row * C + col)) << (8 * c);
+          }
         }
       }
       w[j] = word;
@@ -470,11 +476,11 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
             m = fmaxf(m, fabsf(a[i]));
           }
           const int X = mx_exponent(m);
-          const float s = pow2_exact(X);
+          const float inv = pow2_exact(-X);
           uint4 q4[2];
           uint2* q2 = reinterpret_cast<uint2*>(q4);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) q2[i] = quant8(a + 8 * i, s);
+          for (int i = 0; i < 4; ++i) q2[i] = quant8(a + 8 * i, inv);
           const size_t r = static_cast<size_t>(row0 + row);
           const int col = n * 64 + ch * 32;
           uint4* dst = reinterpret_cast<uint4*>(p.h + r * p.I + col);
