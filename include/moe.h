@@ -93,10 +93,11 @@ typedef struct {
 
 /* Limits of this library (MOE_ERR_UNSUPPORTED beyond them):
  *   1 <= E <= 512;  1 <= k <= min(E, 32);  0 <= T;  T*k < 2^31;
- *   H % 64 == 0, I % 64 == 0 (bf16);  H % 128 == 0, I % 64 == 0 (FP8 per-tensor);
- *   H % 128 == 0, I % 128 == 0 (FP8 blockwise);  H % 128 == 0, I % 64 == 0 (MXFP8);
- *   MOE_PATH_GROUPED: all four modes;  MOE_PATH_ROUTE_DIRECT: per-tensor and blockwise FP8,
- *   T*k <= 1024. */
+ *   H % 64 == 0, I % 64 == 0 (bf16, FP8 per-tensor);  H % 128 == 0, I % 64 == 0 (FP8
+ *   blockwise, whose last 128-column scale group of I may hold 64 columns, and MXFP8);
+ *   MOE_PATH_GROUPED: all four modes;  MOE_PATH_ROUTE_DIRECT: per-tensor and blockwise
+ *   FP8 with H % 128 == 0 (and I % 128 == 0 for blockwise), T*k <= 1024 (AUTO takes the
+ *   grouped path for the other shapes). */
 
 /* ---------------------------------------------------------------- routing
  * moe_route - top-k routing (the routing step of "perf: add small-batch route
@@ -174,9 +175,10 @@ moe_status moe_tile_map(const int32_t* counts, int E, int BM, int32_t* tiles, in
 
 /* ---------------------------------------------------------------- forward
  * moe_select_path - the path moe_forward takes for *p (AUTO resolved):
- * bf16 -> GROUPED; per-tensor FP8 -> ROUTE_DIRECT for T <= 32, blockwise FP8
- * -> ROUTE_DIRECT for T <= 64 (both also need T*k <= 1024), else GROUPED: the
- * crossovers measured on GB300.  Returns p->path when it is not AUTO. */
+ * bf16 and MXFP8 -> GROUPED; per-tensor FP8 -> ROUTE_DIRECT for T <= 32,
+ * blockwise FP8 -> ROUTE_DIRECT for T <= 64 (both also need T*k <= 1024 and the
+ * route-direct shape limits above), else GROUPED: the crossovers measured on
+ * GB300.  Returns p->path when it is not AUTO. */
 moe_path moe_select_path(const moe_problem* p);
 
 /* moe_workspace_size - bytes of device workspace moe_forward needs for *p
@@ -188,9 +190,10 @@ size_t moe_workspace_size(const moe_problem* p);
  *   scores   [T, E]  fp32 router scores
  *   w1       [E, 2I, H] bf16 (MOE_BF16) or e4m3 codes (FP8 modes); rows 0..I-1 gate, I..2I-1 up
  *   w2       [E, H, I]  bf16 or e4m3
- *   w1_scale NULL (bf16) | fp32 [E] (per-tensor) | fp32 [E, 2I/128, H/128] (blockwise)
+ *   w1_scale NULL (bf16) | fp32 [E] (per-tensor) | fp32 [E, 2I/128, H/128] (blockwise; a block
+ *            row of W1 may hold the last gate rows and the first up rows when I % 128 == 64)
  *            | uint8 E8M0 codes [E, 2I, H/32] (MXFP8, passed through this pointer)
- *   w2_scale NULL (bf16) | fp32 [E] (per-tensor) | fp32 [E, H/128, I/128] (blockwise)
+ *   w2_scale NULL (bf16) | fp32 [E] (per-tensor) | fp32 [E, H/128, ceil(I/128)] (blockwise)
  *            | uint8 E8M0 codes [E, H, I/32] (MXFP8)
  *   y        [T, H]  bf16 out, preallocated by the caller (written, never read)
  *   ws       device workspace of at least moe_workspace_size(p) bytes; its

@@ -10,13 +10,19 @@
 // s_a[row, kb] * s_w[block, kb] and add it into fp32 registers ("promotion")
 // while the MMA fills the next buffers.  Two warps share each 32-lane TMEM
 // quadrant (one accumulator row per thread), each holding 64 of the 128
-// columns, so the loads of one warp overlap the FMAs of the other.
+// columns; a warp loads its two 32-column halves one after the other and runs
+// the FMAs of each half while the next half's load is in flight.
 //
 // Gate/Up: N = 64 gate + the matching 64 up rows of W1[e] (two 64-row TMA
-//   boxes), A = expert-sorted e4m3 x rows with their group scales; a warp holds
-//   32 gate and the matching 32 up columns and writes a = silu(g) * u (fp32,
-//   sorted rows, 64 columns per tile); a separate pass quantises a per (row,
-//   128 columns).
+//   boxes), A = expert-sorted e4m3 x rows with their group scales.  Work items
+//   are pairs of units (n = 2g, 2g + 1) of one row tile, processed one after the
+//   other by the same CTA, so that the two units together cover the 128-column
+//   group g of h: a warp holds 32 gate and the matching 32 up columns of a row
+//   and computes a = silu(g) * u; after the first unit it keeps a in shared
+//   memory, after the second the two warps of a quadrant exchange their row
+//   maxima, and each quantises its 64 values of the row with the group's scale
+//   amax / 448 straight into e4m3 h and the fp32 scale (a ragged last group of
+//   64 columns is a single unit).
 // Down: N = 128 rows of W2[e] (one weight scale block), A = e4m3 h rows with
 //   their group scales; the epilogue writes bf16 o for the tile's sorted rows.
 #include "common.cuh"
@@ -29,8 +35,8 @@ constexpr int BM = kGemmBM;  // 128
 constexpr int BN = 128;
 constexpr int BKB = 128;  // K bytes (= e4m3 elements) per stage, one scale block
 constexpr int MAX_STAGES = 6;
-// Gate/Up: 6 stages and 32 KB of staging for the TMA stores of a; Down: 5 stages
-// and 32 KB of output staging.
+// Gate/Up: 6 stages, 32 KB of staging (the first unit's a of a pair) and 1 KB for
+// the row maxima; Down: 5 stages and 32 KB of output staging.
 __host__ __device__ constexpr int stages_of(int mode) { return mode == 0 ? 6 : 5; }
 constexpr int A_BYTES = BM * BKB;
 constexpr int B_BYTES = BN * BKB;
@@ -39,14 +45,14 @@ constexpr int NBUF = 4;           // TMEM partial buffers of 128 columns
 constexpr int TMEM_COLS = NBUF * BN;
 constexpr int EPI_WARPS = 8;      // warps 4..11
 constexpr int THREADS = 32 * (4 + EPI_WARPS);
-constexpr int NUM_BARS = 2 * MAX_STAGES + 2 * NBUF;
-// Down output staging: 32 rows x 128 bytes per epilogue warp, after the barriers
-// (1024-byte aligned: the Gate/Up epilogue's boxes are sources of 128-byte-swizzled TMA stores)
+constexpr int NUM_BARS = 2 * MAX_STAGES + 2 * NBUF + 8;  // + the Gate/Up row-maximum exchange (2 per quadrant)
 __host__ __device__ constexpr int staging_offset(int mode) { return (stages_of(mode) * STAGE_BYTES + 256 + 1023) / 1024 * 1024; }
 constexpr int STAGING_BYTES = EPI_WARPS * 32 * 128;
+constexpr int ROWMAX_BYTES = EPI_WARPS * 32 * 4;
 __host__ __device__ constexpr size_t smem_bytes(int mode) {
-  return 1024 + staging_offset(mode) + STAGING_BYTES;
+  return 1024 + staging_offset(mode) + STAGING_BYTES + (mode == 0 ? ROWMAX_BYTES : 0);
 }
+static_assert(smem_bytes(0) <= 232448 && smem_bytes(1) <= 232448, "shared memory per block");
 
 constexpr int MODE_GATEUP = 0;
 constexpr int MODE_DOWN = 1;
@@ -56,14 +62,15 @@ struct Params {
   const int32_t* num_tiles;
   int max_tiles;
   const int32_t* perm;
-  int nN;          // N tiles per row tile
+  int nN;          // units per row tile (Gate/Up: 64 h columns each; Down: 128 o columns)
   int K;           // reduction length (bytes = elements)
   int I, H;
-  const float* a_scale;  // [R][K/128] scales of the A rows (sorted order)
-  const float* w_scale;  // Gate/Up: [E][2I/128][H/128]; Down: [E][H/128][I/128]
+  const float* a_scale;  // [R][ceil(K/128)] scales of the A rows (sorted order)
+  const float* w_scale;  // Gate/Up: [E][2I/128][H/128]; Down: [E][H/128][ceil(I/128)]
   const float* w_scale2; // the same for the S shared experts (tiles of expert E + s, weights in tmB2)
   int E;
-  float* out_f32;        // Gate/Up: a [R][I]
+  uint8_t* h;            // Gate/Up: e4m3 h [R][I]
+  float* h_scale;        // Gate/Up: [R][ceil(I/128)]
   __nv_bfloat16* out;    // Down: o [R][H]
   DeviceHeader* hdr;
 };
@@ -86,6 +93,22 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
   return r;
 }
 
+// 32 values / s -> 32 e4m3 codes (IEEE division, RNE, saturating), as two 16-byte stores.
+__device__ __forceinline__ void store_e4m3x32(uint8_t* dst, const float* a, float s) {
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    w[i] = static_cast<uint32_t>(cvt_e4m3x2(a[4 * i] / s, a[4 * i + 1] / s)) |
+           (static_cast<uint32_t>(cvt_e4m3x2(a[4 * i + 2] / s, a[4 * i + 3] / s)) << 16);
+  reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// Work items: Gate/Up pairs (row tile, group g = units 2g and 2g + 1, or just 2g for
+// a ragged last group); Down units (row tile, n).
+__device__ __forceinline__ int items_per_tile(int mode, int nN) { return mode == 0 ? (nN + 1) / 2 : nN; }
+__device__ __forceinline__ int subunits(int mode, int nN, int g) { return mode == 0 ? min(2, nN - 2 * g) : 1; }
+
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_blockwise_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -101,6 +124,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   const uint32_t pfull0 = smem_u32(bars + 2 * STAGES), pempty0 = smem_u32(bars + 2 * STAGES + NBUF);
+  // Gate/Up: per quadrant q, xbar0 + 8q (row maxima written) and xbar0 + 8 (4 + q) (read)
+  const uint32_t xbar0 = smem_u32(bars + 2 * STAGES + 2 * NBUF);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -111,6 +136,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(pfull0 + 8 * b, 1);
       mbar_init(pempty0 + 8 * b, EPI_WARPS);  // one arrival per epilogue warp
     }
+    for (int b = 0; b < 8; ++b) mbar_init(xbar0 + 8 * b, 2);  // the two warps of a quadrant
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -130,7 +156,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   dep_wait();  // the tile map and the A rows come from the kernels before (the set-up above overlaps them)
 
   const int ntiles = min(*p.num_tiles, p.max_tiles);
-  const int total = ntiles * p.nN;
+  const int ipt = items_per_tile(MODE, p.nN);
+  const int items = ntiles * ipt;
   const int nk = (p.K + BKB - 1) / BKB;
   const int4* tiles = reinterpret_cast<const int4*>(p.tiles);
 
@@ -139,38 +166,42 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t stage = 0, phase = 0;
     int issued = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const int tile = u / p.nN, n = u - (u / p.nN) * p.nN;
+    for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+      const int tile = it / ipt, g = it - tile * ipt;
       const int4 tl = tiles[tile];
       const int row0 = tl.y;
       const bool shx = tl.x >= p.E;  // a shared expert's tile: its own weight tensor
       const int e = shx ? tl.x - p.E : tl.x;
       const CUtensorMap* tb = shx ? &tmB2 : &tmB;
-      for (int kb = 0; kb < nk; ++kb) {
-        if (lane == 0) {
-          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.hdr, 0x80000u | MODE)) ok = false;
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        if (lane == 0) {
-          const uint32_t full = full0 + 8 * stage;
-          const uint32_t a_dst = smem_u32(smem + stage * STAGE_BYTES), b_dst = a_dst + A_BYTES;
-          const int kc = kb * BKB;
-          mbar_arrive_expect_tx(full, STAGE_BYTES);
-          tma_load_2d(a_dst, &tmA, kc, row0, full);
-          if (MODE == MODE_GATEUP) {
-            const int brow = e * 2 * p.I + n * (BN / 2);
-            tma_load_2d(b_dst, tb, kc, brow, full);                   // 64 gate rows
-            tma_load_2d(b_dst + B_BYTES / 2, tb, kc, brow + p.I, full);  // the matching 64 up rows
-          } else {
-            tma_load_2d(b_dst, tb, kc, e * p.H + n * BN, full);
+      const int nsub = subunits(MODE, p.nN, g);
+      for (int sub = 0; sub < nsub && ok; ++sub) {
+        const int n = MODE == MODE_GATEUP ? 2 * g + sub : g;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (lane == 0) {
+            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.hdr, 0x80000u | MODE)) ok = false;
           }
-        }
-        __syncwarp();
-        ++issued;
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+          if (lane == 0) {
+            const uint32_t full = full0 + 8 * stage;
+            const uint32_t a_dst = smem_u32(smem + stage * STAGE_BYTES), b_dst = a_dst + A_BYTES;
+            const int kc = kb * BKB;
+            mbar_arrive_expect_tx(full, STAGE_BYTES);
+            tma_load_2d(a_dst, &tmA, kc, row0, full);
+            if (MODE == MODE_GATEUP) {
+              const int brow = e * 2 * p.I + n * (BN / 2);
+              tma_load_2d(b_dst, tb, kc, brow, full);                   // 64 gate rows
+              tma_load_2d(b_dst + B_BYTES / 2, tb, kc, brow + p.I, full);  // the matching 64 up rows
+            } else {
+              tma_load_2d(b_dst, tb, kc, e * p.H + n * BN, full);
+            }
+          }
+          __syncwarp();
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
       }
     }
@@ -187,8 +218,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t idesc = make_idesc(0, 0, BM, BN);
       uint32_t stage = 0, phase = 0, pb = 0, pphase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        for (int kb = 0; kb < nk; ++kb) {
+      for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+        const int nsub = subunits(MODE, p.nN, it % ipt);
+        for (int kt = 0; kt < nsub * nk; ++kt) {
           if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.hdr, 0x81000u | MODE) ||
               !mbar_wait(pempty0 + 8 * pb, pphase ^ 1, abort_flag, p.hdr, 0x82000u | MODE)) {
             ok = false;
@@ -229,10 +261,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int c0 = MODE == MODE_GATEUP ? ch * 32 : ch * 64;
     const int c1 = MODE == MODE_GATEUP ? BN / 2 + ch * 32 : ch * 64 + 32;
     uint32_t pb = 0, pphase = 0;
-    const int kblocks = p.K / 128;  // scale groups along K (K is a multiple of 128)
+    const int kblocks = nk;  // scale groups along K: ceil(K / 128)
+    float* rowmax = reinterpret_cast<float*>(smem + staging_offset(MODE) + STAGING_BYTES);  // Gate/Up: [8 warps][32]
+    uint32_t xphase = 0;  // phase of this quadrant's exchange barriers
     bool ok = true;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const int tile = u / p.nN, n = u - (u / p.nN) * p.nN;
+    for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+      const int tile = it / ipt, g = it - tile * ipt;
       const int4 tl = tiles[tile];
       const int row0 = tl.y, nrows = tl.z;
       const bool shx = tl.x >= p.E;
@@ -240,113 +274,160 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float* wsc = shx ? p.w_scale2 : p.w_scale;
       const int arow = row0 + min(row, nrows - 1);
       const float* sa = p.a_scale + static_cast<size_t>(arow) * kblocks;
-      // weight scale rows of this tile's columns (both halves in one block for Down)
-      const float* swg;
-      const float* swu;
-      if (MODE == MODE_GATEUP) {
-        const int nblk = 2 * p.I / 128, hblk = p.H / 128;
-        swg = wsc + (static_cast<size_t>(e) * nblk + (n * (BN / 2)) / 128) * hblk;
-        swu = wsc + (static_cast<size_t>(e) * nblk + (p.I + n * (BN / 2)) / 128) * hblk;
-      } else {
-        const int hblk = p.H / 128, iblk = p.I / 128;
-        swg = wsc + (static_cast<size_t>(e) * hblk + n) * iblk;
-        swu = swg;
-      }
-      float acc[64];
-#pragma unroll
-      for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
-      float sa_next = __ldg(sa), sg_next = __ldg(swg), su_next = __ldg(swu);
-      for (int kb = 0; kb < nk; ++kb) {
-        const float sak = sa_next, sgk = sg_next, suk = su_next;
-        if (kb + 1 < nk) {
-          sa_next = __ldg(sa + kb + 1);
-          sg_next = __ldg(swg + kb + 1);
-          su_next = __ldg(swu + kb + 1);
-        }
-        int good = 1;
-        if (lane == 0) good = mbar_wait(pfull0 + 8 * pb, pphase, abort_flag, p.hdr, 0x83000u | MODE);
-        if (!__shfl_sync(0xffffffffu, good, 0)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + pb * BN;
-        float v0[32], v1[32];
-        tmem_ld32(tbase + c0, v0);
-        tmem_ld32(tbase + c1, v1);
-        tmem_ld_wait();
-        // both column ranges are in registers: hand the buffer back before the FMAs
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(pempty0 + 8 * pb);
-        const float s0 = sak * sgk, s1 = sak * (MODE == MODE_GATEUP ? suk : sgk);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          acc[i] = fmaf(v0[i], s0, acc[i]);
-          acc[32 + i] = fmaf(v1[i], s1, acc[32 + i]);
-        }
-        if (++pb == NBUF) {
-          pb = 0;
-          pphase ^= 1;
-        }
-      }
-      if (!ok) break;
-      if (MODE == MODE_GATEUP) {
-        // each thread's 32 fp32 outputs are one 128-byte piece of its row: the warp
-        // stages them as one [32 rows][32 fp32] box (128-byte swizzle) for a TMA tile
-        // store, or 16-byte stores for a partial tile's rows
-        uint8_t* stg = smem + staging_offset(MODE) + e8 * 4096;
-        const int wrows = min(32, nrows - q * 32), wrow0 = row0 + q * 32;
-        const int col = n * (BN / 2) + ch * 32;
-        if (lane == 0) bulk_wait_group_read0();  // the previous box has left the staging
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          *reinterpret_cast<float4*>(stg + lane * 128 + ((i ^ (lane & 7)) << 4)) =
-              make_float4(silu_mul_fast(acc[4 * i], acc[32 + 4 * i]), silu_mul_fast(acc[4 * i + 1], acc[33 + 4 * i]),
-                          silu_mul_fast(acc[4 * i + 2], acc[34 + 4 * i]), silu_mul_fast(acc[4 * i + 3], acc[35 + 4 * i]));
-        if (wrows == 32) {
-          fence_proxy_async_shared();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmO, smem_u32(stg), col, wrow0);
-            bulk_commit_group();
-          }
-          __syncwarp();
+      const int nsub = subunits(MODE, p.nN, g);
+      float mrow = 0.0f;  // Gate/Up: this thread's row maximum of |a| over the group so far
+      for (int sub = 0; sub < nsub && ok; ++sub) {
+        const int n = MODE == MODE_GATEUP ? 2 * g + sub : g;
+        // weight scale rows of this unit's columns (both halves in one block for Down)
+        const float* swg;
+        const float* swu;
+        if (MODE == MODE_GATEUP) {
+          const int nblk = 2 * p.I / 128, hblk = p.H / 128;
+          swg = wsc + (static_cast<size_t>(e) * nblk + (n * (BN / 2)) / 128) * hblk;
+          swu = wsc + (static_cast<size_t>(e) * nblk + (p.I + n * (BN / 2)) / 128) * hblk;
         } else {
-          __syncwarp();
+          const int hblk = p.H / 128;
+          swg = wsc + (static_cast<size_t>(e) * hblk + n) * kblocks;
+          swu = swg;
+        }
+        float acc[64];
 #pragma unroll
-          for (int it = 0; it < 8; ++it) {  // 4 rows of 32 fp32 (8 lanes each) per instruction
-            const int r = it * 4 + (lane >> 3), j = lane & 7;
+        for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+        float sa_next = __ldg(sa), sg_next = __ldg(swg), su_next = __ldg(swu);
+        // Pipelined promotion: the first half of K block kb is in va when the loop body
+        // starts; the second half's load is issued, the first half's FMAs run, then the
+        // next block's first half is loaded while the second half's FMAs run.
+        float va[32], vb[32];
+        {
+          int good = 1;
+          if (lane == 0) good = mbar_wait(pfull0 + 8 * pb, pphase, abort_flag, p.hdr, 0x83000u | MODE);
+          if (!__shfl_sync(0xffffffffu, good, 0)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + pb * BN + c0, va);
+          tmem_ld_wait_regs(va);
+        }
+        for (int kb = 0; kb < nk; ++kb) {
+          const float sak = sa_next, sgk = sg_next, suk = su_next;
+          if (kb + 1 < nk) {
+            sa_next = __ldg(sa + kb + 1);
+            sg_next = __ldg(swg + kb + 1);
+            su_next = __ldg(swu + kb + 1);
+          }
+          const float s0 = sak * sgk, s1 = sak * (MODE == MODE_GATEUP ? suk : sgk);
+          tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + pb * BN + c1, vb);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] = fmaf(va[i], s0, acc[i]);
+          tmem_ld_wait_regs(vb);
+          // both halves of this buffer are in registers: hand it back to the MMA
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(pempty0 + 8 * pb);
+          if (++pb == NBUF) {
+            pb = 0;
+            pphase ^= 1;
+          }
+          const bool more = kb + 1 < nk;
+          if (more) {
+            int good = 1;
+            if (lane == 0) good = mbar_wait(pfull0 + 8 * pb, pphase, abort_flag, p.hdr, 0x83000u | MODE);
+            if (!__shfl_sync(0xffffffffu, good, 0)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + pb * BN + c0, va);
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[32 + i] = fmaf(vb[i], s1, acc[32 + i]);
+          if (more) tmem_ld_wait_regs(va);
+        }
+        if (!ok) break;
+        if (MODE == MODE_GATEUP) {
+          // a for 32 h columns of this row; the first unit of a pair parks its values in
+          // this warp's staging slot (row-per-lane, 16-byte pieces XOR-swizzled by lane)
+          float a[32];
+          float m = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            a[i] = silu_mul_fast(acc[i], acc[32 + i]);
+            m = fmaxf(m, fabsf(a[i]));
+          }
+          mrow = fmaxf(mrow, m);
+          float4* stg = reinterpret_cast<float4*>(smem + staging_offset(MODE) + e8 * 4096) + lane * 8;
+          if (sub == 0 && nsub == 2) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              stg[i ^ (lane & 7)] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
+          }
+          if (sub == nsub - 1) {
+            // the group's scale: row maximum over both warps of the quadrant (64 columns
+            // each), exchanged through shared memory between the two warps; bounded
+            // mbarrier waits order the write, the partner's read and the next write
+            rowmax[e8 * 32 + lane] = row < nrows ? mrow : 0.0f;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xbar0 + 8 * q);
+            int good = 1;
+            if (lane == 0) good = mbar_wait(xbar0 + 8 * q, xphase, abort_flag, p.hdr, 0x84000u);
+            if (!__shfl_sync(0xffffffffu, good, 0)) {
+              ok = false;
+              break;
+            }
+            const float gm = fmaxf(rowmax[e8 * 32 + lane], rowmax[(e8 ^ 4) * 32 + lane]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xbar0 + 8 * (4 + q));
+            if (lane == 0) good = mbar_wait(xbar0 + 8 * (4 + q), xphase, abort_flag, p.hdr, 0x85000u);
+            if (!__shfl_sync(0xffffffffu, good, 0)) {
+              ok = false;
+              break;
+            }
+            xphase ^= 1;
+            if (row < nrows) {
+              const float sc = e4m3_scale(gm);
+              const size_t r = static_cast<size_t>(row0 + row);
+              uint8_t* hrow = p.h + r * p.I;
+              if (nsub == 2) {
+                float a0[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float4 v = stg[i ^ (lane & 7)];
+                  a0[4 * i] = v.x;
+                  a0[4 * i + 1] = v.y;
+                  a0[4 * i + 2] = v.z;
+                  a0[4 * i + 3] = v.w;
+                }
+                store_e4m3x32(hrow + (2 * g) * 64 + ch * 32, a0, sc);
+                store_e4m3x32(hrow + (2 * g + 1) * 64 + ch * 32, a, sc);
+              } else {
+                store_e4m3x32(hrow + (2 * g) * 64 + ch * 32, a, sc);
+              }
+              if (ch == 0) p.h_scale[r * ((p.I + 127) / 128) + g] = sc;
+            }
+          }
+        } else {
+          // Down rows (sorted order, like h): each thread's 64 bf16 outputs are staged
+          // in shared memory (16-byte pieces XOR-swizzled by row) and the warp writes
+          // four whole 128-byte row segments per store instruction.
+          uint4* stg = reinterpret_cast<uint4*>(smem + staging_offset(MODE)) + e8 * (32 * 8);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) stg[lane * 8 + (i ^ (lane & 7))] = pack_bf16x8(acc + 8 * i);
+          __syncwarp();
+          const int wrows = min(32, nrows - q * 32);  // valid rows of this warp (may be <= 0)
+          const int slot = row0 + row;
+#pragma unroll
+          for (int it2 = 0; it2 < 8; ++it2) {
+            const int r = it2 * 4 + (lane >> 3), j = lane & 7;
+            const int rslot = __shfl_sync(0xffffffffu, slot, r);
             if (r < wrows)
-              *reinterpret_cast<float4*>(p.out_f32 + static_cast<size_t>(wrow0 + r) * p.I + col + 4 * j) =
-                  *reinterpret_cast<const float4*>(stg + r * 128 + ((j ^ (r & 7)) << 4));
+              *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(rslot) * p.H + n * BN + ch * 64 + j * 8) =
+                  stg[r * 8 + (j ^ (r & 7))];
           }
           __syncwarp();
         }
-      } else {
-        // Down rows (sorted order, like h): each thread's 64 bf16 outputs are staged
-        // in shared memory (16-byte pieces XOR-swizzled by row) and the warp writes
-        // four whole 128-byte row segments per store instruction.
-        uint4* stg = reinterpret_cast<uint4*>(smem + staging_offset(MODE)) + e8 * (32 * 8);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) stg[lane * 8 + (i ^ (lane & 7))] = pack_bf16x8(acc + 8 * i);
-        __syncwarp();
-        const int wrows = min(32, nrows - q * 32);  // valid rows of this warp (may be <= 0)
-        const int slot = row0 + row;
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int r = it * 4 + (lane >> 3), j = lane & 7;
-          const int rslot = __shfl_sync(0xffffffffu, slot, r);
-          if (r < wrows)
-            *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(rslot) * p.H + n * BN + ch * 64 + j * 8) =
-                stg[r * 8 + (j ^ (r & 7))];
-        }
-        __syncwarp();
       }
     }
-    if (MODE == MODE_GATEUP && lane == 0) bulk_wait_group0();  // this warp's TMA stores have completed
-    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -354,19 +435,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
-}
-
-// fp32 [outer][inner] tensor in [32 rows][32 columns] boxes, 128-byte swizzle (a of the Gate/Up)
-static bool encode_f32_box32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer) {
-  EncodeTiledFn fn = get_encode_tiled();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner * 4};
-  const cuuint32_t box[2] = {32, 32};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 static bool encode_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_rows) {
@@ -390,16 +458,15 @@ static cudaError_t smem_attr() {
 
 }  // namespace gb
 
-cudaError_t launch_gateup_blockwise(const GroupedArgs& a, const float* xs_scale, cudaStream_t s) {
+cudaError_t launch_gateup_blockwise(const GroupedArgs& a, const float* xs_scale, float* h_scale, cudaStream_t s) {
   using namespace gb;
   if (a.R <= 0) return cudaSuccess;
   cudaError_t err = smem_attr<MODE_GATEUP>();
   if (err != cudaSuccess) return err;
   const int sms = num_sms();
   if (sms <= 0) return cudaErrorNoDevice;
-  CUtensorMap tma, tmb, tmo, tmbs;
-  if (!encode_u8(&tma, a.xs, a.H, a.R, BM) || !encode_u8(&tmb, a.w1, a.H, static_cast<uint64_t>(a.E) * 2 * a.I, BN / 2) ||
-      !encode_f32_box32(&tmo, a.a_f32, a.I, a.R))
+  CUtensorMap tma, tmb, tmbs;
+  if (!encode_u8(&tma, a.xs, a.H, a.R, BM) || !encode_u8(&tmb, a.w1, a.H, static_cast<uint64_t>(a.E) * 2 * a.I, BN / 2))
     return cudaErrorInvalidValue;
   tmbs = tmb;
   if (a.S > 0 && !encode_u8(&tmbs, a.w1s, a.H, static_cast<uint64_t>(a.S) * 2 * a.I, BN / 2))
@@ -417,13 +484,14 @@ cudaError_t launch_gateup_blockwise(const GroupedArgs& a, const float* xs_scale,
   p.w_scale = a.w1_scale;
   p.w_scale2 = a.w1s_scale;
   p.E = a.E;
-  p.out_f32 = static_cast<float*>(a.a_f32);
+  p.h = static_cast<uint8_t*>(a.h);
+  p.h_scale = h_scale;
   p.hdr = a.hdr;
-  const long long units = static_cast<long long>(a.max_tiles) * p.nN;
-  const int grid = static_cast<int>(units < sms ? units : sms);
+  const long long items = static_cast<long long>(a.max_tiles) * ((p.nN + 1) / 2);
+  const int grid = static_cast<int>(items < sms ? items : sms);
   stage_begin("gateup_gemm", s);
   err = launch_dependent(grouped_blockwise_kernel<MODE_GATEUP>, dim3(grid), dim3(THREADS), smem_bytes(MODE_GATEUP), s,
-                         tma, tmb, tmo, tmbs, p);
+                         tma, tmb, tma, tmbs, p);
   stage_end(s);
   return err;
 }

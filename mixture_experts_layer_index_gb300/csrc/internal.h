@@ -131,8 +131,9 @@ struct GroupedArgs {
 cudaError_t launch_gateup_bf16(const GroupedArgs& a, cudaStream_t s);  // bf16 or e4m3 (a.f8)
 cudaError_t launch_down_bf16(const GroupedArgs& a, cudaStream_t s);
 // 128x128-blockwise FP8 grouped GEMMs (grouped_blockwise.cu): xs / h hold e4m3
-// codes, their scales [R, H/128] / [R, I/128] in sorted row order.
-cudaError_t launch_gateup_blockwise(const GroupedArgs& a, const float* xs_scale, cudaStream_t s);
+// codes, their scales [R, H/128] / [R, ceil(I/128)] in sorted row order; the
+// Gate/Up quantises h and writes its scales itself.
+cudaError_t launch_gateup_blockwise(const GroupedArgs& a, const float* xs_scale, float* h_scale, cudaStream_t s);
 cudaError_t launch_down_blockwise(const GroupedArgs& a, const float* h_scale, cudaStream_t s);
 
 // MXFP8 grouped path (mx.cu).  Blocked scale tensors hold (C + 3) / 4 blocks of

@@ -153,6 +153,7 @@ constexpr int kAutoRouteDirectMaxTokensBlockwise = 64;
 static moe_path resolve_path(const moe_problem& p, int S = 0) {
   if (p.path != MOE_PATH_AUTO) return p.path;
   if (p.quant == MOE_BF16 || p.quant == MOE_MXFP8 || S > 0) return MOE_PATH_GROUPED;
+  if (p.H % 128 || (p.quant == MOE_FP8_BLOCK128 && p.I % 128)) return MOE_PATH_GROUPED;
   const int limit = p.quant == MOE_FP8_BLOCK128 ? kAutoRouteDirectMaxTokensBlockwise
                                                 : kAutoRouteDirectMaxTokensPerTensor;
   if (p.T > limit || static_cast<long long>(p.T) * p.k > kRouteDirectMaxRoutes) return MOE_PATH_GROUPED;
@@ -189,10 +190,10 @@ static moe_status validate_shape(const moe_problem& p, int S = 0) {
     return MOE_ERR_UNSUPPORTED;
   if (p.quant == MOE_BF16) {
     if (p.H % 64 || p.I % 64) return MOE_ERR_UNSUPPORTED;
-  } else if (p.quant == MOE_FP8_PER_TENSOR || p.quant == MOE_MXFP8) {
+  } else if (p.quant == MOE_FP8_PER_TENSOR) {
+    if (p.H % 64 || p.I % 64) return MOE_ERR_UNSUPPORTED;
+  } else {  // blockwise FP8 (x scales per 128 columns of H) and MXFP8
     if (p.H % 128 || p.I % 64) return MOE_ERR_UNSUPPORTED;
-  } else {
-    if (p.H % 128 || p.I % 128) return MOE_ERR_UNSUPPORTED;
   }
   if (S < 0) return MOE_ERR_INVALID_ARG;
   if (S > kMaxShared) return MOE_ERR_UNSUPPORTED;
@@ -200,6 +201,9 @@ static moe_status validate_shape(const moe_problem& p, int S = 0) {
   const moe_path path = resolve_path(p, S);
   if (path == MOE_PATH_ROUTE_DIRECT) {
     if (p.quant == MOE_BF16 || p.quant == MOE_MXFP8 || S > 0) return MOE_ERR_UNSUPPORTED;
+    // the route-direct kernels split K in whole 128-byte boxes and work on whole
+    // 128-column groups of I (blockwise)
+    if (p.H % 128 || (p.quant == MOE_FP8_BLOCK128 && p.I % 128)) return MOE_ERR_UNSUPPORTED;
     if (static_cast<long long>(p.T) * p.k > kRouteDirectMaxRoutes) return MOE_ERR_UNSUPPORTED;
     // shared-memory staging of one work item's operand rows
     if (p.I > 4096 || p.H / route_direct_splits(p) > 4096) return MOE_ERR_UNSUPPORTED;
@@ -236,9 +240,9 @@ bool plan_forward(const moe_problem& p, ForwardLayout* out, int S) {
     const size_t eb = p.quant == MOE_BF16 ? 2 : 1;  // bytes per element of the GEMM inputs
     L.xs = take(RS * H * eb);
     if (p.quant == MOE_FP8_BLOCK128) L.xs_scale = take(RS * (H / 128) * 4);
-    if (p.quant == MOE_FP8_PER_TENSOR || p.quant == MOE_FP8_BLOCK128) L.a32 = take(RS * I * 4);
+    if (p.quant == MOE_FP8_PER_TENSOR) L.a32 = take(RS * I * 4);
     L.h = take(RS * I * eb);
-    if (p.quant == MOE_FP8_BLOCK128) L.sh = take(RS * (I / 128) * 4);
+    if (p.quant == MOE_FP8_BLOCK128) L.sh = take(RS * ((I + 127) / 128) * 4);
     if (p.quant == MOE_MXFP8) {
       const int Hc = p.H / 32, Ic = p.I / 32;
       L.xs_sc = take(RS * Hc);
@@ -478,7 +482,7 @@ moe_status moe_forward_ex(const moe_problem* pp, const moe_forward_options* opt,
       g.f8 = f8 || blockwise;
       g.w1_scale = w1_scale;
       g.w2_scale = w2_scale;
-      g.a_f32 = g.f8 ? at<void*>(ws, L.a32) : nullptr;
+      g.a_f32 = f8 ? at<void*>(ws, L.a32) : nullptr;
       if (mxfp8) g.f8 = true;
       g.xs = gather4 ? nullptr : xs;
       g.perm = perm; g.tiles = tiles; g.num_tiles = num_tiles; g.max_tiles = L.max_tiles;
@@ -506,8 +510,7 @@ moe_status moe_forward_ex(const moe_problem* pp, const moe_forward_options* opt,
         if (e == cudaSuccess) e = launch_mx_blocked_tiles(h_sc, Ic, tiles, num_tiles, L.max_tiles, h_sf, s);
         if (e == cudaSuccess) e = launch_down_mx(g, h_sf, w2_sf, w2s_sf, s);
       } else if (blockwise) {
-        e = launch_gateup_blockwise(g, xs_scale, s);
-        if (e == cudaSuccess) e = launch_quant_groups(static_cast<const float*>(g.a_f32), g.h, sh, g.R, p.I, s);
+        e = launch_gateup_blockwise(g, xs_scale, sh, s);
         if (e == cudaSuccess) e = launch_down_blockwise(g, sh, s);
       } else {
         e = launch_gateup_bf16(g, s);

@@ -516,6 +516,10 @@ FP8_BLOCK_GROUPED = [
     W.Workload("f8b_ragged", 300, 16, 4, 384, 384, W.QUANT_FP8_BLOCK, 52),  # 6 Gate/Up N tiles, 3 Down N tiles
     W.Workload("f8b_tiny", 5, 8, 2, 256, 128, W.QUANT_FP8_BLOCK, 53),
     W.Workload("f8b_onexp", 130, 1, 1, 128, 128, W.QUANT_FP8_BLOCK, 54),  # one K block each way, 2 row tiles
+    # a last scale group of I with 64 columns (the route-MMA page's dispatch admits I % 64 == 0):
+    # a single Gate/Up unit for that group, a half K block in the Down GEMM
+    W.Workload("f8b_i320", 300, 16, 4, 384, 320, W.QUANT_FP8_BLOCK, 56),
+    W.Workload("f8b_i64", 70, 8, 2, 256, 64, W.QUANT_FP8_BLOCK, 58),
 ]
 
 
@@ -782,3 +786,19 @@ def test_mxfp8_route_direct_is_rejected(m):
     p = m.problem(2, 16, 4, 256, 128, "mxfp8", m.MOE_PATH_ROUTE_DIRECT)
     assert m.moe_workspace_size(p) == 0
     assert m.moe_select_path(m.problem(2, 16, 4, 256, 128, "mxfp8")) == m.MOE_PATH_GROUPED
+
+
+@pytest.mark.parametrize("wl", [W.Workload("f8b_qwen_i192", 512, 128, 8, 2048, 192, W.QUANT_FP8_BLOCK, 57),
+                                W.Workload("f8t_hunyuan_h4032", 512, 192, 8, 4032, 192, W.QUANT_FP8_TENSOR, 47)],
+                         ids=lambda w: w.name)
+def test_forward_page_admitted_shapes(m, wl):
+    """Shapes the route-MMA page's dispatch admits beyond this library's first
+    limits: blockwise FP8 with I % 128 == 64 and per-tensor FP8 with H % 128 == 64
+    (grouped path; AUTO takes it for these shapes at any T)."""
+    inp = W.make_inputs(wl)
+    p, y, ws = run_forward(m, wl, _dev(inp))
+    assert m.moe_select_path(p) == m.MOE_PATH_GROUPED
+    assert m.moe_select_path(m.problem(1, wl.E, wl.k, wl.H, wl.I, wl.quant)) == m.MOE_PATH_GROUPED
+    ref = O.forward(*oracle_args(inp), wl.k, wl.quant)
+    _check_routing_views(m, wl, p, ws, ref, inp)
+    _check_y(wl, y, ref["y"])
