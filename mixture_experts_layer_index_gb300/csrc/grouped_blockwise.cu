@@ -10,8 +10,7 @@
 // s_a[row, kb] * s_w[block, kb] and add it into fp32 registers ("promotion")
 // while the MMA fills the next buffers.  Two warps share each 32-lane TMEM
 // quadrant (one accumulator row per thread), each holding 64 of the 128
-// columns; a warp loads its two 32-column halves one after the other and runs
-// the FMAs of each half while the next half's load is in flight.
+// columns, so the loads of one warp overlap the FMAs of the other.
 //
 // Gate/Up: N = 64 gate + the matching 64 up rows of W1[e] (two 64-row TMA
 //   boxes), A = expert-sorted e4m3 x rows with their group scales.  Work items
@@ -93,13 +92,17 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
   return r;
 }
 
-// 32 values / s -> 32 e4m3 codes (IEEE division, RNE, saturating), as two 16-byte stores.
-__device__ __forceinline__ void store_e4m3x32(uint8_t* dst, const float* a, float s) {
+// 32 values * inv -> 32 e4m3 codes (RNE, saturating), as two 16-byte stores.  inv is
+// the correctly rounded 1 / s: a * inv can differ from the quotient a / s by one fp32
+// ulp, which changes an e4m3 code only for a value within one ulp of a rounding
+// midpoint (h's codes are not unique anyway: a itself carries the tensor cores'
+// summation order).
+__device__ __forceinline__ void store_e4m3x32(uint8_t* dst, const float* a, float inv) {
   uint32_t w[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
-    w[i] = static_cast<uint32_t>(cvt_e4m3x2(a[4 * i] / s, a[4 * i + 1] / s)) |
-           (static_cast<uint32_t>(cvt_e4m3x2(a[4 * i + 2] / s, a[4 * i + 3] / s)) << 16);
+    w[i] = static_cast<uint32_t>(cvt_e4m3x2(a[4 * i] * inv, a[4 * i + 1] * inv)) |
+           (static_cast<uint32_t>(cvt_e4m3x2(a[4 * i + 2] * inv, a[4 * i + 3] * inv)) << 16);
   reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
   reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
@@ -294,21 +297,6 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
         float sa_next = __ldg(sa), sg_next = __ldg(swg), su_next = __ldg(swu);
-        // Pipelined promotion: the first half of K block kb is in va when the loop body
-        // starts; the second half's load is issued, the first half's FMAs run, then the
-        // next block's first half is loaded while the second half's FMAs run.
-        float va[32], vb[32];
-        {
-          int good = 1;
-          if (lane == 0) good = mbar_wait(pfull0 + 8 * pb, pphase, abort_flag, p.hdr, 0x83000u | MODE);
-          if (!__shfl_sync(0xffffffffu, good, 0)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + pb * BN + c0, va);
-          tmem_ld_wait_regs(va);
-        }
         for (int kb = 0; kb < nk; ++kb) {
           const float sak = sa_next, sgk = sg_next, suk = su_next;
           if (kb + 1 < nk) {
@@ -316,33 +304,32 @@ __global__ void __launch_bounds__(THREADS, 1)
             sg_next = __ldg(swg + kb + 1);
             su_next = __ldg(swu + kb + 1);
           }
-          const float s0 = sak * sgk, s1 = sak * (MODE == MODE_GATEUP ? suk : sgk);
-          tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + pb * BN + c1, vb);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) acc[i] = fmaf(va[i], s0, acc[i]);
-          tmem_ld_wait_regs(vb);
-          // both halves of this buffer are in registers: hand it back to the MMA
+          int good = 1;
+          if (lane == 0) good = mbar_wait(pfull0 + 8 * pb, pphase, abort_flag, p.hdr, 0x83000u | MODE);
+          if (!__shfl_sync(0xffffffffu, good, 0)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + pb * BN;
+          float v0[32], v1[32];
+          tmem_ld32(tbase + c0, v0);
+          tmem_ld32(tbase + c1, v1);
+          tmem_ld_wait();
+          // both column ranges are in registers: hand the buffer back before the FMAs
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(pempty0 + 8 * pb);
+          const float s0 = sak * sgk, s1 = sak * (MODE == MODE_GATEUP ? suk : sgk);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            acc[i] = fmaf(v0[i], s0, acc[i]);
+            acc[32 + i] = fmaf(v1[i], s1, acc[32 + i]);
+          }
           if (++pb == NBUF) {
             pb = 0;
             pphase ^= 1;
           }
-          const bool more = kb + 1 < nk;
-          if (more) {
-            int good = 1;
-            if (lane == 0) good = mbar_wait(pfull0 + 8 * pb, pphase, abort_flag, p.hdr, 0x83000u | MODE);
-            if (!__shfl_sync(0xffffffffu, good, 0)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + pb * BN + c0, va);
-          }
-#pragma unroll
-          for (int i = 0; i < 32; ++i) acc[32 + i] = fmaf(vb[i], s1, acc[32 + i]);
-          if (more) tmem_ld_wait_regs(va);
         }
         if (!ok) break;
         if (MODE == MODE_GATEUP) {
@@ -386,22 +373,24 @@ __global__ void __launch_bounds__(THREADS, 1)
             xphase ^= 1;
             if (row < nrows) {
               const float sc = e4m3_scale(gm);
+              const float inv = 1.0f / sc;
               const size_t r = static_cast<size_t>(row0 + row);
               uint8_t* hrow = p.h + r * p.I;
               if (nsub == 2) {
-                float a0[32];
+                // the first unit's values, 4 at a time from the staging slot
+                uint32_t w[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                   const float4 v = stg[i ^ (lane & 7)];
-                  a0[4 * i] = v.x;
-                  a0[4 * i + 1] = v.y;
-                  a0[4 * i + 2] = v.z;
-                  a0[4 * i + 3] = v.w;
+                  w[i] = static_cast<uint32_t>(cvt_e4m3x2(v.x * inv, v.y * inv)) |
+                         (static_cast<uint32_t>(cvt_e4m3x2(v.z * inv, v.w * inv)) << 16);
                 }
-                store_e4m3x32(hrow + (2 * g) * 64 + ch * 32, a0, sc);
-                store_e4m3x32(hrow + (2 * g + 1) * 64 + ch * 32, a, sc);
+                uint4* d0 = reinterpret_cast<uint4*>(hrow + (2 * g) * 64 + ch * 32);
+                d0[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                d0[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                store_e4m3x32(hrow + (2 * g + 1) * 64 + ch * 32, a, inv);
               } else {
-                store_e4m3x32(hrow + (2 * g) * 64 + ch * 32, a, sc);
+                store_e4m3x32(hrow + (2 * g) * 64 + ch * 32, a, inv);
               }
               if (ch == 0) p.h_scale[r * ((p.I + 127) / 128) + g] = sc;
             }
