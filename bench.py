@@ -413,6 +413,30 @@ def oracle_single_thread():
     return res
 
 
+def gather4_ab(steps: int = 30):
+    """Same-box A/B of the two ways the bf16 Gate/Up GEMM gets its expert-sorted
+    activation rows at the prefill shape: the default (the scatter kernel writes
+    the sorted rows, the GEMM loads plain TMA tiles) against the fused gather
+    (the GEMM gathers x rows itself with TMA tile::gather4, selected by
+    MOE_GATEUP_A=gather4, which the library reads once per process).  Each arm is
+    a fresh process timing whole moe_forward calls (L2 flushed between calls)."""
+    out = {}
+    for arm, extra in (("sorted_rows", {}), ("gather4", {"MOE_GATEUP_A": "gather4"})):
+        env = dict(os.environ, **extra)
+        env.pop("RANK", None)
+        env.pop("WORLD_SIZE", None)
+        try:
+            r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--case", "prefill", "--steps",
+                                str(steps), "--warmup", "3"], env=env, capture_output=True, text=True, timeout=600)
+            line = json.loads(r.stdout.strip().splitlines()[-1])
+            out[arm] = {"us_per_call": line["us_median_eager"], "tokens_per_s": round(16384 / (line["us_median_eager"] * 1e-6), 1)}
+        except (subprocess.TimeoutExpired, ValueError, IndexError, OSError, KeyError) as exc:
+            out[arm] = {"error": str(exc)}
+    out["note"] = ("whole forward per call, median of the eager calls with L2 flushed before each; "
+                   "gather4 fuses the row gather into the GEMM's TMA loads")
+    return out
+
+
 def measure_fp8_peak(torch, dev, n: int = 8192):
     """Dense e4m3 GEMM throughput of the vendor library (torch._scaled_mm, bf16
     out), best of 10 x 5 back-to-back n^3 products: the FP8 roofline peak."""
@@ -657,6 +681,10 @@ def run_ours(args):
     if not args.no_fp8 and rank == 0:
         fp8 = run_fp8_prefill(m, torch, dev, measure_fp8_peak(torch, dev), peaks["bf16_tflops_sustained"])
 
+    gather_ab = None
+    if not args.no_gather_ab and rank == 0 and world == 1:
+        gather_ab = gather4_ab()
+
     cpu = cpu_1t = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(inp, wl, args.cpu_budget)
@@ -709,6 +737,7 @@ def run_ours(args):
         "gpu_launches": launches,
         "clocks": clocks,
         "wall_s_timed": round(wall_s, 3),
+        "gather_ab": gather_ab,
         "world16": w16,
         "decode": decode,
         "fp8_prefill": fp8,
@@ -822,6 +851,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 grouped prefill leg")
     ap.add_argument("--no-world16", action="store_true", help="skip the 16-expert top-8 bf16 layer")
+    ap.add_argument("--no-gather-ab", action="store_true", help="skip the gather4 A/B of the Gate/Up operand")
     ap.add_argument("--decode-reps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--tokens", type=int, default=0,
