@@ -544,36 +544,21 @@ __device__ void reduce_group(const DecodeArgs& a, const UniqView& uv, int g) {
     m = warp_max(m);
     if (lane == 0 && m > 0.0f) atomicMax(&a.hdr->amax_h, __float_as_uint(m));
   } else {
-    // one warp per (route, 128-column group), two tasks per pass so that their
-    // split loads are in flight together
     const int ngi = I / 128;
-    const int ntask = nn * ngi;
-    for (int t0 = warp; t0 < ntask; t0 += 2 * CONSUMERS) {
-      float gg[2][4], uu[2][4];
-      int rr[2], GG[2];
+    for (int task = warp; task < nn * ngi; task += CONSUMERS) {
+      const int n = task / ngi, G = task - n * ngi;
+      const int r = uv.routes()[r_beg + n];
+      float gg[4], uu[4], av[4];
+      sum_splits4_l2(a.part, a.splits, a.R, twoI, I, r, G * 128 + lane * 4, gg, uu);
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int task = min(t0 + j * CONSUMERS, ntask - 1);
-        const int n = task / ngi;
-        GG[j] = task - n * ngi;
-        rr[j] = uv.routes()[r_beg + n];
-        sum_splits4_l2(a.part, a.splits, a.R, twoI, I, rr[j], GG[j] * 128 + lane * 4, gg[j], uu[j]);
-      }
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        if (t0 + j * CONSUMERS >= ntask) break;
-        float av[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) av[q] = silu_mul(gg[j][q], uu[j][q]);
-        float m = fmaxf(fmaxf(fabsf(av[0]), fabsf(av[1])), fmaxf(fabsf(av[2]), fabsf(av[3])));
-        m = warp_max(m);
-        const float sc = e4m3_scale(m);
-        const uint32_t q = static_cast<uint32_t>(cvt_e4m3x2(av[0] / sc, av[1] / sc)) |
-                           (static_cast<uint32_t>(cvt_e4m3x2(av[2] / sc, av[3] / sc)) << 16);
-        *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.act) + static_cast<size_t>(rr[j]) * I + GG[j] * 128 +
-                                     lane * 4) = q;
-        if (lane == 0) a.sh[static_cast<size_t>(rr[j]) * ngi + GG[j]] = sc;
-      }
+      for (int q = 0; q < 4; ++q) av[q] = silu_mul(gg[q], uu[q]);
+      float m = fmaxf(fmaxf(fabsf(av[0]), fabsf(av[1])), fmaxf(fabsf(av[2]), fabsf(av[3])));
+      m = warp_max(m);
+      const float sc = e4m3_scale(m);
+      const uint32_t q = static_cast<uint32_t>(cvt_e4m3x2(av[0] / sc, av[1] / sc)) |
+                         (static_cast<uint32_t>(cvt_e4m3x2(av[2] / sc, av[3] / sc)) << 16);
+      *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.act) + static_cast<size_t>(r) * I + G * 128 + lane * 4) = q;
+      if (lane == 0) a.sh[static_cast<size_t>(r) * ngi + G] = sc;
     }
   }
 }
@@ -955,38 +940,17 @@ __global__ void __launch_bounds__(THREADS, 2) rd_down_kernel(const __grid_consta
           },
           [&](int) { return G; },
           [&](int hb) {
-            // 4 columns per thread; the rows of 4 routes are loaded before they are summed
-            constexpr int Q = ROWS_PER_CTA / 4;
-            for (int idx = threadIdx.x; idx < a.T * Q; idx += 32 * CONSUMERS) {
-              const int t = idx / Q, c = hb * ROWS_PER_CTA + (idx - t * Q) * 4;
-              float acc[4] = {0.f, 0.f, 0.f, 0.f};
-              for (int q0 = 0; q0 < a.k; q0 += 4) {
-                float4 v[4];
-                float wq[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  const int r = t * a.k + min(q0 + j, a.k - 1);
-                  wq[j] = __ldg(a.w + r);
-                  v[j] = __ldcg(reinterpret_cast<const float4*>(a.o + static_cast<size_t>(r) * H + c));
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  if (q0 + j < a.k) {
-                    acc[0] = fmaf(wq[j], v[j].x, acc[0]);
-                    acc[1] = fmaf(wq[j], v[j].y, acc[1]);
-                    acc[2] = fmaf(wq[j], v[j].z, acc[2]);
-                    acc[3] = fmaf(wq[j], v[j].w, acc[3]);
-                  }
-                }
+            for (int idx = threadIdx.x; idx < a.T * ROWS_PER_CTA; idx += 32 * CONSUMERS) {
+              const int t = idx / ROWS_PER_CTA, c = hb * ROWS_PER_CTA + (idx - t * ROWS_PER_CTA);
+              float acc = 0.0f;
+              for (int q = 0; q < a.k; ++q) {
+                const int r = t * a.k + q;
+                acc = fmaf(__ldg(a.w + r), __ldcg(a.o + static_cast<size_t>(r) * H + c), acc);
               }
-              const size_t yo = static_cast<size_t>(t) * H + c;
-              if (a.y_f32) {
-                *reinterpret_cast<float4*>(static_cast<float*>(a.y) + yo) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-              } else {
-                __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0], acc[1]), hi = __floats2bfloat162_rn(acc[2], acc[3]);
-                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.y) + yo) =
-                    make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
-              }
+              if (a.y_f32)
+                static_cast<float*>(a.y)[static_cast<size_t>(t) * H + c] = acc;
+              else
+                static_cast<__nv_bfloat16*>(a.y)[static_cast<size_t>(t) * H + c] = __float2bfloat16_rn(acc);
             }
           });
     }
