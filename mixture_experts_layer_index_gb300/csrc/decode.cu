@@ -563,13 +563,12 @@ __device__ void reduce_group(const DecodeArgs& a, const UniqView& uv, int g) {
   }
 }
 
-// Completion counting by the consumer warps for the n units their CTA touched:
-// unit j has counter cnt[key_of(j)], count_of(j) items done here and total_of(j)
-// items in all; follow(key) runs with every consumer thread for each unit this CTA
-// completed.  Skipped after an abort (the counts then never complete and the
-// status word reports the abort).
-template <typename KeyFn, typename CountFn, typename TotalFn, typename FollowFn>
-__device__ void complete_units(const StreamSmem& m, int32_t* cnt, int n, KeyFn key_of, CountFn count_of,
+// Completion counting by the consumer warps for the units [u_lo, u_hi] their CTA
+// touched (count_of(u) items each, total_of(u) items in all); calls follow(u) with
+// every consumer thread for each unit this CTA completed.  Skipped after an abort
+// (the counts then never complete and the status word reports the abort).
+template <typename CountFn, typename TotalFn, typename FollowFn>
+__device__ void complete_units(const StreamSmem& m, int32_t* cnt, int u_lo, int u_hi, CountFn count_of,
                                TotalFn total_of, FollowFn follow) {
   __shared__ int s_done[32 * CONSUMERS];
   __shared__ int s_ndone;
@@ -579,13 +578,13 @@ __device__ void complete_units(const StreamSmem& m, int32_t* cnt, int n, KeyFn k
   if (threadIdx.x == 0) s_abort = *m.abort_flag;
   consumer_sync();
   const bool aborted = s_abort != 0;
-  for (int base = 0; base < n; base += 32 * CONSUMERS) {
+  for (int base = u_lo; base <= u_hi; base += 32 * CONSUMERS) {
     if (threadIdx.x == 0) s_ndone = 0;
     consumer_sync();
-    const int j = base + static_cast<int>(threadIdx.x);
-    if (!aborted && j < n) {
-      const int c = count_of(j), key = key_of(j);
-      if (c > 0 && atomicAdd(cnt + key, c) + c == total_of(j)) s_done[atomicAdd(&s_ndone, 1)] = key;
+    const int u = base + static_cast<int>(threadIdx.x);
+    if (!aborted && u <= u_hi) {
+      const int c = count_of(u);
+      if (c > 0 && atomicAdd(cnt + u, c) + c == total_of(u)) s_done[atomicAdd(&s_ndone, 1)] = u;
     }
     consumer_sync();
     const int nd = s_ndone;
@@ -775,13 +774,11 @@ __global__ void __launch_bounds__(THREADS, 2) rd_gateup_kernel(const __grid_cons
     }
     // the CTA that finishes the last of a column group's items (all its K splits and
     // row blocks) sums the splits, applies SwiGLU and quantises the Down input
-    if (it1 > it0) {
-      const int g_lo = it0 / per_g;
+    if (it1 > it0)
       complete_units(
-          m, a.cnt, (it1 - 1) / per_g - g_lo + 1, [&](int j) { return g_lo + j; },
-          [&](int j) { return min(it1, (g_lo + j + 1) * per_g) - max(it0, (g_lo + j) * per_g); },
-          [&](int) { return per_g; }, [&](int g) { reduce_group<BLOCKWISE>(a, uv, g); });
-    }
+          m, a.cnt, it0 / per_g, (it1 - 1) / per_g,
+          [&](int g) { return min(it1, (g + 1) * per_g) - max(it0, g * per_g); }, [&](int) { return per_g; },
+          [&](int g) { reduce_group<BLOCKWISE>(a, uv, g); });
   }
   __syncthreads();
 }
@@ -933,13 +930,14 @@ __global__ void __launch_bounds__(THREADS, 2) rd_down_kernel(const __grid_consta
       const int s_lo = span >= nHB ? 0 : it0 % nHB;
       const int s_n = span >= nHB ? nHB : span;
       complete_units(
-          m, a.cnt + (max_uniq(a.R, a.E) + a.R / GROUP + 1), s_n, [&](int j) { return (s_lo + j) % nHB; },
+          m, a.cnt + (max_uniq(a.R, a.E) + a.R / GROUP + 1), 0, s_n - 1,
           [&](int j) {
             const int hb = (s_lo + j) % nHB;  // items it with it % nHB == hb in [it0, it1)
             return (it1 - hb + nHB - 1) / nHB - (it0 - hb + nHB - 1) / nHB;
           },
           [&](int) { return G; },
-          [&](int hb) {
+          [&](int j) {
+            const int hb = (s_lo + j) % nHB;
             for (int idx = threadIdx.x; idx < a.T * ROWS_PER_CTA; idx += 32 * CONSUMERS) {
               const int t = idx / ROWS_PER_CTA, c = hb * ROWS_PER_CTA + (idx - t * ROWS_PER_CTA);
               float acc = 0.0f;
