@@ -355,7 +355,7 @@ moe_status moe_read_device_status(const void* ws, moe_stream_t stream);
  *   measurement of the whole call brackets only the kernel it needs.
  * Stage names: route_rank (with the per-tensor FP8 amax of x), scan_tiles,
  * scatter_gather, gateup_gemm, quant_h, down_gemm, combine (grouped path);
- * rd_prep, rd_gateup, rd_down (route-direct path); scatter,
+ * rd_prep, rd_gateup, rd_reduce, rd_down, combine (route-direct path); scatter,
  * tile_map, header_reset. */
 typedef struct {
   char name[32];

@@ -20,18 +20,15 @@
 //               stage the group's e4m3 x slice when the group changes and feed
 //               16 weight rows each into mma.sync m16n8k32 e4m3 (weights on M,
 //               the group's routes on N); fp32 partials per split.
-//               The CTA that finishes the last item of a column group (its
-//               completion count, see complete_units) then sums the K splits,
-//               applies the scales and SwiGLU; blockwise mode quantises h per
-//               (route, 128 columns), per-tensor mode records the global amax
-//               of h.
+//   rd_reduce   sums the K splits, applies the scales and SwiGLU; blockwise
+//               mode quantises h per (route, 128 columns) here, per-tensor mode
+//               records the global amax of h.
 //   rd_down     persistent like rd_gateup over (column group, 64 rows of
 //               W2[e]), with 256-byte stages for rows of at most 256 bytes; h of
 //               the group's routes is quantised (per-tensor) or copied into
-//               shared memory; fp32 o in route order.  The CTA that finishes the
-//               last column group of a 64-column slice of H runs the contiguous
-//               top-k combine of that slice into y.
-// Three launches; the last two are programmatic dependents of their predecessor.
+//               shared memory; fp32 o in route order.
+//   combine     the contiguous top-k reduction shared with the grouped path.
+// All but rd_prep are launched as programmatic dependents of their predecessor.
 //
 // K permutation: a dot product does not depend on the order of its terms, so
 // each thread loads 16 consecutive bytes of a weight row and of x and feeds
@@ -176,10 +173,6 @@ __global__ void __launch_bounds__(1024) rd_prep_kernel(DecodeArgs a) {
     a.hdr->info = 0u;
     a.hdr->amax_x = 0u;
     a.hdr->amax_h = 0u;
-  }
-  {
-    const int ncnt = max_uniq(R, E) + R / GROUP + 1 + H / ROWS_PER_CTA;
-    for (int i = tid; i < ncnt; i += blockDim.x) a.cnt[i] = 0;
   }
   // x is quantised by warps 1..31 (NQ threads) while warp 0 builds the expert
   // table; their first batch of x loads goes out before the routing so that both
@@ -481,119 +474,6 @@ __device__ __forceinline__ void drain_ring(const StreamSmem& m, uint32_t stage, 
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * CONSUMERS) : "memory"); }
 
-// ------------------------------------------------------------------ completion tails
-// A kernel whose CTAs each finish a share of a unit of work (the K splits and row
-// blocks of a column group; the column groups of a 64-column slice of H) counts
-// the items it finished per unit with one atomicAdd per unit it touched, after a
-// device-scope fence of its own results; the CTA whose count completes a unit
-// runs that unit's follow-up (split reduction; combine) on the other CTAs'
-// results, read from L2.  No CTA ever waits for another.
-
-// Sum over the K splits of (route r, columns i .. i+3) of g and of u, splits in
-// ascending order (the order of the earlier separate reduction pass).
-__device__ __forceinline__ void sum_splits4_l2(const float* part, int splits, int R, int twoI, int I, int r, int i,
-                                               float (&g)[4], float (&u)[4]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) g[q] = u[q] = 0.f;
-  for (int s0 = 0; s0 < splits; s0 += 8) {
-    float4 gv[8], uv[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int s = s0 + j < splits ? s0 + j : 0;
-      const float* pp = part + (static_cast<size_t>(s) * R + r) * twoI;
-      gv[j] = __ldcg(reinterpret_cast<const float4*>(pp + i));
-      uv[j] = __ldcg(reinterpret_cast<const float4*>(pp + I + i));
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (s0 + j < splits) {
-        g[0] += gv[j].x; g[1] += gv[j].y; g[2] += gv[j].z; g[3] += gv[j].w;
-        u[0] += uv[j].x; u[1] += uv[j].y; u[2] += uv[j].z; u[3] += uv[j].w;
-      }
-    }
-  }
-}
-
-// Split reduction + SwiGLU + quantisation of column group g (up to 8 routes of one
-// expert) by the 4 consumer warps: per-tensor mode writes a (fp32) and folds its
-// amax into the header; blockwise mode quantises h per (route, 128 columns).
-template <bool BLOCKWISE>
-__device__ void reduce_group(const DecodeArgs& a, const UniqView& uv, int g) {
-  const int I = a.I, twoI = 2 * I;
-  const int u = uv.gu()[g], e = uv.expert()[u];
-  const int r_beg = uv.off()[u] + uv.gn0()[g];
-  const int nn = min(GROUP, uv.off()[u + 1] - r_beg);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (!BLOCKWISE) {
-    const float sc = a.sx[0] * __ldg(a.w1_scale + e);
-    float m = 0.0f;
-    const int q4 = I / 4;
-    for (int idx = threadIdx.x; idx < nn * q4; idx += 32 * CONSUMERS) {
-      const int n = idx / q4, i = (idx - n * q4) * 4;
-      const int r = uv.routes()[r_beg + n];
-      float gg[4], uu[4];
-      sum_splits4_l2(a.part, a.splits, a.R, twoI, I, r, i, gg, uu);
-      float4 av;
-      av.x = silu_mul(sc * gg[0], sc * uu[0]);
-      av.y = silu_mul(sc * gg[1], sc * uu[1]);
-      av.z = silu_mul(sc * gg[2], sc * uu[2]);
-      av.w = silu_mul(sc * gg[3], sc * uu[3]);
-      *reinterpret_cast<float4*>(static_cast<float*>(a.act) + static_cast<size_t>(r) * I + i) = av;
-      m = fmaxf(m, fmaxf(fmaxf(fabsf(av.x), fabsf(av.y)), fmaxf(fabsf(av.z), fabsf(av.w))));
-    }
-    m = warp_max(m);
-    if (lane == 0 && m > 0.0f) atomicMax(&a.hdr->amax_h, __float_as_uint(m));
-  } else {
-    const int ngi = I / 128;
-    for (int task = warp; task < nn * ngi; task += CONSUMERS) {
-      const int n = task / ngi, G = task - n * ngi;
-      const int r = uv.routes()[r_beg + n];
-      float gg[4], uu[4], av[4];
-      sum_splits4_l2(a.part, a.splits, a.R, twoI, I, r, G * 128 + lane * 4, gg, uu);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) av[q] = silu_mul(gg[q], uu[q]);
-      float m = fmaxf(fmaxf(fabsf(av[0]), fabsf(av[1])), fmaxf(fabsf(av[2]), fabsf(av[3])));
-      m = warp_max(m);
-      const float sc = e4m3_scale(m);
-      const uint32_t q = static_cast<uint32_t>(cvt_e4m3x2(av[0] / sc, av[1] / sc)) |
-                         (static_cast<uint32_t>(cvt_e4m3x2(av[2] / sc, av[3] / sc)) << 16);
-      *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.act) + static_cast<size_t>(r) * I + G * 128 + lane * 4) = q;
-      if (lane == 0) a.sh[static_cast<size_t>(r) * ngi + G] = sc;
-    }
-  }
-}
-
-// Completion counting by the consumer warps for the units [u_lo, u_hi] their CTA
-// touched (count_of(u) items each, total_of(u) items in all); calls follow(u) with
-// every consumer thread for each unit this CTA completed.  Skipped after an abort
-// (the counts then never complete and the status word reports the abort).
-template <typename CountFn, typename TotalFn, typename FollowFn>
-__device__ void complete_units(const StreamSmem& m, int32_t* cnt, int u_lo, int u_hi, CountFn count_of,
-                               TotalFn total_of, FollowFn follow) {
-  __shared__ int s_done[32 * CONSUMERS];
-  __shared__ int s_ndone;
-  __shared__ int s_abort;
-  consumer_sync();  // every consumer's results of this CTA are written
-  __threadfence();  // ... and visible device-wide before the counts
-  if (threadIdx.x == 0) s_abort = *m.abort_flag;
-  consumer_sync();
-  const bool aborted = s_abort != 0;
-  for (int base = u_lo; base <= u_hi; base += 32 * CONSUMERS) {
-    if (threadIdx.x == 0) s_ndone = 0;
-    consumer_sync();
-    const int u = base + static_cast<int>(threadIdx.x);
-    if (!aborted && u <= u_hi) {
-      const int c = count_of(u);
-      if (c > 0 && atomicAdd(cnt + u, c) + c == total_of(u)) s_done[atomicAdd(&s_ndone, 1)] = u;
-    }
-    consumer_sync();
-    const int nd = s_ndone;
-    if (nd > 0) __threadfence();  // the other CTAs' results are read after their counts
-    for (int j = 0; j < nd; ++j) follow(s_done[j]);
-    consumer_sync();
-  }
-}
-
 // ------------------------------------------------------------------ rd_gateup
 // Persistent: two CTAs per SM, each walking a contiguous range of work items
 // (column group g, K split s, 64 rows mb of W1[e]) ordered so that consecutive
@@ -772,15 +652,100 @@ __global__ void __launch_bounds__(THREADS, 2) rd_gateup_kernel(const __grid_cons
         }
       }
     }
-    // the CTA that finishes the last of a column group's items (all its K splits and
-    // row blocks) sums the splits, applies SwiGLU and quantises the Down input
-    if (it1 > it0)
-      complete_units(
-          m, a.cnt, it0 / per_g, (it1 - 1) / per_g,
-          [&](int g) { return min(it1, (g + 1) * per_g) - max(it0, g * per_g); }, [&](int) { return per_g; },
-          [&](int g) { reduce_group<BLOCKWISE>(a, uv, g); });
   }
   __syncthreads();
+}
+
+// Sum of the K-split partials of (route r, column i) and of (r, I + i); the
+// split loads are issued 8 at a time before they are added, in split order.
+__device__ __forceinline__ void sum_splits(const float* part, int splits, int R, int twoI, int I, int r, int i,
+                                           float& g, float& u) {
+  g = 0.f;
+  u = 0.f;
+  for (int s0 = 0; s0 < splits; s0 += 8) {
+    float gv[8], uv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int s = s0 + j < splits ? s0 + j : 0;
+      const float* pp = part + (static_cast<size_t>(s) * R + r) * twoI;
+      gv[j] = pp[i];
+      uv[j] = pp[I + i];
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (s0 + j < splits) {
+        g += gv[j];
+        u += uv[j];
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ rd_reduce
+// per-tensor: one thread per (route, i); blockwise: one warp per (route, 128-column group).
+// Four consecutive columns [i, i + 4) at once (i a multiple of 4): one 16-byte load
+// per split for g and for u, all splits of a batch in flight together; the sums
+// run over the splits in the same ascending order as sum_splits.
+__device__ __forceinline__ void sum_splits4(const float* part, int splits, int R, int twoI, int I, int r, int i,
+                                            float (&g)[4], float (&u)[4]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) g[q] = u[q] = 0.f;
+  for (int s0 = 0; s0 < splits; s0 += 8) {
+    float4 gv[8], uv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int s = s0 + j < splits ? s0 + j : 0;
+      const float* pp = part + (static_cast<size_t>(s) * R + r) * twoI;
+      gv[j] = *reinterpret_cast<const float4*>(pp + i);
+      uv[j] = *reinterpret_cast<const float4*>(pp + I + i);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (s0 + j < splits) {
+        g[0] += gv[j].x; g[1] += gv[j].y; g[2] += gv[j].z; g[3] += gv[j].w;
+        u[0] += uv[j].x; u[1] += uv[j].y; u[2] += uv[j].z; u[3] += uv[j].w;
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) rd_reduce_tensor_kernel(DecodeArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  const int I = a.I, twoI = 2 * I;
+  float av = 0.0f;
+  if (idx < a.R * I) {
+    const int r = idx / I, i = idx - (idx / I) * I;
+    float g, u;
+    sum_splits(a.part, a.splits, a.R, twoI, I, r, i, g, u);
+    const float sc = a.sx[0] * __ldg(a.w1_scale + a.ids[r]);
+    av = silu_mul(sc * g, sc * u);
+    static_cast<float*>(a.act)[idx] = av;
+  }
+  const float m = warp_max(fabsf(av));
+  if ((threadIdx.x & 31) == 0 && m > 0.0f) atomicMax(&a.hdr->amax_h, __float_as_uint(m));
+}
+
+__global__ void __launch_bounds__(256) rd_reduce_block_kernel(DecodeArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int I = a.I, twoI = 2 * I, ngi = I / 128;
+  if (gw >= a.R * ngi) return;
+  const int r = gw / ngi, G = gw - (gw / ngi) * ngi;
+  float av[4], g[4], u[4];
+  sum_splits4(a.part, a.splits, a.R, twoI, I, r, G * 128 + lane * 4, g, u);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) av[q] = silu_mul(g[q], u[q]);
+  float m = fmaxf(fmaxf(fabsf(av[0]), fabsf(av[1])), fmaxf(fabsf(av[2]), fabsf(av[3])));
+  m = warp_max(m);
+  const float sc = e4m3_scale(m);
+  const uint32_t q = static_cast<uint32_t>(cvt_e4m3x2(av[0] / sc, av[1] / sc)) |
+                     (static_cast<uint32_t>(cvt_e4m3x2(av[2] / sc, av[3] / sc)) << 16);
+  *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.act) + static_cast<size_t>(r) * I + G * 128 + lane * 4) = q;
+  if (lane == 0) a.sh[static_cast<size_t>(r) * ngi + G] = sc;
 }
 
 // ------------------------------------------------------------------ rd_down
@@ -922,46 +887,11 @@ __global__ void __launch_bounds__(THREADS, 2) rd_down_kernel(const __grid_consta
         }
       }
     }
-    // the CTA that finishes the last column group of a 64-column slice of H runs the
-    // top-k combine of that slice for every token: y[t, c] = sum_j w[t, j] o[t k + j, c],
-    // fp32, j ascending, rounded to bf16 once (or kept in fp32)
-    if (it1 > it0) {
-      const int span = it1 - it0;
-      const int s_lo = span >= nHB ? 0 : it0 % nHB;
-      const int s_n = span >= nHB ? nHB : span;
-      complete_units(
-          m, a.cnt + (max_uniq(a.R, a.E) + a.R / GROUP + 1), 0, s_n - 1,
-          [&](int j) {
-            const int hb = (s_lo + j) % nHB;  // items it with it % nHB == hb in [it0, it1)
-            return (it1 - hb + nHB - 1) / nHB - (it0 - hb + nHB - 1) / nHB;
-          },
-          [&](int) { return G; },
-          [&](int j) {
-            const int hb = (s_lo + j) % nHB;
-            for (int idx = threadIdx.x; idx < a.T * ROWS_PER_CTA; idx += 32 * CONSUMERS) {
-              const int t = idx / ROWS_PER_CTA, c = hb * ROWS_PER_CTA + (idx - t * ROWS_PER_CTA);
-              float acc = 0.0f;
-              for (int q = 0; q < a.k; ++q) {
-                const int r = t * a.k + q;
-                acc = fmaf(__ldg(a.w + r), __ldcg(a.o + static_cast<size_t>(r) * H + c), acc);
-              }
-              if (a.y_f32)
-                static_cast<float*>(a.y)[static_cast<size_t>(t) * H + c] = acc;
-              else
-                static_cast<__nv_bfloat16*>(a.y)[static_cast<size_t>(t) * H + c] = __float2bfloat16_rn(acc);
-            }
-          });
-    }
   }
   __syncthreads();
 }
 
 }  // namespace rd
-
-size_t route_direct_counter_words(int T, int E, int k, int H) {
-  const int R = T * k;
-  return static_cast<size_t>(rd::max_uniq(R, E) + R / rd::GROUP + 1 + H / rd::ROWS_PER_CTA);
-}
 
 size_t route_direct_uniq_bytes(int T, int E, int k) {
   const int R = T * k;
@@ -1073,6 +1003,18 @@ cudaError_t launch_route_direct(const DecodeArgs& a, cudaStream_t s) {
     const cudaLaunchConfig_t c = config(static_cast<unsigned>(items < sms ? items : sms), THREADS, smem_gu);
     err = bw ? cudaLaunchKernelEx(&c, rd_gateup_kernel<true>, tm1, tm2, a, nMB, a.splits, KS, down_grid)
              : cudaLaunchKernelEx(&c, rd_gateup_kernel<false>, tm1, tm2, a, nMB, a.splits, KS, down_grid);
+  }
+  stage_end(s);
+  if (err != cudaSuccess) return err;
+
+  stage_begin("rd_reduce", s);
+  if (bw) {
+    const int warps = a.R * (a.I / 128);
+    const cudaLaunchConfig_t c = config((warps * 32 + 255) / 256, 256, 0);
+    err = cudaLaunchKernelEx(&c, rd_reduce_block_kernel, a);
+  } else {
+    const cudaLaunchConfig_t c = config((a.R * a.I + 255) / 256, 256, 0);
+    err = cudaLaunchKernelEx(&c, rd_reduce_tensor_kernel, a);
   }
   stage_end(s);
   if (err != cudaSuccess) return err;

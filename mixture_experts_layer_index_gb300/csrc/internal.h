@@ -56,7 +56,6 @@ struct ForwardLayout {
   size_t uniq = 0;    // unique-expert table (see decode.cu)
   size_t part = 0;    // [S, R, 2I] fp32 split-K partials of Gate/Up
   size_t act = 0;     // per-tensor: [R, I] fp32 a;  blockwise: [R, I] e4m3 h
-  size_t cnt = 0;     // route-direct completion counters
   size_t sh = 0;      // blockwise (both paths): [R, I/128] fp32 scales of h
   // MXFP8 (grouped): E8M0 scale codes, row-major and in the blocked layout
   size_t xs_sc = 0, xs_sf = 0;  // x rows [R, H/32]; blocked per tile
@@ -196,17 +195,9 @@ struct DecodeArgs {
   float* o;
   int splits;
   DeviceHeader* hdr;
-  // completion counters (zeroed by the prep kernel): per column group of the
-  // Gate/Up and per 64-column slice of H of the Down; the last CTA to finish a
-  // group runs its split reduction, the last to finish a slice its combine
-  int32_t* cnt;
-  void* y;      // [T, H] bf16, or fp32 when y_f32
-  int y_f32;
 };
 cudaError_t launch_route_direct(const DecodeArgs& a, cudaStream_t s);
 size_t route_direct_uniq_bytes(int T, int E, int k);
-// Completion counters of the route-direct path (int32 words).
-size_t route_direct_counter_words(int T, int E, int k, int H);
 
 // Launch `kernel` as a programmatic dependent of the previous work on the stream:
 // its launch is prepared while the predecessor runs, and it waits for the

@@ -266,7 +266,6 @@ bool plan_forward(const moe_problem& p, ForwardLayout* out, int S) {
     L.act = take(R * I * 4);
     L.sh = take(p.quant == MOE_FP8_BLOCK128 ? R * (I / 128) * 4 : 16);
     L.o = take(R * H * 4);
-    L.cnt = take(route_direct_counter_words(p.T, p.E, p.k, p.H) * 4);
   }
   L.total = off;
   *out = L;
@@ -544,10 +543,12 @@ moe_status moe_forward_ex(const moe_problem* pp, const moe_forward_options* opt,
     d.o = at<float*>(ws, L.o);
     d.splits = L.splits;
     d.hdr = hdr;
-    d.cnt = at<int32_t*>(ws, L.cnt);
-    d.y = y;
-    d.y_f32 = o.y_fp32;
-    e = launch_route_direct(d, s);  // the Down kernel's last CTA per column slice runs the combine
+    e = launch_route_direct(d, s);
+    if (e == cudaSuccess) {
+      CombineArgs c{p.T, p.k, p.H, d.o, true, w, y, nullptr};
+      c.y_f32 = o.y_fp32 != 0;
+      e = launch_combine_pdl(c, s);
+    }
   }
   return from_cuda(e);
 }
