@@ -481,23 +481,31 @@ def run_fp8_prefill(m, torch, dev, fp8_peak, bf16_sustained: float, steps: int =
              "w1_scale": s1, "w2_scale": s2}
         del w1, w2, s1, s2
         p = m.problem(wl.T, wl.E, wl.k, wl.H, wl.I, wl.quant, m.MOE_PATH_GROUPED)
-        ws = torch.empty(m.moe_workspace_size(p), dtype=torch.uint8, device=dev)
+        opt = None
+        s1, s2 = d["w1_scale"], d["w2_scale"]
+        if quant == W.QUANT_MXFP8:
+            # the weights' MX scales are converted to the blocked layout once, as at load time
+            s1 = torch.empty(m.moe_mx_weight_scales_bytes(wl.E, wl.H, wl.I, 1), dtype=torch.uint8, device=dev)
+            s2 = torch.empty(m.moe_mx_weight_scales_bytes(wl.E, wl.H, wl.I, 2), dtype=torch.uint8, device=dev)
+            m.moe_mx_weight_scales(d["w1_scale"], d["w2_scale"], wl.E, wl.H, wl.I, s1, s2)
+            opt = m.forward_options(mx_weight_scales_blocked=True)
+        ws = torch.empty(m.moe_workspace_size_ex(p, opt), dtype=torch.uint8, device=dev)
         y = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
-        args = (p, d["x"], d["scores"], d["w1"], d["w2"], d["w1_scale"], d["w2_scale"], y, ws)
+        args = (p, opt, d["x"], d["scores"], d["w1"], d["w2"], s1, s2, y, ws)
         for _ in range(5):
-            m.moe_forward(*args)
+            m.moe_forward_ex(*args)
         torch.cuda.synchronize()
         # step time without per-kernel events, then the stages from a profiled pass
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for _ in range(steps):
-            m.moe_forward(*args)
+            m.moe_forward_ex(*args)
         e1.record()
         torch.cuda.synchronize()
         step_us = e0.elapsed_time(e1) / steps * 1000.0
         m.moe_profile_start()
         for _ in range(steps):
-            m.moe_forward(*args)
+            m.moe_forward_ex(*args)
         torch.cuda.synchronize()
         stages = m.moe_profile_stop()
         if m.moe_read_device_status(ws) != m.MOE_OK:

@@ -251,11 +251,28 @@ typedef struct {
   const float* w1_shared_scale;
   const float* w2_shared_scale;
   int y_fp32;
+  int mx_weight_scales_blocked; /* MXFP8: 1 = the weight scale pointers (routed and shared) hold
+                                   the blocked layouts of moe_mx_weight_scales instead of the
+                                   row-major E8M0 codes (no per-call conversion) */
 } moe_forward_options;
 size_t moe_workspace_size_ex(const moe_problem* p, const moe_forward_options* opt);
 moe_status moe_forward_ex(const moe_problem* p, const moe_forward_options* opt, const void* x, const float* scores,
                           const void* w1, const void* w2, const float* w1_scale, const float* w2_scale, void* y,
                           void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* moe_mx_weight_scales - the MXFP8 weights' scales in the blocked layout the
+ * forward's block-scaled MMAs read, converted once (e.g. when the weights are
+ * loaded) instead of on every call (moe_forward_options.mx_weight_scales_blocked).
+ *   w1_scale [E, 2I, H/32], w2_scale [E, H, I/32] uint8 E8M0 codes (4-byte aligned)
+ *   w1_blocked, w2_blocked  outputs of moe_mx_weight_scales_bytes(E, H, I, 1 / 2)
+ *                           bytes (16-byte aligned): W1 in blocks of 64 gate rows
+ *                           and the matching 64 up rows of one expert, W2 in
+ *                           blocks of 128 rows, each the 512-byte blocks of
+ *                           moe_mx_blocked_scales.
+ * Errors: INVALID_ARG, UNSUPPORTED (the MXFP8 shape limits), CUDA. */
+size_t moe_mx_weight_scales_bytes(int E, int H, int I, int which);
+moe_status moe_mx_weight_scales(const uint8_t* w1_scale, const uint8_t* w2_scale, int E, int H, int I,
+                                uint8_t* w1_blocked, uint8_t* w2_blocked, moe_stream_t stream);
 
 /* moe_round_bf16 - y[i] = bf16(y32[i]) for i < n (round to nearest even): the
  * single rounding of a sum of partial outputs (moe_forward_ex, y_fp32 = 1).

@@ -54,7 +54,8 @@ class moe_views(ctypes.Structure):
 
 class moe_forward_options(ctypes.Structure):
     _fields_ = [("n_shared", ctypes.c_int), ("w1_shared", ctypes.c_void_p), ("w2_shared", ctypes.c_void_p),
-                ("w1_shared_scale", ctypes.c_void_p), ("w2_shared_scale", ctypes.c_void_p), ("y_fp32", ctypes.c_int)]
+                ("w1_shared_scale", ctypes.c_void_p), ("w2_shared_scale", ctypes.c_void_p), ("y_fp32", ctypes.c_int),
+                ("mx_weight_scales_blocked", ctypes.c_int)]
 
 
 class moe_stage_time(ctypes.Structure):
@@ -79,6 +80,8 @@ _SIGS = {
     "moe_forward_views_ex": (_i, [_P, _O, _vp, _sz, ctypes.POINTER(moe_views)]),
     "moe_round_bf16": (_i, [_vp, _vp, _sz, _vp]),
     "moe_mx_blocked_bytes": (_sz, [_i, _i, _i]),
+    "moe_mx_weight_scales_bytes": (_sz, [_i, _i, _i, _i]),
+    "moe_mx_weight_scales": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp]),
     "moe_mx_blocked_workspace_size": (_sz, [_i, _i]),
     "moe_mx_blocked_scales": (_i, [_vp, _i, _i, _vp, _i, _vp, _sz, _vp, _vp, _sz, _vp]),
     "moe_read_device_status": (_i, [_vp, _vp]),
@@ -196,9 +199,9 @@ def moe_forward(p: moe_problem, x, scores, w1, w2, w1_scale, w2_scale, y, ws, ws
 
 
 def forward_options(n_shared=0, w1_shared=None, w2_shared=None, w1_shared_scale=None, w2_shared_scale=None,
-                    y_fp32=False) -> moe_forward_options:
+                    y_fp32=False, mx_weight_scales_blocked=False) -> moe_forward_options:
     return moe_forward_options(int(n_shared), _ptr(w1_shared), _ptr(w2_shared), _ptr(w1_shared_scale),
-                               _ptr(w2_shared_scale), 1 if y_fp32 else 0)
+                               _ptr(w2_shared_scale), 1 if y_fp32 else 0, 1 if mx_weight_scales_blocked else 0)
 
 
 def _opt_ref(opt):
@@ -228,6 +231,16 @@ def moe_forward_views_ex(p: moe_problem, opt: Optional[moe_forward_options], ws,
 def moe_round_bf16(y32, y, n=None, stream=None) -> None:
     n = y32.numel() if n is None else n
     _check(lib().moe_round_bf16(_ptr(y32), _ptr(y), n, _stream(stream)), "moe_round_bf16")
+
+
+def moe_mx_weight_scales_bytes(E: int, H: int, I: int, which: int) -> int:
+    return int(lib().moe_mx_weight_scales_bytes(E, H, I, which))
+
+
+def moe_mx_weight_scales(w1_scale, w2_scale, E, H, I, w1_blocked, w2_blocked, stream=None) -> None:
+    """MXFP8 weight scales converted once into the forward's blocked layouts."""
+    _check(lib().moe_mx_weight_scales(_ptr(w1_scale), _ptr(w2_scale), E, H, I, _ptr(w1_blocked), _ptr(w2_blocked),
+                                     _stream(stream)), "moe_mx_weight_scales")
 
 
 def moe_mx_blocked_bytes(rows: int, cols: int, groups: int) -> int:

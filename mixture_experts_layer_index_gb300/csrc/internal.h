@@ -61,6 +61,7 @@ struct ForwardLayout {
   size_t xs_sc = 0, xs_sf = 0;  // x rows [R, H/32]; blocked per tile
   size_t h_sc = 0, h_sf = 0;    // h rows [R, I/32]; blocked per tile
   size_t w1_sf = 0, w2_sf = 0, w1s_sf = 0, w2s_sf = 0;  // blocked weight scales (routed, shared)
+  size_t padbase = 0;           // [E + S] int32: padded-row offset of each expert's rows
   int splits = 1;
   size_t total = 0;
 };
@@ -79,7 +80,8 @@ cudaError_t launch_route_rank(const float* scores, const int32_t* ids_in, int T,
 // expert s, numbered expert E + s, over rows [Rr + s*T, Rr + (s+1)*T) (Rr = T*k).
 cudaError_t launch_scan_tiles(int32_t* blockcounts, int nblk, int E, int32_t* counts, int32_t* offsets,
                               int32_t* tiles, int32_t* num_tiles, int max_tiles, int BM, int32_t* tile_scratch,
-                              DeviceHeader* hdr, cudaStream_t s, int T = 0, int S = 0, int Rr = 0);
+                              DeviceHeader* hdr, cudaStream_t s, int T = 0, int S = 0, int Rr = 0,
+                              int32_t* padbase = nullptr);
 cudaError_t launch_scatter(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E, int k,
                            int32_t* perm, int32_t* inv, cudaStream_t s);
 // The scatter-gather kernels also copy each token's row to rows R + s*T + t of
@@ -139,9 +141,11 @@ cudaError_t launch_down_blockwise(const GroupedArgs& a, const float* h_scale, cu
 // MXFP8 grouped path (mx.cu).  Blocked scale tensors hold (C + 3) / 4 blocks of
 // 512 bytes per 128-row block (mx_blocked_bytes).
 size_t mx_blocked_bytes(size_t blocks, int C);
+// Also writes each row's scales straight into the blocked layout xs_sf (row p of
+// expert e at padded row p + padbase[e]).
 cudaError_t launch_scatter_gather_mx(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
-                                     int k, int H, const void* x, void* xs, uint8_t* xs_sc, int32_t* perm,
-                                     int32_t* inv, cudaStream_t s, int S = 0);
+                                     int k, int H, const void* x, void* xs, uint8_t* xs_sc, uint8_t* xs_sf,
+                                     const int32_t* padbase, int32_t* perm, int32_t* inv, cudaStream_t s, int S = 0);
 // Row-major scales [rows, C] -> blocked layout, one block per tile of the tile map.
 cudaError_t launch_mx_blocked_tiles(const uint8_t* sc, int C, const int32_t* tiles, const int32_t* num_tiles,
                                     int max_tiles, uint8_t* out, cudaStream_t s);
@@ -154,8 +158,9 @@ cudaError_t launch_mx_blocked_weights(const uint8_t* w1_sc, const uint8_t* w2_sc
 cudaError_t launch_mx_group_blocked(const uint8_t* sc, int rows, int C, const int32_t* goff, int G, uint8_t* out,
                                     int32_t* starts, int32_t* tiles, int32_t* num_tiles, int max_tiles,
                                     DeviceHeader* hdr, cudaStream_t s);
+// Gate/Up writes h's scales straight into the blocked layout h_sf (block row = tile).
 cudaError_t launch_gateup_mx(const GroupedArgs& a, const uint8_t* xs_sf, const uint8_t* w1_sf, const uint8_t* w1s_sf,
-                             uint8_t* h_sc, cudaStream_t s);
+                             uint8_t* h_sf, cudaStream_t s);
 cudaError_t launch_down_mx(const GroupedArgs& a, const uint8_t* h_sf, const uint8_t* w2_sf, const uint8_t* w2s_sf,
                            cudaStream_t s);
 

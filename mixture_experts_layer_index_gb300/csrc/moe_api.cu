@@ -247,8 +247,8 @@ bool plan_forward(const moe_problem& p, ForwardLayout* out, int S) {
       const int Hc = p.H / 32, Ic = p.I / 32;
       L.xs_sc = take(RS * Hc);
       L.xs_sf = take(mx_blocked_bytes(L.max_tiles, Hc));
-      L.h_sc = take(RS * Ic);
       L.h_sf = take(mx_blocked_bytes(L.max_tiles, Ic));
+      L.padbase = take((E + S) * 4);
       L.w1_sf = take(mx_blocked_bytes(E * (I / 64), Hc));
       L.w2_sf = take(mx_blocked_bytes(E * (H / 128), Ic));
       if (S > 0) {
@@ -403,6 +403,9 @@ moe_status moe_forward_ex(const moe_problem* pp, const moe_forward_options* opt,
   const moe_forward_options o = opt ? *opt : moe_forward_options{};
   const int S = o.n_shared;
   if (o.y_fp32 != 0 && o.y_fp32 != 1) return MOE_ERR_INVALID_ARG;
+  if (o.mx_weight_scales_blocked != 0 && (o.mx_weight_scales_blocked != 1 || p.quant != MOE_MXFP8))
+    return MOE_ERR_INVALID_ARG;
+  if (o.mx_weight_scales_blocked && (!aligned(w1_scale, 16) || !aligned(w2_scale, 16))) return MOE_ERR_INVALID_ARG;
   const moe_status vs = validate_shape(p, S);
   if (vs != MOE_OK) return vs;
   if (p.T == 0) return MOE_OK;
@@ -449,7 +452,7 @@ moe_status moe_forward_ex(const moe_problem* pp, const moe_forward_options* opt,
                             p.quant == MOE_FP8_PER_TENSOR ? x : nullptr, static_cast<size_t>(p.T) * p.H);
     if (e == cudaSuccess)
       e = launch_scan_tiles(bc, L.shuf.nblk, p.E, counts, offsets, tiles, num_tiles, L.max_tiles, kGemmBM, nullptr,
-                            hdr, s, p.T, S, p.T * p.k);
+                            hdr, s, p.T, S, p.T * p.k, p.quant == MOE_MXFP8 ? at<int32_t*>(ws, L.padbase) : nullptr);
     const bool f8 = p.quant == MOE_FP8_PER_TENSOR;
     const bool blockwise = p.quant == MOE_FP8_BLOCK128;
     const bool mxfp8 = p.quant == MOE_MXFP8;
@@ -460,8 +463,8 @@ moe_status moe_forward_ex(const moe_problem* pp, const moe_forward_options* opt,
     float* sh = blockwise ? at<float*>(ws, L.sh) : nullptr;
     if (e == cudaSuccess) {
       if (mxfp8)
-        e = launch_scatter_gather_mx(ids, lrank, bc, p.T, p.E, p.k, p.H, x, xs, at<uint8_t*>(ws, L.xs_sc), perm, inv,
-                                     s, S);
+        e = launch_scatter_gather_mx(ids, lrank, bc, p.T, p.E, p.k, p.H, x, xs, at<uint8_t*>(ws, L.xs_sc),
+                                     at<uint8_t*>(ws, L.xs_sf), at<int32_t*>(ws, L.padbase), perm, inv, s, S);
       else if (f8)
         e = launch_scatter_gather_q(ids, lrank, bc, p.T, p.E, p.k, p.H, x, xs, perm, inv, hdr, s, S);
       else if (blockwise)
@@ -490,24 +493,28 @@ moe_status moe_forward_ex(const moe_problem* pp, const moe_forward_options* opt,
       g.o = at<void*>(ws, L.o);
       g.hdr = hdr;
       if (mxfp8) {
-        const int Hc = p.H / 32, Ic = p.I / 32;
         uint8_t* xs_sf = at<uint8_t*>(ws, L.xs_sf);
-        uint8_t* h_sc = at<uint8_t*>(ws, L.h_sc);
         uint8_t* h_sf = at<uint8_t*>(ws, L.h_sf);
         uint8_t* w1_sf = at<uint8_t*>(ws, L.w1_sf);
         uint8_t* w2_sf = at<uint8_t*>(ws, L.w2_sf);
         uint8_t* w1s_sf = S > 0 ? at<uint8_t*>(ws, L.w1s_sf) : nullptr;
         uint8_t* w2s_sf = S > 0 ? at<uint8_t*>(ws, L.w2s_sf) : nullptr;
-        e = launch_mx_blocked_tiles(at<uint8_t*>(ws, L.xs_sc), Hc, tiles, num_tiles, L.max_tiles, xs_sf, s);
-        if (e == cudaSuccess)
+        if (o.mx_weight_scales_blocked) {  // converted once by the caller
+          w1_sf = const_cast<uint8_t*>(reinterpret_cast<const uint8_t*>(w1_scale));
+          w2_sf = const_cast<uint8_t*>(reinterpret_cast<const uint8_t*>(w2_scale));
+          if (S > 0) {
+            w1s_sf = const_cast<uint8_t*>(reinterpret_cast<const uint8_t*>(o.w1_shared_scale));
+            w2s_sf = const_cast<uint8_t*>(reinterpret_cast<const uint8_t*>(o.w2_shared_scale));
+          }
+        } else {
           e = launch_mx_blocked_weights(reinterpret_cast<const uint8_t*>(w1_scale),
                                         reinterpret_cast<const uint8_t*>(w2_scale), p.E, p.H, p.I, w1_sf, w2_sf, s);
-        if (e == cudaSuccess && S > 0)
-          e = launch_mx_blocked_weights(reinterpret_cast<const uint8_t*>(o.w1_shared_scale),
-                                        reinterpret_cast<const uint8_t*>(o.w2_shared_scale), S, p.H, p.I, w1s_sf,
-                                        w2s_sf, s);
-        if (e == cudaSuccess) e = launch_gateup_mx(g, xs_sf, w1_sf, w1s_sf, h_sc, s);
-        if (e == cudaSuccess) e = launch_mx_blocked_tiles(h_sc, Ic, tiles, num_tiles, L.max_tiles, h_sf, s);
+          if (e == cudaSuccess && S > 0)
+            e = launch_mx_blocked_weights(reinterpret_cast<const uint8_t*>(o.w1_shared_scale),
+                                          reinterpret_cast<const uint8_t*>(o.w2_shared_scale), S, p.H, p.I, w1s_sf,
+                                          w2s_sf, s);
+        }
+        if (e == cudaSuccess) e = launch_gateup_mx(g, xs_sf, w1_sf, w1s_sf, h_sf, s);
         if (e == cudaSuccess) e = launch_down_mx(g, h_sf, w2_sf, w2s_sf, s);
       } else if (blockwise) {
         e = launch_gateup_blockwise(g, xs_scale, sh, s);
@@ -551,6 +558,23 @@ moe_status moe_forward_ex(const moe_problem* pp, const moe_forward_options* opt,
     }
   }
   return from_cuda(e);
+}
+
+size_t moe_mx_weight_scales_bytes(int E, int H, int I, int which) {
+  if (E < 1 || H < 1 || I < 1 || H % 128 || I % 64 || (which != 1 && which != 2)) return 0;
+  return which == 1 ? mx_blocked_bytes(static_cast<size_t>(E) * (I / 64), H / 32)
+                    : mx_blocked_bytes(static_cast<size_t>(E) * (H / 128), I / 32);
+}
+
+moe_status moe_mx_weight_scales(const uint8_t* w1_scale, const uint8_t* w2_scale, int E, int H, int I,
+                                uint8_t* w1_blocked, uint8_t* w2_blocked, moe_stream_t stream) {
+  if (E < 1 || H < 1 || I < 1) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE || H % 128 || I % 64 || static_cast<long long>(E) * 2 * I * H >= (1ll << 40)) return MOE_ERR_UNSUPPORTED;
+  if (!w1_scale || !w2_scale || !w1_blocked || !w2_blocked || !aligned(w1_scale, 4) || !aligned(w2_scale, 4) ||
+      !aligned(w1_blocked, 16) || !aligned(w2_blocked, 16))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(launch_mx_blocked_weights(w1_scale, w2_scale, E, H, I, w1_blocked, w2_blocked,
+                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t moe_mx_blocked_bytes(int rows, int cols, int groups) {

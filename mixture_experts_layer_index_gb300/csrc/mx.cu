@@ -93,7 +93,8 @@ __device__ __forceinline__ uint2 quant8(const float* f, float inv) {
 __global__ void __launch_bounds__(256) scatter_gather_mx_kernel(
     const int32_t* __restrict__ ids, const int32_t* __restrict__ lrank, const int32_t* __restrict__ blockbase, int E,
     int RB, int k, int H, const uint4* __restrict__ x, uint8_t* __restrict__ xs, uint8_t* __restrict__ xs_sc,
-    int32_t* __restrict__ perm, int32_t* __restrict__ inv, int S, int T) {
+    uint8_t* __restrict__ xs_sf, const int32_t* __restrict__ padbase, int32_t* __restrict__ perm,
+    int32_t* __restrict__ inv, int S, int T) {
   extern __shared__ __align__(16) uint8_t s_row[];  // [H] e4m3 codes, then [H/32] scale codes
   dep_wait();  // ranks and block bases
   uint8_t* s_sc = s_row + H;
@@ -125,9 +126,9 @@ __global__ void __launch_bounds__(256) scatter_gather_mx_kernel(
     }
   }
   __syncthreads();
-  const int row16 = H / 16, nsc = H / 32;
+  const int row16 = H / 16, nsc = H / 32, ncb = nsc / 4;  // H % 128 == 0: whole 4-chunk blocks
   for (int j = warp; j < k + S; j += blockDim.x >> 5) {
-    int p;
+    int p, e;
     if (j < k) {
       const int r = t * k + j;
       const int lr = lrank[r];
@@ -135,17 +136,24 @@ __global__ void __launch_bounds__(256) scatter_gather_mx_kernel(
         if (lane == 0) inv[r] = -1;
         continue;
       }
-      p = blockbase[static_cast<size_t>(r / RB) * E + ids[r]] + lr;
+      e = ids[r];
+      p = blockbase[static_cast<size_t>(r / RB) * E + e] + lr;
       if (lane == 0) {
         perm[p] = r;
         inv[r] = p;
       }
     } else {
+      e = E + (j - k);
       p = T * k + (j - k) * T + t;
     }
     uint4* dst = reinterpret_cast<uint4*>(xs + static_cast<size_t>(p) * H);
     for (int c = lane; c < row16; c += 32) dst[c] = reinterpret_cast<const uint4*>(s_row)[c];
     for (int c = lane; c < nsc; c += 32) xs_sc[static_cast<size_t>(p) * nsc + c] = s_sc[c];
+    // the same scales in the blocked layout: padded row pr, four chunks per 4-byte word
+    const int pr = p + __ldg(padbase + e);
+    uint8_t* blk = xs_sf + static_cast<size_t>(pr / BM) * ncb * SF_BYTES + (pr % 32) * 16 + ((pr % BM) / 32) * 4;
+    for (int cb = lane; cb < ncb; cb += 32)
+      *reinterpret_cast<uint32_t*>(blk + cb * SF_BYTES) = reinterpret_cast<const uint32_t*>(s_sc)[cb];
   }
 }
 
@@ -279,7 +287,8 @@ struct Params {
   const uint8_t* w_sf2;  // ... of the shared experts (tiles of expert E + s)
   int ncbA, ncbW;
   uint8_t* h;            // Gate/Up: e4m3 h [R, I]
-  uint8_t* h_sc;         // Gate/Up: E8M0 scale codes of h [R, I/32]
+  uint8_t* h_sc;         // Gate/Up: E8M0 scale codes of h, blocked (block row = tile, ncbH column blocks)
+  int ncbH;
   __nv_bfloat16* o;      // Down: o [R, H]
   DeviceHeader* hdr;
 };
@@ -486,7 +495,15 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
           uint4* dst = reinterpret_cast<uint4*>(p.h + r * p.I + col);
           dst[0] = q4[0];
           dst[1] = q4[1];
-          p.h_sc[r * (p.I / 32) + col / 32] = static_cast<uint8_t>(X + 127);
+          // the scale straight into the blocked layout of the Down GEMM's A scales
+          // (block row = tile, chunk col / 32); the last unit of a ragged I also
+          // zeroes the chunks past I of its block
+          const int c32 = col / 32;
+          uint8_t* sfrow = p.h_sc + (static_cast<size_t>(tile) * p.ncbH + c32 / 4) * SF_BYTES + (row % 32) * 16 +
+                           (row / 32) * 4;
+          sfrow[c32 % 4] = static_cast<uint8_t>(X + 127);
+          if (ch == 1 && n == p.nN - 1)
+            for (int c = c32 % 4 + 1; c < 4; ++c) sfrow[c] = 0;
         }
       } else {
         // Down: the 128 output columns of the unit, staged as two [32 rows][128 bytes]
@@ -594,8 +611,8 @@ static cudaError_t launch_blocked(const uint8_t* sc, int C, const int32_t* tiles
 size_t mx_blocked_bytes(size_t blocks, int C) { return blocks * static_cast<size_t>((C + 3) / 4) * mx::SF_BYTES; }
 
 cudaError_t launch_scatter_gather_mx(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
-                                     int k, int H, const void* x, void* xs, uint8_t* xs_sc, int32_t* perm,
-                                     int32_t* inv, cudaStream_t s, int S) {
+                                     int k, int H, const void* x, void* xs, uint8_t* xs_sc, uint8_t* xs_sf,
+                                     const int32_t* padbase, int32_t* perm, int32_t* inv, cudaStream_t s, int S) {
   if (T <= 0) return cudaSuccess;
   const int RB = route_tokens_per_block(k) * k;
   const size_t smem = static_cast<size_t>(H) + static_cast<size_t>(H / 32);
@@ -603,7 +620,7 @@ cudaError_t launch_scatter_gather_mx(const int32_t* ids, const int32_t* lrank, c
   stage_begin("scatter_gather", s);
   const cudaError_t err = launch_dependent(mx::scatter_gather_mx_kernel, dim3(T), dim3(256), smem, s, ids, lrank,
                                            blockbase, E, RB, k, H, static_cast<const uint4*>(x),
-                                           static_cast<uint8_t*>(xs), xs_sc, perm, inv, S, T);
+                                           static_cast<uint8_t*>(xs), xs_sc, xs_sf, padbase, perm, inv, S, T);
   stage_end(s);
   return err;
 }
@@ -679,6 +696,7 @@ static cudaError_t launch_mx_gemm(int mode, const GroupedArgs& a, const uint8_t*
     p.ncbA = p.ncbW = (a.H / 32 + 3) / 4;
     p.h = static_cast<uint8_t*>(a.h);
     p.h_sc = h_sc;
+    p.ncbH = (a.I / 32 + 3) / 4;
   } else {
     if (!encode_u8(&tma, a.h, a.I, a.R, BM) || !encode_u8(&tmb, a.w2, a.I, static_cast<uint64_t>(a.E) * a.H, BN) ||
         !encode_bf16_out(&tmo, a.o, a.H, a.R))

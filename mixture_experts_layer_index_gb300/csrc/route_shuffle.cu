@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(1024) scan_tiles_kernel(int32_t* __restrict__ 
                                                           int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                           int32_t* __restrict__ tiles, int32_t* __restrict__ num_tiles,
                                                           int max_tiles, int BM, DeviceHeader* hdr, int use_smem,
-                                                          int T, int S, int Rr) {
+                                                          int T, int S, int Rr, int32_t* __restrict__ padbase) {
   __shared__ int s_cnt[kMaxE], s_off[kMaxE + 1], s_toff[kMaxE + 1];
   extern __shared__ int sbc[];
   dep_wait();  // the block counts of the route/rank kernel
@@ -253,6 +253,12 @@ __global__ void __launch_bounds__(1024) scan_tiles_kernel(int32_t* __restrict__ 
     const int idx = s_toff[E] + i;
     if (idx < max_tiles)
       reinterpret_cast<int4*>(tiles)[idx] = make_int4(E + sx, Rr + sx * T + j * BM, min(BM, T - j * BM), 0);
+  }
+  // row p of expert e (or shared expert s) sits at row p + padbase[e] of a layout in
+  // which every expert's rows are padded to whole tiles (the blocked MX scales)
+  if (padbase) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) padbase[e] = BM * s_toff[e] - s_off[e];
+    for (int sx = threadIdx.x; sx < S; sx += blockDim.x) padbase[E + sx] = BM * (s_toff[E] + sx * nts) - (Rr + sx * T);
   }
 }
 
@@ -385,7 +391,7 @@ cudaError_t launch_route_rank(const float* scores, const int32_t* ids_in, int T,
 
 cudaError_t launch_scan_tiles(int32_t* blockcounts, int nblk, int E, int32_t* counts, int32_t* offsets,
                               int32_t* tiles, int32_t* num_tiles, int max_tiles, int BM, int32_t* /*tile_scratch*/,
-                              DeviceHeader* hdr, cudaStream_t s, int T, int S, int Rr) {
+                              DeviceHeader* hdr, cudaStream_t s, int T, int S, int Rr, int32_t* padbase) {
   static const cudaError_t attr = cudaFuncSetAttribute(scan_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                        kScanSmemBytes);
   if (attr != cudaSuccess) return attr;
@@ -394,7 +400,7 @@ cudaError_t launch_scan_tiles(int32_t* blockcounts, int nblk, int E, int32_t* co
   stage_begin("scan_tiles", s);
   const cudaError_t err = launch_dependent(scan_tiles_kernel, dim3(1), dim3(1024), use_smem ? need : 0, s, blockcounts,
                                            nblk, E, counts, offsets, tiles, num_tiles, max_tiles, BM, hdr, use_smem, T,
-                                           S, Rr);
+                                           S, Rr, padbase);
   stage_end(s);
   return err;
 }

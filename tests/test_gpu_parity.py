@@ -802,3 +802,34 @@ def test_forward_page_admitted_shapes(m, wl):
     ref = O.forward(*oracle_args(inp), wl.k, wl.quant)
     _check_routing_views(m, wl, p, ws, ref, inp)
     _check_y(wl, y, ref["y"])
+
+
+def test_mxfp8_weight_scales_converted_once(m):
+    """moe_mx_weight_scales converts the weights' scales into the forward's blocked
+    layouts once; the forward given them (mx_weight_scales_blocked = 1) must give
+    the same y, bit for bit, as the forward that converts on every call, with
+    shared experts converted the same way."""
+    wl = W.Workload("mx_preblocked", 150, 16, 4, 512, 320, W.QUANT_MXFP8, 107)
+    inp = W.make_inputs(wl)
+    shd = _shared_weights(wl, 1, 108)
+    d, sd = _dev(inp), _dev(shd)
+    _, _, y_ref, _ = run_forward_ex(m, wl, d, sd, 1)
+
+    def blocked(w1s, w2s, E):
+        b1 = torch.empty(m.moe_mx_weight_scales_bytes(E, wl.H, wl.I, 1), dtype=torch.uint8, device=DEV)
+        b2 = torch.empty(m.moe_mx_weight_scales_bytes(E, wl.H, wl.I, 2), dtype=torch.uint8, device=DEV)
+        m.moe_mx_weight_scales(w1s, w2s, E, wl.H, wl.I, b1, b2)
+        return b1, b2
+
+    b1, b2 = blocked(d["w1_scale"], d["w2_scale"], wl.E)
+    c1, c2 = blocked(sd["w1_scale"], sd["w2_scale"], 1)
+    p = m.problem(wl.T, wl.E, wl.k, wl.H, wl.I, wl.quant)
+    opt = m.forward_options(1, sd["w1"], sd["w2"], c1, c2, mx_weight_scales_blocked=True)
+    ws = torch.empty(m.moe_workspace_size_ex(p, opt), dtype=torch.uint8, device=DEV)
+    y = torch.empty_like(y_ref)
+    for _ in range(2):
+        y.fill_(0)
+        m.moe_forward_ex(p, opt, d["x"], d["scores"], d["w1"], d["w2"], b1, b2, y, ws)
+        torch.cuda.synchronize()
+        assert m.moe_read_device_status(ws) == m.MOE_OK
+        assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
