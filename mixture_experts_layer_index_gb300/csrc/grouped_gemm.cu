@@ -49,9 +49,8 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;
 // Epilogue warps (from warp 4): one or two per 32-lane TMEM quadrant.  Two, each
 // draining half of the accumulator's columns, pay off where the mainloop of a
-// tile is short next to its epilogue (FP8: 16 K stages and fp32 output in the
-// Gate/Up, 6 K stages in the Down at I = 768).
-__host__ __device__ constexpr int epi_warps(int mode, bool f8) { return f8 ? 8 : 4; }
+// tile is short next to its epilogue (FP8 Gate/Up: 16 K stages and fp32 output).
+__host__ __device__ constexpr int epi_warps(int mode, bool f8) { return (mode == 0 && f8) ? 8 : 4; }
 __host__ __device__ constexpr int threads_of(int mode, bool f8) { return 32 * (4 + epi_warps(mode, f8)); }
 constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
 // epilogue staging: 4 warps x 32 rows x 256 bytes, after the barriers, 1024-byte
@@ -361,62 +360,7 @@ __global__ void __launch_bounds__(threads_of(MODE, F8), 1)
         // (lane 0 issues them; it waits for them to have read the staging before the
         // next pass overwrites it); a warp of a partial tile writes its valid rows with
         // 16-byte stores.  F8: o = s_h * s_w2[e] * acc.
-        // FP8 (a tile's mainloop half as long as bf16's): two warps per quadrant, warp h
-        // draining columns [128h, 128h + 128) through a 4 KB staging box of its own
-        // (64 columns per box, written out before the next is staged)
-        if (NH == 2) {
-          uint8_t* stg = smem + STAGING_OFFSET + e8 * 4096;
-          const int wrows = min(32, nrows - q * 32);
-          const float post = F8 ? e4m3_scale(__uint_as_float(*p.amax_in)) * wscale_of(p, tl.x) : 1.0f;
-          const int wrow0 = row0 + q * 32;
-#pragma unroll 1
-          for (int b = 0; b < 2; ++b) {
-            if (lane == 0) bulk_wait_group_read0();  // the previous box has left the staging
-            __syncwarp();
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              float v[32];
-              tmem_ld32(tbase + h * 128 + b * 64 + c * 32, v);
-              tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] *= post;
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const int cc = c * 4 + i;  // 16-byte chunk of the box row, 0..7
-                *reinterpret_cast<uint4*>(stg + lane * 128 + ((cc ^ (lane & 7)) << 4)) = pack_bf16x8(v + 8 * i);
-              }
-            }
-            if (b == 1) {  // this warp's accumulator columns are read: hand the buffer back
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
-            }
-            const int col0 = n * BN + h * 128 + b * 64;
-            if (wrows == 32) {
-              fence_proxy_async_shared();
-              __syncwarp();
-              if (lane == 0) {
-                if (col0 < p.n_valid) tma_store_2d(&tmO, smem_u32(stg), col0, wrow0);
-                bulk_commit_group();
-              }
-              __syncwarp();
-            } else {
-              __syncwarp();
-#pragma unroll 4
-              for (int it = 0; it < 8; ++it) {
-                const int r = it * 4 + (lane >> 3), j = lane & 7;
-                const int col = col0 + j * 8;
-                if (r < wrows && col < p.n_valid)
-                  *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(wrow0 + r) * p.out_ld + col) =
-                      *reinterpret_cast<const uint4*>(stg + r * 128 + ((j ^ (r & 7)) << 4));
-              }
-              __syncwarp();
-            }
-          }
-          acc ^= 1;
-          if (acc == 0) acc_phase ^= 1;
-          continue;
-        }
+        static_assert(MODE == MODE_GATEUP || epi_warps(MODE, F8) == 4, "Down epilogue: one warp per TMEM quadrant");
         uint8_t* stg = smem + STAGING_OFFSET + q * (32 * 256);
         const int wrows = min(32, nrows - q * 32);  // valid rows of this warp (may be <= 0)
         const float post = F8 ? e4m3_scale(__uint_as_float(*p.amax_in)) * wscale_of(p, tl.x) : 1.0f;
