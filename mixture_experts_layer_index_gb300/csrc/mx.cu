@@ -22,11 +22,12 @@
 //                       CTA: the blocks of the grouped GEMM's tile map (a group
 //                       per expert, padded to whole tiles), the weights' rows, or
 //                       caller-given groups (moe_mx_blocked_scales).
-//   grouped_mx<0>       Gate/Up: 128 sorted rows x (64 gate + the matching 64 up
-//                       rows of W1[e]) per unit; 4 block-scaled MMAs of K=32 per
-//                       128-wide K stage; the epilogue computes a = silu(g) * u
-//                       and quantises it per run of 32 straight into e4m3 h and
-//                       its E8M0 scales (no fp32 round trip).
+//   grouped_mx<0>       Gate/Up: 128 sorted rows x (96 gate + the matching 96 up
+//                       rows of W1[e]) per unit; 4 block-scaled MMAs (N = 192) of
+//                       K=32 per 128-wide K stage; three epilogue warps per TMEM
+//                       quadrant compute a = silu(g) * u and quantise it per run
+//                       of 32 straight into e4m3 h and its E8M0 scales (no fp32
+//                       round trip).
 //   grouped_mx<1>       Down: 128 rows x 128 rows of W2[e]; bf16 o in sorted row
 //                       order (staged, TMA tile stores).
 #include "common.cuh"
@@ -36,25 +37,36 @@ namespace moe {
 namespace mx {
 
 constexpr int BM = kGemmBM;      // 128 rows per tile
-constexpr int BN = 128;          // accumulator columns per unit
 constexpr int BKB = 128;         // K bytes (= e4m3 values) per stage: 4 scale chunks
 constexpr int A_BYTES = BM * BKB;
-constexpr int B_BYTES = BN * BKB;
 constexpr int SF_BYTES = 512;    // one blocked scale block (128 rows x 4 chunks)
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES + 2 * SF_BYTES;  // 33 KB, a multiple of 1024
-constexpr int TMEM_COLS = 512;   // 2 accumulators x 128 columns, then the scale slots
-constexpr int SF_COL0 = 2 * BN;  // first TMEM column of the scale slots (8 columns per stage)
-__host__ __device__ constexpr int stages_of(int mode) { return mode == 0 ? 6 : 5; }
-__host__ __device__ constexpr int epi_warps_of(int mode) { return mode == 0 ? 8 : 4; }
+constexpr int TMEM_COLS = 512;   // 2 accumulators, then the scale slots
+// Gate/Up units: 96 gate + the matching 96 up rows of W1[e] (N = 192: two 192-column
+// accumulators and five stages' scale slots fill the 512 TMEM columns); Down units:
+// 128 rows of W2[e].
+__host__ __device__ constexpr int bn_of(int mode) { return mode == 0 ? 192 : 128; }
+__host__ __device__ constexpr int gu_half() { return 96; }
+__host__ __device__ constexpr int sfb_blocks(int mode) { return mode == 0 ? 2 : 1; }  // 128-row B scale blocks
+__host__ __device__ constexpr int stage_bytes(int mode) {
+  return (A_BYTES + bn_of(mode) * BKB + (1 + sfb_blocks(mode)) * SF_BYTES + 1023) / 1024 * 1024;
+}
+__host__ __device__ constexpr int sf_col0(int mode) { return 2 * bn_of(mode); }
+__host__ __device__ constexpr int sf_cols_per_stage(int mode) { return 4 * (1 + sfb_blocks(mode)); }
+__host__ __device__ constexpr int stages_of(int mode) { return 5; }
+// Gate/Up: three warps per TMEM quadrant, one 32-column run of h each; Down: one.
+__host__ __device__ constexpr int epi_warps_of(int mode) { return mode == 0 ? 12 : 4; }
 __host__ __device__ constexpr int threads_of(int mode) { return 32 * (4 + epi_warps_of(mode)); }
-constexpr int NUM_BARS = 2 * 6 + 4 + 1;
+constexpr int NUM_BARS = 2 * 5 + 4 + 1;
 __host__ __device__ constexpr int staging_offset(int mode) {
-  return (stages_of(mode) * STAGE_BYTES + 256 + 1023) / 1024 * 1024;
+  return (stages_of(mode) * stage_bytes(mode) + 256 + 1023) / 1024 * 1024;
 }
 constexpr int STAGING_BYTES = 4 * 32 * 256;  // Down: 32 rows x 256 bytes per epilogue warp
 __host__ __device__ constexpr size_t smem_bytes(int mode) {
   return 1024 + staging_offset(mode) + (mode == 1 ? STAGING_BYTES : 0);
 }
+static_assert(sf_col0(0) + stages_of(0) * sf_cols_per_stage(0) <= TMEM_COLS, "Gate/Up TMEM columns");
+static_assert(sf_col0(1) + stages_of(1) * sf_cols_per_stage(1) <= TMEM_COLS, "Down TMEM columns");
+static_assert(smem_bytes(0) <= 232448 && smem_bytes(1) <= 232448, "shared memory per block");
 
 // ------------------------------------------------------------------ MX quantisation helpers
 // X = floor(log2(amax)) - 8 in [-127, 127]; -127 when amax == 0.
@@ -165,7 +177,12 @@ __global__ void __launch_bounds__(256) scatter_gather_mx_kernel(
 //            [64n, 64n + 64) then the matching up rows [I + 64n, I + 64n + 64) of
 //            W1[e], the rows of one Gate/Up unit's B operand.
 //   CONTIG   block b = rows [128b, 128b + 128) (all valid).
-constexpr int SRC_TILES = 0, SRC_W1ROWS = 1, SRC_CONTIG = 2;
+//   W1ROWS96 the B operand of one MXFP8 Gate/Up unit (expert e, unit n): gate rows
+//            [96n, 96n + 96) then the matching up rows of W1[e], 192 rows in two
+//            blocks (the second half-padded); a row past I is padding.  Output
+//            block 2 u + h of unit u = e * units + n is stored at ((u * ncb + cb)
+//            * 2 + h) * 512: the two blocks of one column block are adjacent.
+constexpr int SRC_TILES = 0, SRC_W1ROWS = 1, SRC_CONTIG = 2, SRC_W1ROWS96 = 3;
 
 // One CTA per output block: thread i of 32 * ncb writes the 16-byte line (i % 32)
 // of column block i / 32: scales of rows line, line+32, line+64, line+96 of the
@@ -177,8 +194,14 @@ __global__ void __launch_bounds__(256) mx_blocked_kernel(const uint8_t* __restri
                                                          uint8_t* __restrict__ out, int wait_at_end) {
   if (!wait_at_end) dep_wait();  // the scales (and tiles) come from the kernels before
   const int b = blockIdx.x;
-  int row0 = 0, nrows = BM, I2 = 0, e = 0, n = 0;
-  if (SRC == SRC_TILES) {
+  int row0 = 0, nrows = BM, I2 = 0, e = 0, n = 0, half = 0;
+  if (SRC == SRC_W1ROWS96) {
+    const int per = (I + gu_half() - 1) / gu_half();
+    half = b & 1;
+    e = (b >> 1) / per;
+    n = (b >> 1) - e * per;
+    I2 = 2 * I;
+  } else if (SRC == SRC_TILES) {
     if (b >= *num_tiles) return;
     const int4 tl = tiles[b];
     row0 = tl.y;
@@ -200,7 +223,12 @@ __global__ void __launch_bounds__(256) mx_blocked_kernel(const uint8_t* __restri
     for (int j = 0; j < 4; ++j) {
       const int r = 32 * j + line;  // row of the block
       long long src_row = -1;
-      if (SRC == SRC_W1ROWS)
+      if (SRC == SRC_W1ROWS96) {
+        const int br = half * BM + r;                     // row of the unit's 192-row B operand
+        const int col = n * gu_half() + (br < gu_half() ? br : br - gu_half());  // column of h
+        if (br < 2 * gu_half() && col < I)
+          src_row = static_cast<long long>(e) * I2 + (br < gu_half() ? col : I + col);
+      } else if (SRC == SRC_W1ROWS)
         src_row = static_cast<long long>(e) * I2 + (r < 64 ? 64 * n + r : I + 64 * n + (r - 64));
       else if (r < nrows)
         src_row = row0 + r;
@@ -218,7 +246,10 @@ __global__ void __launch_bounds__(256) mx_blocked_kernel(const uint8_t* __restri
       }
       w[j] = word;
     }
-    *reinterpret_cast<uint4*>(blk + cb * SF_BYTES + line * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    uint8_t* dst = SRC == SRC_W1ROWS96
+                       ? out + ((static_cast<size_t>(b >> 1) * ncb + cb) * 2 + (b & 1)) * SF_BYTES
+                       : blk + cb * SF_BYTES;
+    *reinterpret_cast<uint4*>(dst + line * 16) = make_uint4(w[0], w[1], w[2], w[3]);
   }
   if (wait_at_end) dep_wait();  // complete only after the kernel before (keeps the launch chain ordered)
 }
@@ -311,6 +342,10 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
                       const Params p) {
   constexpr int STAGES = stages_of(MODE);
   constexpr int EPI = epi_warps_of(MODE);
+  constexpr int BN = bn_of(MODE);
+  constexpr int STAGE_BYTES = stage_bytes(MODE);
+  constexpr int B_BYTES = BN * BKB;
+  constexpr int NSFB = sfb_blocks(MODE);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
@@ -368,10 +403,9 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
         const int e = shx ? tl.x - p.E : tl.x;
         const CUtensorMap* tb = shx ? &tmB2 : &tmB;
         const uint8_t* wsf = shx ? p.w_sf2 : p.w_sf;
-        // B rows of this unit and the blocked scale block that covers them
-        const int brow = MODE == 0 ? e * 2 * p.I + n * 64 : e * p.H + n * BN;
-        const long long bblk = MODE == 0 ? static_cast<long long>(e) * (p.I / 64) + n
-                                         : static_cast<long long>(e) * (p.H / BN) + n;
+        // B rows of this unit and the blocked scale blocks that cover them
+        const int brow = MODE == 0 ? e * 2 * p.I + n * gu_half() : e * p.H + n * BN;
+        const long long bblk = static_cast<long long>(e) * p.nN + n;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.hdr, 0xA0000u | MODE)) {
             ok = false;
@@ -381,17 +415,18 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
           const uint32_t a_dst = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t b_dst = a_dst + A_BYTES;
           const uint32_t sf_dst = b_dst + B_BYTES;
-          mbar_arrive_expect_tx(full, STAGE_BYTES);
+          mbar_arrive_expect_tx(full, A_BYTES + B_BYTES + (1 + NSFB) * SF_BYTES);
           const int kc = kb * BKB;
           tma_load_2d(a_dst, &tmA, kc, tl.y, full);
           if (MODE == 0) {
-            tma_load_2d(b_dst, tb, kc, brow, full);                   // 64 gate rows
-            tma_load_2d(b_dst + B_BYTES / 2, tb, kc, brow + p.I, full);  // the matching 64 up rows
+            tma_load_2d(b_dst, tb, kc, brow, full);                         // 96 gate rows
+            tma_load_2d(b_dst + B_BYTES / 2, tb, kc, brow + p.I, full);  // the matching 96 up rows
           } else {
             tma_load_2d(b_dst, tb, kc, brow, full);
           }
           bulk_load(sf_dst, p.a_sf + (static_cast<size_t>(tile) * p.ncbA + kb) * SF_BYTES, SF_BYTES, full);
-          bulk_load(sf_dst + SF_BYTES, wsf + (static_cast<size_t>(bblk) * p.ncbW + kb) * SF_BYTES, SF_BYTES, full);
+          bulk_load(sf_dst + SF_BYTES, wsf + (static_cast<size_t>(bblk) * p.ncbW + kb) * (NSFB * SF_BYTES),
+                    NSFB * SF_BYTES, full);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -426,10 +461,12 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
           const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t b_addr = a_addr + A_BYTES;
           const uint32_t sf_addr = b_addr + B_BYTES;
-          const uint32_t sfa_t = tmem_base + SF_COL0 + stage * 8;
+          const uint32_t sfa_t = tmem_base + sf_col0(MODE) + stage * sf_cols_per_stage(MODE);
           const uint32_t sfb_t = sfa_t + 4;
           tmem_cp_32x128b_x4(sfa_t, sf_desc(sf_addr));
-          tmem_cp_32x128b_x4(sfb_t, sf_desc(sf_addr + SF_BYTES));
+#pragma unroll
+          for (int b = 0; b < NSFB; ++b)  // B rows 128b .. 128b + 127 -> columns 4b .. 4b + 3
+            tmem_cp_32x128b_x4(sfb_t + 4 * b, sf_desc(sf_addr + (1 + b) * SF_BYTES));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // K chunk kk of the stage: byte kk of every scale word
             mma_mx(d_tmem, sw128_kmajor_desc(a_addr + kk * 32), sw128_kmajor_desc(b_addr + kk * 32),
@@ -466,17 +503,18 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       if (MODE == 0) {
-        // warp half ch: gate columns [32ch, 32ch + 32) and the matching up columns;
-        // its 32 h values of a row are exactly one MX run
+        // warp run ch of its quadrant: gate columns [32ch, 32ch + 32) and the matching
+        // up columns; its 32 h values of a row are exactly one MX run
         const int ch = e8 >> 2;
         float g[32], up[32];
         tmem_ld32(tbase + ch * 32, g);
-        tmem_ld32(tbase + 64 + ch * 32, up);
+        tmem_ld32(tbase + gu_half() + ch * 32, up);
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
-        if (row < nrows) {
+        const int col = n * gu_half() + ch * 32;  // first h column of this run
+        if (row < nrows && col < p.I) {
           float a[32];
           float m = 0.0f;
 #pragma unroll
@@ -491,20 +529,21 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) q2[i] = quant8(a + 8 * i, inv);
           const size_t r = static_cast<size_t>(row0 + row);
-          const int col = n * 64 + ch * 32;
           uint4* dst = reinterpret_cast<uint4*>(p.h + r * p.I + col);
           dst[0] = q4[0];
           dst[1] = q4[1];
           // the scale straight into the blocked layout of the Down GEMM's A scales
-          // (block row = tile, chunk col / 32); the last unit of a ragged I also
-          // zeroes the chunks past I of its block
+          // (block row = tile, chunk col / 32)
           const int c32 = col / 32;
-          uint8_t* sfrow = p.h_sc + (static_cast<size_t>(tile) * p.ncbH + c32 / 4) * SF_BYTES + (row % 32) * 16 +
-                           (row / 32) * 4;
-          sfrow[c32 % 4] = static_cast<uint8_t>(X + 127);
-          if (ch == 1 && n == p.nN - 1)
-            for (int c = c32 % 4 + 1; c < 4; ++c) sfrow[c] = 0;
+          p.h_sc[(static_cast<size_t>(tile) * p.ncbH + c32 / 4) * SF_BYTES + (row % 32) * 16 + (row / 32) * 4 + c32 % 4] =
+              static_cast<uint8_t>(X + 127);
         }
+        // the last unit's last warp zeroes the scale chunks past I up to whole 4-chunk
+        // blocks: they meet the Down GEMM's zero-filled K tail
+        if (row < nrows && n == p.nN - 1 && ch == 2)
+          for (int c32 = (p.I + 31) / 32; c32 < 4 * p.ncbH; ++c32)
+            p.h_sc[(static_cast<size_t>(tile) * p.ncbH + c32 / 4) * SF_BYTES + (row % 32) * 16 + (row / 32) * 4 +
+                   c32 % 4] = 0;
       } else {
         // Down: the 128 output columns of the unit, staged as two [32 rows][128 bytes]
         // boxes (128-byte swizzle) per warp, written by TMA tile stores when all 32 rows
@@ -639,11 +678,12 @@ cudaError_t launch_mx_blocked_weights(const uint8_t* w1_sc, const uint8_t* w2_sc
   stage_begin("mx_weight_scales", s);
   // these read only the caller's weight scales: their work overlaps the kernel
   // before, and they wait for it only at their end so that the chain stays ordered
-  cudaError_t err = mx::launch_blocked<mx::SRC_W1ROWS>(w1_sc, H / 32, nullptr, nullptr, I, w1_sf,
-                                                       static_cast<unsigned>(E) * (I / 64), true, s);
+  const unsigned units = static_cast<unsigned>((I + mx::gu_half() - 1) / mx::gu_half());
+  cudaError_t err = mx::launch_blocked<mx::SRC_W1ROWS96>(w1_sc, H / 32, nullptr, nullptr, I, w1_sf,
+                                                         static_cast<unsigned>(E) * units * 2, true, s);
   if (err == cudaSuccess)
     err = mx::launch_blocked<mx::SRC_CONTIG>(w2_sc, I / 32, nullptr, nullptr, I, w2_sf,
-                                             static_cast<unsigned>(E) * (H / mx::BN), true, s);
+                                             static_cast<unsigned>(E) * (H / mx::bn_of(1)), true, s);
   stage_end(s);
   return err;
 }
@@ -685,25 +725,27 @@ static cudaError_t launch_mx_gemm(int mode, const GroupedArgs& a, const uint8_t*
   p.w_sf2 = w_sf2 ? w_sf2 : w_sf;
   p.hdr = a.hdr;
   if (mode == 0) {
-    if (!encode_u8(&tma, a.xs, a.H, a.R, BM) || !encode_u8(&tmb, a.w1, a.H, static_cast<uint64_t>(a.E) * 2 * a.I, 64))
+    if (!encode_u8(&tma, a.xs, a.H, a.R, BM) ||
+        !encode_u8(&tmb, a.w1, a.H, static_cast<uint64_t>(a.E) * 2 * a.I, gu_half()))
       return cudaErrorInvalidValue;
     tmb2 = tmb;
-    if (a.S > 0 && !encode_u8(&tmb2, a.w1s, a.H, static_cast<uint64_t>(a.S) * 2 * a.I, 64))
+    if (a.S > 0 && !encode_u8(&tmb2, a.w1s, a.H, static_cast<uint64_t>(a.S) * 2 * a.I, gu_half()))
       return cudaErrorInvalidValue;
     tmo = tma;
-    p.nN = a.I / 64;
+    p.nN = (a.I + gu_half() - 1) / gu_half();
     p.K = a.H;
     p.ncbA = p.ncbW = (a.H / 32 + 3) / 4;
     p.h = static_cast<uint8_t*>(a.h);
     p.h_sc = h_sc;
     p.ncbH = (a.I / 32 + 3) / 4;
   } else {
-    if (!encode_u8(&tma, a.h, a.I, a.R, BM) || !encode_u8(&tmb, a.w2, a.I, static_cast<uint64_t>(a.E) * a.H, BN) ||
+    constexpr int BN1 = bn_of(1);
+    if (!encode_u8(&tma, a.h, a.I, a.R, BM) || !encode_u8(&tmb, a.w2, a.I, static_cast<uint64_t>(a.E) * a.H, BN1) ||
         !encode_bf16_out(&tmo, a.o, a.H, a.R))
       return cudaErrorInvalidValue;
     tmb2 = tmb;
-    if (a.S > 0 && !encode_u8(&tmb2, a.w2s, a.I, static_cast<uint64_t>(a.S) * a.H, BN)) return cudaErrorInvalidValue;
-    p.nN = a.H / BN;
+    if (a.S > 0 && !encode_u8(&tmb2, a.w2s, a.I, static_cast<uint64_t>(a.S) * a.H, BN1)) return cudaErrorInvalidValue;
+    p.nN = a.H / BN1;
     p.K = a.I;
     p.ncbA = p.ncbW = (a.I / 32 + 3) / 4;
     p.o = static_cast<__nv_bfloat16*>(a.o);
