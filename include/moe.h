@@ -268,8 +268,9 @@ moe_status moe_forward_ex(const moe_problem* p, const moe_forward_options* opt, 
  *                           bytes (16-byte aligned): W1 as the B operands of the
  *                           Gate/Up units (96 gate rows and the matching 96 up rows
  *                           of one expert, two 128-row blocks per unit, adjacent
- *                           per column block), W2 in blocks of 128 rows; blocks are
- *                           the 512-byte blocks of moe_mx_blocked_scales.
+ *                           per column block), W2 likewise as the B operands of the
+ *                           Down units (192 rows, two blocks each); blocks are the
+ *                           512-byte blocks of moe_mx_blocked_scales.
  * Errors: INVALID_ARG, UNSUPPORTED (the MXFP8 shape limits), CUDA. */
 size_t moe_mx_weight_scales_bytes(int E, int H, int I, int which);
 moe_status moe_mx_weight_scales(const uint8_t* w1_scale, const uint8_t* w2_scale, int E, int H, int I,

@@ -250,10 +250,10 @@ bool plan_forward(const moe_problem& p, ForwardLayout* out, int S) {
       L.h_sf = take(mx_blocked_bytes(L.max_tiles, Ic));
       L.padbase = take((E + S) * 4);
       L.w1_sf = take(mx_blocked_bytes(E * ((I + 95) / 96) * 2, Hc));  // two blocks per Gate/Up unit
-      L.w2_sf = take(mx_blocked_bytes(E * (H / 128), Ic));
+      L.w2_sf = take(mx_blocked_bytes(E * ((H + 191) / 192) * 2, Ic));  // two blocks per Down unit
       if (S > 0) {
         L.w1s_sf = take(mx_blocked_bytes(static_cast<size_t>(S) * ((I + 95) / 96) * 2, Hc));
-        L.w2s_sf = take(mx_blocked_bytes(static_cast<size_t>(S) * (H / 128), Ic));
+        L.w2s_sf = take(mx_blocked_bytes(static_cast<size_t>(S) * ((H + 191) / 192) * 2, Ic));
       }
     }
     L.o = take(RS * H * 2);
@@ -563,7 +563,7 @@ moe_status moe_forward_ex(const moe_problem* pp, const moe_forward_options* opt,
 size_t moe_mx_weight_scales_bytes(int E, int H, int I, int which) {
   if (E < 1 || H < 1 || I < 1 || H % 128 || I % 64 || (which != 1 && which != 2)) return 0;
   return which == 1 ? mx_blocked_bytes(static_cast<size_t>(E) * ((I + 95) / 96) * 2, H / 32)
-                    : mx_blocked_bytes(static_cast<size_t>(E) * (H / 128), I / 32);
+                    : mx_blocked_bytes(static_cast<size_t>(E) * ((H + 191) / 192) * 2, I / 32);
 }
 
 moe_status moe_mx_weight_scales(const uint8_t* w1_scale, const uint8_t* w2_scale, int E, int H, int I,

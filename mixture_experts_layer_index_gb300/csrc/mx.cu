@@ -41,18 +41,18 @@ constexpr int BKB = 128;         // K bytes (= e4m3 values) per stage: 4 scale c
 constexpr int A_BYTES = BM * BKB;
 constexpr int SF_BYTES = 512;    // one blocked scale block (128 rows x 4 chunks)
 constexpr int TMEM_COLS = 512;   // 2 accumulators, then the scale slots
-// Gate/Up units: 96 gate + the matching 96 up rows of W1[e] (N = 192: two 192-column
-// accumulators and five stages' scale slots fill the 512 TMEM columns); Down units:
-// 128 rows of W2[e].
-__host__ __device__ constexpr int bn_of(int mode) { return mode == 0 ? 192 : 128; }
+// Gate/Up units: 96 gate + the matching 96 up rows of W1[e]; Down units: 192 rows of
+// W2[e] (N = 192 for both: two 192-column accumulators and the stages' scale slots
+// fit the 512 TMEM columns).
+__host__ __device__ constexpr int bn_of(int mode) { return 192; }
 __host__ __device__ constexpr int gu_half() { return 96; }
-__host__ __device__ constexpr int sfb_blocks(int mode) { return mode == 0 ? 2 : 1; }  // 128-row B scale blocks
+__host__ __device__ constexpr int sfb_blocks(int mode) { return 2; }  // 128-row B scale blocks per unit
 __host__ __device__ constexpr int stage_bytes(int mode) {
   return (A_BYTES + bn_of(mode) * BKB + (1 + sfb_blocks(mode)) * SF_BYTES + 1023) / 1024 * 1024;
 }
 __host__ __device__ constexpr int sf_col0(int mode) { return 2 * bn_of(mode); }
 __host__ __device__ constexpr int sf_cols_per_stage(int mode) { return 4 * (1 + sfb_blocks(mode)); }
-__host__ __device__ constexpr int stages_of(int mode) { return 5; }
+__host__ __device__ constexpr int stages_of(int mode) { return mode == 0 ? 5 : 4; }
 // Gate/Up: three warps per TMEM quadrant, one 32-column run of h each; Down: one.
 __host__ __device__ constexpr int epi_warps_of(int mode) { return mode == 0 ? 12 : 4; }
 __host__ __device__ constexpr int threads_of(int mode) { return 32 * (4 + epi_warps_of(mode)); }
@@ -182,7 +182,10 @@ __global__ void __launch_bounds__(256) scatter_gather_mx_kernel(
 //            blocks (the second half-padded); a row past I is padding.  Output
 //            block 2 u + h of unit u = e * units + n is stored at ((u * ncb + cb)
 //            * 2 + h) * 512: the two blocks of one column block are adjacent.
-constexpr int SRC_TILES = 0, SRC_W1ROWS = 1, SRC_CONTIG = 2, SRC_W1ROWS96 = 3;
+//   W2ROWS192 the B operand of one MXFP8 Down unit (expert e, unit n): rows
+//            [192n, 192n + 192) of W2[e] ([H rows]), in two blocks stored like
+//            W1ROWS96; a row past H is padding.
+constexpr int SRC_TILES = 0, SRC_W1ROWS = 1, SRC_CONTIG = 2, SRC_W1ROWS96 = 3, SRC_W2ROWS192 = 4;
 
 // One CTA per output block: thread i of 32 * ncb writes the 16-byte line (i % 32)
 // of column block i / 32: scales of rows line, line+32, line+64, line+96 of the
@@ -195,7 +198,12 @@ __global__ void __launch_bounds__(256) mx_blocked_kernel(const uint8_t* __restri
   if (!wait_at_end) dep_wait();  // the scales (and tiles) come from the kernels before
   const int b = blockIdx.x;
   int row0 = 0, nrows = BM, I2 = 0, e = 0, n = 0, half = 0;
-  if (SRC == SRC_W1ROWS96) {
+  if (SRC == SRC_W2ROWS192) {  // I holds H here
+    const int per = (I + 191) / 192;
+    half = b & 1;
+    e = (b >> 1) / per;
+    n = (b >> 1) - e * per;
+  } else if (SRC == SRC_W1ROWS96) {
     const int per = (I + gu_half() - 1) / gu_half();
     half = b & 1;
     e = (b >> 1) / per;
@@ -223,7 +231,10 @@ __global__ void __launch_bounds__(256) mx_blocked_kernel(const uint8_t* __restri
     for (int j = 0; j < 4; ++j) {
       const int r = 32 * j + line;  // row of the block
       long long src_row = -1;
-      if (SRC == SRC_W1ROWS96) {
+      if (SRC == SRC_W2ROWS192) {
+        const int br = half * BM + r;
+        if (br < 192 && n * 192 + br < I) src_row = static_cast<long long>(e) * I + n * 192 + br;
+      } else if (SRC == SRC_W1ROWS96) {
         const int br = half * BM + r;                     // row of the unit's 192-row B operand
         const int col = n * gu_half() + (br < gu_half() ? br : br - gu_half());  // column of h
         if (br < 2 * gu_half() && col < I)
@@ -246,7 +257,7 @@ __global__ void __launch_bounds__(256) mx_blocked_kernel(const uint8_t* __restri
       }
       w[j] = word;
     }
-    uint8_t* dst = SRC == SRC_W1ROWS96
+    uint8_t* dst = (SRC == SRC_W1ROWS96 || SRC == SRC_W2ROWS192)
                        ? out + ((static_cast<size_t>(b >> 1) * ncb + cb) * 2 + (b & 1)) * SF_BYTES
                        : blk + cb * SF_BYTES;
     *reinterpret_cast<uint4*>(dst + line * 16) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -545,51 +556,59 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
             p.h_sc[(static_cast<size_t>(tile) * p.ncbH + c32 / 4) * SF_BYTES + (row % 32) * 16 + (row / 32) * 4 +
                    c32 % 4] = 0;
       } else {
-        // Down: the 128 output columns of the unit, staged as two [32 rows][128 bytes]
-        // boxes (128-byte swizzle) per warp, written by TMA tile stores when all 32 rows
-        // belong to the tile, else by 16-byte stores
+        // Down: the BN output columns of the unit in passes of two 64-column boxes,
+        // each staged as [32 rows][128 bytes] (128-byte swizzle) per warp and written
+        // by TMA tile stores when all 32 rows belong to the tile, else by 16-byte stores
         uint8_t* stg = smem + staging_offset(MODE) + q * (32 * 256);
         const int wrows = min(32, nrows - q * 32);
         const int wrow0 = row0 + q * 32;
-        if (lane == 0) bulk_wait_group_read0();
-        __syncwarp();
+        constexpr int NBOX = BN / 64;
+#pragma unroll 1
+        for (int b0 = 0; b0 < NBOX; b0 += 2) {
+          const int nb = min(2, NBOX - b0);
+          if (lane == 0) bulk_wait_group_read0();  // the staging's previous stores have read it
+          __syncwarp();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tmem_ld32(tbase + c * 32, v);
-          tmem_ld_wait();
+          for (int c = 0; c < 4; ++c) {
+            if (c < 2 * nb) {
+              float v[32];
+              tmem_ld32(tbase + b0 * 64 + c * 32, v);
+              tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int cc = c * 4 + i;
-            *reinterpret_cast<uint4*>(stg + (cc >> 3) * 4096 + lane * 128 + (((cc & 7) ^ (lane & 7)) << 4)) =
-                pack_bf16x8(v + 8 * i);
+              for (int i = 0; i < 4; ++i) {
+                const int cc = c * 4 + i;
+                *reinterpret_cast<uint4*>(stg + (cc >> 3) * 4096 + lane * 128 + (((cc & 7) ^ (lane & 7)) << 4)) =
+                    pack_bf16x8(v + 8 * i);
+              }
+            }
           }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
-        const int col0 = n * BN;
-        if (wrows == 32) {
-          fence_proxy_async_shared();
-          __syncwarp();
-          if (lane == 0) {
-#pragma unroll
-            for (int b = 0; b < 2; ++b)
-              if (col0 + b * 64 < p.H) tma_store_2d(&tmO, smem_u32(stg + b * 4096), col0 + b * 64, wrow0);
-            bulk_commit_group();
+          if (b0 + 2 >= NBOX) {  // every accumulator column read: hand the buffer back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
           }
-          __syncwarp();
-        } else {
-          __syncwarp();
+          const int col0 = n * BN + b0 * 64;
+          if (wrows == 32) {
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              for (int b = 0; b < nb; ++b)
+                if (col0 + b * 64 < p.H) tma_store_2d(&tmO, smem_u32(stg + b * 4096), col0 + b * 64, wrow0);
+              bulk_commit_group();
+            }
+            __syncwarp();
+          } else {
+            __syncwarp();
 #pragma unroll 4
-          for (int it = 0; it < 16; ++it) {
-            const int r = it * 2 + (lane >> 4), j = lane & 15;
-            const int col = col0 + j * 8;
-            if (r < wrows && col < p.H)
-              *reinterpret_cast<uint4*>(p.o + static_cast<size_t>(wrow0 + r) * p.H + col) =
-                  *reinterpret_cast<const uint4*>(stg + (j >> 3) * 4096 + r * 128 + (((j & 7) ^ (r & 7)) << 4));
+            for (int it = 0; it < 16; ++it) {
+              const int r = it * 2 + (lane >> 4), j = lane & 15;
+              const int col = col0 + j * 8;
+              if (r < wrows && (j >> 3) < nb && col < p.H)
+                *reinterpret_cast<uint4*>(p.o + static_cast<size_t>(wrow0 + r) * p.H + col) =
+                    *reinterpret_cast<const uint4*>(stg + (j >> 3) * 4096 + r * 128 + (((j & 7) ^ (r & 7)) << 4));
+            }
+            __syncwarp();
           }
-          __syncwarp();
         }
       }
       acc ^= 1;
@@ -682,8 +701,8 @@ cudaError_t launch_mx_blocked_weights(const uint8_t* w1_sc, const uint8_t* w2_sc
   cudaError_t err = mx::launch_blocked<mx::SRC_W1ROWS96>(w1_sc, H / 32, nullptr, nullptr, I, w1_sf,
                                                          static_cast<unsigned>(E) * units * 2, true, s);
   if (err == cudaSuccess)
-    err = mx::launch_blocked<mx::SRC_CONTIG>(w2_sc, I / 32, nullptr, nullptr, I, w2_sf,
-                                             static_cast<unsigned>(E) * (H / mx::bn_of(1)), true, s);
+    err = mx::launch_blocked<mx::SRC_W2ROWS192>(w2_sc, I / 32, nullptr, nullptr, H, w2_sf,
+                                                static_cast<unsigned>(E) * ((H + 191) / 192) * 2, true, s);
   stage_end(s);
   return err;
 }
@@ -745,7 +764,7 @@ static cudaError_t launch_mx_gemm(int mode, const GroupedArgs& a, const uint8_t*
       return cudaErrorInvalidValue;
     tmb2 = tmb;
     if (a.S > 0 && !encode_u8(&tmb2, a.w2s, a.I, static_cast<uint64_t>(a.S) * a.H, BN1)) return cudaErrorInvalidValue;
-    p.nN = a.H / BN1;
+    p.nN = (a.H + BN1 - 1) / BN1;
     p.K = a.I;
     p.ncbA = p.ncbW = (a.I / 32 + 3) / 4;
     p.o = static_cast<__nv_bfloat16*>(a.o);
