@@ -96,8 +96,7 @@ typedef struct {
  *   H % 64 == 0, I % 64 == 0 (bf16, FP8 per-tensor);  H % 128 == 0, I % 64 == 0 (FP8
  *   blockwise, whose last 128-column scale group of I may hold 64 columns, and MXFP8);
  *   MOE_PATH_GROUPED: all four modes;  MOE_PATH_ROUTE_DIRECT: per-tensor and blockwise
- *   FP8 with H % 128 == 0 (and I % 128 == 0 for blockwise), T*k <= 1024 (AUTO takes the
- *   grouped path for the other shapes). */
+ *   FP8, T*k <= 1024. */
 
 /* ---------------------------------------------------------------- routing
  * moe_route - top-k routing (the routing step of "perf: add small-batch route
@@ -176,9 +175,9 @@ moe_status moe_tile_map(const int32_t* counts, int E, int BM, int32_t* tiles, in
 /* ---------------------------------------------------------------- forward
  * moe_select_path - the path moe_forward takes for *p (AUTO resolved):
  * bf16 and MXFP8 -> GROUPED; per-tensor FP8 -> ROUTE_DIRECT for T <= 32,
- * blockwise FP8 -> ROUTE_DIRECT for T <= 64 (both also need T*k <= 1024 and the
- * route-direct shape limits above), else GROUPED: the crossovers measured on
- * GB300.  Returns p->path when it is not AUTO. */
+ * blockwise FP8 -> ROUTE_DIRECT for T <= 64 (both also need T*k <= 1024), else
+ * GROUPED: the crossovers measured on GB300.  Returns p->path when it is not
+ * AUTO. */
 moe_path moe_select_path(const moe_problem* p);
 
 /* moe_workspace_size - bytes of device workspace moe_forward needs for *p

@@ -393,7 +393,7 @@ __host__ __device__ constexpr int ring_stage_bytes() { return ROWS_PER_CTA * RCK
 template <int RCK = CK>
 __host__ __device__ inline size_t stream_smem_bytes(int K) {
   const size_t opnd = static_cast<size_t>(GROUP) * opnd_pitch(K);
-  const size_t osc = static_cast<size_t>(GROUP) * (K / 128) * 4;
+  const size_t osc = static_cast<size_t>(GROUP) * ((K + 127) / 128) * 4;
   return 1024 + static_cast<size_t>(ring_ns<RCK>()) * ring_stage_bytes<RCK>() + opnd + ((osc + 15) / 16) * 16 +
          CONSUMERS * 32 * 4 + 2 * ring_ns<RCK>() * 8 + 16;
 }
@@ -405,7 +405,7 @@ __device__ __forceinline__ StreamSmem stream_smem(uint8_t* raw, int K) {
   m.stages = base;  // swizzled TMA box destinations: 1024-byte aligned
   m.opnd = base + ring_ns<RCK>() * ring_stage_bytes<RCK>();
   m.osc = reinterpret_cast<float*>(m.opnd + GROUP * opnd_pitch(K));
-  const size_t osc = static_cast<size_t>(GROUP) * (K / 128) * 4;
+  const size_t osc = static_cast<size_t>(GROUP) * ((K + 127) / 128) * 4;
   m.wsc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(m.osc) + ((osc + 15) / 16) * 16);
   m.full = reinterpret_cast<uint64_t*>(m.wsc + CONSUMERS * 32);
   m.empty = m.full + ring_ns<RCK>();
@@ -732,19 +732,24 @@ __global__ void __launch_bounds__(256) rd_reduce_block_kernel(DecodeArgs a) {
   pdl_wait();
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  const int I = a.I, twoI = 2 * I, ngi = I / 128;
+  // groups of 128 columns; the last one holds I % 128 columns when I % 128 == 64
+  const int I = a.I, twoI = 2 * I, ngi = (I + 127) / 128;
   if (gw >= a.R * ngi) return;
   const int r = gw / ngi, G = gw - (gw / ngi) * ngi;
-  float av[4], g[4], u[4];
-  sum_splits4(a.part, a.splits, a.R, twoI, I, r, G * 128 + lane * 4, g, u);
+  const int col = G * 128 + lane * 4;
+  const bool valid = col < I;
+  float av[4] = {0.f, 0.f, 0.f, 0.f}, g[4], u[4];
+  if (valid) {
+    sum_splits4(a.part, a.splits, a.R, twoI, I, r, col, g, u);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) av[q] = silu_mul(g[q], u[q]);
+    for (int q = 0; q < 4; ++q) av[q] = silu_mul(g[q], u[q]);
+  }
   float m = fmaxf(fmaxf(fabsf(av[0]), fabsf(av[1])), fmaxf(fabsf(av[2]), fabsf(av[3])));
   m = warp_max(m);
   const float sc = e4m3_scale(m);
   const uint32_t q = static_cast<uint32_t>(cvt_e4m3x2(av[0] / sc, av[1] / sc)) |
                      (static_cast<uint32_t>(cvt_e4m3x2(av[2] / sc, av[3] / sc)) << 16);
-  *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.act) + static_cast<size_t>(r) * I + G * 128 + lane * 4) = q;
+  if (valid) *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.act) + static_cast<size_t>(r) * I + col) = q;
   if (lane == 0) a.sh[static_cast<size_t>(r) * ngi + G] = sc;
 }
 
@@ -755,7 +760,7 @@ template <bool BLOCKWISE, int RCK>
 __global__ void __launch_bounds__(THREADS, 2) rd_down_kernel(const __grid_constant__ CUtensorMap tmw, DecodeArgs a, int nHB) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   pdl_trigger();
-  const int I = a.I, H = a.H, ngi = I / 128;
+  const int I = a.I, H = a.H, ngi = (I + 127) / 128;  // 128-column scale groups of h (last may be 64)
   const StreamSmem m = stream_smem<RCK>(smem_raw, I);
   init_ring<RCK>(m);
   pdl_wait();
@@ -796,11 +801,12 @@ __global__ void __launch_bounds__(THREADS, 2) rd_down_kernel(const __grid_consta
         r_beg = uv.off()[u] + uv.gn0()[g];
         nn = min(GROUP, uv.off()[u + 1] - r_beg);
         consumer_sync();
-        const int c4 = I / 4;
+        // blockwise MMAs read whole 128-byte K blocks: columns past I are staged as zeros
+        const int c4 = (BLOCKWISE ? ngi * 128 : I) / 4;
         for (int i = threadIdx.x; i < GROUP * c4; i += 32 * CONSUMERS) {
           const int n = i / c4, c = (i - n * c4) * 4;
           uint32_t q = 0;
-          if (n < nn) {
+          if (n < nn && c < I) {
             const int r = uv.routes()[r_beg + n];
             if (BLOCKWISE) {
               q = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(a.act) + static_cast<size_t>(r) * I + c));
@@ -824,7 +830,7 @@ __global__ void __launch_bounds__(THREADS, 2) rd_down_kernel(const __grid_consta
       const int row = hb * ROWS_PER_CTA + wr;               // rows row and row + 8 of W2[e]
       const uint8_t* hs = m.opnd + g8 * hpitch + 16 * tig;
       const float* sw = BLOCKWISE ? a.w2_scale + (static_cast<size_t>(e) * (H / 128) + row / 128) * ngi : nullptr;
-      // the item's weight scales, staged like rd_gateup's (ngi = I / 128 <= 32)
+      // the item's weight scales, staged like rd_gateup's (ngi = ceil(I / 128) <= 32)
       float* wsl = m.wsc + warp * 32;
       float wreg = 0.0f;
       if (BLOCKWISE && lane < ngi) wreg = __ldg(sw + lane);
@@ -1009,7 +1015,7 @@ cudaError_t launch_route_direct(const DecodeArgs& a, cudaStream_t s) {
 
   stage_begin("rd_reduce", s);
   if (bw) {
-    const int warps = a.R * (a.I / 128);
+    const int warps = a.R * ((a.I + 127) / 128);
     const cudaLaunchConfig_t c = config((warps * 32 + 255) / 256, 256, 0);
     err = cudaLaunchKernelEx(&c, rd_reduce_block_kernel, a);
   } else {

@@ -153,7 +153,6 @@ constexpr int kAutoRouteDirectMaxTokensBlockwise = 64;
 static moe_path resolve_path(const moe_problem& p, int S = 0) {
   if (p.path != MOE_PATH_AUTO) return p.path;
   if (p.quant == MOE_BF16 || p.quant == MOE_MXFP8 || S > 0) return MOE_PATH_GROUPED;
-  if (p.H % 128 || (p.quant == MOE_FP8_BLOCK128 && p.I % 128)) return MOE_PATH_GROUPED;
   const int limit = p.quant == MOE_FP8_BLOCK128 ? kAutoRouteDirectMaxTokensBlockwise
                                                 : kAutoRouteDirectMaxTokensPerTensor;
   if (p.T > limit || static_cast<long long>(p.T) * p.k > kRouteDirectMaxRoutes) return MOE_PATH_GROUPED;
@@ -201,9 +200,7 @@ static moe_status validate_shape(const moe_problem& p, int S = 0) {
   const moe_path path = resolve_path(p, S);
   if (path == MOE_PATH_ROUTE_DIRECT) {
     if (p.quant == MOE_BF16 || p.quant == MOE_MXFP8 || S > 0) return MOE_ERR_UNSUPPORTED;
-    // the route-direct kernels split K in whole 128-byte boxes and work on whole
-    // 128-column groups of I (blockwise)
-    if (p.H % 128 || (p.quant == MOE_FP8_BLOCK128 && p.I % 128)) return MOE_ERR_UNSUPPORTED;
+
     if (static_cast<long long>(p.T) * p.k > kRouteDirectMaxRoutes) return MOE_ERR_UNSUPPORTED;
     // shared-memory staging of one work item's operand rows
     if (p.I > 4096 || p.H / route_direct_splits(p) > 4096) return MOE_ERR_UNSUPPORTED;
@@ -264,7 +261,7 @@ bool plan_forward(const moe_problem& p, ForwardLayout* out, int S) {
     L.uniq = take(route_direct_uniq_bytes(p.T, p.E, p.k));
     L.part = take(static_cast<size_t>(L.splits) * R * 2 * I * 4);
     L.act = take(R * I * 4);
-    L.sh = take(p.quant == MOE_FP8_BLOCK128 ? R * (I / 128) * 4 : 16);
+    L.sh = take(p.quant == MOE_FP8_BLOCK128 ? R * ((I + 127) / 128) * 4 : 16);
     L.o = take(R * H * 4);
   }
   L.total = off;

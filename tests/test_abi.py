@@ -65,11 +65,11 @@ def test_workspace_size_and_path(m):
     # shapes the route-MMA page's dispatch admits: blockwise with a 64-column last scale
     # group of I, per-tensor with H % 128 == 64; the grouped path takes them
     assert m.moe_workspace_size(m.problem(1, 128, 8, 2048, 192, "fp8_block")) > 0
-    assert m.moe_select_path(m.problem(1, 128, 8, 2048, 192, "fp8_block")) == m.MOE_PATH_GROUPED
-    assert m.moe_workspace_size(m.problem(1, 128, 8, 2048, 192, "fp8_block", m.MOE_PATH_ROUTE_DIRECT)) == 0
-    assert m.moe_select_path(m.problem(1, 192, 8, 4032, 192, "fp8_tensor")) == m.MOE_PATH_GROUPED
-    assert m.moe_workspace_size(m.problem(1, 192, 8, 4032, 192, "fp8_tensor", m.MOE_PATH_ROUTE_DIRECT)) == 0
-    assert m.moe_workspace_size(m.problem(1, 192, 8, 4032, 192, "fp8_tensor")) > 0
+    assert m.moe_select_path(m.problem(1, 128, 8, 2048, 192, "fp8_block")) == m.MOE_PATH_ROUTE_DIRECT
+    assert m.moe_select_path(m.problem(512, 128, 8, 2048, 192, "fp8_block")) == m.MOE_PATH_GROUPED
+    assert m.moe_select_path(m.problem(1, 192, 8, 4032, 192, "fp8_tensor")) == m.MOE_PATH_ROUTE_DIRECT
+    assert m.moe_workspace_size(m.problem(1, 192, 8, 4032, 192, "fp8_tensor", m.MOE_PATH_ROUTE_DIRECT)) > 0
+    assert m.moe_workspace_size(m.problem(512, 192, 8, 4032, 192, "fp8_tensor")) > 0
     # grows with T
     a = m.moe_workspace_size(m.problem(1024, 16, 8, 1024, 1024))
     b = m.moe_workspace_size(m.problem(2048, 16, 8, 1024, 1024))

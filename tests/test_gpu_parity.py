@@ -788,17 +788,21 @@ def test_mxfp8_route_direct_is_rejected(m):
     assert m.moe_select_path(m.problem(2, 16, 4, 256, 128, "mxfp8")) == m.MOE_PATH_GROUPED
 
 
+@pytest.mark.parametrize("path", ["grouped", "route_direct"])
 @pytest.mark.parametrize("wl", [W.Workload("f8b_qwen_i192", 512, 128, 8, 2048, 192, W.QUANT_FP8_BLOCK, 57),
                                 W.Workload("f8t_hunyuan_h4032", 512, 192, 8, 4032, 192, W.QUANT_FP8_TENSOR, 47)],
                          ids=lambda w: w.name)
-def test_forward_page_admitted_shapes(m, wl):
+def test_forward_page_admitted_shapes(m, wl, path):
     """Shapes the route-MMA page's dispatch admits beyond this library's first
-    limits: blockwise FP8 with I % 128 == 64 and per-tensor FP8 with H % 128 == 64
-    (grouped path; AUTO takes it for these shapes at any T)."""
+    limits, on both paths: blockwise FP8 with I % 128 == 64 (a 64-column last scale
+    group of h) and per-tensor FP8 with H % 128 == 64 (a half K box at the end of
+    every weight row); the route-direct path at decode sizes."""
+    if path == "route_direct":
+        wl = wl.with_tokens(4)
     inp = W.make_inputs(wl)
-    p, y, ws = run_forward(m, wl, _dev(inp))
-    assert m.moe_select_path(p) == m.MOE_PATH_GROUPED
-    assert m.moe_select_path(m.problem(1, wl.E, wl.k, wl.H, wl.I, wl.quant)) == m.MOE_PATH_GROUPED
+    mp = m.MOE_PATH_GROUPED if path == "grouped" else m.MOE_PATH_ROUTE_DIRECT
+    p, y, ws = run_forward(m, wl, _dev(inp), path=mp)
+    assert m.moe_select_path(m.problem(wl.T, wl.E, wl.k, wl.H, wl.I, wl.quant)) == mp
     ref = O.forward(*oracle_args(inp), wl.k, wl.quant)
     _check_routing_views(m, wl, p, ws, ref, inp)
     _check_y(wl, y, ref["y"])
