@@ -27,6 +27,7 @@ the same workload and metric, each step a bounded token sample.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -270,6 +271,41 @@ def graph_replay_us(m, torch, p, args, flush, reps: int, warm: int = 20):
     return statistics.median(t), t[len(t) // 10], t[(9 * len(t)) // 10]
 
 
+CHAIN_LAYERS = 16
+
+
+def chain_replay_us(m, torch, p, layers, ws, flush, reps: int, warm: int = 10):
+    """Median µs per call of a chain of distinct layers captured in one CUDA
+    graph: layer l reads its own weights and router scores, and its input x is
+    the previous layer's y.  The weights the chain touches exceed L2 and L2 is
+    flushed before every replay (outside the events); the graph's own launch is
+    spread over the layers, as in a model that replays all its layers at once."""
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for (x, sc, w1, w2, s1, s2, y) in layers:  # eager warm-up of every layer
+            m.moe_forward(p, x, sc, w1, w2, s1, s2, y, ws, stream=s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for (x, sc, w1, w2, s1, s2, y) in layers:
+            m.moe_forward(p, x, sc, w1, w2, s1, s2, y, ws, stream=s)
+    times = []
+    with torch.cuda.stream(s):
+        for i in range(reps + warm):
+            flush.fill_(float(i))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            g.replay()
+            b.record(s)
+            b.synchronize()
+            if i >= warm:
+                times.append(a.elapsed_time(b) * 1000.0 / len(layers))
+    del g
+    if m.moe_read_device_status(ws) != m.MOE_OK:
+        raise RuntimeError("device status not OK after chain replays")
+    return statistics.median(times)
+
+
 def run_decode_sweep(m, torch, dev, peaks, reps: int):
     """Both paths at every B: the route-direct path and the grouped path (the
     crossover that sets the AUTO dispatch), reported for the path AUTO takes."""
@@ -280,6 +316,9 @@ def run_decode_sweep(m, torch, dev, peaks, reps: int):
     for name in W.DECODE_SWEEPS:
         base = W.workload(name, 1)
         w1, w2, s1, s2 = W.make_weights(base, device=dev)
+        # the layer chain's weights: copies of the sweep's experts at distinct addresses
+        chain_w = [(w1.clone(), w2.clone(), None if s1 is None else s1.clone(), None if s2 is None else s2.clone())
+                   for _ in range(CHAIN_LAYERS)]
         per_b = []
         for B in range(1, 9):
             wl = W.workload(name, B)
@@ -303,6 +342,19 @@ def run_decode_sweep(m, torch, dev, peaks, reps: int):
             w1e = 2 * wl.I * wl.H + (0 if s1 is None else s1[0].numel() * 4)
             w2e = wl.H * wl.I + (0 if s2 is None else s2[0].numel() * 4)
             algo = U * (w1e + w2e) + wl.T * wl.H * 2 * 2 + wl.T * wl.E * 4
+            # the chain of CHAIN_LAYERS distinct layers on the AUTO path (own scores per layer)
+            pa = m.problem(wl.T, wl.E, wl.k, wl.H, wl.I, wl.quant)
+            wsa = torch.empty(m.moe_workspace_size(pa), dtype=torch.uint8, device=dev)
+            ys = [torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev) for _ in range(CHAIN_LAYERS)]
+            layers, chain_algo = [], 0
+            for li in range(CHAIN_LAYERS):
+                scl = W.make_scores(dataclasses.replace(wl, seed=wl.seed * 1000 + li))
+                Ul = int(torch.unique(torch.topk(scl, wl.k, dim=1).indices).numel())
+                chain_algo += Ul * (w1e + w2e) + wl.T * wl.H * 2 * 2 + wl.T * wl.E * 4
+                cw = chain_w[li]
+                layers.append((x if li == 0 else ys[li - 1], scl.to(dev), cw[0], cw[1], cw[2], cw[3], ys[li]))
+            chain_us = chain_replay_us(m, torch, pa, layers, wsa, flush, reps)
+            del wsa, ys, layers
             per_b.append({"B": B, "auto_path": auto_name, "us": round(us, 3), "p10_us": round(p10, 3),
                           "p90_us": round(p90, 3),
                           "route_direct_us": round(res["route_direct"][0], 3),
@@ -310,13 +362,19 @@ def run_decode_sweep(m, torch, dev, peaks, reps: int):
                           "distinct_experts": U, "algo_bytes": algo,
                           "hbm_gbs": round(algo / (us * 1e-6) / 1e9, 1),
                           "hbm_frac": round(algo / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                          "chain_us": round(chain_us, 3),
+                          "chain_hbm_frac": round(chain_algo / CHAIN_LAYERS / (chain_us * 1e-6) / 1e9
+                                                  / peaks["hbm_gbs"], 4),
                           "h20_route_mma_us": H20_ROUTE_MMA_US[name][B - 1],
                           "tokens_per_s": round(B / (us * 1e-6), 1)})
         out[name] = {"E": base.E, "H": base.H, "I": base.I, "top_k": base.k, "quant": base.quant,
                      "timing": f"CUDA-graph replay, median of {reps} after 20 warm-up replays, "
                                "L2 flushed before each replay (outside the events)",
+                     "chain_timing": f"chain_us: one CUDA graph of {CHAIN_LAYERS} layers with distinct "
+                                     "weights and router scores, each layer's x the previous layer's y; "
+                                     "graph time / layers, L2 flushed before each replay; AUTO path",
                      "by_batch": per_b}
-        del w1, w2, s1, s2
+        del w1, w2, s1, s2, chain_w
         torch.cuda.empty_cache()
     return out
 

@@ -353,6 +353,19 @@ __device__ __forceinline__ void tmem_ld_wait_regs(float (&v)[32]) {
 // ------------------------------------------------------------------ numerics
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
+// Two independent fp32 fused multiply-adds in one instruction (fma.rn.f32x2):
+// d0 = a0 * b0 + d0, d1 = a1 * b1 + d1, each rounded once to nearest even like fmaf.
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rd, {%0, %1};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rd;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // fp32 -> e4m3 (round to nearest even, saturate to +-448), two values per instruction.
 __device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
   uint16_t r;

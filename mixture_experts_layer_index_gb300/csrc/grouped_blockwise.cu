@@ -322,9 +322,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (lane == 0) mbar_arrive(pempty0 + 8 * pb);
           const float s0 = sak * sgk, s1 = sak * (MODE == MODE_GATEUP ? suk : sgk);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            acc[i] = fmaf(v0[i], s0, acc[i]);
-            acc[32 + i] = fmaf(v1[i], s1, acc[32 + i]);
+          for (int i = 0; i < 32; i += 2) {  // packed pairs: half the FMA instructions
+            fma2(acc[i], acc[i + 1], v0[i], v0[i + 1], s0, s0);
+            fma2(acc[32 + i], acc[33 + i], v1[i], v1[i + 1], s1, s1);
           }
           if (++pb == NBUF) {
             pb = 0;
