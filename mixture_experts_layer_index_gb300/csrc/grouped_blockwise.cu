@@ -5,25 +5,29 @@
 // per (row, 128 columns), so every 128-wide K block has its own scale pair and
 // the products cannot be summed inside one accumulator.  Each K block is a
 // 128-byte stage of e4m3: the MMA thread writes that block's partial product
-// (tcgen05.mma kind::f8f6f4, M=128, N=128, 4 x K=32) into one of four TMEM
-// buffers, and eight epilogue warps read it with tcgen05.ld, multiply by
+// (tcgen05.mma kind::f8f6f4, M=128, N=256, 4 x K=32) into one of two 256-column
+// TMEM buffers, and eight epilogue warps read it with tcgen05.ld, multiply by
 // s_a[row, kb] * s_w[block, kb] and add it into fp32 registers ("promotion")
-// while the MMA fills the next buffers.  Two warps share each 32-lane TMEM
-// quadrant (one accumulator row per thread), each holding 64 of the 128
-// columns, so the loads of one warp overlap the FMAs of the other.
+// while the MMA fills the other buffer.  Two warps share each 32-lane TMEM
+// quadrant (one accumulator row per thread), each holding 128 of the 256
+// columns.  A 256-column tile moves 96 bytes of operands per MMA cycle where a
+// 128-column one moves 128: the tile width, not the promotion, bounded the
+// 128-column version of these kernels.
 //
-// Gate/Up: N = 64 gate + the matching 64 up rows of W1[e] (two 64-row TMA
-//   boxes), A = expert-sorted e4m3 x rows with their group scales.  Work items
-//   are pairs of units (n = 2g, 2g + 1) of one row tile, processed one after the
-//   other by the same CTA, so that the two units together cover the 128-column
-//   group g of h: a warp holds 32 gate and the matching 32 up columns of a row
-//   and computes a = silu(g) * u; after the first unit it keeps a in shared
-//   memory, after the second the two warps of a quadrant exchange their row
-//   maxima, and each quantises its 64 values of the row with the group's scale
-//   amax / 448 straight into e4m3 h and the fp32 scale (a ragged last group of
-//   64 columns is a single unit).
-// Down: N = 128 rows of W2[e] (one weight scale block), A = e4m3 h rows with
-//   their group scales; the epilogue writes bf16 o for the tile's sorted rows.
+// Gate/Up: a work item is (row tile, group g of 128 h columns); B = the 128 gate
+//   rows [g*128, g*128 + 128) and the matching 128 up rows [I + g*128, ...) of
+//   W1[e] (two 128-row TMA boxes), so one K loop covers a whole scale group of h.
+//   Warp c of a quadrant holds gate columns [64c, 64c + 64) and the matching up
+//   columns of its rows; after the last K block it computes a = silu(g) * u, the
+//   two warps exchange their row maxima through shared memory (bounded mbarrier
+//   waits), and each quantises its 64 values of the row with the group's scale
+//   amax / 448 straight into e4m3 h and the fp32 scale.  In a ragged last group
+//   (I % 128 == 64) the warp whose columns are >= I skips its stores and
+//   contributes 0 to the row maximum.
+// Down: a work item is (row tile, 256 rows n of W2[e], two weight scale blocks);
+//   warp c holds o columns [n*256 + 128c, + 128) (one scale block) and writes them
+//   as bf16 for the tile's sorted rows, staged in shared memory in two passes of
+//   64 columns.  A ragged last N tile (H % 256 == 128) has no columns for c = 1.
 #include "common.cuh"
 #include "internal.h"
 
@@ -31,27 +35,24 @@ namespace moe {
 namespace gb {
 
 constexpr int BM = kGemmBM;  // 128
-constexpr int BN = 128;
-constexpr int BKB = 128;  // K bytes (= e4m3 elements) per stage, one scale block
-constexpr int MAX_STAGES = 6;
-// Gate/Up: 6 stages, 32 KB of staging (the first unit's a of a pair) and 1 KB for
-// the row maxima; Down: 5 stages and 32 KB of output staging.
-__host__ __device__ constexpr int stages_of(int mode) { return mode == 0 ? 6 : 5; }
-constexpr int A_BYTES = BM * BKB;
-constexpr int B_BYTES = BN * BKB;
+constexpr int BN = 256;
+constexpr int BKB = 128;     // K bytes (= e4m3 elements) per stage, one scale block
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BKB;  // 16 KB
+constexpr int B_BYTES = BN * BKB;  // 32 KB: two 128-row boxes
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NBUF = 4;           // TMEM partial buffers of 128 columns
+constexpr int NBUF = 2;            // TMEM partial buffers of 256 columns
 constexpr int TMEM_COLS = NBUF * BN;
-constexpr int EPI_WARPS = 8;      // warps 4..11
-constexpr int THREADS = 32 * (4 + EPI_WARPS);
-constexpr int NUM_BARS = 2 * MAX_STAGES + 2 * NBUF + 8;  // + the Gate/Up row-maximum exchange (2 per quadrant)
-__host__ __device__ constexpr int staging_offset(int mode) { return (stages_of(mode) * STAGE_BYTES + 256 + 1023) / 1024 * 1024; }
-constexpr int STAGING_BYTES = EPI_WARPS * 32 * 128;
-constexpr int ROWMAX_BYTES = EPI_WARPS * 32 * 4;
-__host__ __device__ constexpr size_t smem_bytes(int mode) {
-  return 1024 + staging_offset(mode) + STAGING_BYTES + (mode == 0 ? ROWMAX_BYTES : 0);
-}
-static_assert(smem_bytes(0) <= 232448 && smem_bytes(1) <= 232448, "shared memory per block");
+constexpr int EPI_WARPS = 8;       // warps 2..9 (the block's registers come in 4-warp groups: 168 a thread)
+constexpr int THREADS = 32 * (2 + EPI_WARPS);
+constexpr int NUM_BARS = 2 * STAGES + 2 * NBUF + 8;
+constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
+constexpr int SCRATCH_OFFSET = BAR_OFFSET + 256;
+// epilogue scratch: Gate/Up row maxima [8 warps][32] fp32; Down output staging [8 warps][32 rows][128 bytes]
+constexpr int SCRATCH_BYTES = EPI_WARPS * 32 * 128;
+constexpr size_t SMEM_BYTES = 1024 + SCRATCH_OFFSET + SCRATCH_BYTES;
+static_assert(NUM_BARS * 8 + 8 <= 256, "barrier region");
+static_assert(SMEM_BYTES <= 232448, "shared memory per block");
 
 constexpr int MODE_GATEUP = 0;
 constexpr int MODE_DOWN = 1;
@@ -60,8 +61,7 @@ struct Params {
   const int32_t* tiles;
   const int32_t* num_tiles;
   int max_tiles;
-  const int32_t* perm;
-  int nN;          // units per row tile (Gate/Up: 64 h columns each; Down: 128 o columns)
+  int nN;          // work items per row tile (Gate/Up: 128-column groups of h; Down: 256-column tiles of o)
   int K;           // reduction length (bytes = elements)
   int I, H;
   const float* a_scale;  // [R][ceil(K/128)] scales of the A rows (sorted order)
@@ -73,6 +73,7 @@ struct Params {
   __nv_bfloat16* out;    // Down: o [R][H]
   DeviceHeader* hdr;
 };
+
 
 // silu(g) * u with the fast exponential and division intrinsics: a is rounded to
 // e4m3 next, far coarser than their error.  Here the SwiGLU runs in the tile's
@@ -108,26 +109,22 @@ __device__ __forceinline__ void store_e4m3x32(uint8_t* dst, const float* a, floa
 }
 
 // Work items: Gate/Up pairs (row tile, group g = units 2g and 2g + 1, or just 2g for
-// a ragged last group); Down units (row tile, n).
-__device__ __forceinline__ int items_per_tile(int mode, int nN) { return mode == 0 ? (nN + 1) / 2 : nN; }
-__device__ __forceinline__ int subunits(int mode, int nN, int g) { return mode == 0 ? min(2, nN - 2 * g) : 1; }
 
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_blockwise_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                             const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmB2,
-                             const Params p) {
-  constexpr int STAGES = stages_of(MODE);
+                             const __grid_constant__ CUtensorMap tmB2, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFFSET);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint8_t* scratch = smem + SCRATCH_OFFSET;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   const uint32_t pfull0 = smem_u32(bars + 2 * STAGES), pempty0 = smem_u32(bars + 2 * STAGES + NBUF);
-  // Gate/Up: per quadrant q, xbar0 + 8q (row maxima written) and xbar0 + 8 (4 + q) (read)
+  // Gate/Up, per quadrant q: xbar0 + 8q (row maxima written), xbar0 + 8 (4 + q) (row maxima read)
   const uint32_t xbar0 = smem_u32(bars + 2 * STAGES + 2 * NBUF);
 
   if (threadIdx.x == 0) {
@@ -148,7 +145,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     prefetch_tensormap(&tmB);
     prefetch_tensormap(&tmB2);
   }
-  if (warp == 2) {
+  if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tmem_relinquish();
   }
@@ -156,11 +153,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  dep_wait();  // the tile map and the A rows come from the kernels before (the set-up above overlaps them)
+  dep_wait();  // the tile map, the A rows and their scales come from the kernels before
 
   const int ntiles = min(*p.num_tiles, p.max_tiles);
-  const int ipt = items_per_tile(MODE, p.nN);
-  const int items = ntiles * ipt;
+  const int items = ntiles * p.nN;
   const int nk = (p.K + BKB - 1) / BKB;
   const int4* tiles = reinterpret_cast<const int4*>(p.tiles);
 
@@ -170,45 +166,40 @@ __global__ void __launch_bounds__(THREADS, 1)
     int issued = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-      const int tile = it / ipt, g = it - tile * ipt;
+      const int tile = it / p.nN, n = it - tile * p.nN;
       const int4 tl = tiles[tile];
-      const int row0 = tl.y;
       const bool shx = tl.x >= p.E;  // a shared expert's tile: its own weight tensor
       const int e = shx ? tl.x - p.E : tl.x;
       const CUtensorMap* tb = shx ? &tmB2 : &tmB;
-      const int nsub = subunits(MODE, p.nN, g);
-      for (int sub = 0; sub < nsub && ok; ++sub) {
-        const int n = MODE == MODE_GATEUP ? 2 * g + sub : g;
-        for (int kb = 0; kb < nk; ++kb) {
-          if (lane == 0) {
-            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.hdr, 0x80000u | MODE)) ok = false;
-          }
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-          if (!ok) break;
-          if (lane == 0) {
-            const uint32_t full = full0 + 8 * stage;
-            const uint32_t a_dst = smem_u32(smem + stage * STAGE_BYTES), b_dst = a_dst + A_BYTES;
-            const int kc = kb * BKB;
-            mbar_arrive_expect_tx(full, STAGE_BYTES);
-            tma_load_2d(a_dst, &tmA, kc, row0, full);
-            if (MODE == MODE_GATEUP) {
-              const int brow = e * 2 * p.I + n * (BN / 2);
-              tma_load_2d(b_dst, tb, kc, brow, full);                   // 64 gate rows
-              tma_load_2d(b_dst + B_BYTES / 2, tb, kc, brow + p.I, full);  // the matching 64 up rows
-            } else {
-              tma_load_2d(b_dst, tb, kc, e * p.H + n * BN, full);
-            }
-          }
-          __syncwarp();
-          ++issued;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
+      // B: Gate/Up the 128 gate rows of group n and the matching 128 up rows; Down 256 rows of W2[e]
+      const int brow0 = MODE == MODE_GATEUP ? e * 2 * p.I + n * 128 : e * p.H + n * BN;
+      const int brow1 = MODE == MODE_GATEUP ? brow0 + p.I : brow0 + 128;
+      for (int kb = 0; kb < nk; ++kb) {
+        int good = 1;
+        if (lane == 0) good = mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.hdr, 0x80000u | MODE);
+        if (!__shfl_sync(0xffffffffu, good, 0)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t full = full0 + 8 * stage;
+          const uint32_t a_dst = smem_u32(smem + stage * STAGE_BYTES), b_dst = a_dst + A_BYTES;
+          const int kc = kb * BKB;
+          mbar_arrive_expect_tx(full, STAGE_BYTES);
+          tma_load_2d(a_dst, &tmA, kc, tl.y, full);
+          tma_load_2d(b_dst, tb, kc, brow0, full);
+          tma_load_2d(b_dst + B_BYTES / 2, tb, kc, brow1, full);
+        }
+        __syncwarp();
+        ++issued;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
         }
       }
     }
     if (!ok && lane == 0) {
+      // aborted: let the copies already issued land before shared memory is released
       for (int i = 0; i < min(issued, STAGES); ++i) {
         stage = (stage + STAGES - 1) % STAGES;
         if (stage == STAGES - 1) phase ^= 1;
@@ -222,8 +213,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t stage = 0, phase = 0, pb = 0, pphase = 0;
       bool ok = true;
       for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-        const int nsub = subunits(MODE, p.nN, it % ipt);
-        for (int kt = 0; kt < nsub * nk; ++kt) {
+        for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.hdr, 0x81000u | MODE) ||
               !mbar_wait(pempty0 + 8 * pb, pphase ^ 1, abort_flag, p.hdr, 0x82000u | MODE)) {
             ok = false;
@@ -253,174 +243,157 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_wait_quiet(pfull0 + 8 * lb, pb == 0 ? (pphase ^ 1) : pphase, 1000000000ull);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  } else {
     // ---------------------------------------------------------------- epilogue (promotion)
-    const int e8 = warp - 4;
-    const int q = e8 & 3;   // TMEM lane quadrant (warp % 4)
-    const int ch = e8 >> 2; // which 64 of the 128 columns
+    const int e8 = warp - 2;
+    const int q = warp & 3;   // TMEM lane quadrant
+    const int c = e8 >> 2;    // which 128 of the tile's 256 accumulator columns (Gate/Up: 64 gate + 64 up)
     const int row = q * 32 + lane;
-    // Gate/Up: gate columns [32ch, 32ch+32) and the matching up columns 64 + [32ch, ...);
-    // Down: columns [64ch, 64ch+64)
-    const int c0 = MODE == MODE_GATEUP ? ch * 32 : ch * 64;
-    const int c1 = MODE == MODE_GATEUP ? BN / 2 + ch * 32 : ch * 64 + 32;
-    uint32_t pb = 0, pphase = 0;
-    const int kblocks = nk;  // scale groups along K: ceil(K / 128)
-    float* rowmax = reinterpret_cast<float*>(smem + staging_offset(MODE) + STAGING_BYTES);  // Gate/Up: [8 warps][32]
-    uint32_t xphase = 0;  // phase of this quadrant's exchange barriers
+    float* rowmax = reinterpret_cast<float*>(scratch);  // Gate/Up: [8 warps][32]
+    uint32_t pb = 0, pphase = 0, xphase = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-      const int tile = it / ipt, g = it - tile * ipt;
+      const int tile = it / p.nN, n = it - tile * p.nN;
       const int4 tl = tiles[tile];
       const int row0 = tl.y, nrows = tl.z;
       const bool shx = tl.x >= p.E;
       const int e = shx ? tl.x - p.E : tl.x;
       const float* wsc = shx ? p.w_scale2 : p.w_scale;
-      const int arow = row0 + min(row, nrows - 1);
-      const float* sa = p.a_scale + static_cast<size_t>(arow) * kblocks;
-      const int nsub = subunits(MODE, p.nN, g);
-      float mrow = 0.0f;  // Gate/Up: this thread's row maximum of |a| over the group so far
-      for (int sub = 0; sub < nsub && ok; ++sub) {
-        const int n = MODE == MODE_GATEUP ? 2 * g + sub : g;
-        // weight scale rows of this unit's columns (both halves in one block for Down)
-        const float* swg;
-        const float* swu;
-        if (MODE == MODE_GATEUP) {
-          const int nblk = 2 * p.I / 128, hblk = p.H / 128;
-          swg = wsc + (static_cast<size_t>(e) * nblk + (n * (BN / 2)) / 128) * hblk;
-          swu = wsc + (static_cast<size_t>(e) * nblk + (p.I + n * (BN / 2)) / 128) * hblk;
-        } else {
-          const int hblk = p.H / 128;
-          swg = wsc + (static_cast<size_t>(e) * hblk + n) * kblocks;
-          swu = swg;
+      // this warp's first output column: Gate/Up an h column, Down an o column
+      const int col = MODE == MODE_GATEUP ? n * 128 + 64 * c : n * BN + 128 * c;
+      const bool valid = col < (MODE == MODE_GATEUP ? p.I : p.H);
+      const float* sa = p.a_scale + static_cast<size_t>(row0 + min(row, nrows - 1)) * nk;
+      // weight scale rows: Gate/Up gate block col/128 and up block (I + col)/128 of
+      // [E][2I/128][H/128]; Down block col/128 of [E][H/128][nk]
+      const int wrows = MODE == MODE_GATEUP ? 2 * p.I / 128 : p.H / 128;
+      const float* sw0 = wsc + (static_cast<size_t>(e) * wrows + col / 128) * nk;
+      const float* sw1 = MODE == MODE_GATEUP ? wsc + (static_cast<size_t>(e) * wrows + (p.I + col) / 128) * nk : sw0;
+      float acc[128];  // Gate/Up: [0, 64) gate, [64, 128) up
+#pragma unroll
+      for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+      float sa_next = 0.0f, s0_next = 0.0f, s1_next = 0.0f;
+      if (valid) {
+        sa_next = __ldg(sa);
+        s0_next = __ldg(sw0);
+        s1_next = __ldg(sw1);
+      }
+      for (int kb = 0; kb < nk; ++kb) {
+        const float sak = sa_next, s0k = s0_next, s1k = s1_next;
+        if (valid && kb + 1 < nk) {
+          sa_next = __ldg(sa + kb + 1);
+          s0_next = __ldg(sw0 + kb + 1);
+          s1_next = __ldg(sw1 + kb + 1);
         }
-        float acc[64];
-#pragma unroll
-        for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
-        float sa_next = __ldg(sa), sg_next = __ldg(swg), su_next = __ldg(swu);
-        for (int kb = 0; kb < nk; ++kb) {
-          const float sak = sa_next, sgk = sg_next, suk = su_next;
-          if (kb + 1 < nk) {
-            sa_next = __ldg(sa + kb + 1);
-            sg_next = __ldg(swg + kb + 1);
-            su_next = __ldg(swu + kb + 1);
-          }
-          int good = 1;
-          if (lane == 0) good = mbar_wait(pfull0 + 8 * pb, pphase, abort_flag, p.hdr, 0x83000u | MODE);
-          if (!__shfl_sync(0xffffffffu, good, 0)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + pb * BN;
-          float v0[32], v1[32];
-          tmem_ld32(tbase + c0, v0);
-          tmem_ld32(tbase + c1, v1);
-          tmem_ld_wait();
-          // both column ranges are in registers: hand the buffer back before the FMAs
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(pempty0 + 8 * pb);
-          const float s0 = sak * sgk, s1 = sak * (MODE == MODE_GATEUP ? suk : sgk);
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {  // packed pairs: half the FMA instructions
-            fma2(acc[i], acc[i + 1], v0[i], v0[i + 1], s0, s0);
-            fma2(acc[32 + i], acc[33 + i], v1[i], v1[i + 1], s1, s1);
-          }
-          if (++pb == NBUF) {
-            pb = 0;
-            pphase ^= 1;
-          }
+        int good = 1;
+        if (lane == 0) good = mbar_wait(pfull0 + 8 * pb, pphase, abort_flag, p.hdr, 0x83000u | MODE);
+        if (!__shfl_sync(0xffffffffu, good, 0)) {
+          ok = false;
+          break;
         }
-        if (!ok) break;
-        if (MODE == MODE_GATEUP) {
-          // a for 32 h columns of this row; the first unit of a pair parks its values in
-          // this warp's staging slot (row-per-lane, 16-byte pieces XOR-swizzled by lane)
-          float a[32];
-          float m = 0.0f;
+        tc_fence_after();
+        // Gate/Up: gate columns at 64c, up columns at 128 + 64c; Down: columns at 128c
+        const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + pb * BN;
+        const uint32_t t0 = tq + (MODE == MODE_GATEUP ? 64 * c : 128 * c);
+        const uint32_t t1 = MODE == MODE_GATEUP ? tq + 128 + 64 * c : t0 + 64;
+        const float s0 = sak * s0k, s1 = sak * s1k;
+        float v[16];
+        // 16 columns at a time (the accumulators take 128 of the 168 registers a thread)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            a[i] = silu_mul_fast(acc[i], acc[32 + i]);
-            m = fmaxf(m, fabsf(a[i]));
-          }
-          mrow = fmaxf(mrow, m);
-          float4* stg = reinterpret_cast<float4*>(smem + staging_offset(MODE) + e8 * 4096) + lane * 8;
-          if (sub == 0 && nsub == 2) {
+        for (int h = 0; h < 4; ++h) {
+          tmem_ld16(t0 + 16 * h, v);
+          tmem_ld_wait_regs16(v);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              stg[i ^ (lane & 7)] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
-          }
-          if (sub == nsub - 1) {
-            // the group's scale: row maximum over both warps of the quadrant (64 columns
-            // each), exchanged through shared memory between the two warps; bounded
-            // mbarrier waits order the write, the partner's read and the next write
-            rowmax[e8 * 32 + lane] = row < nrows ? mrow : 0.0f;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(xbar0 + 8 * q);
-            int good = 1;
-            if (lane == 0) good = mbar_wait(xbar0 + 8 * q, xphase, abort_flag, p.hdr, 0x84000u);
-            if (!__shfl_sync(0xffffffffu, good, 0)) {
-              ok = false;
-              break;
-            }
-            const float gm = fmaxf(rowmax[e8 * 32 + lane], rowmax[(e8 ^ 4) * 32 + lane]);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(xbar0 + 8 * (4 + q));
-            if (lane == 0) good = mbar_wait(xbar0 + 8 * (4 + q), xphase, abort_flag, p.hdr, 0x85000u);
-            if (!__shfl_sync(0xffffffffu, good, 0)) {
-              ok = false;
-              break;
-            }
-            xphase ^= 1;
-            if (row < nrows) {
-              const float sc = e4m3_scale(gm);
-              const float inv = 1.0f / sc;
-              const size_t r = static_cast<size_t>(row0 + row);
-              uint8_t* hrow = p.h + r * p.I;
-              if (nsub == 2) {
-                // the first unit's values, 4 at a time from the staging slot
-                uint32_t w[8];
+          for (int i = 0; i < 16; i += 2) fma2(acc[16 * h + i], acc[16 * h + i + 1], v[i], v[i + 1], s0, s0);
+        }
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  const float4 v = stg[i ^ (lane & 7)];
-                  w[i] = static_cast<uint32_t>(cvt_e4m3x2(v.x * inv, v.y * inv)) |
-                         (static_cast<uint32_t>(cvt_e4m3x2(v.z * inv, v.w * inv)) << 16);
-                }
-                uint4* d0 = reinterpret_cast<uint4*>(hrow + (2 * g) * 64 + ch * 32);
-                d0[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                d0[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                store_e4m3x32(hrow + (2 * g + 1) * 64 + ch * 32, a, inv);
-              } else {
-                store_e4m3x32(hrow + (2 * g) * 64 + ch * 32, a, inv);
-              }
-              if (ch == 0) p.h_scale[r * ((p.I + 127) / 128) + g] = sc;
-            }
-          }
-        } else {
-          // Down rows (sorted order, like h): each thread's 64 bf16 outputs are staged
-          // in shared memory (16-byte pieces XOR-swizzled by row) and the warp writes
-          // four whole 128-byte row segments per store instruction.
-          uint4* stg = reinterpret_cast<uint4*>(smem + staging_offset(MODE)) + e8 * (32 * 8);
+        for (int h = 0; h < 3; ++h) {
+          tmem_ld16(t1 + 16 * h, v);
+          tmem_ld_wait_regs16(v);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) stg[lane * 8 + (i ^ (lane & 7))] = pack_bf16x8(acc + 8 * i);
+          for (int i = 0; i < 16; i += 2)
+            fma2(acc[64 + 16 * h + i], acc[64 + 16 * h + i + 1], v[i], v[i + 1], s1, s1);
+        }
+        tmem_ld16(t1 + 48, v);
+        tmem_ld_wait_regs16(v);
+        // the last columns are in registers: hand the buffer back before their FMAs
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pempty0 + 8 * pb);
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) fma2(acc[112 + i], acc[113 + i], v[i], v[i + 1], s1, s1);
+        if (++pb == NBUF) {
+          pb = 0;
+          pphase ^= 1;
+        }
+      }
+      if (!ok) break;
+      if (MODE == MODE_GATEUP) {
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          acc[i] = silu_mul_fast(acc[i], acc[64 + i]);  // a
+          m = fmaxf(m, fabsf(acc[i]));
+        }
+        // the group's scale: row maximum over the quadrant's two warps (64 columns each)
+        rowmax[e8 * 32 + lane] = (valid && row < nrows) ? m : 0.0f;
+        __syncwarp();
+        int good = 1;
+        if (lane == 0) {
+          mbar_arrive(xbar0 + 8 * q);
+          good = mbar_wait(xbar0 + 8 * q, xphase, abort_flag, p.hdr, 0x84000u);
+        }
+        if (!__shfl_sync(0xffffffffu, good, 0)) {
+          ok = false;
+          break;
+        }
+        const float gm = fmaxf(rowmax[e8 * 32 + lane], rowmax[(e8 ^ 4) * 32 + lane]);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(xbar0 + 8 * (4 + q));
+          good = mbar_wait(xbar0 + 8 * (4 + q), xphase, abort_flag, p.hdr, 0x85000u);
+        }
+        if (!__shfl_sync(0xffffffffu, good, 0)) {
+          ok = false;
+          break;
+        }
+        xphase ^= 1;
+        if (valid && row < nrows) {
+          const float sc = e4m3_scale(gm);
+          const float inv = 1.0f / sc;
+          const size_t r = static_cast<size_t>(row0 + row);
+          store_e4m3x32(p.h + r * p.I + col, acc, inv);
+          store_e4m3x32(p.h + r * p.I + col + 32, acc + 32, inv);
+          if (c == 0) p.h_scale[r * p.nN + n] = sc;
+        }
+      } else if (valid) {
+        // o rows (sorted order, like h): each thread's 128 bf16 outputs go through this
+        // warp's 4 KB of staging in two passes of 64 columns (16-byte pieces XOR-swizzled
+        // by row), and the warp writes four whole 128-byte row segments per store.
+        uint4* stg = reinterpret_cast<uint4*>(scratch) + e8 * (32 * 8);
+        const int vrows = min(32, nrows - q * 32);  // valid rows of this warp (may be <= 0)
+        const int slot = row0 + row;
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+          __syncwarp();  // the previous pass's reads of the staging are done
+#pragma unroll
+          for (int i = 0; i < 8; ++i) stg[lane * 8 + (i ^ (lane & 7))] = pack_bf16x8(acc + 64 * pass + 8 * i);
           __syncwarp();
-          const int wrows = min(32, nrows - q * 32);  // valid rows of this warp (may be <= 0)
-          const int slot = row0 + row;
 #pragma unroll
           for (int it2 = 0; it2 < 8; ++it2) {
             const int r = it2 * 4 + (lane >> 3), j = lane & 7;
             const int rslot = __shfl_sync(0xffffffffu, slot, r);
-            if (r < wrows)
-              *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(rslot) * p.H + n * BN + ch * 64 + j * 8) =
+            if (r < vrows)
+              *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(rslot) * p.H + col + 64 * pass + j * 8) =
                   stg[r * 8 + (j ^ (r & 7))];
           }
-          __syncwarp();
         }
+        __syncwarp();
       }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
@@ -441,7 +414,7 @@ static bool encode_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64
 template <int MODE>
 static cudaError_t smem_attr() {
   static const cudaError_t st = cudaFuncSetAttribute(grouped_blockwise_kernel<MODE>,
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes(MODE));
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   return st;
 }
 
@@ -455,17 +428,16 @@ cudaError_t launch_gateup_blockwise(const GroupedArgs& a, const float* xs_scale,
   const int sms = num_sms();
   if (sms <= 0) return cudaErrorNoDevice;
   CUtensorMap tma, tmb, tmbs;
-  if (!encode_u8(&tma, a.xs, a.H, a.R, BM) || !encode_u8(&tmb, a.w1, a.H, static_cast<uint64_t>(a.E) * 2 * a.I, BN / 2))
+  if (!encode_u8(&tma, a.xs, a.H, a.R, BM) || !encode_u8(&tmb, a.w1, a.H, static_cast<uint64_t>(a.E) * 2 * a.I, 128))
     return cudaErrorInvalidValue;
   tmbs = tmb;
-  if (a.S > 0 && !encode_u8(&tmbs, a.w1s, a.H, static_cast<uint64_t>(a.S) * 2 * a.I, BN / 2))
+  if (a.S > 0 && !encode_u8(&tmbs, a.w1s, a.H, static_cast<uint64_t>(a.S) * 2 * a.I, 128))
     return cudaErrorInvalidValue;
   Params p{};
   p.tiles = a.tiles;
   p.num_tiles = a.num_tiles;
   p.max_tiles = a.max_tiles;
-  p.perm = a.perm;
-  p.nN = a.I / (BN / 2);
+  p.nN = (a.I + 127) / 128;
   p.K = a.H;
   p.I = a.I;
   p.H = a.H;
@@ -476,11 +448,11 @@ cudaError_t launch_gateup_blockwise(const GroupedArgs& a, const float* xs_scale,
   p.h = static_cast<uint8_t*>(a.h);
   p.h_scale = h_scale;
   p.hdr = a.hdr;
-  const long long items = static_cast<long long>(a.max_tiles) * ((p.nN + 1) / 2);
+  const long long items = static_cast<long long>(a.max_tiles) * p.nN;
   const int grid = static_cast<int>(items < sms ? items : sms);
   stage_begin("gateup_gemm", s);
-  err = launch_dependent(grouped_blockwise_kernel<MODE_GATEUP>, dim3(grid), dim3(THREADS), smem_bytes(MODE_GATEUP), s,
-                         tma, tmb, tma, tmbs, p);
+  err = launch_dependent(grouped_blockwise_kernel<MODE_GATEUP>, dim3(grid), dim3(THREADS), SMEM_BYTES, s, tma, tmb,
+                         tmbs, p);
   stage_end(s);
   return err;
 }
@@ -493,16 +465,15 @@ cudaError_t launch_down_blockwise(const GroupedArgs& a, const float* h_scale, cu
   const int sms = num_sms();
   if (sms <= 0) return cudaErrorNoDevice;
   CUtensorMap tma, tmb, tmbs;
-  if (!encode_u8(&tma, a.h, a.I, a.R, BM) || !encode_u8(&tmb, a.w2, a.I, static_cast<uint64_t>(a.E) * a.H, BN))
+  if (!encode_u8(&tma, a.h, a.I, a.R, BM) || !encode_u8(&tmb, a.w2, a.I, static_cast<uint64_t>(a.E) * a.H, 128))
     return cudaErrorInvalidValue;
   tmbs = tmb;
-  if (a.S > 0 && !encode_u8(&tmbs, a.w2s, a.I, static_cast<uint64_t>(a.S) * a.H, BN)) return cudaErrorInvalidValue;
+  if (a.S > 0 && !encode_u8(&tmbs, a.w2s, a.I, static_cast<uint64_t>(a.S) * a.H, 128)) return cudaErrorInvalidValue;
   Params p{};
   p.tiles = a.tiles;
   p.num_tiles = a.num_tiles;
   p.max_tiles = a.max_tiles;
-  p.perm = a.perm;
-  p.nN = a.H / BN;
+  p.nN = (a.H + BN - 1) / BN;
   p.K = a.I;
   p.I = a.I;
   p.H = a.H;
@@ -515,8 +486,8 @@ cudaError_t launch_down_blockwise(const GroupedArgs& a, const float* h_scale, cu
   const long long units = static_cast<long long>(a.max_tiles) * p.nN;
   const int grid = static_cast<int>(units < sms ? units : sms);
   stage_begin("down_gemm", s);
-  err = launch_dependent(grouped_blockwise_kernel<MODE_DOWN>, dim3(grid), dim3(THREADS), smem_bytes(MODE_DOWN), s,
-                         tma, tmb, tma, tmbs, p);
+  err = launch_dependent(grouped_blockwise_kernel<MODE_DOWN>, dim3(grid), dim3(THREADS), SMEM_BYTES, s, tma, tmb, tmbs,
+                         p);
   stage_end(s);
   return err;
 }
