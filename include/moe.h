@@ -174,7 +174,7 @@ moe_status moe_tile_map(const int32_t* counts, int E, int BM, int32_t* tiles, in
 
 /* ---------------------------------------------------------------- forward
  * moe_select_path - the path moe_forward takes for *p (AUTO resolved):
- * bf16 and MXFP8 -> GROUPED; per-tensor FP8 -> ROUTE_DIRECT for T <= 32,
+ * bf16 and MXFP8 -> GROUPED; per-tensor FP8 -> ROUTE_DIRECT for T <= 96,
  * blockwise FP8 -> ROUTE_DIRECT for T <= 64 (both also need T*k <= 1024), else
  * GROUPED: the crossovers measured on GB300.  Returns p->path when it is not
  * AUTO. */

@@ -142,10 +142,11 @@ ShuffleLayout plan_shuffle(int T, int E, int k, size_t base) {
 // Largest T for which AUTO takes the route-direct path (beyond it, the grouped
 // path), per FP8 mode.  Measured on GB300 with both paths captured in CUDA
 // graphs, L2 flushed between calls, k = 8: per-tensor (E=192, H=4096, I=192)
-// route-direct is faster through T=32 and the grouped path from T=48;
-// blockwise (E=128, H=2048, I=768 / H=4096, I=512) route-direct is faster
-// through T=96 / T=48 and the grouped path from T=128 / T=64.
-constexpr int kAutoRouteDirectMaxTokensPerTensor = 32;
+// route-direct is faster through T=96 (156.8 vs 166.7 us), even at T=112 and
+// slower at T=128; blockwise (E=128, H=2048, I=768 / H=4096, I=512)
+// route-direct is faster through T=64 (140.4 vs 144.5 / 183.4 vs 189.6 us) and
+// even or slower at T=96.
+constexpr int kAutoRouteDirectMaxTokensPerTensor = 96;
 constexpr int kAutoRouteDirectMaxTokensBlockwise = 64;
 
 // S shared experts run on the grouped path only (their rows join the expert-sorted

@@ -47,9 +47,10 @@ def test_workspace_size_and_path(m):
     assert m.moe_workspace_size(p) > 0
     q = m.problem(1, 192, 8, 4096, 192, "fp8_tensor")
     assert m.moe_select_path(q) == m.MOE_PATH_ROUTE_DIRECT
-    # AUTO crossovers: per-tensor FP8 up to T = 32, blockwise up to T = 64, and T*k <= 1024
-    assert m.moe_select_path(m.problem(32, 192, 8, 4096, 192, "fp8_tensor")) == m.MOE_PATH_ROUTE_DIRECT
-    assert m.moe_select_path(m.problem(33, 192, 8, 4096, 192, "fp8_tensor")) == m.MOE_PATH_GROUPED
+    # AUTO crossovers: per-tensor FP8 up to T = 96, blockwise up to T = 64, and T*k <= 1024
+    assert m.moe_select_path(m.problem(96, 192, 8, 4096, 192, "fp8_tensor")) == m.MOE_PATH_ROUTE_DIRECT
+    assert m.moe_select_path(m.problem(97, 192, 8, 4096, 192, "fp8_tensor")) == m.MOE_PATH_GROUPED
+    assert m.moe_select_path(m.problem(96, 192, 16, 4096, 192, "fp8_tensor")) == m.MOE_PATH_GROUPED
     assert m.moe_select_path(m.problem(64, 128, 8, 2048, 768, "fp8_block")) == m.MOE_PATH_ROUTE_DIRECT
     assert m.moe_select_path(m.problem(65, 128, 8, 2048, 768, "fp8_block")) == m.MOE_PATH_GROUPED
     assert m.moe_select_path(m.problem(40, 128, 32, 2048, 768, "fp8_block")) == m.MOE_PATH_GROUPED

@@ -494,8 +494,22 @@ def test_forward_grouped_fp8_hunyuan_shape_and_auto_switch(m):
     ref = O.forward(*oracle_args(inp), wl.k, wl.quant)
     _check_routing_views(m, wl, p, ws, ref, inp)
     _check_y(wl, y, ref["y"])
-    assert m.moe_select_path(m.problem(32, wl.E, wl.k, wl.H, wl.I, wl.quant)) == m.MOE_PATH_ROUTE_DIRECT
-    assert m.moe_select_path(m.problem(33, wl.E, wl.k, wl.H, wl.I, wl.quant)) == m.MOE_PATH_GROUPED
+    assert m.moe_select_path(m.problem(96, wl.E, wl.k, wl.H, wl.I, wl.quant)) == m.MOE_PATH_ROUTE_DIRECT
+    assert m.moe_select_path(m.problem(97, wl.E, wl.k, wl.H, wl.I, wl.quant)) == m.MOE_PATH_GROUPED
+
+
+@pytest.mark.parametrize("name,T", [("hunyuan", 96), ("qwen3a", 64), ("qwen3b", 64)])
+def test_forward_auto_route_direct_at_its_largest_batch(m, name, T):
+    """The largest batch AUTO sends down the route-direct path, at the decode shapes
+    the crossover was measured on: 768 / 512 routes over most of the experts."""
+    wl = W.workload(name, 1).with_tokens(T)
+    w1, w2, s1, s2 = _decode_weights(name)
+    inp = {"x": W.make_x(wl), "scores": W.make_scores(wl), "w1": w1, "w2": w2, "w1_scale": s1, "w2_scale": s2}
+    p, y, ws = run_forward(m, wl, _dev(inp))
+    assert m.moe_select_path(p) == m.MOE_PATH_ROUTE_DIRECT
+    ref = O.forward(*oracle_args(inp), wl.k, wl.quant)
+    _check_routing_views(m, wl, p, ws, ref, inp)
+    _check_y(wl, y, ref["y"])
 
 
 @pytest.mark.parametrize("T", [4, 24])
@@ -513,11 +527,12 @@ def test_fp8_grouped_and_route_direct_agree(m, T):
 
 FP8_BLOCK_GROUPED = [
     W.Workload("f8b_small", 64, 32, 8, 512, 256, W.QUANT_FP8_BLOCK, 51),
-    W.Workload("f8b_ragged", 300, 16, 4, 384, 384, W.QUANT_FP8_BLOCK, 52),  # 6 Gate/Up N tiles, 3 Down N tiles
+    # 3 Gate/Up groups of 128 h columns; 2 Down N tiles of 256 columns, the second with 128
+    W.Workload("f8b_ragged", 300, 16, 4, 384, 384, W.QUANT_FP8_BLOCK, 52),
     W.Workload("f8b_tiny", 5, 8, 2, 256, 128, W.QUANT_FP8_BLOCK, 53),
     W.Workload("f8b_onexp", 130, 1, 1, 128, 128, W.QUANT_FP8_BLOCK, 54),  # one K block each way, 2 row tiles
     # a last scale group of I with 64 columns (the route-MMA page's dispatch admits I % 64 == 0):
-    # a single Gate/Up unit for that group, a half K block in the Down GEMM
+    # half of that Gate/Up group's columns idle, a half K block in the Down GEMM
     W.Workload("f8b_i320", 300, 16, 4, 384, 320, W.QUANT_FP8_BLOCK, 56),
     W.Workload("f8b_i64", 70, 8, 2, 256, 64, W.QUANT_FP8_BLOCK, 58),
 ]
