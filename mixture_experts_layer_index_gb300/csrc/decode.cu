@@ -801,22 +801,44 @@ __global__ void __launch_bounds__(THREADS, 2) rd_down_kernel(const __grid_consta
         r_beg = uv.off()[u] + uv.gn0()[g];
         nn = min(GROUP, uv.off()[u + 1] - r_beg);
         consumer_sync();
-        // blockwise MMAs read whole 128-byte K blocks: columns past I are staged as zeros
-        const int c4 = (BLOCKWISE ? ngi * 128 : I) / 4;
-        for (int i = threadIdx.x; i < GROUP * c4; i += 32 * CONSUMERS) {
-          const int n = i / c4, c = (i - n * c4) * 4;
-          uint32_t q = 0;
-          if (n < nn && c < I) {
-            const int r = uv.routes()[r_beg + n];
-            if (BLOCKWISE) {
-              q = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(a.act) + static_cast<size_t>(r) * I + c));
-            } else {
+        // blockwise MMAs read whole 128-byte K blocks: columns past I are staged as zeros.
+        // Blockwise rows are copied with 8 loads in flight per thread; per-tensor rows
+        // are quantised on the way (an IEEE division per value), one piece at a time:
+        // batching those measured 3 us slower per call
+        if (BLOCKWISE) {
+          const int c4 = ngi * 128 / 4;
+          constexpr int SB = 8;
+          for (int base = 0; base < GROUP * c4; base += SB * 32 * CONSUMERS) {
+            uint32_t v[SB];
+#pragma unroll
+            for (int j = 0; j < SB; ++j) {
+              const int i = base + threadIdx.x + j * 32 * CONSUMERS;
+              const int n = i / c4, c = (i - n * c4) * 4;
+              v[j] = 0u;
+              if (n < nn && c < I)
+                v[j] = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(a.act) +
+                                                               static_cast<size_t>(uv.routes()[r_beg + n]) * I + c));
+            }
+#pragma unroll
+            for (int j = 0; j < SB; ++j) {
+              const int i = base + threadIdx.x + j * 32 * CONSUMERS;
+              const int n = i / c4, c = (i - n * c4) * 4;
+              if (n < GROUP) *reinterpret_cast<uint32_t*>(m.opnd + n * hpitch + c) = v[j];
+            }
+          }
+        } else {
+          const int c4 = I / 4;
+          for (int i = threadIdx.x; i < GROUP * c4; i += 32 * CONSUMERS) {
+            const int n = i / c4, c = (i - n * c4) * 4;
+            uint32_t q = 0;
+            if (n < nn) {
+              const int r = uv.routes()[r_beg + n];
               const float4 v = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(a.act) + static_cast<size_t>(r) * I + c));
               q = static_cast<uint32_t>(cvt_e4m3x2(v.x / s_h_t, v.y / s_h_t)) |
                   (static_cast<uint32_t>(cvt_e4m3x2(v.z / s_h_t, v.w / s_h_t)) << 16);
             }
+            *reinterpret_cast<uint32_t*>(m.opnd + n * hpitch + c) = q;
           }
-          *reinterpret_cast<uint32_t*>(m.opnd + n * hpitch + c) = q;
         }
         if (BLOCKWISE) {
           for (int i = threadIdx.x; i < GROUP * ngi; i += 32 * CONSUMERS) {
