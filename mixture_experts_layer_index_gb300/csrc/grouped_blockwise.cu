@@ -47,8 +47,9 @@ constexpr int EPI_WARPS = 8;       // warps 2..9 (the block's registers come in 
 constexpr int THREADS = 32 * (2 + EPI_WARPS);
 constexpr int NUM_BARS = 2 * STAGES + 2 * NBUF + 8;
 constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
-constexpr int SCRATCH_OFFSET = BAR_OFFSET + 256;
-// epilogue scratch: Gate/Up row maxima [8 warps][32] fp32; Down output staging [8 warps][32 rows][128 bytes]
+// epilogue scratch, 1024-byte aligned: Gate/Up row maxima [8 warps][32] fp32; Down output
+// staging [8 warps][32 rows][128 bytes], each warp's 4 KB a 128-byte-swizzled TMA store box
+constexpr int SCRATCH_OFFSET = (BAR_OFFSET + 256 + 1023) / 1024 * 1024;
 constexpr int SCRATCH_BYTES = EPI_WARPS * 32 * 128;
 constexpr size_t SMEM_BYTES = 1024 + SCRATCH_OFFSET + SCRATCH_BYTES;
 static_assert(NUM_BARS * 8 + 8 <= 256, "barrier region");
@@ -113,7 +114,8 @@ __device__ __forceinline__ void store_e4m3x32(uint8_t* dst, const float* a, floa
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_blockwise_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                             const __grid_constant__ CUtensorMap tmB2, const Params p) {
+                             const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmO,
+                             const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFFSET);
@@ -144,6 +146,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
     prefetch_tensormap(&tmB2);
+    if (MODE == MODE_DOWN) prefetch_tensormap(&tmO);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -367,29 +370,42 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       } else if (valid) {
         // o rows (sorted order, like h): each thread's 128 bf16 outputs go through this
-        // warp's 4 KB of staging in two passes of 64 columns (16-byte pieces XOR-swizzled
-        // by row), and the warp writes four whole 128-byte row segments per store.
+        // warp's 4 KB of staging in two passes of 64 columns, 16-byte pieces placed as the
+        // 128-byte swizzle has them (piece c of row r at c ^ (r & 7)); a warp whose 32 rows
+        // all belong to the tile hands the box to a TMA tile store, otherwise it writes
+        // four whole 128-byte row segments per store instruction.
         uint4* stg = reinterpret_cast<uint4*>(scratch) + e8 * (32 * 8);
         const int vrows = min(32, nrows - q * 32);  // valid rows of this warp (may be <= 0)
         const int slot = row0 + row;
 #pragma unroll
         for (int pass = 0; pass < 2; ++pass) {
-          __syncwarp();  // the previous pass's reads of the staging are done
+          if (lane == 0) bulk_wait_group_read0();  // the previous TMA store has read the staging
+          __syncwarp();                            // and the previous pass's loads are done
 #pragma unroll
           for (int i = 0; i < 8; ++i) stg[lane * 8 + (i ^ (lane & 7))] = pack_bf16x8(acc + 64 * pass + 8 * i);
-          __syncwarp();
+          if (vrows == 32) {
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmO, smem_u32(stg), col + 64 * pass, row0 + q * 32);
+              bulk_commit_group();
+            }
+          } else {
+            __syncwarp();
 #pragma unroll
-          for (int it2 = 0; it2 < 8; ++it2) {
-            const int r = it2 * 4 + (lane >> 3), j = lane & 7;
-            const int rslot = __shfl_sync(0xffffffffu, slot, r);
-            if (r < vrows)
-              *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(rslot) * p.H + col + 64 * pass + j * 8) =
-                  stg[r * 8 + (j ^ (r & 7))];
+            for (int it2 = 0; it2 < 8; ++it2) {
+              const int r = it2 * 4 + (lane >> 3), j = lane & 7;
+              const int rslot = __shfl_sync(0xffffffffu, slot, r);
+              if (r < vrows)
+                *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(rslot) * p.H + col + 64 * pass + j * 8) =
+                    stg[r * 8 + (j ^ (r & 7))];
+            }
           }
         }
         __syncwarp();
       }
     }
+    if (MODE == MODE_DOWN && lane == 0) bulk_wait_group0();  // this warp's TMA stores have completed
   }
   tc_fence_before();
   __syncthreads();
@@ -409,6 +425,19 @@ static bool encode_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// o [R][H] bf16 as TMA store boxes of 32 rows x 64 columns (128-byte swizzle).
+static bool encode_o(CUtensorMap* map, void* base, uint64_t H, uint64_t R) {
+  EncodeTiledFn fn = get_encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {H, R};
+  const cuuint64_t strides[1] = {H * 2};
+  const cuuint32_t box[2] = {64, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
 }
 
 template <int MODE>
@@ -452,7 +481,7 @@ cudaError_t launch_gateup_blockwise(const GroupedArgs& a, const float* xs_scale,
   const int grid = static_cast<int>(items < sms ? items : sms);
   stage_begin("gateup_gemm", s);
   err = launch_dependent(grouped_blockwise_kernel<MODE_GATEUP>, dim3(grid), dim3(THREADS), SMEM_BYTES, s, tma, tmb,
-                         tmbs, p);
+                         tmbs, tma, p);
   stage_end(s);
   return err;
 }
@@ -464,8 +493,9 @@ cudaError_t launch_down_blockwise(const GroupedArgs& a, const float* h_scale, cu
   if (err != cudaSuccess) return err;
   const int sms = num_sms();
   if (sms <= 0) return cudaErrorNoDevice;
-  CUtensorMap tma, tmb, tmbs;
-  if (!encode_u8(&tma, a.h, a.I, a.R, BM) || !encode_u8(&tmb, a.w2, a.I, static_cast<uint64_t>(a.E) * a.H, 128))
+  CUtensorMap tma, tmb, tmbs, tmo;
+  if (!encode_u8(&tma, a.h, a.I, a.R, BM) || !encode_u8(&tmb, a.w2, a.I, static_cast<uint64_t>(a.E) * a.H, 128) ||
+      !encode_o(&tmo, a.o, a.H, a.R))
     return cudaErrorInvalidValue;
   tmbs = tmb;
   if (a.S > 0 && !encode_u8(&tmbs, a.w2s, a.I, static_cast<uint64_t>(a.S) * a.H, 128)) return cudaErrorInvalidValue;
@@ -487,7 +517,7 @@ cudaError_t launch_down_blockwise(const GroupedArgs& a, const float* h_scale, cu
   const int grid = static_cast<int>(units < sms ? units : sms);
   stage_begin("down_gemm", s);
   err = launch_dependent(grouped_blockwise_kernel<MODE_DOWN>, dim3(grid), dim3(THREADS), SMEM_BYTES, s, tma, tmb, tmbs,
-                         p);
+                         tmo, p);
   stage_end(s);
   return err;
 }
