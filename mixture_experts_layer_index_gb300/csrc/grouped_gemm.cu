@@ -83,7 +83,7 @@ struct Params {
   const float* wscale2;           // [S] scales of the shared experts' matrices
   const unsigned int* amax_in;    // fp32 bits of the amax of the A operand's source (x or a)
   unsigned int* amax_out;         // Gate/Up: receives the amax of a
-  float* out_f32;                 // Gate/Up: a [R, I] fp32 (quantised by the next pass)
+  __nv_bfloat16* out_a;           // F8 Gate/Up: a [R, I] bf16 (quantised by the next pass)
 };
 
 __device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
@@ -282,10 +282,11 @@ __global__ void __launch_bounds__(threads_of(MODE, F8), 1)
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       if (MODE == MODE_GATEUP) {
         // bf16: direct stores (each thread writes whole 64-byte pieces of its own
-        // sorted row).  F8: a = silu(sc g) * (sc u) with sc = s_x * s_w1[e], kept
-        // in fp32 for the per-tensor quantisation of h, whose amax is recorded here;
-        // each warp stages one [32 rows][32 fp32] box per iteration (128-byte
-        // swizzle) and stores it by TMA when all 32 rows belong to the tile.
+        // sorted row).  F8: a = silu(sc g) * (sc u) with sc = s_x * s_w1[e]; the
+        // amax of a (fp32) for the per-tensor quantisation of h is recorded here, and
+        // a itself is kept in bf16 for that second pass: the two 32-column halves of
+        // a warp's 64 columns fill one [32 rows][64 bf16] box of its staging
+        // (128-byte swizzle), stored by TMA when all 32 rows belong to the tile.
         const float sc = F8 ? e4m3_scale(__uint_as_float(*p.amax_in)) * wscale_of(p, tl.x) : 1.0f;
         float amax = 0.0f;
         __nv_bfloat16* out_row = p.out + static_cast<size_t>(row0 + row) * p.out_ld;
@@ -303,40 +304,46 @@ __global__ void __launch_bounds__(threads_of(MODE, F8), 1)
           }
           const int col = n * (BN / 2) + c;
           if (F8) {
+            static_assert(MODE != MODE_GATEUP || !F8 || GC == 64, "F8 Gate/Up: 64 columns (two halves of 32) per warp");
             uint8_t* stg = smem + STAGING_OFFSET + e8 * 4096;
             const int wrows = min(32, nrows - q * 32), wrow0 = row0 + q * 32;
-            if (lane == 0) bulk_wait_group_read0();  // the previous box has left the staging
-            __syncwarp();
+            const int half = (c - h * GC) >> 5;  // which 32 of the box's 64 columns
+            if (half == 0) {
+              if (lane == 0) bulk_wait_group_read0();  // the previous box has left the staging
+              __syncwarp();
+            }
             float hv[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) hv[i] = silu_mul(sc * g[i], sc * up[i]);
             const bool valid = row < nrows && col < p.n_valid;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              *reinterpret_cast<float4*>(stg + lane * 128 + ((i ^ (lane & 7)) << 4)) =
-                  make_float4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+            for (int i = 0; i < 4; ++i) {
+              *reinterpret_cast<uint4*>(stg + lane * 128 + (((half * 4 + i) ^ (lane & 7)) << 4)) = pack_bf16x8(hv + 8 * i);
               if (valid)
-                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(hv[4 * i]), fabsf(hv[4 * i + 1])),
-                                         fmaxf(fabsf(hv[4 * i + 2]), fabsf(hv[4 * i + 3]))));
-            }
-            if (wrows == 32) {
-              fence_proxy_async_shared();
-              __syncwarp();
-              if (lane == 0) {
-                if (col < p.n_valid) tma_store_2d(&tmO, smem_u32(stg), col, wrow0);
-                bulk_commit_group();
-              }
-              __syncwarp();
-            } else {
-              __syncwarp();
 #pragma unroll
-              for (int it = 0; it < 8; ++it) {  // 4 rows of 32 fp32 (8 lanes each) per instruction
-                const int r = it * 4 + (lane >> 3), j = lane & 7;
-                if (r < wrows && col + 4 * j < p.n_valid)
-                  *reinterpret_cast<float4*>(p.out_f32 + static_cast<size_t>(wrow0 + r) * p.out_ld + col + 4 * j) =
-                      *reinterpret_cast<const float4*>(stg + r * 128 + ((j ^ (r & 7)) << 4));
+                for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(hv[8 * i + j]));
+            }
+            if (half == 1) {
+              const int col0 = col - 32;  // the box's first column (a multiple of 64; I % 64 == 0)
+              if (wrows == 32) {
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                  if (col0 < p.n_valid) tma_store_2d(&tmO, smem_u32(stg), col0, wrow0);
+                  bulk_commit_group();
+                }
+                __syncwarp();
+              } else {
+                __syncwarp();
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {  // 4 rows of 64 bf16 (8 lanes each) per instruction
+                  const int r = it * 4 + (lane >> 3), j = lane & 7;
+                  if (r < wrows && col0 + 8 * j < p.n_valid)
+                    *reinterpret_cast<uint4*>(p.out_a + static_cast<size_t>(wrow0 + r) * p.out_ld + col0 + 8 * j) =
+                        *reinterpret_cast<const uint4*>(stg + r * 128 + ((j ^ (r & 7)) << 4));
+                }
+                __syncwarp();
               }
-              __syncwarp();
             }
           } else if (row < nrows && col < p.n_valid) {
             float hv[32];
@@ -444,20 +451,6 @@ static bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64
   return r == CUDA_SUCCESS;
 }
 
-// fp32 [outer][inner] tensor, 128-byte swizzle (TMA stores of the FP8 Gate/Up output a)
-static bool encode_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-                          uint32_t box_outer) {
-  EncodeTiledFn fn = get_encode_tiled();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner * 4};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int MODE, bool F8>
 static cudaError_t set_smem_attr() {
   static cudaError_t st = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, F8>,
@@ -515,9 +508,9 @@ cudaError_t launch_gateup_bf16(const GroupedArgs& a, cudaStream_t s) {
   p.wscale2 = a.w1s_scale;
   p.amax_in = &a.hdr->amax_x;
   p.amax_out = &a.hdr->amax_h;
-  p.out_f32 = static_cast<float*>(a.a_f32);
-  CUtensorMap tma32 = tmx;  // F8: a [R rows][I] fp32, stored in [32 rows][32 columns] boxes
-  if (a.f8 && !encode_2d_f32(&tma32, a.a_f32, a.I, a.R, 32, 32)) return cudaErrorInvalidValue;
+  p.out_a = static_cast<__nv_bfloat16*>(a.a_bf16);
+  CUtensorMap tmab = tmx;  // F8: a [R rows][I] bf16, stored in [32 rows][64 columns] boxes
+  if (a.f8 && !encode_2d(&tmab, a.a_bf16, a.I, a.R, 64, 32)) return cudaErrorInvalidValue;
   p.nN = (a.I + BN / 2 - 1) / (BN / 2);
   p.K = a.H;
   p.b_rows_per_expert = 2 * a.I;
@@ -530,7 +523,7 @@ cudaError_t launch_gateup_bf16(const GroupedArgs& a, cudaStream_t s) {
   stage_begin("gateup_gemm", s);
   if (a.f8)
     err = launch_dependent(grouped_gemm_kernel<MODE_GATEUP, true>, dim3(grid), dim3(threads_of(MODE_GATEUP, true)),
-                           SMEM_BYTES, s, tmx, tmw1, tma32, tmw1s, p);
+                           SMEM_BYTES, s, tmx, tmw1, tmab, tmw1s, p);
   else
     err = launch_dependent(grouped_gemm_kernel<MODE_GATEUP, false>, dim3(grid), dim3(threads_of(MODE_GATEUP, false)),
                            SMEM_BYTES, s, tmx, tmw1, tmx, tmw1s, p);

@@ -47,7 +47,7 @@ struct ForwardLayout {
   int max_tiles = 0;
   size_t xs = 0;      // grouped: [R, H] x rows in sorted order (Gate/Up A operand; bf16 or e4m3)
   size_t xs_scale = 0;  // grouped blockwise FP8: [R, H/128] fp32 scales of xs
-  size_t a32 = 0;     // grouped FP8: [R, I] fp32 a before its quantisation
+  size_t abf = 0;     // grouped per-tensor FP8: [R, I] bf16 a before its quantisation
   size_t h = 0;       // grouped: [R, I] h in sorted order (bf16 or e4m3)
   size_t o = 0;       // grouped: [R, H] bf16 (sorted order); route-direct: [R, H] fp32 (route order)
   // route-direct
@@ -93,7 +93,8 @@ cudaError_t launch_scatter_gather(const int32_t* ids, const int32_t* lrank, cons
 cudaError_t launch_scatter_gather_q(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
                                     int k, int H, const void* x, void* xs, int32_t* perm, int32_t* inv,
                                     const DeviceHeader* hdr, cudaStream_t s, int S = 0);
-cudaError_t launch_quant_rows(const float* a, void* h, size_t n, const DeviceHeader* hdr, cudaStream_t s);
+// h = e4m3(a / s) for n values of bf16 a (n % 8 == 0), s = amax_h / 448 from hdr.
+cudaError_t launch_quant_rows(const void* a, void* h, size_t n, const DeviceHeader* hdr, cudaStream_t s);
 // Blockwise (one scale per row and 128 columns) passes of the grouped FP8 path (quant.cu).
 cudaError_t launch_scatter_gather_qb(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
                                      int k, int H, const void* x, void* xs, float* xs_scale, int32_t* perm,
@@ -128,7 +129,7 @@ struct GroupedArgs {
   bool f8;
   const float* w1_scale;
   const float* w2_scale;
-  void* a_f32;           // Gate/Up output a [R, I] fp32 (f8)
+  void* a_bf16;          // per-tensor FP8 Gate/Up output a [R, I] bf16 (its amax in hdr, taken in fp32)
 };
 cudaError_t launch_gateup_bf16(const GroupedArgs& a, cudaStream_t s);  // bf16 or e4m3 (a.f8)
 cudaError_t launch_down_bf16(const GroupedArgs& a, cudaStream_t s);

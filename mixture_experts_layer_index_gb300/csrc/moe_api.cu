@@ -238,7 +238,7 @@ bool plan_forward(const moe_problem& p, ForwardLayout* out, int S) {
     const size_t eb = p.quant == MOE_BF16 ? 2 : 1;  // bytes per element of the GEMM inputs
     L.xs = take(RS * H * eb);
     if (p.quant == MOE_FP8_BLOCK128) L.xs_scale = take(RS * (H / 128) * 4);
-    if (p.quant == MOE_FP8_PER_TENSOR) L.a32 = take(RS * I * 4);
+    if (p.quant == MOE_FP8_PER_TENSOR) L.abf = take(RS * I * 2);
     L.h = take(RS * I * eb);
     if (p.quant == MOE_FP8_BLOCK128) L.sh = take(RS * ((I + 127) / 128) * 4);
     if (p.quant == MOE_MXFP8) {
@@ -483,7 +483,7 @@ moe_status moe_forward_ex(const moe_problem* pp, const moe_forward_options* opt,
       g.f8 = f8 || blockwise;
       g.w1_scale = w1_scale;
       g.w2_scale = w2_scale;
-      g.a_f32 = f8 ? at<void*>(ws, L.a32) : nullptr;
+      g.a_bf16 = f8 ? at<void*>(ws, L.abf) : nullptr;
       if (mxfp8) g.f8 = true;
       g.xs = gather4 ? nullptr : xs;
       g.perm = perm; g.tiles = tiles; g.num_tiles = num_tiles; g.max_tiles = L.max_tiles;
@@ -520,7 +520,7 @@ moe_status moe_forward_ex(const moe_problem* pp, const moe_forward_options* opt,
       } else {
         e = launch_gateup_bf16(g, s);
         if (e == cudaSuccess && f8)
-          e = launch_quant_rows(static_cast<const float*>(g.a_f32), g.h, static_cast<size_t>(g.R) * p.I, hdr, s);
+          e = launch_quant_rows(g.a_bf16, g.h, static_cast<size_t>(g.R) * p.I, hdr, s);
         if (e == cudaSuccess) e = launch_down_bf16(g, s);
       }
     }

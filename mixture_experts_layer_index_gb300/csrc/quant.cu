@@ -87,8 +87,21 @@ __global__ void __launch_bounds__(256) scatter_gather_tok_q_kernel(
 }
 
 // h = e4m3(a / s_h), s_h = e4m3_scale(amax of a); 4 values per thread-iteration.
-__global__ void __launch_bounds__(256) quant_rows_kernel(const float4* __restrict__ a, uint32_t* __restrict__ h,
-                                                         size_t n4, const DeviceHeader* hdr) {
+// 8 bf16 values (one 16-byte piece) / s -> 8 e4m3 codes.
+__device__ __forceinline__ uint2 quant_bf16x8(const uint4& v, float s) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t q[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float f0 = __uint_as_float(w[2 * i] << 16), f1 = __uint_as_float(w[2 * i] & 0xFFFF0000u);
+    const float f2 = __uint_as_float(w[2 * i + 1] << 16), f3 = __uint_as_float(w[2 * i + 1] & 0xFFFF0000u);
+    q[i] = static_cast<uint32_t>(cvt_e4m3x2(f0 / s, f1 / s)) | (static_cast<uint32_t>(cvt_e4m3x2(f2 / s, f3 / s)) << 16);
+  }
+  return make_uint2(q[0], q[1]);
+}
+
+__global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict__ a, uint2* __restrict__ h,
+                                                         size_t n8, const DeviceHeader* hdr) {
   dep_wait();  // a and its amax from the Gate/Up GEMM
   const float s = e4m3_scale(__uint_as_float(hdr->amax_h));
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
@@ -96,22 +109,14 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const float4* __restric
   // evicted from L2 first and the h rows just written stay for the Down GEMM
   const uint64_t pol = l2_evict_first_policy();
   size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
-  for (; i + 3 * stride < n4; i += 4 * stride) {
+  for (; i + 3 * stride < n8; i += 4 * stride) {
     uint4 v[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) v[j] = ld_nc_v4_hint(a + i + j * stride, pol);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float4 f = make_float4(__uint_as_float(v[j].x), __uint_as_float(v[j].y), __uint_as_float(v[j].z),
-                                   __uint_as_float(v[j].w));
-      h[i + j * stride] = static_cast<uint32_t>(cvt_e4m3x2(f.x / s, f.y / s)) |
-                          (static_cast<uint32_t>(cvt_e4m3x2(f.z / s, f.w / s)) << 16);
-    }
+    for (int j = 0; j < 4; ++j) h[i + j * stride] = quant_bf16x8(v[j], s);
   }
-  for (; i < n4; i += stride) {
-    const float4 v = __ldg(a + i);
-    h[i] = static_cast<uint32_t>(cvt_e4m3x2(v.x / s, v.y / s)) | (static_cast<uint32_t>(cvt_e4m3x2(v.z / s, v.w / s)) << 16);
-  }
+  for (; i < n8; i += stride) h[i] = quant_bf16x8(__ldg(a + i), s);
 }
 
 // h = e4m3(a / s), one scale per (row, 128 columns): one warp per group, 4
@@ -183,12 +188,12 @@ cudaError_t launch_scatter_gather_q(const int32_t* ids, const int32_t* lrank, co
   return launch_tok_q(false, ids, lrank, blockbase, T, E, k, H, x, xs, nullptr, perm, inv, hdr, s, S);
 }
 
-cudaError_t launch_quant_rows(const float* a, void* h, size_t n, const DeviceHeader* hdr, cudaStream_t s) {
-  const size_t n4 = n / 4;
-  if (n4 == 0) return cudaSuccess;
+cudaError_t launch_quant_rows(const void* a, void* h, size_t n, const DeviceHeader* hdr, cudaStream_t s) {
+  const size_t n8 = n / 8;
+  if (n8 == 0) return cudaSuccess;
   stage_begin("quant_h", s);
-  const cudaError_t err = launch_dependent(quant_rows_kernel, dim3(grid_for(n4, 256)), dim3(256), 0, s,
-                                           reinterpret_cast<const float4*>(a), static_cast<uint32_t*>(h), n4, hdr);
+  const cudaError_t err = launch_dependent(quant_rows_kernel, dim3(grid_for(n8, 256)), dim3(256), 0, s,
+                                           static_cast<const uint4*>(a), static_cast<uint2*>(h), n8, hdr);
   stage_end(s);
   return err;
 }
