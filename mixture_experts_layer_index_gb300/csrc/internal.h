@@ -99,7 +99,6 @@ cudaError_t launch_quant_rows(const void* a, void* h, size_t n, const DeviceHead
 cudaError_t launch_scatter_gather_qb(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
                                      int k, int H, const void* x, void* xs, float* xs_scale, int32_t* perm,
                                      int32_t* inv, cudaStream_t s, int S = 0);
-cudaError_t launch_quant_groups(const float* a, void* h, float* sh, int rows, int cols, cudaStream_t s);
 cudaError_t launch_tile_map(const int32_t* counts, int E, int BM, int32_t* tiles, int32_t* num_tiles,
                             int max_tiles, int32_t* tile_scratch, DeviceHeader* hdr, cudaStream_t s);
 cudaError_t launch_reset_header(DeviceHeader* hdr, cudaStream_t s);
@@ -147,9 +146,6 @@ size_t mx_blocked_bytes(size_t blocks, int C);
 cudaError_t launch_scatter_gather_mx(const int32_t* ids, const int32_t* lrank, const int32_t* blockbase, int T, int E,
                                      int k, int H, const void* x, void* xs, uint8_t* xs_sc, uint8_t* xs_sf,
                                      const int32_t* padbase, int32_t* perm, int32_t* inv, cudaStream_t s, int S = 0);
-// Row-major scales [rows, C] -> blocked layout, one block per tile of the tile map.
-cudaError_t launch_mx_blocked_tiles(const uint8_t* sc, int C, const int32_t* tiles, const int32_t* num_tiles,
-                                    int max_tiles, uint8_t* out, cudaStream_t s);
 // W1 scales [E, 2I, H/32] (blocks of 64 gate + the matching 64 up rows) and W2
 // scales [E, H, I/32] (blocks of 128 rows) -> blocked layouts.
 cudaError_t launch_mx_blocked_weights(const uint8_t* w1_sc, const uint8_t* w2_sc, int E, int H, int I, uint8_t* w1_sf,

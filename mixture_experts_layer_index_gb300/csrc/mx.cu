@@ -683,15 +683,6 @@ cudaError_t launch_scatter_gather_mx(const int32_t* ids, const int32_t* lrank, c
   return err;
 }
 
-cudaError_t launch_mx_blocked_tiles(const uint8_t* sc, int C, const int32_t* tiles, const int32_t* num_tiles,
-                                    int max_tiles, uint8_t* out, cudaStream_t s) {
-  stage_begin("mx_scales", s);
-  const cudaError_t err = mx::launch_blocked<mx::SRC_TILES>(sc, C, tiles, num_tiles, 0, out,
-                                                            static_cast<unsigned>(max_tiles), false, s);
-  stage_end(s);
-  return err;
-}
-
 cudaError_t launch_mx_blocked_weights(const uint8_t* w1_sc, const uint8_t* w2_sc, int E, int H, int I, uint8_t* w1_sf,
                                       uint8_t* w2_sf, cudaStream_t s) {
   stage_begin("mx_weight_scales", s);

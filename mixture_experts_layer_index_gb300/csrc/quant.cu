@@ -119,42 +119,6 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
   for (; i < n8; i += stride) h[i] = quant_bf16x8(__ldg(a + i), s);
 }
 
-// h = e4m3(a / s), one scale per (row, 128 columns): one warp per group, 4
-// values per lane; rows x groups items, 4 of them in flight per warp.
-__global__ void __launch_bounds__(256) quant_groups_kernel(const float4* __restrict__ a, uint32_t* __restrict__ h,
-                                                           float* __restrict__ sh, size_t items) {
-  dep_wait();  // a from the Gate/Up GEMM
-  const int lane = threadIdx.x & 31;
-  const size_t nw = (static_cast<size_t>(gridDim.x) * blockDim.x) >> 5;
-  // eight groups per warp and pass (their loads in flight together, their amax
-  // reductions interleaved); a is read once: L2 evicts it first, keeping h for Down
-  constexpr int NG = 8;
-  const uint64_t pol = l2_evict_first_policy();
-  for (size_t g0 = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; g0 < items; g0 += NG * nw) {
-    float4 v[NG];
-#pragma unroll
-    for (int j = 0; j < NG; ++j) {
-      const size_t g = g0 + j * nw;
-      v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (g < items) {
-        const uint4 u = ld_nc_v4_hint(a + g * 32 + lane, pol);
-        v[j] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < NG; ++j) {
-      const size_t g = g0 + j * nw;
-      const float m = warp_max(fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
-      const float s = e4m3_scale(m);
-      if (g < items) {
-        h[g * 32 + lane] = static_cast<uint32_t>(cvt_e4m3x2(v[j].x / s, v[j].y / s)) |
-                           (static_cast<uint32_t>(cvt_e4m3x2(v[j].z / s, v[j].w / s)) << 16);
-        if (lane == 0) sh[g] = s;
-      }
-    }
-  }
-}
-
 static unsigned grid_for(size_t work, unsigned per_block) {
   const int sms = num_sms();
   const size_t cap = static_cast<size_t>(sms > 0 ? sms : 148) * 16;
@@ -202,16 +166,6 @@ cudaError_t launch_scatter_gather_qb(const int32_t* ids, const int32_t* lrank, c
                                      int k, int H, const void* x, void* xs, float* xs_scale, int32_t* perm,
                                      int32_t* inv, cudaStream_t s, int S) {
   return launch_tok_q(true, ids, lrank, blockbase, T, E, k, H, x, xs, xs_scale, perm, inv, nullptr, s, S);
-}
-
-cudaError_t launch_quant_groups(const float* a, void* h, float* sh, int rows, int cols, cudaStream_t s) {
-  const size_t items = static_cast<size_t>(rows) * (cols / 128);
-  if (items == 0) return cudaSuccess;
-  stage_begin("quant_h", s);
-  const cudaError_t err = launch_dependent(quant_groups_kernel, dim3(grid_for(items * 32, 256 * 8)), dim3(256), 0, s,
-                                           reinterpret_cast<const float4*>(a), static_cast<uint32_t*>(h), sh, items);
-  stage_end(s);
-  return err;
 }
 
 }  // namespace moe
