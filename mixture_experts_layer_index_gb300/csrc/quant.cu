@@ -2,9 +2,11 @@
 // small-batch route MMA for MoE", Summary: per-tensor FP8 with dynamic
 // activation scales): the expert-sorted copy of x quantised with s_x = amax/448
 // (the amax of x comes from extra blocks of the route/rank kernel), and the
-// quantisation of a (the SwiGLU output) with its global scale s_h; plus the
-// blockwise forms.  Scales: amax / 448 in fp32 (1 when amax == 0); codes: round
-// to nearest even with saturation (cvt.rn.satfinite).
+// quantisation of a (the SwiGLU output, held in bf16) with its global scale s_h;
+// plus the blockwise form of the scatter (x quantised per (row, 128 columns); the
+// blockwise h is quantised in the Gate/Up epilogue).  Scales: amax / 448 in fp32
+// (1 when amax == 0); codes: round to nearest even with saturation
+// (cvt.rn.satfinite).
 #include "common.cuh"
 #include "internal.h"
 
