@@ -227,7 +227,7 @@ moe_status moe_forward(const moe_problem* p, const void* x, const float* scores,
  *   w1_shared        [S, 2I, H] bf16 | e4m3 (rows 0..I-1 gate, I..2I-1 up)
  *   w2_shared        [S, H, I]
  *   w1_shared_scale  NULL (bf16) | fp32 [S] | fp32 [S, 2I/128, H/128]
- *   w2_shared_scale  NULL (bf16) | fp32 [S] | fp32 [S, H/128, I/128]
+ *   w2_shared_scale  NULL (bf16) | fp32 [S] | fp32 [S, H/128, ceil(I/128)]
  * Shared experts run on the grouped path (AUTO takes it; an explicit
  * MOE_PATH_ROUTE_DIRECT with S > 0 is UNSUPPORTED).  0 <= S <= 16.
  *
